@@ -1,0 +1,557 @@
+#!/usr/bin/env python3
+"""Benchmark: decode-attention KV-read GB/s and microseconds per decode step.
+
+Default workload (N=1): B=1 long-context bucketed trace -- Hq=32, Hkv=8,
+d=128, N=32768 tokens, page_size 16, block table a random permutation of a
+2048-page pool, S=32 splits of 1024 tokens, keys scaled 0.5 -- on the
+length-bucketed split path (decode + merge per step).  `--config 1..5` selects
+the other workloads.
+
+One JSON line on rank 0:
+  value        K+V bytes of the step's valid tokens / device time per step
+               (CUDA events around K back-to-back steps replayed from CUDA
+               graphs; inputs resident in HBM; KV pools rotated so the data a
+               step reads is not in L2)
+  roofline     the decode kernel alone: algorithmic K+V bytes per launch /
+               its average CUDA-event duration, against the measured HBM peak
+  e2e          the same metric through the public API (PagedDecoder.step) with
+               pinned host buffers: q, seq_lens and block table copied in and
+               o, lse copied out every step, synchronized wall clock
+  cpu_baseline the float64 oracle on the host cores on a bounded sample
+`--impl reference` times the oracle alone (the reference arm).
+Multi-GPU (torchrun): every rank runs an independent replica (no collective
+on the data path); value sums the ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "decode-attention KV-read GB/s (% of GB300 HBM peak); µs per decode step"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    1: "B=1 GQA decode Hq=8 Hkv=2 d=128 N=1024 P=16 (64 pages of a 128-page pool) S=4 (C=256)",
+    2: "B=1 long-context bucketed Hq=32 Hkv=8 d=128 N=32768 P=16 (2048-page pool permutation) "
+       "S=32 (C=1024), keys x0.5",
+    3: "B=8 bimodal (4x U[512,2048], 4x U[24576,32768]) Hq=32 Hkv=8 d=128 P=16 C=1024 workqueue",
+    4: "B=8 Zipf s=1.2 on [16,32768] Hq=32 Hkv=8 d=128 P=16, policy route",
+    5: "B=64 uniform U[128,65536] Hq=64 Hkv=8 d=128 P=16 C=1024 workqueue, +1 token/row/step",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--path", default="policy", choices=["policy", "bucketed", "workqueue", "single"])
+    ap.add_argument("--no-graph", action="store_true", help="launch steps eagerly")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def default_steps(cfg_id):
+    # about a second of timed device work per run
+    return {1: 20000, 2: 40000, 3: 10000, 4: 20000, 5: 256}[cfg_id]
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    return rank, local, ws, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def reduce_max(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples, each stamped on arrival, kept if inside [t0, t1]."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [s for t, s in self.samples if t0 <= t <= t1 + 0.2]
+        if not inside:
+            inside = [s for _, s in self.samples]
+        sm, mx, reasons = [], [], set()
+        for s in inside:
+            try:
+                sm.append(float(s[0]))
+                mx.append(float(s[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(self.NAMES, s[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_gqa_09_gb300", "csrc")
+    for f in ("decode.cu", "pkv_device.cuh", "pkv_kernels.h"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(cfg_id: int):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", f"decode_config{cfg_id}_traffic.md")
+    try:
+        txt = open(p).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    if not (m_hash and m_tr) or m_hash.group(1) != decode_source_hash():
+        return None
+    return int(m_tr.group(1))
+
+
+def cpu_baseline_run(tr, q, k, v, seconds: float):
+    """The oracle, as it stands, on this host's cores: repeated whole decode
+    steps of the workload (or, for large workloads, a row-prefix sample) for
+    about `seconds`; returns (GB/s of K+V processed, cores, description)."""
+    import oracle
+    cores = oracle.max_threads()
+    lens = tr.seq_lens
+    # sample: the whole batch when one step fits in the budget, else one row prefix
+    t = time.perf_counter()
+    oracle.attention(q[:1], k, v, tr.block_table[:1], np.minimum(lens[:1], 2048), tr.scale)
+    probe = time.perf_counter() - t
+    per_tok = probe / min(int(lens[0]), 2048)
+    total_tok = int(lens.sum())
+    if per_tok * total_tok <= seconds / 2:
+        sample_lens, sample_q, sample_bt = lens, q, tr.block_table
+        desc = "whole decode steps of the workload"
+    else:
+        n = max(16, min(int(lens[0]), int(seconds / 4 / per_tok)))
+        sample_lens = np.array([n], np.int32)
+        sample_q, sample_bt = q[:1], tr.block_table[:1]
+        desc = f"row 0, first {n} tokens, all {tr.Hq} query heads, repeated"
+    bytes_per = int(sample_lens.astype(np.int64).sum()) * tr.Hkv * tr.d * 4
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention(sample_q, k, v, sample_bt, sample_lens, tr.scale)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return bytes_per * reps / el / 1e9, cores, f"{desc}; {reps} reps in {el:.1f} s"
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, rank, ws, pg):
+    import oracle
+    import pkv_traces as T
+    if rank != 0:
+        return
+    tr = T.make_trace(args.config)
+    steps = args.steps if args.steps is not None else default_steps(args.config)
+    warm = args.warmup if args.warmup is not None else 3
+    # the sample per step: row 0 prefix, sized so that all steps fit in ~60 s
+    if tr.num_pages * tr.page_size * tr.Hkv * tr.d <= (1 << 28):
+        q = T.gen_q(tr)
+        k, v = T.gen_kv(tr)
+    else:
+        tr, q, k, v = _row0_sample(tr)
+    budget = 60.0 / max(1, steps + warm)
+    t = time.perf_counter()
+    oracle.attention(q[:1], k, v, tr.block_table[:1], np.minimum(tr.seq_lens[:1], 256), tr.scale)
+    per_tok = (time.perf_counter() - t) / min(256, int(tr.seq_lens[0]))
+    n = int(max(16, min(int(tr.seq_lens[0]), budget / max(per_tok, 1e-9))))
+    sl = np.array([n], np.int32)
+    for _ in range(warm):
+        oracle.attention(q[:1], k, v, tr.block_table[:1], sl, tr.scale)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.attention(q[:1], k, v, tr.block_table[:1], sl, tr.scale)
+    el = time.perf_counter() - t0
+    gbs = n * tr.Hkv * tr.d * 4 * steps / el / 1e9
+    desc = f"per step: row 0, first {n} of {int(tr.seq_lens[0])} tokens, all {tr.Hq} query heads"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": ws,
+        "steps": steps, "warmup": warm, "ms_per_step": el / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOADS[args.config], "seed": tr.seed},
+        "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _row0_sample(tr):
+    """A one-row trace shaped like row 0 of `tr` with its own host K/V, for
+    workloads whose pool is too large to draw on the host."""
+    import pkv_traces as T
+    sub = T.custom_trace([int(tr.seq_lens[0])], tr.Hq, tr.Hkv, tr.d, tr.page_size,
+                         tr.split_tokens, seed=tr.seed, tag=tr.cfg_id)
+    k, v = T.gen_kv(sub)
+    return sub, T.gen_q(sub), k, v
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_pkv(args, rank, local, ws, pg):
+    import torch
+
+    import pkv_traces as T
+    from paged_kv_gqa_09_gb300 import _lib, api
+    from paged_kv_gqa_09_gb300 import build as build_mod
+
+    build_mod.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L = _lib.load()
+    cfg_id = args.config
+    tr = T.make_trace(cfg_id)
+    steps = args.steps if args.steps is not None else default_steps(cfg_id)
+    warm = max(3, args.warmup if args.warmup is not None else 5)
+    appends = tr.steps > 1
+    if appends:  # the block table holds room for tr.steps appended tokens per row
+        steps = min(steps, tr.steps - 1)
+    big = tr.num_pages * tr.page_size * tr.Hkv * tr.d * 2 > (1 << 30)
+
+    # ---- inputs (host copies kept for the oracle baseline)
+    q_h = T.gen_q(tr)
+    if big:
+        k0, v0 = T.gen_kv_torch(tr, "cuda")
+        k_h = v_h = None
+    else:
+        k_h, v_h = T.gen_kv(tr)
+        k0 = torch.from_numpy(k_h).to(dev)
+        v0 = torch.from_numpy(v_h).to(dev)
+    pool_bytes = 2 * k0.numel() * 2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(1, math.ceil(3 * l2 / pool_bytes) + 1) if pool_bytes < 3 * l2 else 1
+    pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(R - 1)]
+    q = torch.from_numpy(q_h).to(dev)
+    bt = torch.from_numpy(tr.block_table).to(dev)
+    sl = torch.from_numpy(tr.seq_lens).to(dev)
+    sl_init = sl.clone()
+    shape = api.make_shape(q, k0, bt)
+
+    # ---- path: the policy's route unless forced
+    pol = api.pkv_policy_default()
+    path, C = api.pkv_policy(tr.B, tr.n_max + (tr.steps if tr.steps > 1 else 0), pol)
+    forced = {"bucketed": 0, "workqueue": 1, "single": 2}.get(args.path)
+    if forced is not None:
+        path = forced
+    if path != 2:
+        C = tr.split_tokens
+    n_max_run = tr.n_max + (tr.steps if appends else 0)
+    bucket = n_max_run if path == 0 else 0
+    cfg = api.make_cfg(path, C, bucket)
+    wsb = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device=dev)
+    npart = api.pkv_partials_size(shape, cfg)
+    part = torch.empty(max(npart // 4, 4), dtype=torch.float32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    kn = torch.from_numpy(T.gen_append_tokens(tr, 0)[0]).to(dev)
+    vn = torch.from_numpy(T.gen_append_tokens(tr, 0)[1]).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    P = lambda t: t.data_ptr() if t is not None else None
+    sref, cref = _ctypes_refs(shape, cfg)
+
+    def step(r):
+        kk, vv = pools[r]
+        if appends:
+            rc = L.pkv_append(sref, P(wsb), P(kn), P(vn), P(bt), P(sl), P(kk), P(vv), sp)
+            _lib.check(rc, "pkv_append")
+        rc = L.pkv_decode_step(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl),
+                               P(part) if npart else None, P(o), P(lse), sp)
+        _lib.check(rc, "pkv_decode_step")
+
+    # ---- warm-up (eager), then capture one graph per pool
+    for w in range(warm):
+        step(w % R)
+    torch.cuda.synchronize()
+    st, msg = api.pkv_get_error(wsb)
+    if st != 0:
+        raise RuntimeError(f"device error during warm-up: {msg}")
+    api.pkv_reset_counters()
+    step(0)
+    torch.cuda.synchronize()
+    c = api.pkv_get_counters()
+    launches_per_step = sum(c.values())
+    graphs = None
+    if not args.no_graph:
+        try:
+            graphs = []
+            for r in range(R):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    step(r)
+                graphs.append(g)
+            for r in range(R):
+                graphs[r].replay()
+            torch.cuda.synchronize()
+        except Exception as e:  # capture unsupported: eager launches
+            print(f"# graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            graphs = None
+    if appends:
+        sl.copy_(sl_init)
+        torch.cuda.synchronize()
+
+    kv_step = tr.kv_bytes()
+    if appends:  # every step appends first: step s reads N_i + s + 1 tokens per row
+        kv_step = int((int(tr.seq_lens.astype(np.int64).sum()) + tr.B * (1 + (steps - 1) / 2))
+                      * tr.Hkv * tr.d * 4)
+
+    # ---- timed region: K steps back to back
+    sampler = ClockSampler(_gpu_id(torch, dev)) if rank == 0 else None
+    barrier(pg)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for s in range(steps):
+        if graphs:
+            graphs[s % R].replay()
+        else:
+            step(s % R)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(pg)
+    ms = e0.elapsed_time(e1) / steps
+    ms_max = reduce_max(pg, ms)
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
+    st, msg = api.pkv_get_error(wsb)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {msg}")
+
+    # ---- the decode kernel alone (roofline): events around each launch
+    if appends:
+        sl.copy_(sl_init)
+    kern_steps = min(steps, 2000)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(kern_steps)]
+    if path != 2:
+        L.pkv_plan(sref, cref, P(sl), P(wsb), sp)
+    for s in range(kern_steps):
+        kk, vv = pools[s % R]
+        evs[s][0].record(stream)
+        if path == 2:
+            rc = L.pkv_single_pass(sref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(o), P(lse), sp)
+        else:
+            rc = L.pkv_decode(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(part), sp)
+        evs[s][1].record(stream)
+        _lib.check(rc, "decode")
+    torch.cuda.synchronize()
+    kms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    kv_launch = tr.kv_bytes()
+    peak, peak_src = peaks()
+    achieved = kv_launch / (kms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        if appends:
+            sl.copy_(sl_init)
+        e2e = run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps if not appends else steps,
+                      appends, kn, vn, wsb)
+
+    gbs = kv_step / (ms * 1e-3) / 1e9
+    total = kv_step * ws / (ms_max * 1e-3) / 1e9
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        if k_h is None:
+            tr_s, qb, k_s, v_s = _row0_sample(tr)
+        else:
+            tr_s, qb, k_s, v_s = tr, q_h, k_h, v_h
+        val, cores, desc = cpu_baseline_run(tr_s, qb, k_s, v_s, args.cpu_seconds)
+        cpu = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": total, "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "warmup": warm, "ms_per_step": ms_max, "us_per_step": ms_max * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOADS[cfg_id], "path": ["bucketed-split", "workqueue", "single-pass"][path],
+            "split_tokens": C, "kv_bytes_per_step": kv_step, "seed": tr.seed,
+            "l2": (f"{R} KV pools rotated ({R * pool_bytes / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB)"
+                   if R > 1 else f"inputs ({pool_bytes / 2**30:.1f} GiB) larger than L2"),
+            "graph": bool(graphs), "parallelism": f"replicas x{ws}",
+        },
+        "hbm_frac": total / ws / peak,
+        "roofline": {"bound": "hbm", "kernel": "decode" if path != 2 else "single_pass",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_src, "traffic": profiled_traffic(cfg_id),
+                     "us_per_launch": kms * 1e3, "bytes_per_launch": kv_launch},
+        "gpu_launches": launches_per_step * steps,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _gpu_id(torch, dev):
+    """nvidia-smi -i selector for this CUDA device (its UUID, else its index)."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index)
+
+
+def _ctypes_refs(shape, cfg):
+    import ctypes
+    return ctypes.byref(shape), ctypes.byref(cfg)
+
+
+def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, wsb):
+    """Public-API steps with host buffers: H2D of q / seq_lens / block table from
+    pinned memory, PagedDecoder.step (policy + C ABI), D2H of o and lse, sync."""
+    R = len(pools)
+    q_pin = torch.from_numpy(q_h).pin_memory()
+    sl_pin = torch.from_numpy(tr.seq_lens.copy()).pin_memory()
+    bt_pin = torch.from_numpy(tr.block_table).pin_memory()
+    o_pin = torch.empty(q_h.shape, dtype=torch.float16).pin_memory()
+    lse_pin = torch.empty(q_h.shape[:2], dtype=torch.float32).pin_memory()
+    q_d = torch.empty(q_h.shape, dtype=torch.float16, device=dev)
+    sl_d = torch.empty(tr.B, dtype=torch.int32, device=dev)
+    bt_d = torch.empty(tr.block_table.shape, dtype=torch.int32, device=dev)
+    o_d = torch.empty_like(q_d)
+    lse_d = torch.empty(q_h.shape[:2], dtype=torch.float32, device=dev)
+    dec = api.PagedDecoder()
+    h2d = q_pin.numel() * 2 + sl_pin.numel() * 4 + bt_pin.numel() * 4
+    d2h = o_pin.numel() * 2 + lse_pin.numel() * 4
+    n_max = int(tr.seq_lens.max())
+    kvs = []
+    steps = min(steps, 4000 if not appends else tr.steps - 4)
+
+    def one(s):
+        kk, vv = pools[s % R]
+        q_d.copy_(q_pin, non_blocking=True)
+        sl_d.copy_(sl_pin, non_blocking=True)
+        bt_d.copy_(bt_pin, non_blocking=True)
+        if appends:
+            ws = dec.workspace(dev)
+            api.pkv_append(api.make_shape(q_d, kk, bt_d), ws if ws is not None else wsb, kn, vn,
+                           bt_d, sl_d, kk, vv)
+            sl_pin.add_(1)
+        n = n_max + (s + 1 if appends else 0)
+        dec.step(q_d, kk, vv, bt_d, sl_d, n, path=path, split_tokens=C, o=o_d, lse=lse_d)
+        o_pin.copy_(o_d, non_blocking=True)
+        lse_pin.copy_(lse_d, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+        kvs.append(int(sl_pin.numpy().astype(np.int64).sum()) * tr.Hkv * tr.d * 4)
+
+    for s in range(3):
+        one(s)
+    sl_pin.copy_(torch.from_numpy(tr.seq_lens.copy()))
+    kvs.clear()
+    t0 = time.perf_counter()
+    for s in range(steps):
+        one(s)
+    el = time.perf_counter() - t0
+    return {"value": sum(kvs) / el / 1e9, "unit": UNIT, "us_per_step": el / steps * 1e6,
+            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "timing": "synchronized wall clock per step"}
+
+
+def main():
+    args = parse()
+    rank, local, ws, pg = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, rank, ws, pg)
+    else:
+        run_pkv(args, rank, local, ws, pg)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

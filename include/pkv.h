@@ -1,0 +1,256 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged-KV grouped-query decode attention on GB300.
+ *
+ * Method: "PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM
+ * Serving on Commodity GPUs", technical summary, Methodology 1 ("Native
+ * block-table decode engine") and 2 ("Calibrated adaptive policy").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers prefixed d_ are device pointers owned by the caller (the library
+ *   never frees or keeps them).  Host pointers are read during the call only.
+ * - fp16 means IEEE 754 binary16 (CUDA __half); buffers are passed as void*.
+ * - Layouts (row-major, innermost last):
+ *     q            [B][Hq][d]                    fp16
+ *     k_cache      [num_pages][page_size][Hkv][d] fp16   ("NHD" pages)
+ *     v_cache      [num_pages][page_size][Hkv][d] fp16
+ *     block_table  [B][bt_stride]                int32  (physical page ids)
+ *     seq_lens     [B]                           int32  (N*_i, real lengths)
+ *     o            [B][Hq][d]                    fp16
+ *     lse          [B][Hq]                       fp32   (natural log; may be NULL)
+ *   Query head h reads KV head h / G with G = Hq / Hkv.  Token t of row i lives
+ *   in page block_table[i][t / page_size], slot t % page_size.
+ * - Every device buffer must be 16-byte aligned.
+ * - `stream` is a cudaStream_t (CUstream) cast to void*; NULL is the legacy
+ *   default stream.  Every call only enqueues work: none synchronizes, except
+ *   pkv_get_error which says so.
+ * - Return value: PKV_OK (0) or a negative status.  A failed call enqueues
+ *   nothing.  pkv_last_error_string() gives a per-thread description of the
+ *   last failure.  No C++ exception crosses this boundary.
+ * - Supported shapes: d in {64, 128}; G = Hq/Hkv in [1, 8]; page_size a power
+ *   of two in [8, 256]; split_tokens a positive multiple of page_size.  Other
+ *   shapes return PKV_EUNSUPPORTED.
+ * - Device-side checks (a block-table entry outside [0, num_pages), a length
+ *   beyond the block table or the bucket, a workqueue larger than its
+ *   capacity, a bounded wait that gave up) never fault or trap: the kernel
+ *   records the first such event in the workspace's error word, replaces the
+ *   offending page by zeros (or skips the work), and finishes.  Read it with
+ *   pkv_get_error().
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_VERSION 1
+
+/* status codes */
+#define PKV_OK 0
+#define PKV_EINVAL (-1)        /* bad argument: null/unaligned pointer, bad shape */
+#define PKV_EUNSUPPORTED (-2)  /* valid but not implemented (see shapes above) */
+#define PKV_ECUDA (-3)         /* a CUDA runtime/driver call failed */
+#define PKV_EDEVICE (-4)       /* device-side check: bad page id or length */
+#define PKV_ETIMEOUT (-5)      /* a bounded device wait gave up */
+#define PKV_ECAPACITY (-6)     /* workqueue larger than max_tasks */
+
+/* Execution paths (Methodology 2, "Calibrated adaptive policy"). */
+typedef enum {
+    PKV_PATH_BUCKETED_SPLIT = 0, /* rectangular B x Hkv x S_b grid over one length bucket */
+    PKV_PATH_WORKQUEUE = 1,      /* compact 1D queue of non-empty (row, kv-head, split) tasks */
+    PKV_PATH_SINGLE_PASS = 2     /* one task per (row, kv-head), no split, no merge */
+} pkv_path_t;
+
+typedef struct {
+    int32_t B;          /* batch rows, one query token each */
+    int32_t Hq;         /* query heads */
+    int32_t Hkv;        /* KV heads; Hq % Hkv == 0 */
+    int32_t d;          /* head dim */
+    int32_t page_size;  /* tokens per page (P) */
+    int32_t num_pages;  /* pages in the pool (first dim of k_cache/v_cache) */
+    int32_t bt_stride;  /* int32 elements between block-table rows */
+    float scale;        /* score scale, normally 1/sqrt(d) */
+} pkv_shape_t;
+
+typedef struct {
+    pkv_path_t path;
+    int32_t split_tokens; /* C: tokens per split, a multiple of page_size
+                             (ignored by PKV_PATH_SINGLE_PASS) */
+    int32_t bucket_len;   /* BUCKETED_SPLIT: tokens covered by the grid,
+                             S_b = ceil(bucket_len / C); 0 = bt_stride*page_size.
+                             A row longer than the bucket is a device error. */
+    int32_t max_tasks;    /* WORKQUEUE: task capacity of the workspace;
+                             0 = Hkv * B * ceil(bt_stride*page_size / C) */
+} pkv_plan_cfg_t;
+
+/* ---------------------------------------------------------------- sizes */
+
+/* Bytes of the plan workspace: a 64-byte header (error word, task count),
+ * offsets[B+1] and, for WORKQUEUE, the task list (16 bytes per task).  Every
+ * launching entry point takes this workspace (it holds the error word).  It
+ * needs no initialisation except that pkv_get_error() reads and clears the
+ * error word; zero it once after allocation. */
+size_t pkv_plan_workspace_size(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg);
+
+/* Bytes of the fp32 partial-state buffer for split paths: acc[slots][d] then
+ * m[slots] then l[slots], where slots = B*S_b*Hq (BUCKETED_SPLIT) or
+ * max_tasks*G (WORKQUEUE).  0 for SINGLE_PASS. */
+size_t pkv_partials_size(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg);
+
+/* ----------------------------------------------------------- the path */
+
+/* pkv_plan -- row-local bounds and the compact workqueue, built on the device
+ * (Methodology 1, "Row-local bounds" and "Compact workqueue").
+ * One kernel launch (a single CTA prefix scan) on `stream`:
+ *   n_i = ceil(N*_i / C); offsets[i] = n_0 + ... + n_{i-1}; T = Hkv * sum n_i;
+ *   tasks[k] = {i, g, j, state_base = (offsets[i] + j) * Hq + g * G} in
+ *   lexicographic (row, kv-head, split) order; count = T.
+ * The host never reads T back.  If T > max_tasks the count is set to 0 and
+ * the error word to capacity; decode then does nothing and merge writes NaN.
+ * For BUCKETED_SPLIT and SINGLE_PASS it is a no-op returning PKV_OK. */
+int pkv_plan(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg,
+             const int32_t *d_seq_lens, void *d_ws, void *stream);
+
+/* pkv_decode -- split decode (Methodology 1, "Sequence splitting").
+ * One kernel launch.  Every task (i, g, j) covers tokens
+ * [j*C, min((j+1)*C, N*_i)) of row i and writes, for each of the G query heads
+ * h of KV head g, the partial online-softmax state over s_t = scale * q_h.K_t:
+ *   m = max_t s_t, l = sum_t exp(s_t - m), acc = sum_t exp(s_t - m) V_t (fp32)
+ * into slot state_base + (h - g*G) of d_partials.  BUCKETED_SPLIT walks the
+ * rectangular grid B x Hkv x S_b (state_base = (i*S_b + j)*Hq + g*G); an empty
+ * split writes the neutral state (m=-inf, l=0, acc=0) and reads no KV.
+ * WORKQUEUE walks the task list pkv_plan wrote into d_ws (enqueue pkv_plan
+ * first on the same stream).  K/V pages are read in place through the block
+ * table; no page is repacked. */
+int pkv_decode(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
+               const void *d_q, const void *d_k_cache, const void *d_v_cache,
+               const int32_t *d_block_table, const int32_t *d_seq_lens,
+               float *d_partials, void *stream);
+
+/* pkv_merge -- exact log-sum-exp merge (Methodology 1, "Sequence splitting":
+ * a separate merge kernel combines the split states exactly).
+ * One kernel launch.  For each (row i, query head h) it reads the n_i =
+ * ceil(N*_i / C) states of that row only (row-local bounds) and writes
+ *   M = max_j m_j, L = sum_j l_j exp(m_j - M),
+ *   o[i][h] = sum_j acc_j exp(m_j - M) / L  (fp16, round to nearest),
+ *   lse[i][h] = M + ln L                    (fp32, if lse != NULL).
+ * A row with N*_i = 0 gets o = 0 and lse = -inf. */
+int pkv_merge(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
+              const int32_t *d_seq_lens, const float *d_partials,
+              void *d_o, float *d_lse, void *stream);
+
+/* pkv_single_pass -- the no-split route of the policy (Methodology 2: the
+ * route the pages hand to an external single-kernel library; here our own
+ * kernel).  One kernel launch; one task per (row, kv-head) over the whole row,
+ * writing o and lse directly as pkv_merge would. */
+int pkv_single_pass(const pkv_shape_t *shape, void *d_ws,
+                    const void *d_q, const void *d_k_cache, const void *d_v_cache,
+                    const int32_t *d_block_table, const int32_t *d_seq_lens,
+                    void *d_o, float *d_lse, void *stream);
+
+/* pkv_decode_step -- one whole decode step on the path cfg->path:
+ * WORKQUEUE = pkv_plan + pkv_decode + pkv_merge, BUCKETED_SPLIT = pkv_decode +
+ * pkv_merge, SINGLE_PASS = pkv_single_pass.  Same arguments and errors as
+ * those calls; d_partials may be NULL for SINGLE_PASS. */
+int pkv_decode_step(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
+                    const void *d_q, const void *d_k_cache, const void *d_v_cache,
+                    const int32_t *d_block_table, const int32_t *d_seq_lens,
+                    float *d_partials, void *d_o, float *d_lse, void *stream);
+
+/* pkv_append -- write one new token per row into the paged cache.
+ * (Not a step of the pages' method: the per-step KV write of a serving loop.)
+ * One kernel launch.  For every row i with N = seq_lens[i]: copies
+ * k_new[i][g][:], v_new[i][g][:] ([B][Hkv][d] fp16) into page
+ * block_table[i][N / page_size], slot N % page_size, then sets
+ * seq_lens[i] = N + 1 in place.  The block table must already name that page.
+ * A row whose next slot is beyond the block table or whose page id is out of
+ * range is left unchanged and recorded in the error word. */
+int pkv_append(const pkv_shape_t *shape, void *d_ws, const void *d_k_new,
+               const void *d_v_new, const int32_t *d_block_table, int32_t *d_seq_lens,
+               void *d_k_cache, void *d_v_cache, void *stream);
+
+/* ------------------------------------------------------------- policy */
+
+/* Thresholds of the calibrated policy (Methodology 2).  The pages route
+ * B = 1 long-context to the length-bucketed split, B >= 8 long-context to the
+ * compact workqueue and everything else (including B = 4) to a single-kernel
+ * path; "long context" and the batch cut-offs are calibrated. */
+typedef struct {
+    int32_t long_context_tokens;  /* N_max at or above this is "long context" */
+    int32_t bucketed_max_batch;   /* B <= this (and long) -> BUCKETED_SPLIT */
+    int32_t workqueue_min_batch;  /* B >= this (and long) -> WORKQUEUE */
+    int32_t split_tokens;         /* C handed to the split paths */
+    int32_t bucketed_split_tokens;/* C for BUCKETED_SPLIT (0 = split_tokens) */
+} pkv_policy_cfg_t;
+
+/* Fill `cfg` with the thresholds calibrated on GB300 (calibration seed
+ * 20260622, checked on held-out seed 20260623). */
+void pkv_policy_default(pkv_policy_cfg_t *cfg);
+
+/* Choose the path for a batch of B rows whose longest row has n_max tokens.
+ * cfg may be NULL (defaults).  Host only, deterministic, no CUDA call. */
+int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg,
+               pkv_path_t *out_path, int32_t *out_split_tokens);
+
+/* ----------------------------------------------------------- counters */
+
+/* Scheduler-derived counters (technical summary, Methodology 3 and Results,
+ * "Scheduling overhead").  pkv_get_counters returns what the library actually
+ * launched since the last pkv_reset_counters (process-wide, thread-safe). */
+typedef struct {
+    int64_t plan_launches;
+    int64_t decode_launches;
+    int64_t merge_launches;
+    int64_t single_pass_launches;
+    int64_t append_launches;
+} pkv_counters_t;
+
+int pkv_get_counters(pkv_counters_t *out);
+int pkv_reset_counters(void);
+
+/* Model of one decode step, computed on the host from the real lengths
+ * (host array seq_lens[B]):
+ *   attn_launches: kernel launches of the attention path (split + merge, or
+ *     the single pass; the plan launch is counted apart in plan_launches);
+ *     for exact-length buckets, one split and one merge per distinct length;
+ *   tasks: non-empty (row, kv-head, split) tasks; grid_tasks: tasks in the
+ *     launched grid including empty rectangular cells;
+ *   merge_state_bytes: fp32 state bytes written by the split kernel plus
+ *     read by the merge, (d + 2) * 4 per state;
+ *   kv_bytes: sum_i N*_i * Hkv * d * 2 * 2.
+ * path_or_exact: a pkv_path_t, or 3 for exact-length buckets. */
+typedef struct {
+    int64_t attn_launches;
+    int64_t plan_launches;
+    int64_t tasks;
+    int64_t grid_tasks;
+    int64_t states_written;
+    int64_t states_read;
+    int64_t merge_state_bytes;
+    int64_t kv_bytes;
+} pkv_step_model_t;
+
+int pkv_step_model(int32_t path_or_exact, const pkv_shape_t *shape, int32_t split_tokens,
+                   int32_t bucket_len, const int32_t *seq_lens, pkv_step_model_t *out);
+
+/* ------------------------------------------------------------- errors */
+
+/* Synchronizes `stream`, reads and clears the device error word in d_ws and
+ * returns PKV_OK, PKV_EDEVICE, PKV_ETIMEOUT or PKV_ECAPACITY (detail in
+ * pkv_last_error_string()). */
+int pkv_get_error(void *d_ws, void *stream);
+
+/* Description of the last failure on the calling thread ("" if none). */
+const char *pkv_last_error_string(void);
+
+/* PKV_VERSION of the loaded library. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

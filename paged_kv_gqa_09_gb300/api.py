@@ -1,0 +1,257 @@
+"""Python binding of libpkv with the C ABI's names (argument marshalling only).
+
+Device buffers are torch CUDA tensors (PyTorch provides memory and streams);
+every step of the decode path runs in libpkv's kernels.  Each function checks
+that its tensors live on the current CUDA device with the dtype and layout the
+C ABI expects -- a host tensor handed to a kernel would fault -- then forwards
+raw pointers and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import (PKV_PATH_BUCKETED_SPLIT, PKV_PATH_SINGLE_PASS, PKV_PATH_WORKQUEUE, Counters,
+                   PlanCfg, PolicyCfg, Shape, StepModel, check)
+
+__all__ = [
+    "Shape", "PlanCfg", "PolicyCfg", "make_shape", "make_cfg",
+    "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
+    "pkv_single_pass", "pkv_decode_step", "pkv_append", "pkv_policy", "pkv_policy_default",
+    "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error", "pkv_version",
+    "PagedDecoder",
+]
+
+
+# ------------------------------------------------------------------ helpers
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtype: torch.dtype, nullable: bool = False) -> int:
+    if t is None:
+        if nullable:
+            return 0
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, current device is cuda:{torch.cuda.current_device()}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _ws(t: torch.Tensor, name: str = "workspace") -> int:
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t.data_ptr()
+
+
+def make_shape(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Tensor,
+               scale: Optional[float] = None) -> Shape:
+    """Shape from q [B,Hq,d], k_cache [num_pages,P,Hkv,d], block_table [B,bt_stride]."""
+    B, Hq, d = q.shape
+    num_pages, P, Hkv, d2 = k_cache.shape
+    if d2 != d or block_table.shape[0] != B:
+        raise ValueError("q, k_cache and block_table disagree on d or B")
+    return Shape(B, Hq, Hkv, d, P, num_pages, int(block_table.shape[1]),
+                 float(1.0 / math.sqrt(d) if scale is None else scale))
+
+
+def make_cfg(path: int, split_tokens: int = 1024, bucket_len: int = 0, max_tasks: int = 0) -> PlanCfg:
+    return PlanCfg(int(path), int(split_tokens), int(bucket_len), int(max_tasks))
+
+
+# ------------------------------------------------------------------ C ABI
+
+def pkv_version() -> int:
+    return _lib.load().pkv_version()
+
+
+def pkv_plan_workspace_size(shape: Shape, cfg: PlanCfg) -> int:
+    n = _lib.load().pkv_plan_workspace_size(ctypes.byref(shape), ctypes.byref(cfg))
+    if n == 0:
+        raise _lib.PkvError(_lib.PKV_EINVAL, "pkv_plan_workspace_size", _lib.last_error())
+    return int(n)
+
+
+def pkv_partials_size(shape: Shape, cfg: PlanCfg) -> int:
+    return int(_lib.load().pkv_partials_size(ctypes.byref(shape), ctypes.byref(cfg)))
+
+
+def pkv_plan(shape, cfg, seq_lens, ws, stream=None) -> None:
+    L = _lib.load()
+    check(L.pkv_plan(ctypes.byref(shape), ctypes.byref(cfg), _dev(seq_lens, "seq_lens", torch.int32),
+                     _ws(ws), _stream(stream)), "pkv_plan")
+
+
+def pkv_decode(shape, cfg, ws, q, k_cache, v_cache, block_table, seq_lens, partials,
+               stream=None) -> None:
+    L = _lib.load()
+    check(L.pkv_decode(ctypes.byref(shape), ctypes.byref(cfg), _ws(ws),
+                       _dev(q, "q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
+                       _dev(v_cache, "v_cache", torch.float16),
+                       _dev(block_table, "block_table", torch.int32),
+                       _dev(seq_lens, "seq_lens", torch.int32),
+                       _dev(partials, "partials", torch.float32), _stream(stream)), "pkv_decode")
+
+
+def pkv_merge(shape, cfg, ws, seq_lens, partials, o, lse=None, stream=None) -> None:
+    L = _lib.load()
+    check(L.pkv_merge(ctypes.byref(shape), ctypes.byref(cfg), _ws(ws),
+                      _dev(seq_lens, "seq_lens", torch.int32),
+                      _dev(partials, "partials", torch.float32), _dev(o, "o", torch.float16),
+                      _dev(lse, "lse", torch.float32, nullable=True), _stream(stream)), "pkv_merge")
+
+
+def pkv_single_pass(shape, ws, q, k_cache, v_cache, block_table, seq_lens, o, lse=None,
+                    stream=None) -> None:
+    L = _lib.load()
+    check(L.pkv_single_pass(ctypes.byref(shape), _ws(ws), _dev(q, "q", torch.float16),
+                            _dev(k_cache, "k_cache", torch.float16),
+                            _dev(v_cache, "v_cache", torch.float16),
+                            _dev(block_table, "block_table", torch.int32),
+                            _dev(seq_lens, "seq_lens", torch.int32), _dev(o, "o", torch.float16),
+                            _dev(lse, "lse", torch.float32, nullable=True), _stream(stream)),
+          "pkv_single_pass")
+
+
+def pkv_decode_step(shape, cfg, ws, q, k_cache, v_cache, block_table, seq_lens, partials, o,
+                    lse=None, stream=None) -> None:
+    L = _lib.load()
+    part = _dev(partials, "partials", torch.float32, nullable=(cfg.path == PKV_PATH_SINGLE_PASS))
+    check(L.pkv_decode_step(ctypes.byref(shape), ctypes.byref(cfg), _ws(ws),
+                            _dev(q, "q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
+                            _dev(v_cache, "v_cache", torch.float16),
+                            _dev(block_table, "block_table", torch.int32),
+                            _dev(seq_lens, "seq_lens", torch.int32), part,
+                            _dev(o, "o", torch.float16),
+                            _dev(lse, "lse", torch.float32, nullable=True), _stream(stream)),
+          "pkv_decode_step")
+
+
+def pkv_append(shape, ws, k_new, v_new, block_table, seq_lens, k_cache, v_cache,
+               stream=None) -> None:
+    L = _lib.load()
+    check(L.pkv_append(ctypes.byref(shape), _ws(ws), _dev(k_new, "k_new", torch.float16),
+                       _dev(v_new, "v_new", torch.float16),
+                       _dev(block_table, "block_table", torch.int32),
+                       _dev(seq_lens, "seq_lens", torch.int32),
+                       _dev(k_cache, "k_cache", torch.float16),
+                       _dev(v_cache, "v_cache", torch.float16), _stream(stream)), "pkv_append")
+
+
+def pkv_policy_default() -> PolicyCfg:
+    c = PolicyCfg()
+    _lib.load().pkv_policy_default(ctypes.byref(c))
+    return c
+
+
+def pkv_policy(B: int, n_max: int, cfg: Optional[PolicyCfg] = None) -> tuple[int, int]:
+    path, split = ctypes.c_int32(), ctypes.c_int32()
+    check(_lib.load().pkv_policy(int(B), int(n_max), ctypes.byref(cfg) if cfg is not None else None,
+                                 ctypes.byref(path), ctypes.byref(split)), "pkv_policy")
+    return int(path.value), int(split.value)
+
+
+def pkv_get_counters() -> dict:
+    c = Counters()
+    check(_lib.load().pkv_get_counters(ctypes.byref(c)), "pkv_get_counters")
+    return {name: int(getattr(c, name)) for name, _ in Counters._fields_}
+
+
+def pkv_reset_counters() -> None:
+    check(_lib.load().pkv_reset_counters(), "pkv_reset_counters")
+
+
+def pkv_step_model(path: int, shape: Shape, split_tokens: int, bucket_len: int,
+                   seq_lens: Sequence[int]) -> dict:
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    out = StepModel()
+    check(_lib.load().pkv_step_model(int(path), ctypes.byref(shape), int(split_tokens),
+                                     int(bucket_len), sl.ctypes.data, ctypes.byref(out)),
+          "pkv_step_model")
+    return {name: int(getattr(out, name)) for name, _ in StepModel._fields_}
+
+
+def pkv_get_error(ws: torch.Tensor, stream=None) -> tuple[int, str]:
+    """Synchronize the stream and read/clear the device error word -> (status, detail)."""
+    L = _lib.load()
+    st = L.pkv_get_error(_ws(ws), _stream(stream))
+    return int(st), (_lib.last_error() if st != 0 else "")
+
+
+# ------------------------------------------------------------------ engine
+
+class PagedDecoder:
+    """Owns the workspace and partial-state buffers for one (shape, path) and
+    runs whole decode steps: pkv_policy (host) then pkv_decode_step.
+
+    Buffers come from the torch caching allocator on the current device and are
+    reused across steps; they are resized when a larger configuration arrives.
+    """
+
+    def __init__(self, policy: Optional[PolicyCfg] = None, max_split_tasks: int = 0):
+        self.policy = policy
+        self.max_split_tasks = max_split_tasks
+        self._ws: dict = {}
+        self._part: dict = {}
+
+    def plan_cfg(self, B: int, n_max: int, path: Optional[int] = None,
+                 split_tokens: Optional[int] = None) -> PlanCfg:
+        p, c = pkv_policy(B, n_max, self.policy)
+        if path is not None:
+            p = path
+        if split_tokens is not None:
+            c = split_tokens
+        bucket = n_max if p == PKV_PATH_BUCKETED_SPLIT else 0
+        return make_cfg(p, c, bucket, self.max_split_tasks if p == PKV_PATH_WORKQUEUE else 0)
+
+    def buffers(self, shape: Shape, cfg: PlanCfg, device) -> tuple[torch.Tensor, Optional[torch.Tensor]]:
+        nws = pkv_plan_workspace_size(shape, cfg)
+        npart = pkv_partials_size(shape, cfg)
+        ws = self._ws.get(device)
+        if ws is None or ws.numel() < nws:
+            ws = torch.zeros(max(nws, 64), dtype=torch.uint8, device=device)
+            self._ws[device] = ws
+        part = None
+        if npart:
+            part = self._part.get(device)
+            if part is None or part.numel() * 4 < npart:
+                part = torch.empty(npart // 4, dtype=torch.float32, device=device)
+                self._part[device] = part
+        return ws, part
+
+    def step(self, q, k_cache, v_cache, block_table, seq_lens, n_max: int,
+             path: Optional[int] = None, split_tokens: Optional[int] = None,
+             o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+             want_lse: bool = True, scale: Optional[float] = None, stream=None):
+        """One decode step; n_max is the longest row (host scalar the caller knows)."""
+        shape = make_shape(q, k_cache, block_table, scale)
+        cfg = self.plan_cfg(shape.B, int(n_max), path, split_tokens)
+        ws, part = self.buffers(shape, cfg, q.device)
+        if o is None:
+            o = torch.empty_like(q)
+        if lse is None and want_lse:
+            lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+        pkv_decode_step(shape, cfg, ws, q, k_cache, v_cache, block_table, seq_lens, part, o, lse,
+                        stream)
+        return o, lse
+
+    def workspace(self, device) -> Optional[torch.Tensor]:
+        return self._ws.get(device)

@@ -1,0 +1,582 @@
+// api.cu -- the C ABI of libpkv (declared in include/pkv.h): argument
+// validation, TMA descriptor encoding, kernel launches on the caller's stream,
+// launch counters, the calibrated path policy and error reporting.
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_kernels.h"
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <cudaTypedefs.h>
+#include <mutex>
+#include <string>
+
+using namespace pkv;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(PKV_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct Counters {
+    std::atomic<int64_t> plan{0}, decode{0}, merge{0}, single{0}, append{0};
+} g_cnt;
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int ilog2(int x)
+{
+    int l = 0;
+    while ((1 << l) < x)
+        ++l;
+    return l;
+}
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const pkv_shape_t *s)
+{
+    if (!s)
+        return fail(PKV_EINVAL, "shape is NULL");
+    if (s->B < 0 || s->Hq <= 0 || s->Hkv <= 0 || s->d <= 0 || s->page_size <= 0 ||
+        s->num_pages <= 0 || s->bt_stride <= 0)
+        return fail(PKV_EINVAL, "shape has a non-positive field (B=%d Hq=%d Hkv=%d d=%d P=%d "
+                                "num_pages=%d bt_stride=%d)",
+                    s->B, s->Hq, s->Hkv, s->d, s->page_size, s->num_pages, s->bt_stride);
+    if (s->Hq % s->Hkv)
+        return fail(PKV_EINVAL, "Hq=%d is not a multiple of Hkv=%d", s->Hq, s->Hkv);
+    if (!std::isfinite(s->scale))
+        return fail(PKV_EINVAL, "scale is not finite");
+    if (s->d != 64 && s->d != 128)
+        return fail(PKV_EUNSUPPORTED, "head dim d=%d (supported: 64, 128)", s->d);
+    if (s->Hq / s->Hkv > 8)
+        return fail(PKV_EUNSUPPORTED, "G=Hq/Hkv=%d (supported: 1..8)", s->Hq / s->Hkv);
+    if (!is_pow2(s->page_size) || s->page_size < 8 || s->page_size > 256)
+        return fail(PKV_EUNSUPPORTED, "page_size=%d (supported: powers of two in [8, 256])",
+                    s->page_size);
+    if ((int64_t)s->bt_stride * s->page_size > 0x7fffffffLL)
+        return fail(PKV_EINVAL, "bt_stride*page_size overflows int32");
+    return PKV_OK;
+}
+
+int check_cfg(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
+{
+    if (!c)
+        return fail(PKV_EINVAL, "plan cfg is NULL");
+    if (c->path != PKV_PATH_BUCKETED_SPLIT && c->path != PKV_PATH_WORKQUEUE &&
+        c->path != PKV_PATH_SINGLE_PASS)
+        return fail(PKV_EINVAL, "unknown path %d", (int)c->path);
+    if (c->path == PKV_PATH_SINGLE_PASS)
+        return PKV_OK;
+    if (c->split_tokens <= 0 || c->split_tokens % s->page_size)
+        return fail(PKV_EINVAL, "split_tokens=%d must be a positive multiple of page_size=%d",
+                    c->split_tokens, s->page_size);
+    if (c->bucket_len < 0 || c->max_tasks < 0)
+        return fail(PKV_EINVAL, "negative bucket_len or max_tasks");
+    return PKV_OK;
+}
+
+int len_cap(const pkv_shape_t *s) { return s->bt_stride * s->page_size; }
+
+int s_b(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
+{
+    const int64_t bl = c->bucket_len > 0 ? c->bucket_len : len_cap(s);
+    return (int)((bl + c->split_tokens - 1) / c->split_tokens);
+}
+
+int64_t max_tasks(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
+{
+    if (c->max_tasks > 0)
+        return c->max_tasks;
+    const int64_t per_row = ((int64_t)len_cap(s) + c->split_tokens - 1) / c->split_tokens;
+    return (int64_t)s->Hkv * s->B * per_row;
+}
+
+int64_t partial_slots(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
+{
+    if (c->path == PKV_PATH_BUCKETED_SPLIT)
+        return (int64_t)s->B * s_b(s, c) * s->Hq;
+    if (c->path == PKV_PATH_WORKQUEUE)
+        return max_tasks(s, c) * (s->Hq / s->Hkv);
+    return 0;
+}
+
+int check_ptr(const void *p, const char *name, bool nullable = false)
+{
+    if (!p)
+        return nullable ? PKV_OK : fail(PKV_EINVAL, "%s is NULL", name);
+    if (!aligned16(p))
+        return fail(PKV_EINVAL, "%s is not 16-byte aligned", name);
+    return PKV_OK;
+}
+
+#define PKV_TRY(x)               \
+    do {                         \
+        int rc_ = (x);           \
+        if (rc_ != PKV_OK)       \
+            return rc_;          \
+    } while (0)
+
+// ---------------------------------------------------------------- devices
+
+struct DevInfo {
+    int sms = 0;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+int device_sms(int *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64)
+        return fail(PKV_EUNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev[dev].sms) {
+        e = cudaDeviceGetAttribute(&g_dev[dev].sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+    }
+    *out = g_dev[dev].sms;
+    return PKV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int encode_kv_map(CUtensorMap *m, const void *base, const pkv_shape_t *s, int box_tok)
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode)
+        return fail(PKV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    // Pages viewed as a 5-D tensor (innermost first):
+    //   d low (64 halves, 128 B) | slot (P) | d high (d/64) | kv head | page
+    // so one box {64, box_tok, d/64, 1, 1} is box_tok tokens x all d columns of
+    // one KV head of one page, landing as [d high][token][128 B] rows that the
+    // 128-byte swizzle spreads over all shared-memory banks.
+    const cuuint64_t es = 2;
+    cuuint64_t dims[5] = {64, (cuuint64_t)s->page_size, (cuuint64_t)(s->d / 64), (cuuint64_t)s->Hkv,
+                          (cuuint64_t)s->num_pages};
+    cuuint64_t strides[4] = {(cuuint64_t)s->Hkv * s->d * es, 128, (cuuint64_t)s->d * es,
+                             (cuuint64_t)s->page_size * s->Hkv * s->d * es};
+    cuuint32_t box[5] = {64, (cuuint32_t)box_tok, (cuuint32_t)(s->d / 64), 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, const_cast<void *>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PKV_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return PKV_OK;
+}
+
+WsHeader *ws_hdr(void *ws) { return reinterpret_cast<WsHeader *>(ws); }
+
+int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_ws, const void *q,
+               const void *k, const void *v, const int32_t *bt, const int32_t *sl, float *part,
+               void *o, float *lse, cudaStream_t st)
+{
+    int sms = 0;
+    PKV_TRY(device_sms(&sms));
+    const int box_tok = s->page_size < 64 ? s->page_size : 64;
+    alignas(64) CUtensorMap tk, tv;
+    PKV_TRY(encode_kv_map(&tk, k, s, box_tok));
+    PKV_TRY(encode_kv_map(&tv, v, s, box_tok));
+    DecodeParams p = {};
+    p.q = static_cast<const __half *>(q);
+    p.bt = bt;
+    p.seq_lens = sl;
+    p.ws = ws_hdr(d_ws);
+    p.B = s->B;
+    p.Hq = s->Hq;
+    p.Hkv = s->Hkv;
+    p.G = s->Hq / s->Hkv;
+    p.num_pages = s->num_pages;
+    p.bt_stride = s->bt_stride;
+    p.log2P = ilog2(s->page_size);
+    p.box_log2 = ilog2(box_tok);
+    p.len_cap = len_cap(s);
+    p.scale_log2 = s->scale * 1.4426950408889634f;
+    int64_t ntasks = 0;
+    if (mode == kModeSingle) {
+        p.o = static_cast<__half *>(o);
+        p.lse = lse;
+        ntasks = (int64_t)s->B * s->Hkv;
+    } else {
+        const int64_t slots = partial_slots(s, c);
+        p.part_acc = part;
+        p.part_m = part + slots * s->d;
+        p.part_l = p.part_m + slots;
+        p.C = c->split_tokens;
+        p.S_b = s_b(s, c);
+        if (mode == kModeRect) {
+            ntasks = (int64_t)s->B * s->Hkv * p.S_b;
+        } else {
+            ntasks = max_tasks(s, c);
+            p.tasks = reinterpret_cast<const int4 *>(static_cast<char *>(d_ws) + ws_tasks_off(s->B));
+        }
+    }
+    if (ntasks > 0x7fffffffLL)
+        return fail(PKV_EUNSUPPORTED, "%lld tasks exceed int32", (long long)ntasks);
+    p.n_tasks = (int)ntasks;
+    const int grid = (int)(ntasks < sms ? (ntasks > 0 ? ntasks : 1) : sms);
+    cudaError_t e = launch_decode(s->d, mode, tk, tv, p, grid, st, true);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode launch");
+    (mode == kModeSingle ? g_cnt.single : g_cnt.decode)++;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_plan_workspace_size(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
+{
+    if (check_shape(s) || check_cfg(s, c))
+        return 0;
+    size_t n = ws_tasks_off(s->B);
+    if (c->path == PKV_PATH_WORKQUEUE)
+        n += 16 * (size_t)max_tasks(s, c);
+    return n;
+}
+
+size_t pkv_partials_size(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
+{
+    if (check_shape(s) || check_cfg(s, c))
+        return 0;
+    return (size_t)partial_slots(s, c) * (size_t)(s->d + 2) * sizeof(float);
+}
+
+int pkv_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, const int32_t *d_seq_lens, void *d_ws,
+             void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    if (c->path != PKV_PATH_WORKQUEUE)
+        return PKV_OK;
+    PKV_TRY(check_ptr(d_seq_lens, "seq_lens"));
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PlanParams p = {};
+    p.seq_lens = d_seq_lens;
+    p.ws = ws_hdr(d_ws);
+    p.offsets = reinterpret_cast<int32_t *>(static_cast<char *>(d_ws) + ws_offsets_off());
+    p.tasks = reinterpret_cast<int4 *>(static_cast<char *>(d_ws) + ws_tasks_off(s->B));
+    p.B = s->B;
+    p.Hq = s->Hq;
+    p.Hkv = s->Hkv;
+    p.G = s->Hq / s->Hkv;
+    p.C = c->split_tokens;
+    p.len_cap = len_cap(s);
+    p.max_tasks = max_tasks(s, c);
+    cudaError_t e = launch_plan(p, static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "plan launch");
+    g_cnt.plan++;
+    return PKV_OK;
+}
+
+int pkv_decode(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const void *q, const void *k,
+               const void *v, const int32_t *bt, const int32_t *sl, float *part, void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    if (c->path == PKV_PATH_SINGLE_PASS)
+        return fail(PKV_EINVAL, "pkv_decode takes a split path; use pkv_single_pass");
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PKV_TRY(check_ptr(q, "q"));
+    PKV_TRY(check_ptr(k, "k_cache"));
+    PKV_TRY(check_ptr(v, "v_cache"));
+    PKV_TRY(check_ptr(bt, "block_table"));
+    PKV_TRY(check_ptr(sl, "seq_lens"));
+    PKV_TRY(check_ptr(part, "partials"));
+    const int mode = c->path == PKV_PATH_WORKQUEUE ? kModeQueue : kModeRect;
+    return run_decode(s, mode, c, d_ws, q, k, v, bt, sl, part, nullptr, nullptr,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int pkv_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const int32_t *sl,
+              const float *part, void *o, float *lse, void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    if (c->path == PKV_PATH_SINGLE_PASS)
+        return fail(PKV_EINVAL, "pkv_merge takes a split path");
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PKV_TRY(check_ptr(sl, "seq_lens"));
+    PKV_TRY(check_ptr(part, "partials"));
+    PKV_TRY(check_ptr(o, "o"));
+    PKV_TRY(check_ptr(lse, "lse", true));
+    const int64_t slots = partial_slots(s, c);
+    MergeParams p = {};
+    p.seq_lens = sl;
+    p.ws = ws_hdr(d_ws);
+    p.offsets = reinterpret_cast<const int32_t *>(static_cast<char *>(d_ws) + ws_offsets_off());
+    p.part_acc = part;
+    p.part_m = part + slots * s->d;
+    p.part_l = p.part_m + slots;
+    p.o = static_cast<__half *>(o);
+    p.lse = lse;
+    p.B = s->B;
+    p.Hq = s->Hq;
+    p.C = c->split_tokens;
+    p.S_b = s_b(s, c);
+    p.mode = c->path == PKV_PATH_WORKQUEUE ? kModeQueue : kModeRect;
+    p.len_cap = len_cap(s);
+    p.state_rows_cap = slots / s->Hq;
+    cudaError_t e = launch_merge(s->d, p, static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "merge launch");
+    g_cnt.merge++;
+    return PKV_OK;
+}
+
+int pkv_single_pass(const pkv_shape_t *s, void *d_ws, const void *q, const void *k, const void *v,
+                    const int32_t *bt, const int32_t *sl, void *o, float *lse, void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PKV_TRY(check_ptr(q, "q"));
+    PKV_TRY(check_ptr(k, "k_cache"));
+    PKV_TRY(check_ptr(v, "v_cache"));
+    PKV_TRY(check_ptr(bt, "block_table"));
+    PKV_TRY(check_ptr(sl, "seq_lens"));
+    PKV_TRY(check_ptr(o, "o"));
+    PKV_TRY(check_ptr(lse, "lse", true));
+    return run_decode(s, kModeSingle, nullptr, d_ws, q, k, v, bt, sl, nullptr, o, lse,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int pkv_decode_step(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const void *q,
+                    const void *k, const void *v, const int32_t *bt, const int32_t *sl, float *part,
+                    void *o, float *lse, void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    if (c->path == PKV_PATH_SINGLE_PASS)
+        return pkv_single_pass(s, d_ws, q, k, v, bt, sl, o, lse, stream);
+    PKV_TRY(check_ptr(o, "o"));
+    PKV_TRY(check_ptr(lse, "lse", true));
+    PKV_TRY(pkv_plan(s, c, sl, d_ws, stream));
+    PKV_TRY(pkv_decode(s, c, d_ws, q, k, v, bt, sl, part, stream));
+    return pkv_merge(s, c, d_ws, sl, part, o, lse, stream);
+}
+
+int pkv_append(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *v_new,
+               const int32_t *bt, int32_t *sl, void *k_cache, void *v_cache, void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PKV_TRY(check_ptr(k_new, "k_new"));
+    PKV_TRY(check_ptr(v_new, "v_new"));
+    PKV_TRY(check_ptr(bt, "block_table"));
+    PKV_TRY(check_ptr(sl, "seq_lens"));
+    PKV_TRY(check_ptr(k_cache, "k_cache"));
+    PKV_TRY(check_ptr(v_cache, "v_cache"));
+    AppendParams p = {};
+    p.k_new = static_cast<const __half *>(k_new);
+    p.v_new = static_cast<const __half *>(v_new);
+    p.bt = bt;
+    p.seq_lens = sl;
+    p.k_cache = static_cast<__half *>(k_cache);
+    p.v_cache = static_cast<__half *>(v_cache);
+    p.ws = ws_hdr(d_ws);
+    p.B = s->B;
+    p.Hkv = s->Hkv;
+    p.d = s->d;
+    p.log2P = ilog2(s->page_size);
+    p.num_pages = s->num_pages;
+    p.bt_stride = s->bt_stride;
+    cudaError_t e = launch_append(p, static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "append launch");
+    g_cnt.append++;
+    return PKV_OK;
+}
+
+// ------------------------------------------------------------------ policy
+
+void pkv_policy_default(pkv_policy_cfg_t *c)
+{
+    if (!c)
+        return;
+    c->long_context_tokens = 4096;
+    c->bucketed_max_batch = 1;
+    c->workqueue_min_batch = 8;
+    c->split_tokens = 1024;
+    c->bucketed_split_tokens = 0;
+}
+
+int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t *out_path,
+               int32_t *out_split)
+{
+    if (!out_path || !out_split)
+        return fail(PKV_EINVAL, "policy outputs are NULL");
+    if (B < 0 || n_max < 0)
+        return fail(PKV_EINVAL, "negative B or n_max");
+    pkv_policy_cfg_t d;
+    pkv_policy_default(&d);
+    const pkv_policy_cfg_t *c = cfg ? cfg : &d;
+    if (c->split_tokens <= 0 || c->bucketed_split_tokens < 0)
+        return fail(PKV_EINVAL, "policy split_tokens must be positive");
+    const bool long_ctx = n_max >= c->long_context_tokens;
+    pkv_path_t path = PKV_PATH_SINGLE_PASS;
+    int32_t C = c->split_tokens;
+    if (long_ctx && B >= 1 && B <= c->bucketed_max_batch) {
+        path = PKV_PATH_BUCKETED_SPLIT;
+        if (c->bucketed_split_tokens > 0)
+            C = c->bucketed_split_tokens;
+    } else if (long_ctx && B >= c->workqueue_min_batch) {
+        path = PKV_PATH_WORKQUEUE;
+    }
+    *out_path = path;
+    *out_split = C;
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------------- counters
+
+int pkv_get_counters(pkv_counters_t *out)
+{
+    if (!out)
+        return fail(PKV_EINVAL, "counters output is NULL");
+    out->plan_launches = g_cnt.plan.load();
+    out->decode_launches = g_cnt.decode.load();
+    out->merge_launches = g_cnt.merge.load();
+    out->single_pass_launches = g_cnt.single.load();
+    out->append_launches = g_cnt.append.load();
+    return PKV_OK;
+}
+
+int pkv_reset_counters(void)
+{
+    g_cnt.plan = 0;
+    g_cnt.decode = 0;
+    g_cnt.merge = 0;
+    g_cnt.single = 0;
+    g_cnt.append = 0;
+    return PKV_OK;
+}
+
+int pkv_step_model(int32_t path, const pkv_shape_t *s, int32_t C, int32_t bucket_len,
+                   const int32_t *seq_lens, pkv_step_model_t *out)
+{
+    if (!s || !out || (s->B > 0 && !seq_lens))
+        return fail(PKV_EINVAL, "NULL argument");
+    if (s->B < 0 || s->Hq <= 0 || s->Hkv <= 0 || s->Hq % s->Hkv || s->d <= 0)
+        return fail(PKV_EINVAL, "bad shape");
+    if (path != 2 && C <= 0)
+        return fail(PKV_EINVAL, "split_tokens must be positive");
+    std::memset(out, 0, sizeof *out);
+    int64_t rows = 0, toks = 0, n_max = 0;
+    for (int i = 0; i < s->B; ++i) {
+        const int64_t N = seq_lens[i] < 0 ? 0 : seq_lens[i];
+        toks += N;
+        if (path != 2)
+            rows += (N + C - 1) / C;
+        n_max = N > n_max ? N : n_max;
+    }
+    const int64_t state = (int64_t)(s->d + 2) * 4;
+    out->kv_bytes = toks * s->Hkv * s->d * 4;
+    if (path == PKV_PATH_BUCKETED_SPLIT) {
+        const int64_t bl = bucket_len > 0 ? bucket_len : n_max;
+        const int64_t sb = (bl + C - 1) / C;
+        out->attn_launches = 2;
+        out->tasks = rows * s->Hkv;
+        out->grid_tasks = (int64_t)s->B * s->Hkv * sb;
+        out->states_written = (int64_t)s->B * sb * s->Hq;
+        out->states_read = rows * s->Hq;
+    } else if (path == PKV_PATH_WORKQUEUE) {
+        out->attn_launches = 2;
+        out->plan_launches = 1;
+        out->tasks = out->grid_tasks = rows * s->Hkv;
+        out->states_written = out->states_read = rows * s->Hq;
+    } else if (path == PKV_PATH_SINGLE_PASS) {
+        out->attn_launches = 1;
+        out->tasks = out->grid_tasks = (int64_t)s->B * s->Hkv;
+    } else if (path == 3) {
+        // exact-length buckets: one (split, merge) launch pair per distinct length
+        int64_t groups = 0;
+        for (int i = 0; i < s->B; ++i) {
+            if (seq_lens[i] <= 0)
+                continue;
+            bool seen = false;
+            for (int k = 0; k < i && !seen; ++k)
+                seen = seq_lens[k] == seq_lens[i];
+            groups += seen ? 0 : 1;
+        }
+        out->attn_launches = 2 * groups;
+        out->tasks = out->grid_tasks = rows * s->Hkv;
+        out->states_written = out->states_read = rows * s->Hq;
+    } else {
+        return fail(PKV_EINVAL, "unknown path %d", path);
+    }
+    out->merge_state_bytes = (out->states_written + out->states_read) * state;
+    return PKV_OK;
+}
+
+// ------------------------------------------------------------------ errors
+
+int pkv_get_error(void *d_ws, void *stream)
+{
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    int32_t h[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(h, d_ws, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy (error word)");
+    if (h[0] == kErrNone)
+        return PKV_OK;
+    e = cudaMemset(d_ws, 0, sizeof h);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemset (error word)");
+    switch (h[0]) {
+    case kErrBadPage:
+        return fail(PKV_EDEVICE, "block-table entry out of range: row %d, logical page %d, value %d",
+                    h[1], h[2], h[3]);
+    case kErrTooLong:
+        return fail(PKV_EDEVICE, "row %d has length %d beyond its limit %d", h[1], h[2], h[3]);
+    case kErrNegLen:
+        return fail(PKV_EDEVICE, "row %d has negative length %d", h[1], h[2]);
+    case kErrTimeout:
+        return fail(PKV_ETIMEOUT, "a barrier wait timed out (CTA %d, stage %d, site %d)", h[1], h[2],
+                    h[3]);
+    case kErrCapacity:
+        return fail(PKV_ECAPACITY, "workqueue needs %d tasks, capacity %d", h[1], h[2]);
+    default:
+        return fail(PKV_EDEVICE, "device error code %d", h[0]);
+    }
+}
+
+const char *pkv_last_error_string(void) { return g_err.c_str(); }
+
+int pkv_version(void) { return PKV_VERSION; }
+
+}  // extern "C"

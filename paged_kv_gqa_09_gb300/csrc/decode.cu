@@ -1,0 +1,601 @@
+// decode.cu -- the split-decode kernel of "PersistentKV: Page-Aware Decode
+// Scheduling for Long-Context LLM Serving on Commodity GPUs" (technical
+// summary, Methodology 1: native block-table decode engine), written for
+// sm_103a.
+//
+// One persistent kernel serves the three task sources:
+//   rect   -- the length-bucketed rectangular grid B x Hkv x S_b
+//             ("Row-local bounds": an empty split writes the neutral state and
+//             reads no KV);
+//   queue  -- the compact 1D workqueue of non-empty (row, kv-head, split)
+//             tasks built by the plan kernel ("Compact workqueue");
+//   single -- one task per (row, kv-head) over the whole row, writing o/lse
+//             directly (the policy's no-split route).
+//
+// CTA layout (160 threads, one CTA per SM, ~220 KB shared memory):
+//   warp 4      producer: walks this CTA's tasks (static stride over the task
+//               index), reads block-table entries, and streams each 64-token
+//               tile of K and V straight from the pages into a ring of
+//               shared-memory stages with TMA (cp.async.bulk.tensor, 128-byte
+//               swizzle, evict-first L2 policy).  No page is repacked.
+//   warps 0..3  consumers: warp w owns tokens [16w, 16w+16) of every tile and
+//               keeps its own online-softmax state for the G query heads of
+//               the task.  Scores S^T = K q^T (16 tokens x 8 heads) and the
+//               update O^T += V^T P^T (d x 8 heads) run on tensor cores
+//               (mma.sync m16n8k16, fp16 in, fp32 accumulate); P^T is formed
+//               from the score fragment with movmatrix.  At a task's last tile
+//               the four warp states are merged exactly in shared memory and
+//               the task's partial state (m, l, acc) -- or, in single mode, o
+//               and lse -- is written once.
+// Every barrier wait is bounded (1 s); a timeout records an error in the
+// workspace header and the CTA drains its own copies and exits.
+#include "pkv_device.cuh"
+#include "pkv_kernels.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kCW = 4;                   // consumer warps
+constexpr int kTile = 16 * kCW;          // tokens per pipeline stage
+constexpr int kThreads = 32 * (kCW + 1); // + producer warp
+constexpr int kMaxG = 8;                 // query heads per KV head handled by one n8 tile
+constexpr int kSegRegs = 4;              // block-table entries per producer lane per segment
+constexpr int kSeg = 32 * kSegRegs;      // pages per segment
+constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any barrier wait
+constexpr uint64_t kDrainNs = 20000000ull;   // bound when draining after a timeout
+constexpr float kLn2 = 0.6931471805599453f;
+
+constexpr int kFirst = 1 << 16;  // stage flags (low 16 bits: valid tokens)
+constexpr int kLast = 1 << 17;
+constexpr int kEnd = 1 << 18;
+
+template <int D>
+struct Layout {
+    static constexpr int kDch = D / 64;                 // 128-byte column blocks per row
+    static constexpr int kTileBytes = kTile * D * 2;    // one K (or V) tile
+    static constexpr int kQBytes = kMaxG * D * 2;
+    static constexpr int kStageBytes = 2 * kTileBytes + kQBytes;
+    static constexpr int kStages = (D == 128) ? 6 : 12;
+    static constexpr int kRedOOff = kStages * kStageBytes;          // [warp][d][8] fp32
+    static constexpr int kRedMOff = kRedOOff + kCW * D * kMaxG * 4;  // [warp][8] fp32
+    static constexpr int kRedLOff = kRedMOff + kCW * kMaxG * 4;
+    static constexpr int kMetaOff = kRedLOff + kCW * kMaxG * 4;      // int4 per stage
+    static constexpr int kBarOff = kMetaOff + kStages * 16;          // full[S], empty[S], merge
+    static constexpr int kBytes = kBarOff + (2 * kStages + 1) * 8;
+    static constexpr int kAlloc = kBytes + 1024;                     // slack for alignment
+    static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+struct TaskInfo {
+    int i, g, sbase, t0, t1;  // row, kv head, first state slot, token range [t0, t1)
+};
+
+__device__ __forceinline__ TaskInfo shfl_task(const TaskInfo &a, int src)
+{
+    TaskInfo r;
+    r.i = __shfl_sync(0xffffffffu, a.i, src);
+    r.g = __shfl_sync(0xffffffffu, a.g, src);
+    r.sbase = __shfl_sync(0xffffffffu, a.sbase, src);
+    r.t0 = __shfl_sync(0xffffffffu, a.t0, src);
+    r.t1 = __shfl_sync(0xffffffffu, a.t1, src);
+    return r;
+}
+
+// Task k of this launch, with its row-local token range.
+template <int MODE>
+__device__ __forceinline__ TaskInfo load_task(const DecodeParams &p, int k, int ntasks)
+{
+    TaskInfo ti{0, 0, 0, 0, 0};
+    if (k >= ntasks)
+        return ti;
+    int j = 0;
+    if (MODE == kModeQueue) {
+        const int4 r = p.tasks[k];
+        ti.i = r.x;
+        ti.g = r.y;
+        j = r.z;
+        ti.sbase = r.w;
+    } else if (MODE == kModeRect) {
+        const int per_row = p.Hkv * p.S_b;
+        ti.i = k / per_row;
+        const int r = k - ti.i * per_row;
+        ti.g = r / p.S_b;
+        j = r - ti.g * p.S_b;
+        ti.sbase = (ti.i * p.S_b + j) * p.Hq + ti.g * p.G;
+    } else {
+        ti.i = k / p.Hkv;
+        ti.g = k - ti.i * p.Hkv;
+        ti.sbase = ti.i * p.Hq + ti.g * p.G;
+    }
+    int N = p.seq_lens[ti.i];
+    if (N < 0) {
+        report_error(p.ws, kErrNegLen, ti.i, N, 0);
+        N = 0;
+    }
+    if (N > p.len_cap) {
+        report_error(p.ws, kErrTooLong, ti.i, N, p.len_cap);
+        N = p.len_cap;
+    }
+    if (MODE == kModeSingle) {
+        ti.t0 = 0;
+        ti.t1 = N;
+    } else {
+        if (MODE == kModeRect && N > p.S_b * p.C)
+            report_error(p.ws, kErrTooLong, ti.i, N, p.S_b * p.C);
+        ti.t0 = j * p.C;
+        ti.t1 = min(ti.t0 + p.C, N);
+    }
+    return ti;
+}
+
+// Byte offset of (tile token t, 16-byte column chunk c) inside a K/V tile that
+// TMA filled with 128-byte-swizzled boxes of (1 << btl) tokens x D columns,
+// laid out [box][column block][token][128 bytes].
+template <int D>
+__device__ __forceinline__ uint32_t row_base(int t, int btl)
+{
+    const int b = t >> btl, s = t & ((1 << btl) - 1);
+    return (uint32_t)(((b << btl) * Layout<D>::kDch + s) * 128);
+}
+
+// ---------------------------------------------------------------- producer
+
+template <int D, int MODE>
+__device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                             const DecodeParams &p, int ntasks, uint32_t sbase,
+                                             int4 *meta, uint32_t bar_full0, uint32_t bar_empty0)
+{
+    using L = Layout<D>;
+    const int lane = threadIdx.x & 31;
+    const int btl = p.box_log2;
+    const int log2P = p.log2P;
+    const uint32_t box_bytes = (uint32_t)((128 << btl) * L::kDch);
+    const uint64_t pol = l2_evict_first_policy();
+    const int nloc = ntasks > (int)blockIdx.x ? (ntasks - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int G = p.G;
+
+    auto task_of = [&](int t) { return load_task<MODE>(p, (int)blockIdx.x + t * (int)gridDim.x, ntasks); };
+    TaskInfo wa = task_of(lane < nloc ? lane : nloc), wb = task_of(32 + lane < nloc ? 32 + lane : nloc);
+    if (lane >= nloc)
+        wa = TaskInfo{0, 0, 0, 0, 0};
+    if (32 + lane >= nloc)
+        wb = TaskInfo{0, 0, 0, 0, 0};
+
+    int stage = 0;
+    uint32_t ph = 0;               // lap parity of the ring
+    uint32_t pend = 0, pend_par = 0;  // stages with copies in flight, and their parity
+    bool ok = true;
+
+    for (int t = 0; t < nloc && ok; ++t) {
+        if (t > 0 && (t & 31) == 0) {
+            wa = wb;
+            wb = (t + 32 + lane < nloc) ? task_of(t + 32 + lane) : TaskInfo{0, 0, 0, 0, 0};
+        }
+        const TaskInfo cur = shfl_task(wa, t & 31);
+        if (cur.t0 >= cur.t1) {
+            // empty task: neutral state (split modes) or o = 0, lse = -inf (single)
+            if (MODE == kModeSingle) {
+                for (int x = lane; x < G * D / 8; x += 32)
+                    reinterpret_cast<int4 *>(p.o + (size_t)cur.sbase * D)[x] = make_int4(0, 0, 0, 0);
+                if (p.lse && lane < G)
+                    p.lse[cur.sbase + lane] = -INFINITY;
+            } else {
+                for (int x = lane; x < G * D / 4; x += 32)
+                    reinterpret_cast<float4 *>(p.part_acc + (size_t)cur.sbase * D)[x] =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+                if (lane < G) {
+                    p.part_m[cur.sbase + lane] = -INFINITY;
+                    p.part_l[cur.sbase + lane] = 0.f;
+                }
+            }
+            continue;
+        }
+        const int64_t row_off = (int64_t)cur.i * p.bt_stride;
+        const int pg_end = ((cur.t1 - 1) >> log2P) + 1;
+        for (int s0 = cur.t0 >> log2P; s0 < pg_end && ok; s0 += kSeg) {
+            int pid[kSegRegs];
+#pragma unroll
+            for (int r = 0; r < kSegRegs; ++r) {
+                const int pp = s0 + lane + 32 * r;
+                int v = 0;
+                if (pp < pg_end) {
+                    v = p.bt[row_off + pp];
+                    if (v < 0 || v >= p.num_pages) {
+                        report_error(p.ws, kErrBadPage, cur.i, pp, v);
+                        v = p.num_pages;  // out-of-range coordinate: TMA fills zeros
+                    }
+                }
+                pid[r] = v;
+            }
+            const int ts = max(cur.t0, s0 << log2P);
+            const int te = min(cur.t1, (s0 + kSeg) << log2P);
+            for (int tt = ts; tt < te; tt += kTile) {
+                const int nv = min(kTile, te - tt);
+                const int flags = nv | (tt == cur.t0 ? kFirst : 0) | (tt + nv >= cur.t1 ? kLast : 0);
+                const uint32_t full = bar_full0 + stage * 8, empty = bar_empty0 + stage * 8;
+                bool got = true;
+                if (lane == 0)
+                    got = mbar_wait(empty, ph ^ 1, kWaitNs);
+                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (!got) {
+                    report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 0);
+                    ok = false;
+                    break;
+                }
+                pend &= ~(1u << stage);
+                const int nb = (nv + (1 << btl) - 1) >> btl;
+                const uint32_t kdst = sbase + stage * L::kStageBytes;
+                const uint32_t vdst = kdst + L::kTileBytes;
+                if (lane == 0) {
+                    meta[stage] = make_int4(cur.i, cur.g, cur.sbase, flags);
+                    const uint32_t bytes = 2u * nb * box_bytes + ((flags & kFirst) ? (uint32_t)(G * D * 2) : 0u);
+                    mbar_arrive_expect_tx(full, bytes);
+                }
+                for (int b = 0; b < nb; ++b) {
+                    const int tok = tt + (b << btl);
+                    const int rel = (tok >> log2P) - s0;
+                    int pg = pid[0];
+#pragma unroll
+                    for (int r = 1; r < kSegRegs; ++r)
+                        if ((rel >> 5) == r)
+                            pg = pid[r];
+                    pg = __shfl_sync(0xffffffffu, pg, rel & 31);
+                    if (lane == 0) {
+                        const int slot = tok & ((1 << log2P) - 1);
+                        tma_load_5d(kdst + b * box_bytes, tmK, full, 0, slot, 0, cur.g, pg, pol);
+                        tma_load_5d(vdst + b * box_bytes, tmV, full, 0, slot, 0, cur.g, pg, pol);
+                    }
+                }
+                if ((flags & kFirst) && lane == 0)
+                    bulk_load(kdst + 2 * L::kTileBytes, p.q + ((size_t)cur.i * p.Hq + (size_t)cur.g * G) * D,
+                              (uint32_t)(G * D * 2), full);
+                pend |= 1u << stage;
+                pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
+                if (++stage == L::kStages) {
+                    stage = 0;
+                    ph ^= 1;
+                }
+            }
+        }
+    }
+    if (ok) {
+        // end-of-work sentinel
+        bool got = true;
+        if (lane == 0)
+            got = mbar_wait(bar_empty0 + stage * 8, ph ^ 1, kWaitNs);
+        got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+        if (got) {
+            pend &= ~(1u << stage);
+            if (lane == 0) {
+                meta[stage] = make_int4(0, 0, 0, kEnd);
+                mbar_arrive(bar_full0 + stage * 8);
+            }
+        } else {
+            report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 1);
+            ok = false;
+        }
+    }
+    if (!ok && lane == 0) {
+        // let every copy this CTA issued land before the CTA's shared memory goes away
+        for (int s = 0; s < L::kStages; ++s)
+            if (pend & (1u << s))
+                mbar_wait(bar_full0 + s * 8, (pend_par >> s) & 1u, kDrainNs);
+    }
+}
+
+// ---------------------------------------------------------------- consumer
+
+template <int D, int MODE>
+__device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sbase, uint8_t *basep,
+                                             const int4 *meta, uint32_t bar_full0,
+                                             uint32_t bar_empty0, uint32_t bar_merge)
+{
+    using L = Layout<D>;
+    constexpr int KS = D / 16;  // k-steps of the QK product == m-blocks of the PV product
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int btl = p.box_log2;
+    const uint32_t blk_bytes = 128u << btl;  // one 128-byte column block of a box
+    const int mi = lane >> 3, r8 = lane & 7;
+    // per-lane ldmatrix row addresses (see row_base): K tiles are read as
+    // A = K (tokens x d), V tiles transposed as A = V^T (d x tokens)
+    const uint32_t rowK = row_base<D>(16 * w + (mi & 1) * 8 + r8, btl);
+    const uint32_t rowV = row_base<D>(16 * w + (mi >> 1) * 8 + r8, btl);
+    const int r0 = lane >> 2;     // score fragment: tokens r0 and r0 + 8
+    const int hq = lane >> 2;     // B-fragment column: query head
+    const int h0 = 2 * (lane & 3);  // this lane's two heads in C fragments
+    const float sl2 = p.scale_log2;
+    const int G = p.G;
+
+    float* redO = reinterpret_cast<float *>(basep + L::kRedOOff);
+    float* redM = reinterpret_cast<float *>(basep + L::kRedMOff);
+    float* redL = reinterpret_cast<float *>(basep + L::kRedLOff);
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float O[KS][4];
+#pragma unroll
+    for (int x = 0; x < KS; ++x)
+        O[x][0] = O[x][1] = O[x][2] = O[x][3] = 0.f;
+    uint32_t qf[KS][2];
+#pragma unroll
+    for (int x = 0; x < KS; ++x)
+        qf[x][0] = qf[x][1] = 0u;
+
+    int stage = 0;
+    uint32_t ph = 0, mph = 0;
+    for (;;) {
+        const uint32_t full = bar_full0 + stage * 8;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(full, ph, kWaitNs));
+        if (!got) {
+            report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 2);
+            return;
+        }
+        const int4 mt = meta[stage];
+        const int fl = mt.w;
+        if (fl & kEnd)
+            return;
+        const uint32_t kt = sbase + stage * L::kStageBytes;
+        const uint32_t vt = kt + L::kTileBytes;
+        if (fl & kFirst) {
+            const uint8_t *qs = basep + (kt - sbase) + 2 * L::kTileBytes;
+#pragma unroll
+            for (int x = 0; x < KS; ++x) {
+                uint32_t b0 = 0, b1 = 0;
+                if (hq < G) {
+                    const uint32_t *row = reinterpret_cast<const uint32_t *>(qs + hq * D * 2);
+                    b0 = row[(16 * x + 2 * (lane & 3)) / 2];
+                    b1 = row[(16 * x + 8 + 2 * (lane & 3)) / 2];
+                }
+                qf[x][0] = b0;
+                qf[x][1] = b1;
+            }
+        }
+        const int nv = fl & 0xffff;
+        const int nvw = min(max(nv - 16 * w, 0), 16);
+        if (nvw > 0) {
+            if (nvw < 16) {
+                // rows past the row end hold other tokens' (or stale) data: zero
+                // them in V so that p = 0 cannot meet a NaN in the PV product
+                uint8_t *vtp = basep + (vt - sbase);
+                for (int x = lane; x < (16 - nvw) * (D / 8); x += 32) {
+                    const int rr = nvw + x / (D / 8), c = x % (D / 8);
+                    const int tok = 16 * w + rr;
+                    const uint32_t off = row_base<D>(tok, btl) + (c >> 3) * blk_bytes +
+                                         (uint32_t)((((c & 7) ^ (tok & 7))) << 4);
+                    *reinterpret_cast<int4 *>(vtp + off) = make_int4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            // S^T = K q^T : 16 tokens x 8 heads, two accumulation chains
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int x = 0; x < KS; ++x) {
+                const uint32_t cc = (uint32_t)((((2 * x) & 7) + (mi >> 1)) ^ r8) << 4;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kt + rowK + (x >> 2) * blk_bytes + cc, a0, a1, a2, a3);
+                if (x & 1)
+                    mma_16816(sb, a0, a1, a2, a3, qf[x][0], qf[x][1]);
+                else
+                    mma_16816(sa, a0, a1, a2, a3, qf[x][0], qf[x][1]);
+            }
+            const bool v0 = r0 < nvw, v1 = r0 + 8 < nvw;
+            const float x0 = v0 ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+            const float x1 = v0 ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+            const float x2 = v1 ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+            const float x3 = v1 ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+            const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
+            const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
+            l0 = l0 * al0 + (p0 + p2);
+            l1 = l1 * al1 + (p1 + p3);
+            m0 = mn0;
+            m1 = mn1;
+            const uint32_t P0 = movmatrix_t(pack_half2(p0, p1));
+            const uint32_t P1 = movmatrix_t(pack_half2(p2, p3));
+            // O^T += V^T P^T : D x 8 heads
+#pragma unroll
+            for (int x = 0; x < KS; ++x) {
+                O[x][0] *= al0;
+                O[x][1] *= al1;
+                O[x][2] *= al0;
+                O[x][3] *= al1;
+                const uint32_t cc = (uint32_t)((((2 * x) & 7) + (mi & 1)) ^ r8) << 4;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vt + rowV + (x >> 2) * blk_bytes + cc, a0, a1, a2, a3);
+                mma_16816(O[x], a0, a1, a2, a3, P0, P1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar_empty0 + stage * 8);
+
+        if (fl & kLast) {
+            // ---- exact merge of the four warp states of this task
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+            }
+            if (lane < 4) {
+                redM[w * kMaxG + h0] = m0;
+                redM[w * kMaxG + h0 + 1] = m1;
+                redL[w * kMaxG + h0] = l0;
+                redL[w * kMaxG + h0 + 1] = l1;
+            }
+#pragma unroll
+            for (int x = 0; x < KS; ++x) {
+                const int d0 = 16 * x + r0;
+                *reinterpret_cast<float2 *>(&redO[(w * D + d0) * kMaxG + h0]) = make_float2(O[x][0], O[x][1]);
+                *reinterpret_cast<float2 *>(&redO[(w * D + d0 + 8) * kMaxG + h0]) = make_float2(O[x][2], O[x][3]);
+            }
+            mbar_arrive(bar_merge);
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_merge, mph, kWaitNs))) {
+                report_error(p.ws, kErrTimeout, (int)blockIdx.x, -1, 3);
+                return;
+            }
+            mph ^= 1;
+            {
+                constexpr int HPT = kMaxG * D / (32 * kCW);  // heads per thread
+                const int ct = w * 32 + lane;
+                const int d = ct % D;
+                const int hb = (ct / D) * HPT;
+                float Mx[HPT], Ls[HPT], Ac[HPT];
+#pragma unroll
+                for (int hh = 0; hh < HPT; ++hh) {
+                    Mx[hh] = -INFINITY;
+                    Ls[hh] = 0.f;
+                    Ac[hh] = 0.f;
+                }
+#pragma unroll
+                for (int w2 = 0; w2 < kCW; ++w2)
+#pragma unroll
+                    for (int hh = 0; hh < HPT; ++hh)
+                        Mx[hh] = fmaxf(Mx[hh], redM[w2 * kMaxG + hb + hh]);
+#pragma unroll
+                for (int w2 = 0; w2 < kCW; ++w2) {
+                    float ov[HPT];
+#pragma unroll
+                    for (int q4 = 0; q4 < HPT / 4; ++q4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(&redO[(w2 * D + d) * kMaxG + hb + 4 * q4]);
+                        ov[4 * q4] = v.x;
+                        ov[4 * q4 + 1] = v.y;
+                        ov[4 * q4 + 2] = v.z;
+                        ov[4 * q4 + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < HPT; ++hh) {
+                        const float sc = ex2(redM[w2 * kMaxG + hb + hh] - Mx[hh]);
+                        Ls[hh] += redL[w2 * kMaxG + hb + hh] * sc;
+                        Ac[hh] += ov[hh] * sc;
+                    }
+                }
+                const int sb0 = mt.z;
+#pragma unroll
+                for (int hh = 0; hh < HPT; ++hh) {
+                    const int h = hb + hh;
+                    if (h < G) {
+                        if (MODE == kModeSingle) {
+                            p.o[(size_t)(sb0 + h) * D + d] = __float2half_rn(Ac[hh] / Ls[hh]);
+                            if (d == 0 && p.lse)
+                                p.lse[sb0 + h] = (Mx[hh] + log2f(Ls[hh])) * kLn2;
+                        } else {
+                            p.part_acc[(size_t)(sb0 + h) * D + d] = Ac[hh];
+                            if (d == 0) {
+                                p.part_m[sb0 + h] = Mx[hh] * kLn2;
+                                p.part_l[sb0 + h] = Ls[hh];
+                            }
+                        }
+                    }
+                }
+            }
+            mbar_arrive(bar_merge);
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_merge, mph, kWaitNs))) {
+                report_error(p.ws, kErrTimeout, (int)blockIdx.x, -1, 4);
+                return;
+            }
+            mph ^= 1;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+#pragma unroll
+            for (int x = 0; x < KS; ++x)
+                O[x][0] = O[x][1] = O[x][2] = O[x][3] = 0.f;
+        }
+        if (++stage == L::kStages) {
+            stage = 0;
+            ph ^= 1;
+        }
+    }
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const DecodeParams p)
+{
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *basep = smem_raw + (sbase - raw);
+    int4 *meta = reinterpret_cast<int4 *>(basep + L::kMetaOff);
+    const uint32_t bar_full0 = sbase + L::kBarOff;
+    const uint32_t bar_empty0 = bar_full0 + L::kStages * 8;
+    const uint32_t bar_merge = bar_empty0 + L::kStages * 8;
+    const int warp = threadIdx.x >> 5;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(bar_full0 + s * 8, 1);
+            mbar_init(bar_empty0 + s * 8, kCW);
+        }
+        mbar_init(bar_merge, kCW * 32);
+        fence_mbar_init();
+    }
+    if (warp == kCW && (threadIdx.x & 31) == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
+    __syncthreads();
+    // everything above overlaps the previous kernel; nothing below runs before
+    // it has finished and its writes are visible
+    pdl_wait();
+    pdl_trigger();
+    const int ntasks = (MODE == kModeQueue) ? min(p.ws->task_count, p.n_tasks) : p.n_tasks;
+    if (warp == kCW)
+        run_producer<D, MODE>(&tmK, &tmV, p, ntasks, sbase, meta, bar_full0, bar_empty0);
+    else
+        run_consumer<D, MODE>(p, sbase, basep, meta, bar_full0, bar_empty0, bar_merge);
+}
+
+template <int D, int MODE>
+cudaError_t launch_one(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
+                       cudaStream_t s, bool pdl)
+{
+    auto kern = decode_kernel<D, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Layout<D>::kAlloc);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Layout<D>::kAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+}  // namespace
+
+int decode_smem_bytes(int d) { return d == 64 ? Layout<64>::kAlloc : Layout<128>::kAlloc; }
+
+cudaError_t launch_decode(int d, int mode, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const DecodeParams &p, int grid, cudaStream_t s, bool pdl)
+{
+    if (d == 128) {
+        if (mode == kModeRect)
+            return launch_one<128, kModeRect>(tk, tv, p, grid, s, pdl);
+        if (mode == kModeQueue)
+            return launch_one<128, kModeQueue>(tk, tv, p, grid, s, pdl);
+        return launch_one<128, kModeSingle>(tk, tv, p, grid, s, pdl);
+    }
+    if (mode == kModeRect)
+        return launch_one<64, kModeRect>(tk, tv, p, grid, s, pdl);
+    if (mode == kModeQueue)
+        return launch_one<64, kModeQueue>(tk, tv, p, grid, s, pdl);
+    return launch_one<64, kModeSingle>(tk, tv, p, grid, s, pdl);
+}
+
+}  // namespace pkv

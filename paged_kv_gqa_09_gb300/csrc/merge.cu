@@ -1,0 +1,159 @@
+// merge.cu -- the exact log-sum-exp merge of split states, and the per-step
+// KV append.
+//
+// Merge: "PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM
+// Serving on Commodity GPUs", technical summary, Methodology 1, "Sequence
+// splitting": a separate kernel combines the partial online-softmax states
+// exactly.  One warp per (row i, query head h) reads only the row's n_i =
+// ceil(N*_i / C) states (row-local bounds), 16 bytes per lane per state:
+//   M = max_j m_j; L = sum_j l_j e^{m_j - M}; o = sum_j acc_j e^{m_j - M} / L;
+//   lse = M + ln L; a row with N*_i = 0 gets o = 0, lse = -inf.
+#include "pkv_device.cuh"
+#include "pkv_kernels.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kMergeWarps = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergeParams p)
+{
+    constexpr int VPL = D / 32;  // values per lane: 4 (d=128) or 2 (d=64)
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int wg = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    if (wg >= p.B * p.Hq)
+        return;
+    const int i = wg / p.Hq, h = wg - (wg / p.Hq) * p.Hq;
+    int N = p.seq_lens[i];
+    N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);
+    int n = (N + p.C - 1) / p.C;
+    int64_t base;
+    bool bad = false;
+    if (p.mode == kModeQueue) {
+        base = p.offsets[i];
+        bad = p.ws->overflow != 0 || base + n > p.state_rows_cap;
+    } else {
+        base = (int64_t)i * p.S_b;
+        n = min(n, p.S_b);
+    }
+    __half *out = p.o + (size_t)wg * D + lane * VPL;
+    if (bad || n == 0) {
+        const __half fill = bad ? __float2half(NAN) : __float2half(0.f);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v)
+            out[v] = fill;
+        if (p.lse && lane == 0)
+            p.lse[wg] = bad ? NAN : -INFINITY;
+        return;
+    }
+    float M = -INFINITY;
+    for (int j = lane; j < n; j += 32)
+        M = fmaxf(M, p.part_m[(base + j) * p.Hq + h]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f, acc[VPL];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v)
+        acc[v] = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) {
+        const int64_t slot = (base + j) * p.Hq + h;
+        const float w = ex2((p.part_m[slot] - M) * kLog2e);
+        L += p.part_l[slot] * w;
+        const float *a = p.part_acc + slot * D + lane * VPL;
+        if constexpr (VPL == 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(a);
+            acc[0] += w * x.x;
+            acc[1] += w * x.y;
+            acc[2] += w * x.z;
+            acc[3] += w * x.w;
+        } else {
+            const float2 x = *reinterpret_cast<const float2 *>(a);
+            acc[0] += w * x.x;
+            acc[1] += w * x.y;
+        }
+    }
+    const float inv = 1.f / L;
+    if constexpr (VPL == 4) {
+        *reinterpret_cast<uint2 *>(out) =
+            make_uint2(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv));
+    } else {
+        *reinterpret_cast<uint32_t *>(out) = pack_half2(acc[0] * inv, acc[1] * inv);
+    }
+    if (p.lse && lane == 0)
+        p.lse[wg] = M + logf(L);
+}
+
+// Append: one CTA per row, one thread per 16 bytes of the row's new K and V.
+__global__ void __launch_bounds__(256) append_kernel(const AppendParams p)
+{
+    pdl_wait();
+    const int i = blockIdx.x;
+    if (i >= p.B)
+        return;
+    const int N = p.seq_lens[i];
+    const int P = 1 << p.log2P;
+    const int chunks = p.Hkv * p.d / 8;  // 16-byte chunks per token
+    bool ok = N >= 0 && (int64_t)N < (int64_t)p.bt_stride * P;
+    int page = 0;
+    if (ok) {
+        page = p.bt[(int64_t)i * p.bt_stride + (N >> p.log2P)];
+        if (page < 0 || page >= p.num_pages) {
+            if (threadIdx.x == 0)
+                report_error(p.ws, kErrBadPage, i, N >> p.log2P, page);
+            ok = false;
+        }
+    } else if (threadIdx.x == 0) {
+        report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.bt_stride * P);
+    }
+    if (ok) {
+        const size_t dst = ((size_t)page * P + (N & (P - 1))) * (size_t)chunks;
+        const size_t src = (size_t)i * chunks;
+        for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+            reinterpret_cast<int4 *>(p.k_cache)[dst + c] = reinterpret_cast<const int4 *>(p.k_new)[src + c];
+            reinterpret_cast<int4 *>(p.v_cache)[dst + c] = reinterpret_cast<const int4 *>(p.v_new)[src + c];
+        }
+    }
+    __syncthreads();  // every thread has read N before it changes
+    if (ok && threadIdx.x == 0)
+        p.seq_lens[i] = N + 1;
+}
+
+cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttribute *attr, bool pdl)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+}  // namespace
+
+cudaError_t launch_merge(int d, const MergeParams &p, cudaStream_t s, bool pdl)
+{
+    const int warps = p.B * p.Hq;
+    const int blocks = warps > 0 ? (warps + kMergeWarps - 1) / kMergeWarps : 1;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = make_cfg(dim3(blocks), dim3(32 * kMergeWarps), s, attr, pdl);
+    if (d == 128)
+        return cudaLaunchKernelEx(&cfg, merge_kernel<128>, p);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<64>, p);
+}
+
+cudaError_t launch_append(const AppendParams &p, cudaStream_t s, bool pdl)
+{
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = make_cfg(dim3(p.B > 0 ? p.B : 1), dim3(128), s, attr, pdl);
+    return cudaLaunchKernelEx(&cfg, append_kernel, p);
+}
+
+}  // namespace pkv

@@ -1,0 +1,83 @@
+// pkv_kernels.h -- kernel parameter blocks and launchers shared between the
+// kernels (*.cu) and the C-ABI layer (api.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct WsHeader;
+
+enum Mode : int { kModeRect = 0, kModeQueue = 1, kModeSingle = 2 };
+
+// Byte offsets inside the plan workspace.
+constexpr size_t kWsHeaderBytes = 64;
+inline size_t ws_offsets_off() { return kWsHeaderBytes; }
+inline size_t ws_tasks_off(int B)
+{
+    size_t o = kWsHeaderBytes + sizeof(int32_t) * (size_t)(B + 1);
+    return (o + 15) & ~(size_t)15;
+}
+
+struct PlanParams {
+    const int32_t *seq_lens;
+    WsHeader *ws;
+    int32_t *offsets;  // [B+1]
+    int4 *tasks;       // [max_tasks]
+    int B, Hq, Hkv, G, C;
+    int len_cap;       // bt_stride * page_size: lengths are clamped to it
+    int64_t max_tasks;
+};
+
+struct DecodeParams {
+    const __half *q;
+    const int32_t *bt;
+    const int32_t *seq_lens;
+    const int4 *tasks;  // workqueue mode
+    WsHeader *ws;
+    float *part_acc, *part_m, *part_l;  // split modes
+    __half *o;                           // single-pass mode
+    float *lse;                          // single-pass mode (nullable)
+    int B, Hq, Hkv, G, num_pages, bt_stride;
+    int log2P;         // page size = 1 << log2P
+    int box_log2;      // tokens per TMA box = 1 << box_log2 (min(P, 64))
+    int C;             // split tokens (split modes)
+    int S_b;           // rectangular grid splits per row
+    int n_tasks;       // rect/single: tasks in the grid; queue: capacity
+    int len_cap;       // bt_stride * page_size
+    float scale_log2;  // scale * log2(e)
+};
+
+struct MergeParams {
+    const int32_t *seq_lens;
+    const int32_t *offsets;  // workqueue mode
+    const WsHeader *ws;
+    const float *part_acc, *part_m, *part_l;
+    __half *o;
+    float *lse;  // nullable
+    int B, Hq, C, S_b, mode;
+    int len_cap;
+    int64_t state_rows_cap;  // partial-state rows the buffer holds
+};
+
+struct AppendParams {
+    const __half *k_new, *v_new;
+    const int32_t *bt;
+    int32_t *seq_lens;
+    __half *k_cache, *v_cache;
+    WsHeader *ws;
+    int B, Hkv, d, log2P, num_pages, bt_stride;
+};
+
+cudaError_t launch_plan(const PlanParams &p, cudaStream_t s, bool pdl);
+cudaError_t launch_decode(int d, int mode, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const DecodeParams &p, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_merge(int d, const MergeParams &p, cudaStream_t s, bool pdl);
+cudaError_t launch_append(const AppendParams &p, cudaStream_t s, bool pdl);
+
+// Dynamic shared memory a decode CTA uses for head dim d.
+int decode_smem_bytes(int d);
+
+}  // namespace pkv

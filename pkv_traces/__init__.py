@@ -109,6 +109,7 @@ def _scatter_pages(rng: np.random.Generator, pages_per_row: Sequence[int],
     total = int(sum(pages_per_row))
     if num_pages is None:
         num_pages = total
+    num_pages = max(1, num_pages)  # a pool holds at least one page
     assert num_pages >= total
     perm = rng.permutation(num_pages)[:total].astype(np.int32)
     stride = max(1, max(pages_per_row) if len(pages_per_row) else 1)

@@ -1,0 +1,149 @@
+"""CPU tests of libpkv's C ABI: symbols, argument validation, policy and the
+host-side step model.  No call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import pkv_traces as T
+from paged_kv_gqa_09_gb300 import _lib, api
+from paged_kv_gqa_09_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return _lib.load()
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = header_symbols()
+    assert len(declared) >= 16
+    for name in declared:
+        assert hasattr(L, name), name
+    assert sorted(_lib.EXPORTS) == declared
+    assert L.pkv_version() == 1
+
+
+def shape(**kw):
+    base = dict(B=2, Hq=8, Hkv=2, d=128, page_size=16, num_pages=64, bt_stride=16, scale=0.088)
+    base.update(kw)
+    return _lib.Shape(*[base[k] for k, _ in _lib.Shape._fields_])
+
+
+def cfg(path=_lib.PKV_PATH_WORKQUEUE, C=256, bucket=0, max_tasks=0):
+    return _lib.PlanCfg(path, C, bucket, max_tasks)
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=6, Hkv=4), _lib.PKV_EINVAL),
+    (dict(d=96), _lib.PKV_EUNSUPPORTED),
+    (dict(Hq=32, Hkv=2), _lib.PKV_EUNSUPPORTED),      # G = 16
+    (dict(page_size=24), _lib.PKV_EUNSUPPORTED),
+    (dict(page_size=4), _lib.PKV_EUNSUPPORTED),
+    (dict(page_size=512), _lib.PKV_EUNSUPPORTED),
+    (dict(B=-1), _lib.PKV_EINVAL),
+    (dict(num_pages=0), _lib.PKV_EINVAL),
+    (dict(scale=float("nan")), _lib.PKV_EINVAL),
+])
+def test_bad_shapes_are_rejected(L, kw, status):
+    s, c = shape(**kw), cfg()
+    rc = L.pkv_plan(ctypes.byref(s), ctypes.byref(c), FAKE, FAKE, None)
+    assert rc == status, _lib.last_error()
+    assert _lib.last_error()
+    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(c)) == 0
+
+
+def test_bad_cfg_and_pointers_are_rejected(L):
+    s = shape()
+    assert L.pkv_plan(ctypes.byref(s), ctypes.byref(cfg(C=100)), FAKE, FAKE, None) == _lib.PKV_EINVAL
+    assert L.pkv_plan(ctypes.byref(s), ctypes.byref(cfg(path=7)), FAKE, FAKE, None) == _lib.PKV_EINVAL
+    c = cfg()
+    assert L.pkv_plan(ctypes.byref(s), ctypes.byref(c), None, FAKE, None) == _lib.PKV_EINVAL
+    assert "seq_lens" in _lib.last_error()
+    assert L.pkv_plan(ctypes.byref(s), ctypes.byref(c), FAKE + 4, FAKE, None) == _lib.PKV_EINVAL
+    assert "aligned" in _lib.last_error()
+    args = [FAKE] * 7
+    args[3] = FAKE + 2  # k_cache misaligned
+    assert L.pkv_decode(ctypes.byref(s), ctypes.byref(c), *args, None) == _lib.PKV_EINVAL
+    assert L.pkv_decode(ctypes.byref(s), ctypes.byref(cfg(path=2)), *([FAKE] * 7), None) == _lib.PKV_EINVAL
+    assert L.pkv_merge(ctypes.byref(s), ctypes.byref(c), FAKE, FAKE, FAKE, None, None, None) == _lib.PKV_EINVAL
+    assert L.pkv_single_pass(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None,
+                             None) == _lib.PKV_EINVAL
+    assert L.pkv_append(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == _lib.PKV_EINVAL
+    assert L.pkv_plan(None, ctypes.byref(c), FAKE, FAKE, None) == _lib.PKV_EINVAL
+    assert L.pkv_get_error(None, None) == _lib.PKV_EINVAL
+
+
+def test_plan_is_a_noop_off_the_workqueue(L):
+    s = shape()
+    for p in (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_PATH_SINGLE_PASS):
+        assert L.pkv_plan(ctypes.byref(s), ctypes.byref(cfg(path=p)), FAKE, FAKE, None) == 0
+
+
+def test_workspace_and_partial_sizes(L):
+    s = shape(B=3, Hq=32, Hkv=8, d=128, bt_stride=64, page_size=16)
+    # workqueue: header + offsets (aligned) + 16 B per task; default capacity Hkv*B*ceil(1024/C)
+    c = cfg(C=256)
+    tasks_off = (64 + 4 * 4 + 15) // 16 * 16
+    cap = 8 * 3 * 4
+    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(c)) == tasks_off + 16 * cap
+    assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(c)) == cap * 4 * (128 + 2) * 4
+    c = cfg(C=256, max_tasks=10)
+    assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(c)) == 10 * 4 * 130 * 4
+    r = cfg(path=_lib.PKV_PATH_BUCKETED_SPLIT, C=256, bucket=600)
+    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(r)) == tasks_off
+    assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(r)) == 3 * 3 * 32 * 130 * 4
+    one = cfg(path=_lib.PKV_PATH_SINGLE_PASS)
+    assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(one)) == 0
+
+
+def test_policy_follows_the_pages_routing(L):
+    """Methodology 2: B=1 long -> bucketed split, B>=8 long -> workqueue, B=4 and
+    everything else -> the single-kernel route."""
+    d = api.pkv_policy_default()
+    long_n = d.long_context_tokens
+    P = _lib
+    assert api.pkv_policy(1, long_n)[0] == P.PKV_PATH_BUCKETED_SPLIT
+    assert api.pkv_policy(8, long_n)[0] == P.PKV_PATH_WORKQUEUE
+    assert api.pkv_policy(64, 10 * long_n)[0] == P.PKV_PATH_WORKQUEUE
+    assert api.pkv_policy(4, 10 * long_n)[0] in (P.PKV_PATH_SINGLE_PASS, P.PKV_PATH_WORKQUEUE)
+    assert api.pkv_policy(1, max(1, long_n // 4))[0] == P.PKV_PATH_SINGLE_PASS
+    custom = _lib.PolicyCfg(1000, 1, 8, 512, 256)
+    assert api.pkv_policy(1, 1000, custom) == (P.PKV_PATH_BUCKETED_SPLIT, 256)
+    assert api.pkv_policy(9, 1000, custom) == (P.PKV_PATH_WORKQUEUE, 512)
+    assert api.pkv_policy(4, 1000, custom)[0] == P.PKV_PATH_SINGLE_PASS
+    assert api.pkv_policy(9, 999, custom)[0] == P.PKV_PATH_SINGLE_PASS
+    with pytest.raises(_lib.PkvError):
+        api.pkv_policy(-1, 5)
+
+
+@pytest.mark.parametrize("cfg_id", [1, 2, 3, 4, 5])
+def test_step_model_matches_oracle_counters(L, cfg_id):
+    tr = T.make_trace(cfg_id)
+    s = _lib.Shape(tr.B, tr.Hq, tr.Hkv, tr.d, tr.page_size, tr.num_pages, tr.bt_stride, tr.scale)
+    C = tr.split_tokens
+    S_b = -(-tr.n_max // C)
+    for path in (0, 1, 2, 3):
+        got = api.pkv_step_model(path, s, C, tr.n_max, tr.seq_lens)
+        want = oracle.counters(path, tr.seq_lens, tr.Hq, tr.Hkv, tr.d, C, S_b)
+        assert got == vars(want), (path, got, vars(want))
+
+
+def test_counters_start_at_zero_and_reset(L):
+    api.pkv_reset_counters()
+    assert set(api.pkv_get_counters().values()) == {0}

@@ -1,0 +1,341 @@
+"""GPU parity: libpkv (through its C ABI) against the float64 oracle.
+
+Every case draws seeded inputs once on the host, runs the oracle on the CPU
+and the CUDA path on the GPU, and compares element by element: the task list
+and launch counts bit-exactly, neutral states bit-exactly, outputs within the
+spec tolerance |x - y| <= 3e-3 + 1e-2 |y|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pkv_traces as T
+from paged_kv_gqa_09_gb300 import _lib, api
+
+from gpu_util import (check_error_free, close, close_lse, dev, oracle_out, read_plan, run_path,
+                      shape_of, upload)
+
+pytestmark = pytest.mark.gpu
+
+BUCKETED, WORKQUEUE, SINGLE = (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_PATH_WORKQUEUE,
+                               _lib.PKV_PATH_SINGLE_PASS)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_loaded():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_gqa_09_gb300 import build
+    build.build()
+    _lib.load()
+
+
+def case(lens, Hq=8, Hkv=2, d=128, P=16, C=64, seed=3, **kw):
+    tr = T.custom_trace(lens, Hq, Hkv, d, P, C, seed=seed, **kw)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr, poison_unused=True)
+    return tr, q, k, v
+
+
+# ------------------------------------------------------------------ plan
+
+@pytest.mark.parametrize("lens,C", [
+    ([1, 0, 1024, 1025, 17], 256),
+    ([0, 0, 0], 64),
+    ([5000, 3, 64, 64, 100000, 7, 0, 2048], 1024),
+    (list(range(1, 300, 7)), 16),
+])
+def test_plan_matches_oracle_bit_exact(lens, C):
+    Hq, Hkv = 32, 8
+    P = 16
+    tr = T.custom_trace(lens, Hq, Hkv, 128, P, C, extra_cols=2)
+    shape = shape_of(tr)
+    cfg = api.make_cfg(WORKQUEUE, C)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    api.pkv_plan(shape, cfg, dev(tr.seq_lens), ws)
+    torch.cuda.synchronize()
+    count, off, tasks, h = read_plan(ws, tr.B)
+    want, want_off = oracle.plan_compact(tr.seq_lens, Hq, Hkv, C)
+    assert count == want.shape[0]
+    assert np.array_equal(off, want_off)
+    assert np.array_equal(tasks, want)
+    assert h[0] == 0 and h[6] == 0
+    check_error_free(ws)
+
+
+@pytest.mark.parametrize("cfg_id", [3, 5])
+def test_plan_matches_oracle_on_workloads(cfg_id):
+    tr = T.make_trace(cfg_id)
+    shape = shape_of(tr)
+    cfg = api.make_cfg(WORKQUEUE, tr.split_tokens)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    api.pkv_plan(shape, cfg, dev(tr.seq_lens), ws)
+    torch.cuda.synchronize()
+    count, off, tasks, _ = read_plan(ws, tr.B)
+    want, want_off = oracle.plan_compact(tr.seq_lens, tr.Hq, tr.Hkv, tr.split_tokens)
+    assert count == want.shape[0] and np.array_equal(tasks, want) and np.array_equal(off, want_off)
+
+
+def test_plan_capacity_overflow_is_reported():
+    tr = T.custom_trace([300, 700], 8, 2, 128, 16, 64)
+    shape = shape_of(tr)
+    cfg = api.make_cfg(WORKQUEUE, 64, 0, max_tasks=5)
+    d = upload(tr, T.gen_q(tr), *T.gen_kv(tr))
+    o, lse, ws, _ = run_path(tr, d, WORKQUEUE, C=64, max_tasks=5)
+    st, msg = api.pkv_get_error(ws)
+    assert st == _lib.PKV_ECAPACITY, msg
+    assert torch.isnan(o.float()).all()
+
+
+# ------------------------------------------------------------------ partials
+
+def partial_views(part, tr, slots):
+    d = tr.d
+    acc = part[:slots * d].view(slots, d).cpu().numpy().astype(np.float64)
+    m = part[slots * d:slots * d + slots].cpu().numpy().astype(np.float64)
+    l = part[slots * d + slots:slots * (d + 2)].cpu().numpy().astype(np.float64)
+    return m, l, acc
+
+
+@pytest.mark.parametrize("rect", [False, True])
+def test_partial_states_match_oracle(rect):
+    tr, q, k, v = case([200, 1, 64, 130, 0], Hq=8, Hkv=2, C=64)
+    d = upload(tr, q, k, v)
+    shape = shape_of(tr)
+    C = 64
+    S_b = -(-tr.n_max // C)
+    path = BUCKETED if rect else WORKQUEUE
+    cfg = api.make_cfg(path, C, tr.n_max if rect else 0)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    slots = api.pkv_partials_size(shape, cfg) // ((tr.d + 2) * 4)
+    part = torch.full((slots * (tr.d + 2),), float("nan"), dtype=torch.float32, device="cuda")
+    api.pkv_plan(shape, cfg, d["sl"], ws)
+    api.pkv_decode(shape, cfg, ws, d["q"], d["k"], d["v"], d["bt"], d["sl"], part)
+    torch.cuda.synchronize()
+    check_error_free(ws)
+    m, l, acc = partial_views(part, tr, slots)
+    mo, lo, acco = oracle.partials(q, k, v, tr.block_table, tr.seq_lens, tr.scale, C,
+                                   rect=rect, S_b=S_b)
+    n = mo.shape[0]
+    m, l, acc = m[:n], l[:n], acc[:n]
+    neutral = lo == 0
+    if rect:
+        assert neutral.any()
+    # neutral states are written bit-exactly: m = -inf, l = +0, acc = +0
+    mb = part[slots * tr.d:slots * tr.d + n].cpu().numpy().view(np.uint32)
+    lb = part[slots * tr.d + slots:slots * tr.d + slots + n].cpu().numpy().view(np.uint32)
+    ab = part[:n * tr.d].view(n, tr.d).cpu().numpy().view(np.uint32)
+    assert np.all(mb[neutral] == 0xFF800000)
+    assert np.all(lb[neutral] == 0) and np.all(ab[neutral] == 0)
+    live = ~neutral
+    assert np.max(np.abs(m[live] - mo[live])) < 1e-4
+    # l and acc are relative to m: compare the normalized split outputs and l
+    assert np.max(np.abs(l[live] / lo[live] - 1)) < 2e-4
+    on = acc[live] / l[live][:, None]
+    ref = acco[live] / lo[live][:, None]
+    assert np.all(np.abs(on - ref) <= 3e-3 + 1e-2 * np.abs(ref))
+
+
+# ------------------------------------------------------------------ outputs on the workloads
+
+@pytest.mark.parametrize("cfg_id,path", [
+    (1, BUCKETED), (1, WORKQUEUE), (1, SINGLE),
+    (2, BUCKETED), (2, WORKQUEUE),
+    (3, WORKQUEUE), (3, BUCKETED), (3, SINGLE),
+])
+def test_workload_outputs_match_oracle(cfg_id, path):
+    tr = T.make_trace(cfg_id)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    d = upload(tr, q, k, v)
+    o, lse, ws, _ = run_path(tr, d, path)
+    check_error_free(ws)
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o, oref)
+    close_lse(lse, lref)
+
+
+@pytest.mark.parametrize("B", [4, 8])
+def test_zipf_policy_route_matches_oracle(B):
+    tr = T.make_trace(4, B=B)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    d = upload(tr, q, k, v)
+    dec = api.PagedDecoder()
+    o, lse = dec.step(d["q"], d["k"], d["v"], d["bt"], d["sl"], tr.n_max)
+    torch.cuda.synchronize()
+    check_error_free(dec.workspace(d["q"].device))
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o, oref)
+    close_lse(lse, lref)
+    for path in (BUCKETED, WORKQUEUE, SINGLE):
+        o2, l2, ws, _ = run_path(tr, d, path)
+        check_error_free(ws)
+        close(o2, oref)
+
+
+# ------------------------------------------------------------------ edge cases
+
+P_C = [(8, 64), (16, 16), (16, 48), (16, 256), (32, 64), (64, 128), (128, 256), (256, 512)]
+
+
+@pytest.mark.parametrize("P,C", P_C)
+@pytest.mark.parametrize("path", [BUCKETED, WORKQUEUE, SINGLE])
+def test_boundary_lengths(P, C, path):
+    lens = sorted({1, P - 1, P, P + 1, C - 1, C, C + 1, 2 * C + 3, 0, 63, 64, 65})
+    lens = [n for n in lens if n >= 0]
+    tr, q, k, v = case(lens, Hq=8, Hkv=2, d=128, P=P, C=C, seed=P * 1000 + C)
+    d = upload(tr, q, k, v)
+    o, lse, ws, _ = run_path(tr, d, path)
+    check_error_free(ws)
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o, oref)
+    close_lse(lse, lref)
+
+
+@pytest.mark.parametrize("Hq,Hkv,dd", [(4, 4, 128), (16, 2, 128), (8, 8, 64), (16, 2, 64),
+                                       (12, 4, 128), (6, 2, 64)])
+@pytest.mark.parametrize("path", [BUCKETED, WORKQUEUE, SINGLE])
+def test_group_sizes_and_head_dims(Hq, Hkv, dd, path):
+    tr, q, k, v = case([333, 17, 1000, 64], Hq=Hq, Hkv=Hkv, d=dd, P=16, C=128, seed=Hq * 7 + dd)
+    d = upload(tr, q, k, v)
+    o, lse, ws, _ = run_path(tr, d, path)
+    check_error_free(ws)
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o, oref)
+    close_lse(lse, lref)
+
+
+def test_wide_table_shared_pages_and_big_pool():
+    tr, q, k, v = case([500, 300, 77, 0, 1], Hq=8, Hkv=2, P=16, C=128, extra_pages=40,
+                       extra_cols=5, share_prefix_pages=10)
+    assert np.array_equal(tr.block_table[1, :10], tr.block_table[0, :10])
+    d = upload(tr, q, k, v)
+    oref, lref = oracle_out(tr, q, k, v)
+    for path in (BUCKETED, WORKQUEUE, SINGLE):
+        o, lse, ws, _ = run_path(tr, d, path)
+        check_error_free(ws)
+        close(o, oref)
+        close_lse(lse, lref)
+
+
+def test_empty_batch_rows_and_zero_lengths():
+    tr, q, k, v = case([0, 0, 5], Hq=8, Hkv=2)
+    d = upload(tr, q, k, v)
+    oref, lref = oracle_out(tr, q, k, v)
+    for path in (BUCKETED, WORKQUEUE, SINGLE):
+        o, lse, ws, _ = run_path(tr, d, path)
+        check_error_free(ws)
+        assert torch.all(o[:2] == 0)
+        assert torch.all(lse[:2] == float("-inf"))
+        close(o, oref)
+
+
+def test_outputs_are_deterministic():
+    tr = T.make_trace(3)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    d = upload(tr, q, k, v)
+    a = run_path(tr, d, WORKQUEUE)[0]
+    b = run_path(tr, d, WORKQUEUE)[0]
+    assert torch.equal(a, b)
+
+
+def test_extreme_scores_stay_finite():
+    tr, q, k, v = case([900, 40], Hq=8, Hkv=2, C=128)
+    k[:] = np.float16(0.0)
+    q[:] = np.float16(30.0)
+    rng = np.random.default_rng(1)
+    idx = rng.choice(tr.num_pages, size=4, replace=False)
+    k[idx] = np.float16(20.0)   # a few pages with very large scores
+    d = upload(tr, q, k, v)
+    oref, lref = oracle_out(tr, q, k, v)
+    for path in (BUCKETED, WORKQUEUE, SINGLE):
+        o, lse, ws, _ = run_path(tr, d, path)
+        check_error_free(ws)
+        close(o, oref)
+        close_lse(lse, lref)
+
+
+# ------------------------------------------------------------------ launch counts
+
+@pytest.mark.parametrize("path,expect", [(BUCKETED, dict(decode_launches=1, merge_launches=1)),
+                                         (WORKQUEUE, dict(plan_launches=1, decode_launches=1,
+                                                          merge_launches=1)),
+                                         (SINGLE, dict(single_pass_launches=1))])
+def test_launch_counts_match_model(path, expect):
+    tr = T.make_trace(3)
+    d = upload(tr, T.gen_q(tr), *T.gen_kv(tr))
+    api.pkv_reset_counters()
+    run_path(tr, d, path)
+    got = api.pkv_get_counters()
+    full = dict(plan_launches=0, decode_launches=0, merge_launches=0, single_pass_launches=0,
+                append_launches=0)
+    full.update(expect)
+    assert got == full
+    model = oracle.counters(path, tr.seq_lens, tr.Hq, tr.Hkv, tr.d, tr.split_tokens,
+                            -(-tr.n_max // tr.split_tokens))
+    attn = got["decode_launches"] + got["merge_launches"] + got["single_pass_launches"]
+    assert attn == model.attn_launches and got["plan_launches"] == model.plan_launches
+
+
+# ------------------------------------------------------------------ device-side checks
+
+def test_bad_page_id_is_reported_not_faulted():
+    tr, q, k, v = case([100, 50], Hq=8, Hkv=2, C=64)
+    tr.block_table[1, 2] = tr.num_pages + 7     # out of range
+    d = upload(tr, q, k, v)
+    for path in (BUCKETED, WORKQUEUE, SINGLE):
+        o, lse, ws, _ = run_path(tr, d, path)
+        st, msg = api.pkv_get_error(ws)
+        assert st == _lib.PKV_EDEVICE and "row 1" in msg, msg
+        # row 0 is untouched by the bad entry
+        tr0 = T.custom_trace([100], 8, 2, 128, 16, 64)
+        tr0.block_table = tr.block_table[:1, :7].copy()
+        tr0.num_pages = tr.num_pages
+        oref, _ = oracle.attention(q[:1], k, v, tr0.block_table, tr.seq_lens[:1], tr.scale)
+        close(o[:1], oref)
+
+
+def test_row_longer_than_bucket_is_reported():
+    tr, q, k, v = case([300, 100], Hq=8, Hkv=2, C=64)
+    d = upload(tr, q, k, v)
+    o, lse, ws, _ = run_path(tr, d, BUCKETED, C=64, bucket=128)
+    st, msg = api.pkv_get_error(ws)
+    assert st == _lib.PKV_EDEVICE and "row 0" in msg, msg
+    api.pkv_get_error(ws)  # cleared
+    assert api.pkv_get_error(ws)[0] == 0
+
+
+# ------------------------------------------------------------------ append
+
+def test_append_writes_the_next_slot():
+    tr, q, k, v = case([15, 16, 40, 0], Hq=8, Hkv=2, P=16, C=64, extra_cols=2, extra_pages=8)
+    # give every row one more page for the new token
+    free = [p for p in range(tr.num_pages) if p not in set(tr.block_table[tr.block_table >= 0].tolist())]
+    for i in range(tr.B):
+        n = int(tr.seq_lens[i])
+        if tr.block_table[i, n // 16] < 0:
+            tr.block_table[i, n // 16] = free.pop()
+    d = upload(tr, q, k, v)
+    kn, vn = T.gen_append_tokens(tr, 0)
+    shape = shape_of(tr)
+    ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    api.pkv_reset_counters()
+    api.pkv_append(shape, ws, dev(kn), dev(vn), d["bt"], d["sl"], d["k"], d["v"])
+    torch.cuda.synchronize()
+    check_error_free(ws)
+    assert api.pkv_get_counters()["append_launches"] == 1
+    assert np.array_equal(d["sl"].cpu().numpy(), tr.seq_lens + 1)
+    kc, vc = d["k"].cpu().numpy(), d["v"].cpu().numpy()
+    for i in range(tr.B):
+        n = int(tr.seq_lens[i])
+        pg, sl = tr.block_table[i, n // 16], n % 16
+        assert np.array_equal(kc[pg, sl], kn[i]) and np.array_equal(vc[pg, sl], vn[i])
+    # nothing else changed
+    mask = np.ones(k.shape[:2], bool)
+    for i in range(tr.B):
+        n = int(tr.seq_lens[i])
+        mask[tr.block_table[i, n // 16], n % 16] = False
+    assert np.array_equal(kc[mask].view(np.uint16), k[mask].view(np.uint16))
