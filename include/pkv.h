@@ -173,6 +173,31 @@ int pkv_append(const pkv_shape_t *shape, void *d_ws, const void *d_k_new,
                const void *d_v_new, const int32_t *d_block_table, int32_t *d_seq_lens,
                void *d_k_cache, void *d_v_cache, void *stream);
 
+/* pkv_decode_step_noalloc -- pkv_decode_step for callers that cannot
+ * allocate device memory.  No counterpart in the paper: it serves callers that
+ * must not call cudaMalloc -- code running inside an allocator's callbacks,
+ * plugins of runtimes that own every device allocation, paths that must avoid
+ * the allocator's implicit synchronisation -- and so cannot supply the plan
+ * workspace and partial-state buffers.  The caller passes inputs and outputs
+ * as for pkv_decode_step; the scratch is a file-scope device array of
+ * PKV_NOALLOC_SCRATCH_BYTES that every GPU loading libpkv holds until the
+ * process exits.  The call allocates nothing.
+ * - A step whose plan workspace (rounded up to 256 bytes) plus partial states
+ *   exceed PKV_NOALLOC_SCRATCH_BYTES is rejected with PKV_ECAPACITY.
+ * - The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ * - Every call shares the one array and it keeps the last call's contents:
+ *   the call clears the error word and task count itself, but calls that
+ *   overlap on the GPU (different streams, or other host threads) race --
+ *   serialize them.  Device-side check results stay in the array and are not
+ *   reported; callers needing pkv_get_error use pkv_decode_step. */
+#define PKV_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+
+int pkv_decode_step_noalloc(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg,
+                            const void *d_q, const void *d_k_cache, const void *d_v_cache,
+                            const int32_t *d_block_table, const int32_t *d_seq_lens,
+                            void *d_o, float *d_lse, void *stream);
+
 /* ------------------------------------------------------------- policy */
 
 /* Thresholds of the calibrated policy (Methodology 2).  The pages route

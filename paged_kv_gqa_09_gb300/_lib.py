@@ -24,6 +24,8 @@ PKV_PATH_WORKQUEUE = 1
 PKV_PATH_SINGLE_PASS = 2
 PATH_EXACT_BUCKETS = 3  # step-model only
 
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # PKV_NOALLOC_SCRATCH_BYTES in include/pkv.h
+
 STATUS_NAMES = {
     PKV_OK: "PKV_OK", PKV_EINVAL: "PKV_EINVAL", PKV_EUNSUPPORTED: "PKV_EUNSUPPORTED",
     PKV_ECUDA: "PKV_ECUDA", PKV_EDEVICE: "PKV_EDEVICE", PKV_ETIMEOUT: "PKV_ETIMEOUT",
@@ -33,7 +35,7 @@ STATUS_NAMES = {
 # every symbol include/pkv.h declares
 EXPORTS = [
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
-    "pkv_single_pass", "pkv_decode_step", "pkv_append", "pkv_policy_default", "pkv_policy",
+    "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc", "pkv_append", "pkv_policy_default", "pkv_policy",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error",
     "pkv_last_error_string", "pkv_version",
 ]
@@ -110,6 +112,7 @@ def load() -> ctypes.CDLL:
             "pkv_merge": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp]),
             "pkv_single_pass": (ctypes.c_int, [S, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_decode_step": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "pkv_decode_step_noalloc": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_append": (ctypes.c_int, [S, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_policy_default": (None, [PC]),
             "pkv_policy": (ctypes.c_int, [i32, i32, PC, ctypes.POINTER(ctypes.c_int32),

@@ -22,7 +22,7 @@ from ._lib import (PKV_PATH_BUCKETED_SPLIT, PKV_PATH_SINGLE_PASS, PKV_PATH_WORKQ
 __all__ = [
     "Shape", "PlanCfg", "PolicyCfg", "make_shape", "make_cfg",
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
-    "pkv_single_pass", "pkv_decode_step", "pkv_append", "pkv_policy", "pkv_policy_default",
+    "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc", "pkv_append", "pkv_policy", "pkv_policy_default",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error", "pkv_version",
     "PagedDecoder",
 ]
@@ -143,6 +143,23 @@ def pkv_decode_step(shape, cfg, ws, q, k_cache, v_cache, block_table, seq_lens, 
                             _dev(o, "o", torch.float16),
                             _dev(lse, "lse", torch.float32, nullable=True), _stream(stream)),
           "pkv_decode_step")
+
+
+def pkv_decode_step_noalloc(shape, cfg, q, k_cache, v_cache, block_table, seq_lens, o, lse=None,
+                            stream=None) -> None:
+    """pkv_decode_step with the library's static scratch: for callers that
+    cannot allocate device memory (see include/pkv.h for the size limit and the
+    rules on overlapping calls)."""
+    L = _lib.load()
+    check(L.pkv_decode_step_noalloc(ctypes.byref(shape), ctypes.byref(cfg),
+                                    _dev(q, "q", torch.float16),
+                                    _dev(k_cache, "k_cache", torch.float16),
+                                    _dev(v_cache, "v_cache", torch.float16),
+                                    _dev(block_table, "block_table", torch.int32),
+                                    _dev(seq_lens, "seq_lens", torch.int32),
+                                    _dev(o, "o", torch.float16),
+                                    _dev(lse, "lse", torch.float32, nullable=True),
+                                    _stream(stream)), "pkv_decode_step_noalloc")
 
 
 def pkv_append(shape, ws, k_new, v_new, block_table, seq_lens, k_cache, v_cache,

@@ -253,6 +253,8 @@ int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_
 
 }  // namespace
 
+int pkv::record_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
 extern "C" {
 
 size_t pkv_plan_workspace_size(const pkv_shape_t *s, const pkv_plan_cfg_t *c)

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -79,5 +80,8 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t s, bool pdl);
 
 // Dynamic shared memory a decode CTA uses for head dim d.
 int decode_smem_bytes(int d);
+
+// Set the calling thread's pkv_last_error_string() and return `code`.
+int record_error(int code, const char *msg);
 
 }  // namespace pkv
