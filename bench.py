@@ -288,6 +288,9 @@ def run_pkv(args, rank, local, ws, pg):
     build_mod.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    # everything runs on one non-default stream (graph capture needs one)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
     L = _lib.load()
     cfg_id = args.config
     tr = T.make_trace(cfg_id)
@@ -335,7 +338,6 @@ def run_pkv(args, rank, local, ws, pg):
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
     kn = torch.from_numpy(T.gen_append_tokens(tr, 0)[0]).to(dev)
     vn = torch.from_numpy(T.gen_append_tokens(tr, 0)[1]).to(dev)
-    stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     P = lambda t: t.data_ptr() if t is not None else None
     sref, cref = _ctypes_refs(shape, cfg)

@@ -137,11 +137,13 @@ int check_ptr(const void *p, const char *name, bool nullable = false)
 
 struct DevInfo {
     int sms = 0;
+    int ctas_per_sm[2] = {0, 0};  // decode CTAs an SM holds, d = 64 / 128
 };
 std::mutex g_dev_mu;
 DevInfo g_dev[64];
 
-int device_sms(int *out)
+// Resident decode CTAs the current device holds at once (SMs x occupancy).
+int device_slots(int d, int *out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -150,12 +152,21 @@ int device_sms(int *out)
     if (dev < 0 || dev >= 64)
         return fail(PKV_EUNSUPPORTED, "device ordinal %d", dev);
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].sms) {
-        e = cudaDeviceGetAttribute(&g_dev[dev].sms, cudaDevAttrMultiProcessorCount, dev);
+    DevInfo &di = g_dev[dev];
+    if (!di.sms) {
+        e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaDeviceGetAttribute");
     }
-    *out = g_dev[dev].sms;
+    int &occ = di.ctas_per_sm[d == 128 ? 1 : 0];
+    if (!occ) {
+        e = decode_ctas_per_sm(d, &occ);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "occupancy query");
+        if (occ < 1)
+            return fail(PKV_ECUDA, "decode kernel does not fit on an SM");
+    }
+    *out = di.sms * occ;
     return PKV_OK;
 }
 
@@ -200,8 +211,8 @@ int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_
                const void *k, const void *v, const int32_t *bt, const int32_t *sl, float *part,
                void *o, float *lse, cudaStream_t st)
 {
-    int sms = 0;
-    PKV_TRY(device_sms(&sms));
+    int slots = 0;
+    PKV_TRY(device_slots(s->d, &slots));
     const int box_tok = s->page_size < 64 ? s->page_size : 64;
     alignas(64) CUtensorMap tk, tv;
     PKV_TRY(encode_kv_map(&tk, k, s, box_tok));
@@ -243,7 +254,7 @@ int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_
     if (ntasks > 0x7fffffffLL)
         return fail(PKV_EUNSUPPORTED, "%lld tasks exceed int32", (long long)ntasks);
     p.n_tasks = (int)ntasks;
-    const int grid = (int)(ntasks < sms ? (ntasks > 0 ? ntasks : 1) : sms);
+    const int grid = (int)(ntasks < slots ? (ntasks > 0 ? ntasks : 1) : slots);
     cudaError_t e = launch_decode(s->d, mode, tk, tv, p, grid, st, true);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");

@@ -12,7 +12,7 @@
 //   single -- one task per (row, kv-head) over the whole row, writing o/lse
 //             directly (the policy's no-split route).
 //
-// CTA layout (160 threads, one CTA per SM, ~220 KB shared memory):
+// CTA layout (160 threads, two CTAs per SM, ~104 KB shared memory each):
 //   warp 4      producer: walks this CTA's tasks (static stride over the task
 //               index), reads block-table entries, and streams each 64-token
 //               tile of K and V straight from the pages into a ring of
@@ -24,9 +24,12 @@
 //               update O^T += V^T P^T (d x 8 heads) run on tensor cores
 //               (mma.sync m16n8k16, fp16 in, fp32 accumulate); P^T is formed
 //               from the score fragment with movmatrix.  At a task's last tile
-//               the four warp states are merged exactly in shared memory and
-//               the task's partial state (m, l, acc) -- or, in single mode, o
-//               and lse -- is written once.
+//               warps 1..3 park their states in their own, already consumed,
+//               K rows of that stage; warp 0 merges the four states exactly,
+//               writes the task's partial state (m, l, acc) -- or, in single
+//               mode, o and lse -- and releases the stage for all four warps.
+// Two CTAs per SM keep every task of a 256-task launch in flight at once, so
+// the DRAM bandwidth is shared per task rather than per wave of tasks.
 // Every barrier wait is bounded (1 s); a timeout records an error in the
 // workspace header and the CTA drains its own copies and exits.
 #include "pkv_device.cuh"
@@ -55,16 +58,15 @@ struct Layout {
     static constexpr int kTileBytes = kTile * D * 2;    // one K (or V) tile
     static constexpr int kQBytes = kMaxG * D * 2;
     static constexpr int kStageBytes = 2 * kTileBytes + kQBytes;
-    static constexpr int kStages = (D == 128) ? 6 : 12;
-    static constexpr int kRedOOff = kStages * kStageBytes;          // [warp][d][8] fp32
-    static constexpr int kRedMOff = kRedOOff + kCW * D * kMaxG * 4;  // [warp][8] fp32
-    static constexpr int kRedLOff = kRedMOff + kCW * kMaxG * 4;
-    static constexpr int kMetaOff = kRedLOff + kCW * kMaxG * 4;      // int4 per stage
-    static constexpr int kBarOff = kMetaOff + kStages * 16;          // full[S], empty[S], merge
-    static constexpr int kBytes = kBarOff + (2 * kStages + 1) * 8;
+    static constexpr int kStages = (D == 128) ? 3 : 6;
+    static constexpr int kMetaOff = kStages * kStageBytes;           // int4 per stage
+    static constexpr int kRedOff = kMetaOff + kStages * 16;          // [stage][warp 1..3][m 8, l 8]
+    static constexpr int kBarOff = kRedOff + kStages * (kCW - 1) * 2 * kMaxG * 4;
+    // barriers: full[S], empty[S], merge[S]
+    static constexpr int kBytes = kBarOff + 3 * kStages * 8;
     static constexpr int kAlloc = kBytes + 1024;                     // slack for alignment
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+    static_assert(2 * (kAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
 struct TaskInfo {
@@ -286,10 +288,24 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
 
 // ---------------------------------------------------------------- consumer
 
+// Shared-memory address where lane `lane` of consumer warp w parks 16-byte
+// chunk x of its state at a task's end: inside the warp's own 16 K rows of
+// the stage (16 rows x D*2 bytes == 32 lanes x D/16 chunks), chunks XOR-spread
+// over the row's 16-byte slots.
+template <int D>
+__device__ __forceinline__ uint32_t park_addr(uint32_t ktile, int w, int lane, int x, int btl)
+{
+    constexpr int CPR = D / 8;  // 16-byte chunks per row
+    const int e = lane * (D / 16) + x;
+    const int r = e / CPR, c = e % CPR;
+    return ktile + row_base<D>(16 * w + r, btl) + (uint32_t)((c >> 3) * (128 << btl)) +
+           (uint32_t)(((c & 7) ^ (r & 7)) << 4);
+}
+
 template <int D, int MODE>
 __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sbase, uint8_t *basep,
                                              const int4 *meta, uint32_t bar_full0,
-                                             uint32_t bar_empty0, uint32_t bar_merge)
+                                             uint32_t bar_empty0, uint32_t bar_merge0)
 {
     using L = Layout<D>;
     constexpr int KS = D / 16;  // k-steps of the QK product == m-blocks of the PV product
@@ -301,15 +317,12 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
     // A = K (tokens x d), V tiles transposed as A = V^T (d x tokens)
     const uint32_t rowK = row_base<D>(16 * w + (mi & 1) * 8 + r8, btl);
     const uint32_t rowV = row_base<D>(16 * w + (mi >> 1) * 8 + r8, btl);
-    const int r0 = lane >> 2;     // score fragment: tokens r0 and r0 + 8
-    const int hq = lane >> 2;     // B-fragment column: query head
+    const int r0 = lane >> 2;       // score fragment: tokens r0 and r0 + 8
+    const int hq = lane >> 2;       // B-fragment column: query head
     const int h0 = 2 * (lane & 3);  // this lane's two heads in C fragments
     const float sl2 = p.scale_log2;
     const int G = p.G;
-
-    float* redO = reinterpret_cast<float *>(basep + L::kRedOOff);
-    float* redM = reinterpret_cast<float *>(basep + L::kRedMOff);
-    float* redL = reinterpret_cast<float *>(basep + L::kRedLOff);
+    float *red = reinterpret_cast<float *>(basep + L::kRedOff);
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float O[KS][4];
@@ -322,7 +335,7 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
         qf[x][0] = qf[x][1] = 0u;
 
     int stage = 0;
-    uint32_t ph = 0, mph = 0;
+    uint32_t ph = 0, mpar = 0;  // ring lap parity; per-stage merge-barrier parities
     for (;;) {
         const uint32_t full = bar_full0 + stage * 8;
         const bool got = __all_sync(0xffffffffu, mbar_wait(full, ph, kWaitNs));
@@ -414,94 +427,121 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
             }
         }
         __syncwarp();
-        if (lane == 0)
-            mbar_arrive(bar_empty0 + stage * 8);
-
-        if (fl & kLast) {
+        if (!(fl & kLast)) {
+            if (lane == 0)
+                mbar_arrive(bar_empty0 + stage * 8);
+        } else {
             // ---- exact merge of the four warp states of this task
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) {
                 l0 += __shfl_xor_sync(0xffffffffu, l0, o);
                 l1 += __shfl_xor_sync(0xffffffffu, l1, o);
             }
-            if (lane < 4) {
-                redM[w * kMaxG + h0] = m0;
-                redM[w * kMaxG + h0 + 1] = m1;
-                redL[w * kMaxG + h0] = l0;
-                redL[w * kMaxG + h0 + 1] = l1;
-            }
+            float *rs = red + stage * (kCW - 1) * 2 * kMaxG;  // [warp 1..3][m 8 | l 8]
+            const uint32_t mbar = bar_merge0 + stage * 8;
+            const uint32_t mp = (mpar >> stage) & 1u;
+            mpar ^= 1u << stage;
+            if (w > 0) {
+                // park: this warp has finished reading its K rows of the stage
 #pragma unroll
-            for (int x = 0; x < KS; ++x) {
-                const int d0 = 16 * x + r0;
-                *reinterpret_cast<float2 *>(&redO[(w * D + d0) * kMaxG + h0]) = make_float2(O[x][0], O[x][1]);
-                *reinterpret_cast<float2 *>(&redO[(w * D + d0 + 8) * kMaxG + h0]) = make_float2(O[x][2], O[x][3]);
-            }
-            mbar_arrive(bar_merge);
-            if (!__all_sync(0xffffffffu, mbar_wait(bar_merge, mph, kWaitNs))) {
-                report_error(p.ws, kErrTimeout, (int)blockIdx.x, -1, 3);
-                return;
-            }
-            mph ^= 1;
-            {
-                constexpr int HPT = kMaxG * D / (32 * kCW);  // heads per thread
-                const int ct = w * 32 + lane;
-                const int d = ct % D;
-                const int hb = (ct / D) * HPT;
-                float Mx[HPT], Ls[HPT], Ac[HPT];
+                for (int x = 0; x < KS; ++x)
+                    *reinterpret_cast<float4 *>(basep + (park_addr<D>(kt, w, lane, x, btl) - sbase)) =
+                        make_float4(O[x][0], O[x][1], O[x][2], O[x][3]);
+                if (lane < 4) {
+                    rs[(w - 1) * 16 + h0] = m0;
+                    rs[(w - 1) * 16 + h0 + 1] = m1;
+                    rs[(w - 1) * 16 + 8 + h0] = l0;
+                    rs[(w - 1) * 16 + 8 + h0 + 1] = l1;
+                }
+                fence_proxy_async_smem();  // these K rows are refilled by TMA later
+                mbar_arrive(mbar);
+                // warp 0 releases the stage once it has read the parked states
+            } else {
+                if (!__all_sync(0xffffffffu, mbar_wait(mbar, mp, kWaitNs))) {
+                    report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 3);
+                    return;
+                }
+                float M0 = m0, M1 = m1;
 #pragma unroll
-                for (int hh = 0; hh < HPT; ++hh) {
-                    Mx[hh] = -INFINITY;
-                    Ls[hh] = 0.f;
-                    Ac[hh] = 0.f;
+                for (int w2 = 0; w2 < kCW - 1; ++w2) {
+                    M0 = fmaxf(M0, rs[w2 * 16 + h0]);
+                    M1 = fmaxf(M1, rs[w2 * 16 + h0 + 1]);
+                }
+                float s0 = ex2(m0 - M0), s1 = ex2(m1 - M1);
+                float L0 = l0 * s0, L1 = l1 * s1;
+#pragma unroll
+                for (int x = 0; x < KS; ++x) {
+                    O[x][0] *= s0;
+                    O[x][1] *= s1;
+                    O[x][2] *= s0;
+                    O[x][3] *= s1;
                 }
 #pragma unroll
-                for (int w2 = 0; w2 < kCW; ++w2)
+                for (int w2 = 1; w2 < kCW; ++w2) {
+                    const float t0 = ex2(rs[(w2 - 1) * 16 + h0] - M0);
+                    const float t1 = ex2(rs[(w2 - 1) * 16 + h0 + 1] - M1);
+                    L0 += rs[(w2 - 1) * 16 + 8 + h0] * t0;
+                    L1 += rs[(w2 - 1) * 16 + 8 + h0 + 1] * t1;
 #pragma unroll
-                    for (int hh = 0; hh < HPT; ++hh)
-                        Mx[hh] = fmaxf(Mx[hh], redM[w2 * kMaxG + hb + hh]);
-#pragma unroll
-                for (int w2 = 0; w2 < kCW; ++w2) {
-                    float ov[HPT];
-#pragma unroll
-                    for (int q4 = 0; q4 < HPT / 4; ++q4) {
-                        const float4 v = *reinterpret_cast<const float4 *>(&redO[(w2 * D + d) * kMaxG + hb + 4 * q4]);
-                        ov[4 * q4] = v.x;
-                        ov[4 * q4 + 1] = v.y;
-                        ov[4 * q4 + 2] = v.z;
-                        ov[4 * q4 + 3] = v.w;
-                    }
-#pragma unroll
-                    for (int hh = 0; hh < HPT; ++hh) {
-                        const float sc = ex2(redM[w2 * kMaxG + hb + hh] - Mx[hh]);
-                        Ls[hh] += redL[w2 * kMaxG + hb + hh] * sc;
-                        Ac[hh] += ov[hh] * sc;
+                    for (int x = 0; x < KS; ++x) {
+                        const float4 v = *reinterpret_cast<const float4 *>(
+                            basep + (park_addr<D>(kt, w2, lane, x, btl) - sbase));
+                        O[x][0] += v.x * t0;
+                        O[x][1] += v.y * t1;
+                        O[x][2] += v.z * t0;
+                        O[x][3] += v.w * t1;
                     }
                 }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_n(bar_empty0 + stage * 8, kCW);  // release for all four warps
                 const int sb0 = mt.z;
+                const bool ok0 = h0 < G, ok1 = h0 + 1 < G;
+                if (MODE == kModeSingle) {
+                    const float i0 = 1.f / L0, i1 = 1.f / L1;
 #pragma unroll
-                for (int hh = 0; hh < HPT; ++hh) {
-                    const int h = hb + hh;
-                    if (h < G) {
-                        if (MODE == kModeSingle) {
-                            p.o[(size_t)(sb0 + h) * D + d] = __float2half_rn(Ac[hh] / Ls[hh]);
-                            if (d == 0 && p.lse)
-                                p.lse[sb0 + h] = (Mx[hh] + log2f(Ls[hh])) * kLn2;
-                        } else {
-                            p.part_acc[(size_t)(sb0 + h) * D + d] = Ac[hh];
-                            if (d == 0) {
-                                p.part_m[sb0 + h] = Mx[hh] * kLn2;
-                                p.part_l[sb0 + h] = Ls[hh];
-                            }
+                    for (int x = 0; x < KS; ++x) {
+                        const int d0 = 16 * x + r0;
+                        if (ok0) {
+                            p.o[(size_t)(sb0 + h0) * D + d0] = __float2half_rn(O[x][0] * i0);
+                            p.o[(size_t)(sb0 + h0) * D + d0 + 8] = __float2half_rn(O[x][2] * i0);
+                        }
+                        if (ok1) {
+                            p.o[(size_t)(sb0 + h0 + 1) * D + d0] = __float2half_rn(O[x][1] * i1);
+                            p.o[(size_t)(sb0 + h0 + 1) * D + d0 + 8] = __float2half_rn(O[x][3] * i1);
+                        }
+                    }
+                    if (lane < 4 && p.lse) {
+                        if (ok0)
+                            p.lse[sb0 + h0] = (M0 + log2f(L0)) * kLn2;
+                        if (ok1)
+                            p.lse[sb0 + h0 + 1] = (M1 + log2f(L1)) * kLn2;
+                    }
+                } else {
+#pragma unroll
+                    for (int x = 0; x < KS; ++x) {
+                        const int d0 = 16 * x + r0;
+                        if (ok0) {
+                            p.part_acc[(size_t)(sb0 + h0) * D + d0] = O[x][0];
+                            p.part_acc[(size_t)(sb0 + h0) * D + d0 + 8] = O[x][2];
+                        }
+                        if (ok1) {
+                            p.part_acc[(size_t)(sb0 + h0 + 1) * D + d0] = O[x][1];
+                            p.part_acc[(size_t)(sb0 + h0 + 1) * D + d0 + 8] = O[x][3];
+                        }
+                    }
+                    if (lane < 4) {
+                        if (ok0) {
+                            p.part_m[sb0 + h0] = M0 * kLn2;
+                            p.part_l[sb0 + h0] = L0;
+                        }
+                        if (ok1) {
+                            p.part_m[sb0 + h0 + 1] = M1 * kLn2;
+                            p.part_l[sb0 + h0 + 1] = L1;
                         }
                     }
                 }
             }
-            mbar_arrive(bar_merge);
-            if (!__all_sync(0xffffffffu, mbar_wait(bar_merge, mph, kWaitNs))) {
-                report_error(p.ws, kErrTimeout, (int)blockIdx.x, -1, 4);
-                return;
-            }
-            mph ^= 1;
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
 #pragma unroll
@@ -516,7 +556,7 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p)
 {
@@ -528,15 +568,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int4 *meta = reinterpret_cast<int4 *>(basep + L::kMetaOff);
     const uint32_t bar_full0 = sbase + L::kBarOff;
     const uint32_t bar_empty0 = bar_full0 + L::kStages * 8;
-    const uint32_t bar_merge = bar_empty0 + L::kStages * 8;
+    const uint32_t bar_merge0 = bar_empty0 + L::kStages * 8;
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(bar_full0 + s * 8, 1);
             mbar_init(bar_empty0 + s * 8, kCW);
+            mbar_init(bar_merge0 + s * 8, (kCW - 1) * 32);
         }
-        mbar_init(bar_merge, kCW * 32);
         fence_mbar_init();
     }
     if (warp == kCW && (threadIdx.x & 31) == 0) {
@@ -552,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kCW)
         run_producer<D, MODE>(&tmK, &tmV, p, ntasks, sbase, meta, bar_full0, bar_empty0);
     else
-        run_consumer<D, MODE>(p, sbase, basep, meta, bar_full0, bar_empty0, bar_merge);
+        run_consumer<D, MODE>(p, sbase, basep, meta, bar_full0, bar_empty0, bar_merge0);
 }
 
 template <int D, int MODE>
@@ -577,9 +617,25 @@ cudaError_t launch_one(const CUtensorMap &tk, const CUtensorMap &tv, const Decod
     return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
+template <int D>
+cudaError_t occupancy(int *out)
+{
+    auto kern = decode_kernel<D, kModeQueue>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Layout<D>::kAlloc);
+    if (e != cudaSuccess)
+        return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kern, kThreads, Layout<D>::kAlloc);
+}
+
 }  // namespace
 
 int decode_smem_bytes(int d) { return d == 64 ? Layout<64>::kAlloc : Layout<128>::kAlloc; }
+
+cudaError_t decode_ctas_per_sm(int d, int *out)
+{
+    return d == 64 ? occupancy<64>(out) : occupancy<128>(out);
+}
 
 cudaError_t launch_decode(int d, int mode, const CUtensorMap &tk, const CUtensorMap &tv,
                           const DecodeParams &p, int grid, cudaStream_t s, bool pdl)

@@ -4,10 +4,13 @@
 // Merge: "PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM
 // Serving on Commodity GPUs", technical summary, Methodology 1, "Sequence
 // splitting": a separate kernel combines the partial online-softmax states
-// exactly.  One warp per (row i, query head h) reads only the row's n_i =
-// ceil(N*_i / C) states (row-local bounds), 16 bytes per lane per state:
+// exactly.  One 4-warp CTA per (row i, query head h) reads only the row's
+// n_i = ceil(N*_i / C) states (row-local bounds):
 //   M = max_j m_j; L = sum_j l_j e^{m_j - M}; o = sum_j acc_j e^{m_j - M} / L;
 //   lse = M + ln L; a row with N*_i = 0 gets o = 0, lse = -inf.
+// The states are few and were just written (L2-resident), so the kernel is
+// latency-bound: warp w takes states j = w, w+4, ... with all of its loads
+// in flight at once, and the four partial sums meet in shared memory.
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
 
@@ -21,9 +24,12 @@ template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergeParams p)
 {
     constexpr int VPL = D / 32;  // values per lane: 4 (d=128) or 2 (d=64)
+    __shared__ float s_max[kMergeWarps];
+    __shared__ float s_l[kMergeWarps];
+    __shared__ __align__(16) float s_acc[kMergeWarps][D];
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int wg = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wg = blockIdx.x;
     if (wg >= p.B * p.Hq)
         return;
     const int i = wg / p.Hq, h = wg - (wg / p.Hq) * p.Hq;
@@ -39,28 +45,38 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
         base = (int64_t)i * p.S_b;
         n = min(n, p.S_b);
     }
-    __half *out = p.o + (size_t)wg * D + lane * VPL;
     if (bad || n == 0) {
-        const __half fill = bad ? __float2half(NAN) : __float2half(0.f);
+        if (warp == 0) {
+            __half *out = p.o + (size_t)wg * D + lane * VPL;
+            const __half fill = bad ? __float2half(NAN) : __float2half(0.f);
 #pragma unroll
-        for (int v = 0; v < VPL; ++v)
-            out[v] = fill;
-        if (p.lse && lane == 0)
-            p.lse[wg] = bad ? NAN : -INFINITY;
+            for (int v = 0; v < VPL; ++v)
+                out[v] = fill;
+            if (p.lse && lane == 0)
+                p.lse[wg] = bad ? NAN : -INFINITY;
+        }
         return;
     }
+    // M = max_j m_j over the row's states
     float M = -INFINITY;
-    for (int j = lane; j < n; j += 32)
+    for (int j = threadIdx.x; j < n; j += 32 * kMergeWarps)
         M = fmaxf(M, p.part_m[(base + j) * p.Hq + h]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0)
+        s_max[warp] = M;
+    __syncthreads();
+#pragma unroll
+    for (int w2 = 0; w2 < kMergeWarps; ++w2)
+        M = fmaxf(M, s_max[w2]);
+    // this warp's share of L and acc
     float L = 0.f, acc[VPL];
 #pragma unroll
     for (int v = 0; v < VPL; ++v)
         acc[v] = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < n; ++j) {
+#pragma unroll 8
+    for (int j = warp; j < n; j += kMergeWarps) {
         const int64_t slot = (base + j) * p.Hq + h;
         const float w = ex2((p.part_m[slot] - M) * kLog2e);
         L += p.part_l[slot] * w;
@@ -77,15 +93,36 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
             acc[1] += w * x.y;
         }
     }
-    const float inv = 1.f / L;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v)
+        s_acc[warp][lane * VPL + v] = acc[v];
+    if (lane == 0)
+        s_l[warp] = L;
+    __syncthreads();
+    if (warp != 0)
+        return;
+    float Lt = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < kMergeWarps; ++w2)
+        Lt += s_l[w2];
+    const float inv = 1.f / Lt;
+    float o[VPL];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+        float t = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kMergeWarps; ++w2)
+            t += s_acc[w2][lane * VPL + v];
+        o[v] = t * inv;
+    }
+    __half *out = p.o + (size_t)wg * D + lane * VPL;
     if constexpr (VPL == 4) {
-        *reinterpret_cast<uint2 *>(out) =
-            make_uint2(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv));
+        *reinterpret_cast<uint2 *>(out) = make_uint2(pack_half2(o[0], o[1]), pack_half2(o[2], o[3]));
     } else {
-        *reinterpret_cast<uint32_t *>(out) = pack_half2(acc[0] * inv, acc[1] * inv);
+        *reinterpret_cast<uint32_t *>(out) = pack_half2(o[0], o[1]);
     }
     if (p.lse && lane == 0)
-        p.lse[wg] = M + logf(L);
+        p.lse[wg] = M + logf(Lt);
 }
 
 // Append: one CTA per row, one thread per 16 bytes of the row's new K and V.
@@ -140,8 +177,7 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAtt
 
 cudaError_t launch_merge(int d, const MergeParams &p, cudaStream_t s, bool pdl)
 {
-    const int warps = p.B * p.Hq;
-    const int blocks = warps > 0 ? (warps + kMergeWarps - 1) / kMergeWarps : 1;
+    const int blocks = p.B * p.Hq > 0 ? p.B * p.Hq : 1;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = make_cfg(dim3(blocks), dim3(32 * kMergeWarps), s, attr, pdl);
     if (d == 128)

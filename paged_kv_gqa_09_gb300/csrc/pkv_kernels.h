@@ -78,8 +78,10 @@ cudaError_t launch_decode(int d, int mode, const CUtensorMap &tk, const CUtensor
 cudaError_t launch_merge(int d, const MergeParams &p, cudaStream_t s, bool pdl);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s, bool pdl);
 
-// Dynamic shared memory a decode CTA uses for head dim d.
+// Dynamic shared memory a decode CTA uses for head dim d, and how many such
+// CTAs an SM holds.
 int decode_smem_bytes(int d);
+cudaError_t decode_ctas_per_sm(int d, int *out);
 
 // Set the calling thread's pkv_last_error_string() and return `code`.
 int record_error(int code, const char *msg);
