@@ -143,6 +143,29 @@ __device__ __forceinline__ uint32_t row_base(int t, int btl)
 
 // ---------------------------------------------------------------- producer
 
+// Block-table entries of pages [s0, s0 + kSeg) of row i, clipped to pg_end:
+// lane l holds pages s0 + l + 32 r in pid[r].  An entry outside
+// [0, num_pages) is reported and replaced by num_pages, an out-of-range page
+// coordinate that TMA fills with zeros.
+__device__ __forceinline__ void load_pages(const DecodeParams &p, int i, int s0, int pg_end, int lane,
+                                           int (&pid)[kSegRegs])
+{
+    const int64_t row_off = (int64_t)i * p.bt_stride;
+#pragma unroll
+    for (int r = 0; r < kSegRegs; ++r) {
+        const int pp = s0 + lane + 32 * r;
+        pid[r] = pp < pg_end ? p.bt[row_off + pp] : 0;
+    }
+#pragma unroll
+    for (int r = 0; r < kSegRegs; ++r) {
+        const int pp = s0 + lane + 32 * r;
+        if (pp < pg_end && (pid[r] < 0 || pid[r] >= p.num_pages)) {
+            report_error(p.ws, kErrBadPage, i, pp, pid[r]);
+            pid[r] = p.num_pages;
+        }
+    }
+}
+
 template <int D, int MODE>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUtensorMap *tmV,
                                              const DecodeParams &p, int ntasks, uint32_t sbase,
@@ -157,24 +180,36 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
     const int nloc = ntasks > (int)blockIdx.x ? (ntasks - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int G = p.G;
 
-    auto task_of = [&](int t) { return load_task<MODE>(p, (int)blockIdx.x + t * (int)gridDim.x, ntasks); };
-    TaskInfo wa = task_of(lane < nloc ? lane : nloc), wb = task_of(32 + lane < nloc ? 32 + lane : nloc);
-    if (lane >= nloc)
-        wa = TaskInfo{0, 0, 0, 0, 0};
-    if (32 + lane >= nloc)
-        wb = TaskInfo{0, 0, 0, 0, 0};
+    // task infos of this CTA's local tasks t, lane-held in windows of 32
+    auto task_of = [&](int t) {
+        return t < nloc ? load_task<MODE>(p, (int)blockIdx.x + t * (int)gridDim.x, ntasks)
+                        : TaskInfo{0, 0, 0, 0, 0};
+    };
+    TaskInfo wa = task_of(lane), wb = task_of(32 + lane);
+    auto seg_end = [&](const TaskInfo &ti) { return ((ti.t1 - 1) >> log2P) + 1; };
+
+    int pid[kSegRegs], pnx[kSegRegs];
+    TaskInfo cur = shfl_task(wa, 0);
+    if (nloc > 0 && cur.t0 < cur.t1)
+        load_pages(p, cur.i, cur.t0 >> log2P, min(seg_end(cur), (cur.t0 >> log2P) + kSeg), lane, pid);
 
     int stage = 0;
-    uint32_t ph = 0;               // lap parity of the ring
+    uint32_t ph = 0;                  // lap parity of the ring
     uint32_t pend = 0, pend_par = 0;  // stages with copies in flight, and their parity
     bool ok = true;
 
     for (int t = 0; t < nloc && ok; ++t) {
         if (t > 0 && (t & 31) == 0) {
             wa = wb;
-            wb = (t + 32 + lane < nloc) ? task_of(t + 32 + lane) : TaskInfo{0, 0, 0, 0, 0};
+            wb = task_of(t + 32 + lane);
         }
-        const TaskInfo cur = shfl_task(wa, t & 31);
+        // the next task's first block-table entries load while this one streams
+        const int tn = t + 1;
+        const TaskInfo nxt = shfl_task(((tn & 31) != 0) ? wa : wb, tn & 31);
+        const bool nxt_live = tn < nloc && nxt.t0 < nxt.t1;
+        if (nxt_live)
+            load_pages(p, nxt.i, nxt.t0 >> log2P, min(seg_end(nxt), (nxt.t0 >> log2P) + kSeg), lane, pnx);
+
         if (cur.t0 >= cur.t1) {
             // empty task: neutral state (split modes) or o = 0, lse = -inf (single)
             if (MODE == kModeSingle) {
@@ -191,83 +226,68 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                     p.part_l[cur.sbase + lane] = 0.f;
                 }
             }
-            continue;
-        }
-        const int64_t row_off = (int64_t)cur.i * p.bt_stride;
-        const int pg_end = ((cur.t1 - 1) >> log2P) + 1;
-        for (int s0 = cur.t0 >> log2P; s0 < pg_end && ok; s0 += kSeg) {
-            int pid[kSegRegs];
-#pragma unroll
-            for (int r = 0; r < kSegRegs; ++r) {
-                const int pp = s0 + lane + 32 * r;
-                int v = 0;
-                if (pp < pg_end) {
-                    v = p.bt[row_off + pp];
-                    if (v < 0 || v >= p.num_pages) {
-                        report_error(p.ws, kErrBadPage, cur.i, pp, v);
-                        v = p.num_pages;  // out-of-range coordinate: TMA fills zeros
+        } else {
+            const int pg_end = seg_end(cur);
+            for (int s0 = cur.t0 >> log2P; s0 < pg_end && ok; s0 += kSeg) {
+                if (s0 != (cur.t0 >> log2P))  // later segments of long single-pass rows
+                    load_pages(p, cur.i, s0, min(pg_end, s0 + kSeg), lane, pid);
+                const int ts = max(cur.t0, s0 << log2P);
+                const int te = min(cur.t1, (s0 + kSeg) << log2P);
+                for (int tt = ts; tt < te; tt += kTile) {
+                    const int nv = min(kTile, te - tt);
+                    const int flags = nv | (tt == cur.t0 ? kFirst : 0) | (tt + nv >= cur.t1 ? kLast : 0);
+                    const uint32_t full = bar_full0 + stage * 8, empty = bar_empty0 + stage * 8;
+                    if (!__all_sync(0xffffffffu, mbar_wait(empty, ph ^ 1, kWaitNs))) {
+                        report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 0);
+                        ok = false;
+                        break;
                     }
-                }
-                pid[r] = v;
-            }
-            const int ts = max(cur.t0, s0 << log2P);
-            const int te = min(cur.t1, (s0 + kSeg) << log2P);
-            for (int tt = ts; tt < te; tt += kTile) {
-                const int nv = min(kTile, te - tt);
-                const int flags = nv | (tt == cur.t0 ? kFirst : 0) | (tt + nv >= cur.t1 ? kLast : 0);
-                const uint32_t full = bar_full0 + stage * 8, empty = bar_empty0 + stage * 8;
-                bool got = true;
-                if (lane == 0)
-                    got = mbar_wait(empty, ph ^ 1, kWaitNs);
-                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-                if (!got) {
-                    report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 0);
-                    ok = false;
-                    break;
-                }
-                pend &= ~(1u << stage);
-                const int nb = (nv + (1 << btl) - 1) >> btl;
-                const uint32_t kdst = sbase + stage * L::kStageBytes;
-                const uint32_t vdst = kdst + L::kTileBytes;
-                if (lane == 0) {
-                    meta[stage] = make_int4(cur.i, cur.g, cur.sbase, flags);
-                    const uint32_t bytes = 2u * nb * box_bytes + ((flags & kFirst) ? (uint32_t)(G * D * 2) : 0u);
-                    mbar_arrive_expect_tx(full, bytes);
-                }
-                for (int b = 0; b < nb; ++b) {
-                    const int tok = tt + (b << btl);
-                    const int rel = (tok >> log2P) - s0;
-                    int pg = pid[0];
-#pragma unroll
-                    for (int r = 1; r < kSegRegs; ++r)
-                        if ((rel >> 5) == r)
-                            pg = pid[r];
-                    pg = __shfl_sync(0xffffffffu, pg, rel & 31);
+                    pend &= ~(1u << stage);
+                    const int nb = (nv + (1 << btl) - 1) >> btl;
+                    const uint32_t kdst = sbase + stage * L::kStageBytes;
+                    const uint32_t vdst = kdst + L::kTileBytes;
                     if (lane == 0) {
-                        const int slot = tok & ((1 << log2P) - 1);
+                        meta[stage] = make_int4(cur.i, cur.g, cur.sbase, flags);
+                        const uint32_t bytes =
+                            2u * nb * box_bytes + ((flags & kFirst) ? (uint32_t)(G * D * 2) : 0u);
+                        mbar_arrive_expect_tx(full, bytes);
+                        if (flags & kFirst)
+                            bulk_load(kdst + 2 * L::kTileBytes,
+                                      p.q + ((size_t)cur.i * p.Hq + (size_t)cur.g * G) * D,
+                                      (uint32_t)(G * D * 2), full);
+                    }
+                    __syncwarp();
+                    // box b of the tile is page rel0 + b of the segment; the lane
+                    // holding that page's entry issues its K and V copies
+                    const int rel0 = (tt >> log2P) - s0;
+                    const int b = (lane - rel0) & 31;
+                    if (b < nb) {
+                        int pg = pid[0];
+#pragma unroll
+                        for (int r = 1; r < kSegRegs; ++r)
+                            if ((rel0 >> 5) == r)
+                                pg = pid[r];
+                        const int slot = (tt + (b << btl)) & ((1 << log2P) - 1);
                         tma_load_5d(kdst + b * box_bytes, tmK, full, 0, slot, 0, cur.g, pg, pol);
                         tma_load_5d(vdst + b * box_bytes, tmV, full, 0, slot, 0, cur.g, pg, pol);
                     }
-                }
-                if ((flags & kFirst) && lane == 0)
-                    bulk_load(kdst + 2 * L::kTileBytes, p.q + ((size_t)cur.i * p.Hq + (size_t)cur.g * G) * D,
-                              (uint32_t)(G * D * 2), full);
-                pend |= 1u << stage;
-                pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
-                if (++stage == L::kStages) {
-                    stage = 0;
-                    ph ^= 1;
+                    pend |= 1u << stage;
+                    pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
+                    if (++stage == L::kStages) {
+                        stage = 0;
+                        ph ^= 1;
+                    }
                 }
             }
         }
+        cur = nxt;
+#pragma unroll
+        for (int r = 0; r < kSegRegs; ++r)
+            pid[r] = pnx[r];
     }
     if (ok) {
         // end-of-work sentinel
-        bool got = true;
-        if (lane == 0)
-            got = mbar_wait(bar_empty0 + stage * 8, ph ^ 1, kWaitNs);
-        got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-        if (got) {
+        if (__all_sync(0xffffffffu, mbar_wait(bar_empty0 + stage * 8, ph ^ 1, kWaitNs))) {
             pend &= ~(1u << stage);
             if (lane == 0) {
                 meta[stage] = make_int4(0, 0, 0, kEnd);
