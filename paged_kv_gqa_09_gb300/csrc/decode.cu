@@ -147,8 +147,8 @@ __device__ __forceinline__ uint32_t row_base(int t, int btl)
 // lane l holds pages s0 + l + 32 r in pid[r].  An entry outside
 // [0, num_pages) is reported and replaced by num_pages, an out-of-range page
 // coordinate that TMA fills with zeros.
-__device__ __forceinline__ void load_pages(const DecodeParams &p, int i, int s0, int pg_end, int lane,
-                                           int (&pid)[kSegRegs])
+__device__ __forceinline__ void fetch_pages(const DecodeParams &p, int i, int s0, int pg_end, int lane,
+                                            int (&pid)[kSegRegs])
 {
     const int64_t row_off = (int64_t)i * p.bt_stride;
 #pragma unroll
@@ -156,6 +156,11 @@ __device__ __forceinline__ void load_pages(const DecodeParams &p, int i, int s0,
         const int pp = s0 + lane + 32 * r;
         pid[r] = pp < pg_end ? p.bt[row_off + pp] : 0;
     }
+}
+
+__device__ __forceinline__ void check_pages(const DecodeParams &p, int i, int s0, int pg_end, int lane,
+                                            int (&pid)[kSegRegs])
+{
 #pragma unroll
     for (int r = 0; r < kSegRegs; ++r) {
         const int pp = s0 + lane + 32 * r;
@@ -164,6 +169,13 @@ __device__ __forceinline__ void load_pages(const DecodeParams &p, int i, int s0,
             pid[r] = p.num_pages;
         }
     }
+}
+
+__device__ __forceinline__ void load_pages(const DecodeParams &p, int i, int s0, int pg_end, int lane,
+                                           int (&pid)[kSegRegs])
+{
+    fetch_pages(p, i, s0, pg_end, lane, pid);
+    check_pages(p, i, s0, pg_end, lane, pid);
 }
 
 template <int D, int MODE>
@@ -185,13 +197,32 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
         return t < nloc ? load_task<MODE>(p, (int)blockIdx.x + t * (int)gridDim.x, ntasks)
                         : TaskInfo{0, 0, 0, 0, 0};
     };
-    TaskInfo wa = task_of(lane), wb = task_of(32 + lane);
     auto seg_end = [&](const TaskInfo &ti) { return ((ti.t1 - 1) >> log2P) + 1; };
-
     int pid[kSegRegs], pnx[kSegRegs];
+    // The first task's block-table entries are fetched before its length is
+    // known (the widest range the task can cover, clipped to the row), so
+    // the two loads overlap; only entries below the row end are checked.
+    if (nloc > 0) {
+        int i0, j0;
+        if (MODE == kModeQueue) {
+            const int4 r = p.tasks[blockIdx.x];
+            i0 = r.x;
+            j0 = r.z;
+        } else if (MODE == kModeRect) {
+            i0 = (int)blockIdx.x / (p.Hkv * p.S_b);
+            j0 = (int)blockIdx.x % p.S_b;
+        } else {
+            i0 = (int)blockIdx.x / p.Hkv;
+            j0 = 0;
+        }
+        const int s00 = MODE == kModeSingle ? 0 : (j0 * p.C) >> log2P;
+        const int span = MODE == kModeSingle ? kSeg : min(kSeg, p.C >> log2P);
+        fetch_pages(p, i0, s00, min(p.bt_stride, s00 + span), lane, pid);
+    }
+    TaskInfo wa = task_of(lane), wb = task_of(32 + lane);
     TaskInfo cur = shfl_task(wa, 0);
     if (nloc > 0 && cur.t0 < cur.t1)
-        load_pages(p, cur.i, cur.t0 >> log2P, min(seg_end(cur), (cur.t0 >> log2P) + kSeg), lane, pid);
+        check_pages(p, cur.i, cur.t0 >> log2P, min(seg_end(cur), (cur.t0 >> log2P) + kSeg), lane, pid);
 
     int stage = 0;
     uint32_t ph = 0;                  // lap parity of the ring

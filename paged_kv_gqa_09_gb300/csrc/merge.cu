@@ -57,54 +57,59 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
         }
         return;
     }
-    // M = max_j m_j over the row's states
-    float M = -INFINITY;
-    for (int j = threadIdx.x; j < n; j += 32 * kMergeWarps)
-        M = fmaxf(M, p.part_m[(base + j) * p.Hq + h]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (lane == 0)
-        s_max[warp] = M;
-    __syncthreads();
-#pragma unroll
-    for (int w2 = 0; w2 < kMergeWarps; ++w2)
-        M = fmaxf(M, s_max[w2]);
-    // this warp's share of L and acc
-    float L = 0.f, acc[VPL];
+    // warp w folds states j = w, w+4, ... with its own running maximum, all
+    // of its loads in flight together; the four warp results are then
+    // rescaled to the common maximum (exact: every term keeps its e^{m_j - M})
+    float Mw = -INFINITY, L = 0.f, acc[VPL];
 #pragma unroll
     for (int v = 0; v < VPL; ++v)
         acc[v] = 0.f;
 #pragma unroll 8
     for (int j = warp; j < n; j += kMergeWarps) {
         const int64_t slot = (base + j) * p.Hq + h;
-        const float w = ex2((p.part_m[slot] - M) * kLog2e);
-        L += p.part_l[slot] * w;
+        const float mj = p.part_m[slot];
+        const float lj = p.part_l[slot];
         const float *a = p.part_acc + slot * D + lane * VPL;
+        float x[VPL];
         if constexpr (VPL == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(a);
-            acc[0] += w * x.x;
-            acc[1] += w * x.y;
-            acc[2] += w * x.z;
-            acc[3] += w * x.w;
+            const float4 t = *reinterpret_cast<const float4 *>(a);
+            x[0] = t.x;
+            x[1] = t.y;
+            x[2] = t.z;
+            x[3] = t.w;
         } else {
-            const float2 x = *reinterpret_cast<const float2 *>(a);
-            acc[0] += w * x.x;
-            acc[1] += w * x.y;
+            const float2 t = *reinterpret_cast<const float2 *>(a);
+            x[0] = t.x;
+            x[1] = t.y;
         }
+        const float mn = fmaxf(Mw, mj);
+        const float so = ex2((Mw - mn) * kLog2e), sj = ex2((mj - mn) * kLog2e);
+        L = L * so + lj * sj;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v)
+            acc[v] = acc[v] * so + x[v] * sj;
+        Mw = mn;
+    }
+    if (lane == 0) {
+        s_max[warp] = Mw;
+        s_l[warp] = L;
     }
 #pragma unroll
     for (int v = 0; v < VPL; ++v)
         s_acc[warp][lane * VPL + v] = acc[v];
-    if (lane == 0)
-        s_l[warp] = L;
     __syncthreads();
     if (warp != 0)
         return;
-    float Lt = 0.f;
+    float M = -INFINITY;
 #pragma unroll
     for (int w2 = 0; w2 < kMergeWarps; ++w2)
-        Lt += s_l[w2];
+        M = fmaxf(M, s_max[w2]);
+    float sc[kMergeWarps], Lt = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < kMergeWarps; ++w2) {
+        sc[w2] = ex2((s_max[w2] - M) * kLog2e);  // 0 for a warp that saw no state
+        Lt += s_l[w2] * sc[w2];
+    }
     const float inv = 1.f / Lt;
     float o[VPL];
 #pragma unroll
@@ -112,7 +117,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
         float t = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < kMergeWarps; ++w2)
-            t += s_acc[w2][lane * VPL + v];
+            t += s_acc[w2][lane * VPL + v] * sc[w2];
         o[v] = t * inv;
     }
     __half *out = p.o + (size_t)wg * D + lane * VPL;
