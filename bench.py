@@ -326,8 +326,8 @@ def run_pkv(args, rank, local, ws, pg):
     forced = {"bucketed": 0, "workqueue": 1, "single": 2}.get(args.path)
     if forced is not None:
         path = forced
-    if path != 2:
-        C = tr.split_tokens
+    if path != 2 and tr.path_hint != "policy":
+        C = tr.split_tokens  # the workload fixes its split size (S splits)
     n_max_run = tr.n_max + (tr.steps if appends else 0)
     bucket = n_max_run if path == 0 else 0
     cfg = api.make_cfg(path, C, bucket)

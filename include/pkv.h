@@ -203,13 +203,18 @@ int pkv_decode_step_noalloc(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg,
 /* Thresholds of the calibrated policy (Methodology 2).  The pages route
  * B = 1 long-context to the length-bucketed split, B >= 8 long-context to the
  * compact workqueue and everything else (including B = 4) to a single-kernel
- * path; "long context" and the batch cut-offs are calibrated. */
+ * path; what counts as "long" and the batch cut-offs are calibrated.  Here
+ * each split route has its own long-context cut-off:
+ *   B <= bucketed_max_batch  and N_max >= bucketed_min_tokens  -> BUCKETED_SPLIT
+ *   else B >= workqueue_min_batch and N_max >= workqueue_min_tokens -> WORKQUEUE
+ *   else SINGLE_PASS. */
 typedef struct {
-    int32_t long_context_tokens;  /* N_max at or above this is "long context" */
-    int32_t bucketed_max_batch;   /* B <= this (and long) -> BUCKETED_SPLIT */
-    int32_t workqueue_min_batch;  /* B >= this (and long) -> WORKQUEUE */
-    int32_t split_tokens;         /* C handed to the split paths */
-    int32_t bucketed_split_tokens;/* C for BUCKETED_SPLIT (0 = split_tokens) */
+    int32_t bucketed_min_tokens;   /* long-context cut-off of the bucketed route */
+    int32_t bucketed_max_batch;    /* largest B routed to BUCKETED_SPLIT */
+    int32_t workqueue_min_tokens;  /* long-context cut-off of the workqueue route */
+    int32_t workqueue_min_batch;   /* smallest B routed to WORKQUEUE */
+    int32_t split_tokens;          /* C handed to WORKQUEUE */
+    int32_t bucketed_split_tokens; /* C handed to BUCKETED_SPLIT */
 } pkv_policy_cfg_t;
 
 /* Fill `cfg` with the thresholds calibrated on GB300 (calibration seed

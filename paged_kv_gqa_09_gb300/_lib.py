@@ -64,9 +64,9 @@ class PlanCfg(ctypes.Structure):
 
 
 class PolicyCfg(ctypes.Structure):
-    _fields_ = [("long_context_tokens", ctypes.c_int32), ("bucketed_max_batch", ctypes.c_int32),
-                ("workqueue_min_batch", ctypes.c_int32), ("split_tokens", ctypes.c_int32),
-                ("bucketed_split_tokens", ctypes.c_int32)]
+    _fields_ = [("bucketed_min_tokens", ctypes.c_int32), ("bucketed_max_batch", ctypes.c_int32),
+                ("workqueue_min_tokens", ctypes.c_int32), ("workqueue_min_batch", ctypes.c_int32),
+                ("split_tokens", ctypes.c_int32), ("bucketed_split_tokens", ctypes.c_int32)]
 
 
 class Counters(ctypes.Structure):

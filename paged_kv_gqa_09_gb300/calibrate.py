@@ -1,0 +1,192 @@
+"""Calibrate pkv_policy's thresholds on the current GPU.
+
+"PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM Serving on
+Commodity GPUs", technical summary, Methodology 2 (a hand-calibrated policy
+choosing the route by batch size B and the longest context N_max) and Results
+(thresholds fixed on calibration seed 20260622, reported on held-out seed
+20260623).
+
+Procedure:
+1. For every trace of a grid -- families bucketed / bimodal / uniform / Zipf,
+   B in {1..64}, N_max in {256..32768}, Hq=32, Hkv=8, d=128, page_size 16 --
+   time every route (bucketed split and workqueue at several split sizes C,
+   single pass) as synchronized wall-clock per decode step through the C ABI
+   (host planning and launches included, as the pages measure).
+2. Search the policy parameters (two long-context cut-offs, two batch cut-offs,
+   one C per split route) minimising the mean ratio of the chosen route's time
+   to the best route's time over the calibration traces.
+3. Re-time the same grid drawn with the held-out seed and report the chosen
+   policy's regret there.
+
+Usage (GPU):  python -m paged_kv_gqa_09_gb300.calibrate --out result.json
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import itertools
+import json
+import math
+import sys
+import time
+
+import numpy as np
+
+import pkv_traces as T
+
+HQ, HKV, D, P = 32, 8, 128, 16
+BATCHES = [1, 2, 4, 8, 16, 32, 64]
+NMAX = [256, 512, 1024, 2048, 4096, 8192, 16384, 32768]
+FAMILIES = ["bucketed", "bimodal", "uniform", "zipf"]
+BUCKETED_C = [128, 256, 512, 1024, 2048]
+WORKQUEUE_C = [256, 512, 1024, 2048]
+TOKEN_CUTS = [0, 256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 1 << 30]
+BATCH_CUTS_MAX = [0, 1, 2, 4, 8, 16, 32, 64]
+BATCH_CUTS_MIN = [1, 2, 4, 8, 16, 32, 64, 1 << 30]
+
+
+def lengths(family: str, B: int, n_max: int, rng: np.random.Generator) -> np.ndarray:
+    if family == "bucketed":
+        n = np.full(B, n_max)
+    elif family == "bimodal":
+        short = rng.integers(max(1, n_max // 16), max(1, n_max // 4), size=B // 2, endpoint=True)
+        long_ = rng.integers(3 * n_max // 4, n_max, size=B - B // 2, endpoint=True)
+        n = rng.permutation(np.concatenate([short, long_]))
+    elif family == "uniform":
+        n = rng.integers(max(1, n_max // 8), n_max, size=B, endpoint=True)
+    else:
+        n = T.zipf_lengths(rng, B, lo=16, hi=max(16, n_max))
+    n = np.asarray(n, dtype=np.int32)
+    n[np.argmax(n)] = n_max  # the longest row is N_max
+    return n
+
+
+def routes():
+    out = [("bucketed", c) for c in BUCKETED_C] + [("workqueue", c) for c in WORKQUEUE_C]
+    return out + [("single", 0)]
+
+
+def measure(seed: int, reps: int = 7, warm: int = 2, log=print):
+    import torch
+
+    from paged_kv_gqa_09_gb300 import _lib, api
+
+    L = _lib.load()
+    dev = torch.device("cuda")
+    max_pages = max(BATCHES) * max(NMAX) // P + 1024
+    k = torch.randn((max_pages, P, HKV, D), dtype=torch.float16, device=dev)
+    v = torch.randn_like(k)
+    rng = np.random.default_rng([seed, 77])
+    results = []
+    stream = torch.cuda.current_stream().cuda_stream
+    for fam, B, n_max in itertools.product(FAMILIES, BATCHES, NMAX):
+        lens = lengths(fam, B, n_max, rng)
+        npg = (lens + P - 1) // P
+        stride = int(npg.max())
+        pages = rng.permutation(max_pages)[: int(npg.sum())]
+        bt = np.full((B, stride), -1, np.int32)
+        pos = 0
+        for i in range(B):
+            bt[i, : npg[i]] = pages[pos: pos + npg[i]]
+            pos += npg[i]
+        q = torch.randn((B, HQ, D), dtype=torch.float16, device=dev)
+        btd = torch.from_numpy(bt).to(dev)
+        sld = torch.from_numpy(lens).to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, HQ), dtype=torch.float32, device=dev)
+        shape = _lib.Shape(B, HQ, HKV, D, P, max_pages, stride, 1.0 / math.sqrt(D))
+        times = {}
+        for name, C in routes():
+            path = {"bucketed": 0, "workqueue": 1, "single": 2}[name]
+            cfg = api.make_cfg(path, C if C else 1024, n_max if path == 0 else 0)
+            ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device=dev)
+            npart = api.pkv_partials_size(shape, cfg)
+            part = torch.empty(max(4, npart // 4), dtype=torch.float32, device=dev)
+            args = (ctypes.byref(shape), ctypes.byref(cfg), ws.data_ptr(), q.data_ptr(), k.data_ptr(),
+                    v.data_ptr(), btd.data_ptr(), sld.data_ptr(), part.data_ptr() if npart else None,
+                    o.data_ptr(), lse.data_ptr(), stream)
+            ts = []
+            for r in range(warm + reps):
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                rc = L.pkv_decode_step(*args)
+                torch.cuda.synchronize()
+                t1 = time.perf_counter()
+                if rc != 0:
+                    raise RuntimeError(_lib.last_error())
+                if r >= warm:
+                    ts.append(t1 - t0)
+            st, msg = api.pkv_get_error(ws)
+            if st != 0:
+                raise RuntimeError(msg)
+            times[f"{name}:{C}"] = float(np.median(ts)) * 1e6
+        results.append({"family": fam, "B": B, "n_max": n_max,
+                        "kv_bytes": int(lens.astype(np.int64).sum()) * HKV * D * 4, "us": times})
+        best = min(times, key=times.get)
+        log(f"{fam:9s} B={B:3d} Nmax={n_max:6d}: best {best:15s} {times[best]:8.1f} us")
+    return results
+
+
+def choose(params, B, n_max):
+    bmin_tok, bmax_b, wmin_tok, wmin_b, c_wq, c_b = params
+    if 1 <= B <= bmax_b and n_max >= bmin_tok:
+        return f"bucketed:{c_b}"
+    if B >= wmin_b and n_max >= wmin_tok:
+        return f"workqueue:{c_wq}"
+    return "single:0"
+
+
+def regret(params, results):
+    r = [res["us"][choose(params, res["B"], res["n_max"])] / min(res["us"].values()) for res in results]
+    return float(np.mean(r)), float(np.max(r))
+
+
+def fit(results):
+    names = [f"{n}:{c}" for n, c in routes()]
+    tmat = np.array([[res["us"][k] for k in names] for res in results])
+    best = tmat.min(axis=1)
+    Bv = np.array([res["B"] for res in results])
+    Nv = np.array([res["n_max"] for res in results])
+    col = {k: i for i, k in enumerate(names)}
+    best_params, best_score = None, math.inf
+    for bmin_tok, bmax_b, wmin_tok, wmin_b in itertools.product(TOKEN_CUTS, BATCH_CUTS_MAX,
+                                                                TOKEN_CUTS, BATCH_CUTS_MIN):
+        is_b = (Bv >= 1) & (Bv <= bmax_b) & (Nv >= bmin_tok)
+        is_w = ~is_b & (Bv >= wmin_b) & (Nv >= wmin_tok)
+        single = tmat[:, col["single:0"]]
+        for c_wq in WORKQUEUE_C:
+            wq = tmat[:, col[f"workqueue:{c_wq}"]]
+            for c_b in BUCKETED_C:
+                bk = tmat[:, col[f"bucketed:{c_b}"]]
+                chosen = np.where(is_b, bk, np.where(is_w, wq, single))
+                score = float(np.mean(chosen / best))
+                if score < best_score - 1e-12:
+                    best_score = score
+                    best_params = (bmin_tok, bmax_b, wmin_tok, wmin_b, c_wq, c_b)
+    return best_params, best_score
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default="policy_calibration.json")
+    ap.add_argument("--reps", type=int, default=7)
+    a = ap.parse_args(argv)
+    cal = measure(T.CALIBRATION_SEED, a.reps)
+    params, score = fit(cal)
+    held = measure(T.HELDOUT_SEED, a.reps)
+    pages_default = (4096, 1, 4096, 8, 1024, 1024)  # the pages' routing, RTX 3060-era cut-offs
+    out = {
+        "params": dict(zip(["bucketed_min_tokens", "bucketed_max_batch", "workqueue_min_tokens",
+                            "workqueue_min_batch", "split_tokens", "bucketed_split_tokens"], params)),
+        "calibration_mean_regret": score,
+        "heldout_mean_max_regret": regret(params, held),
+        "pages_structure_default_heldout_regret": regret(pages_default, held),
+        "calibration": cal, "heldout": held,
+    }
+    json.dump(out, open(a.out, "w"), indent=1)
+    print(json.dumps({k: out[k] for k in list(out)[:4]}))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

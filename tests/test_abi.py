@@ -112,24 +112,26 @@ def test_workspace_and_partial_sizes(L):
     assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(one)) == 0
 
 
-def test_policy_follows_the_pages_routing(L):
-    """Methodology 2: B=1 long -> bucketed split, B>=8 long -> workqueue, B=4 and
-    everything else -> the single-kernel route."""
-    d = api.pkv_policy_default()
-    long_n = d.long_context_tokens
+def test_policy_routes_by_batch_and_length(L):
+    """Methodology 2: by (B, N_max) to the bucketed split, the workqueue or the
+    single-kernel route, with calibrated cut-offs."""
     P = _lib
-    assert api.pkv_policy(1, long_n)[0] == P.PKV_PATH_BUCKETED_SPLIT
-    assert api.pkv_policy(8, long_n)[0] == P.PKV_PATH_WORKQUEUE
-    assert api.pkv_policy(64, 10 * long_n)[0] == P.PKV_PATH_WORKQUEUE
-    assert api.pkv_policy(4, 10 * long_n)[0] in (P.PKV_PATH_SINGLE_PASS, P.PKV_PATH_WORKQUEUE)
-    assert api.pkv_policy(1, max(1, long_n // 4))[0] == P.PKV_PATH_SINGLE_PASS
-    custom = _lib.PolicyCfg(1000, 1, 8, 512, 256)
+    custom = _lib.PolicyCfg(1000, 1, 2000, 8, 512, 256)
     assert api.pkv_policy(1, 1000, custom) == (P.PKV_PATH_BUCKETED_SPLIT, 256)
-    assert api.pkv_policy(9, 1000, custom) == (P.PKV_PATH_WORKQUEUE, 512)
-    assert api.pkv_policy(4, 1000, custom)[0] == P.PKV_PATH_SINGLE_PASS
-    assert api.pkv_policy(9, 999, custom)[0] == P.PKV_PATH_SINGLE_PASS
+    assert api.pkv_policy(1, 999, custom)[0] == P.PKV_PATH_SINGLE_PASS
+    assert api.pkv_policy(9, 2000, custom) == (P.PKV_PATH_WORKQUEUE, 512)
+    assert api.pkv_policy(9, 1999, custom)[0] == P.PKV_PATH_SINGLE_PASS
+    assert api.pkv_policy(4, 10 ** 6, custom)[0] == P.PKV_PATH_SINGLE_PASS   # the pages' B=4 gap
+    assert api.pkv_policy(0, 10 ** 6, custom)[0] == P.PKV_PATH_SINGLE_PASS   # empty batch
+    d = api.pkv_policy_default()
+    assert d.split_tokens > 0 and d.bucketed_split_tokens > 0
+    path, C = api.pkv_policy(1, 32768)
+    assert path == P.PKV_PATH_BUCKETED_SPLIT and C == d.bucketed_split_tokens
+    assert api.pkv_policy(64, 65536)[0] == P.PKV_PATH_WORKQUEUE
     with pytest.raises(_lib.PkvError):
         api.pkv_policy(-1, 5)
+    with pytest.raises(_lib.PkvError):
+        api.pkv_policy(1, 5, _lib.PolicyCfg(0, 1, 0, 8, 0, 256))
 
 
 @pytest.mark.parametrize("cfg_id", [1, 2, 3, 4, 5])
