@@ -25,6 +25,7 @@ on the data path); value sums the ranks' bytes over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -320,10 +321,13 @@ def run_pkv(args, rank, local, ws, pg):
     sl_init = sl.clone()
     shape = api.make_shape(q, k0, bt)
 
-    # ---- path: the policy's route unless forced
+    # ---- path: the one the workload names, else the policy's route (or --path)
     pol = api.pkv_policy_default()
     path, C = api.pkv_policy(tr.B, tr.n_max + (tr.steps if tr.steps > 1 else 0), pol)
-    forced = {"bucketed": 0, "workqueue": 1, "single": 2}.get(args.path)
+    named = {"bucketed": 0, "workqueue": 1, "single": 2}
+    if tr.path_hint in named:
+        path = named[tr.path_hint]
+    forced = named.get(args.path)
     if forced is not None:
         path = forced
     if path != 2 and tr.path_hint != "policy":
@@ -494,54 +498,62 @@ def _ctypes_refs(shape, cfg):
 
 
 def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, wsb):
-    """Public-API steps with host buffers: H2D of q / seq_lens / block table from
-    pinned memory, PagedDecoder.step (policy + C ABI), D2H of o and lse, sync."""
+    """Public-API steps with host buffers (HostDecodeLoop -> pkv_decode_step_host):
+    every step copies q, the block table and the lengths in from pinned memory
+    (and, when the workload appends, the new K/V token), decodes, copies o and
+    lse out and synchronizes; timed on the wall clock."""
+    from paged_kv_gqa_09_gb300 import _lib
     R = len(pools)
+    n_max = int(tr.seq_lens.max()) + (tr.steps if appends else 0)
+    loops = [api.HostDecodeLoop(kk, vv, tr.B, tr.Hq, tr.bt_stride, n_max, path=path, split_tokens=C)
+             for kk, vv in pools]
     q_pin = torch.from_numpy(q_h).pin_memory()
-    sl_pin = torch.from_numpy(tr.seq_lens.copy()).pin_memory()
+    sl0 = torch.from_numpy(tr.seq_lens.copy())
+    sl_pin = sl0.clone().pin_memory()
     bt_pin = torch.from_numpy(tr.block_table).pin_memory()
-    o_pin = torch.empty(q_h.shape, dtype=torch.float16).pin_memory()
-    lse_pin = torch.empty(q_h.shape[:2], dtype=torch.float32).pin_memory()
-    q_d = torch.empty(q_h.shape, dtype=torch.float16, device=dev)
-    sl_d = torch.empty(tr.B, dtype=torch.int32, device=dev)
-    bt_d = torch.empty(tr.block_table.shape, dtype=torch.int32, device=dev)
-    o_d = torch.empty_like(q_d)
-    lse_d = torch.empty(q_h.shape[:2], dtype=torch.float32, device=dev)
-    dec = api.PagedDecoder()
+    kn_pin, vn_pin = kn.cpu().pin_memory(), vn.cpu().pin_memory()
     h2d = q_pin.numel() * 2 + sl_pin.numel() * 4 + bt_pin.numel() * 4
-    d2h = o_pin.numel() * 2 + lse_pin.numel() * 4
-    n_max = int(tr.seq_lens.max())
-    kvs = []
+    if appends:
+        h2d += (kn_pin.numel() + vn_pin.numel()) * 2
+    d2h = q_pin.numel() * 2 + q_pin.shape[0] * q_pin.shape[1] * 4
     steps = min(steps, 4000 if not appends else tr.steps - 4)
+    L = _lib.load()
+    stream = torch.cuda.current_stream(dev)
+    kv_total = [0]
 
     def one(s):
-        kk, vv = pools[s % R]
-        q_d.copy_(q_pin, non_blocking=True)
-        sl_d.copy_(sl_pin, non_blocking=True)
-        bt_d.copy_(bt_pin, non_blocking=True)
+        lp = loops[s % R]
         if appends:
-            ws = dec.workspace(dev)
-            api.pkv_append(api.make_shape(q_d, kk, bt_d), ws if ws is not None else wsb, kn, vn,
-                           bt_d, sl_d, kk, vv)
-            sl_pin.add_(1)
-        n = n_max + (s + 1 if appends else 0)
-        dec.step(q_d, kk, vv, bt_d, sl_d, n, path=path, split_tokens=C, o=o_d, lse=lse_d)
-        o_pin.copy_(o_d, non_blocking=True)
-        lse_pin.copy_(lse_d, non_blocking=True)
-        torch.cuda.current_stream(dev).synchronize()
-        kvs.append(int(sl_pin.numpy().astype(np.int64).sum()) * tr.Hkv * tr.d * 4)
+            # the new token's K/V come from the host too; the append kernel writes
+            # them into their pages and advances the device lengths
+            kn.copy_(kn_pin, non_blocking=True)
+            vn.copy_(vn_pin, non_blocking=True)
+            lp.sl.copy_(sl_pin, non_blocking=True)
+            rc = L.pkv_append(ctypes.byref(lp.shape), lp.ws.data_ptr(), kn.data_ptr(), vn.data_ptr(),
+                              lp.bt.data_ptr(), lp.sl.data_ptr(), lp.k.data_ptr(), lp.v.data_ptr(),
+                              stream.cuda_stream)
+            _lib.check(rc, "pkv_append")
+            lp.step(q_pin, bt_pin if s == 0 else None, None)
+            sl_pin.add_(1)  # after the synchronized step: the copy above has read it
+        else:
+            lp.step(q_pin, bt_pin, sl_pin)
+        kv_total[0] += int(sl_pin.numpy().astype(np.int64).sum()) * tr.Hkv * tr.d * 4
 
+    if appends:  # the append needs the block table on the device before the first step
+        for lp in loops:
+            lp.bt.copy_(bt_pin)
     for s in range(3):
         one(s)
-    sl_pin.copy_(torch.from_numpy(tr.seq_lens.copy()))
-    kvs.clear()
+    sl_pin.copy_(sl0)
+    kv_total[0] = 0
+    torch.cuda.synchronize()
     t0 = time.perf_counter()
     for s in range(steps):
         one(s)
     el = time.perf_counter() - t0
-    return {"value": sum(kvs) / el / 1e9, "unit": UNIT, "us_per_step": el / steps * 1e6,
+    return {"value": kv_total[0] / el / 1e9, "unit": UNIT, "us_per_step": el / steps * 1e6,
             "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "timing": "synchronized wall clock per step"}
+            "timing": "synchronized wall clock per step (pkv_decode_step_host)"}
 
 
 def main():

@@ -161,6 +161,22 @@ int pkv_decode_step(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d
                     const int32_t *d_block_table, const int32_t *d_seq_lens,
                     float *d_partials, void *d_o, float *d_lse, void *stream);
 
+/* pkv_decode_step_host -- one decode step with the step's inputs and outputs in
+ * host memory, for a serving loop that keeps the KV cache resident on the
+ * device: copies h_q into d_q (and, when non-NULL, h_block_table into
+ * d_block_table and h_seq_lens into d_seq_lens) on `stream`, runs
+ * pkv_decode_step, copies d_o into h_o (and d_lse into h_lse when both are
+ * non-NULL), then synchronizes `stream`.  One cudaMemcpyAsync per buffer; host
+ * buffers should be page-locked for the copies to run asynchronously.  All
+ * arguments are checked before anything is enqueued.  Same path semantics,
+ * layouts and errors as pkv_decode_step. */
+int pkv_decode_step_host(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
+                         float *d_partials, const void *h_q, void *d_q,
+                         const int32_t *h_block_table, int32_t *d_block_table,
+                         const int32_t *h_seq_lens, int32_t *d_seq_lens,
+                         const void *d_k_cache, const void *d_v_cache,
+                         void *d_o, void *h_o, float *d_lse, float *h_lse, void *stream);
+
 /* pkv_append -- write one new token per row into the paged cache.
  * (Not a step of the pages' method: the per-step KV write of a serving loop.)
  * One kernel launch.  For every row i with N = seq_lens[i]: copies

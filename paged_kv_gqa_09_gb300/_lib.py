@@ -35,7 +35,8 @@ STATUS_NAMES = {
 # every symbol include/pkv.h declares
 EXPORTS = [
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
-    "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc", "pkv_append", "pkv_policy_default", "pkv_policy",
+    "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc", "pkv_decode_step_host",
+    "pkv_append", "pkv_policy_default", "pkv_policy",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error",
     "pkv_last_error_string", "pkv_version",
 ]
@@ -113,6 +114,7 @@ def load() -> ctypes.CDLL:
             "pkv_single_pass": (ctypes.c_int, [S, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_decode_step": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_decode_step_noalloc": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "pkv_decode_step_host": (ctypes.c_int, [S, C] + [vp] * 15),
             "pkv_append": (ctypes.c_int, [S, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_policy_default": (None, [PC]),
             "pkv_policy": (ctypes.c_int, [i32, i32, PC, ctypes.POINTER(ctypes.c_int32),

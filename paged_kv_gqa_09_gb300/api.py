@@ -22,9 +22,10 @@ from ._lib import (PKV_PATH_BUCKETED_SPLIT, PKV_PATH_SINGLE_PASS, PKV_PATH_WORKQ
 __all__ = [
     "Shape", "PlanCfg", "PolicyCfg", "make_shape", "make_cfg",
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
-    "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc", "pkv_append", "pkv_policy", "pkv_policy_default",
+    "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc",
+    "pkv_decode_step_host", "pkv_append", "pkv_policy", "pkv_policy_default",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error", "pkv_version",
-    "PagedDecoder",
+    "PagedDecoder", "HostDecodeLoop",
 ]
 
 
@@ -162,6 +163,35 @@ def pkv_decode_step_noalloc(shape, cfg, q, k_cache, v_cache, block_table, seq_le
                                     _stream(stream)), "pkv_decode_step_noalloc")
 
 
+def _host(t: Optional[torch.Tensor], name: str, dtype: torch.dtype, nullable: bool = False) -> int:
+    if t is None:
+        if nullable:
+            return 0
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor")
+    return t.data_ptr()
+
+
+def pkv_decode_step_host(shape, cfg, ws, partials, h_q, q, h_block_table, block_table, h_seq_lens,
+                         seq_lens, k_cache, v_cache, o, h_o, lse=None, h_lse=None,
+                         stream=None) -> None:
+    """One synchronized decode step with host inputs/outputs (see include/pkv.h)."""
+    L = _lib.load()
+    part = _dev(partials, "partials", torch.float32, nullable=(cfg.path == PKV_PATH_SINGLE_PASS))
+    check(L.pkv_decode_step_host(
+        ctypes.byref(shape), ctypes.byref(cfg), _ws(ws), part, _host(h_q, "h_q", torch.float16),
+        _dev(q, "q", torch.float16), _host(h_block_table, "h_block_table", torch.int32, True),
+        _dev(block_table, "block_table", torch.int32),
+        _host(h_seq_lens, "h_seq_lens", torch.int32, True), _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(k_cache, "k_cache", torch.float16), _dev(v_cache, "v_cache", torch.float16),
+        _dev(o, "o", torch.float16), _host(h_o, "h_o", torch.float16),
+        _dev(lse, "lse", torch.float32, nullable=True), _host(h_lse, "h_lse", torch.float32, True),
+        _stream(stream)), "pkv_decode_step_host")
+
+
 def pkv_append(shape, ws, k_new, v_new, block_table, seq_lens, k_cache, v_cache,
                stream=None) -> None:
     L = _lib.load()
@@ -272,3 +302,58 @@ class PagedDecoder:
 
     def workspace(self, device) -> Optional[torch.Tensor]:
         return self._ws.get(device)
+
+
+class HostDecodeLoop:
+    """A serving loop whose per-step inputs (q, block table, lengths) and outputs
+    (o, lse) live in host memory while the KV cache stays on the device: one
+    pkv_decode_step_host call per step (copies in, decode, copies out, sync).
+
+    The shape and path are fixed at construction (policy route for the given
+    B and n_max unless `path` is given); device staging buffers, the workspace
+    and the partial-state buffer are allocated once; outputs land in pinned
+    host tensors `h_o` and `h_lse`, reused across steps.
+    """
+
+    def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, B: int, Hq: int, bt_stride: int,
+                 n_max: int, path: Optional[int] = None, split_tokens: Optional[int] = None,
+                 policy: Optional[PolicyCfg] = None, scale: Optional[float] = None,
+                 max_tasks: int = 0):
+        dev = k_cache.device
+        d = int(k_cache.shape[3])
+        self.q = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
+        self.bt = torch.empty((B, bt_stride), dtype=torch.int32, device=dev)
+        self.sl = torch.empty((B,), dtype=torch.int32, device=dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        self.h_o = torch.empty(self.q.shape, dtype=torch.float16).pin_memory()
+        self.h_lse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        self.shape = make_shape(self.q, k_cache, self.bt, scale)
+        p, c = pkv_policy(B, n_max, policy)
+        if path is not None:
+            p = path
+        if split_tokens is not None:
+            c = split_tokens
+        self.cfg = make_cfg(p, c, n_max if p == PKV_PATH_BUCKETED_SPLIT else 0,
+                            max_tasks if p == PKV_PATH_WORKQUEUE else 0)
+        self.ws = torch.zeros(pkv_plan_workspace_size(self.shape, self.cfg), dtype=torch.uint8, device=dev)
+        npart = pkv_partials_size(self.shape, self.cfg)
+        self.partials = torch.empty(max(npart // 4, 4), dtype=torch.float32, device=dev) if npart else None
+        self.k, self.v = k_cache, v_cache
+        self._fn = _lib.load().pkv_decode_step_host
+        self._refs = (ctypes.byref(self.shape), ctypes.byref(self.cfg))
+
+    def step(self, h_q: torch.Tensor, h_block_table: Optional[torch.Tensor] = None,
+             h_seq_lens: Optional[torch.Tensor] = None, stream=None):
+        """Run one synchronized step; returns the pinned host (o, lse)."""
+        st = _stream(stream)
+        rc = self._fn(self._refs[0], self._refs[1], self.ws.data_ptr(),
+                      self.partials.data_ptr() if self.partials is not None else None,
+                      h_q.data_ptr(), self.q.data_ptr(),
+                      h_block_table.data_ptr() if h_block_table is not None else None,
+                      self.bt.data_ptr(),
+                      h_seq_lens.data_ptr() if h_seq_lens is not None else None, self.sl.data_ptr(),
+                      self.k.data_ptr(), self.v.data_ptr(), self.o.data_ptr(), self.h_o.data_ptr(),
+                      self.lse.data_ptr(), self.h_lse.data_ptr(), st)
+        check(rc, "pkv_decode_step_host")
+        return self.h_o, self.h_lse

@@ -399,6 +399,46 @@ int pkv_decode_step(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, c
     return pkv_merge(s, c, d_ws, sl, part, o, lse, stream);
 }
 
+int pkv_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, float *part,
+                         const void *h_q, void *d_q, const int32_t *h_bt, int32_t *d_bt,
+                         const int32_t *h_sl, int32_t *d_sl, const void *k, const void *v, void *d_o,
+                         void *h_o, float *d_lse, float *h_lse, void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PKV_TRY(check_ptr(d_q, "q"));
+    PKV_TRY(check_ptr(k, "k_cache"));
+    PKV_TRY(check_ptr(v, "v_cache"));
+    PKV_TRY(check_ptr(d_bt, "block_table"));
+    PKV_TRY(check_ptr(d_sl, "seq_lens"));
+    PKV_TRY(check_ptr(d_o, "o"));
+    PKV_TRY(check_ptr(d_lse, "lse", true));
+    if (c->path != PKV_PATH_SINGLE_PASS)
+        PKV_TRY(check_ptr(part, "partials"));
+    if (!h_q || !h_o)
+        return fail(PKV_EINVAL, "host q and o are required");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t qbytes = (size_t)s->B * s->Hq * s->d * 2;
+    cudaError_t e = cudaMemcpyAsync(d_q, h_q, qbytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && h_bt)
+        e = cudaMemcpyAsync(d_bt, h_bt, (size_t)s->B * s->bt_stride * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && h_sl)
+        e = cudaMemcpyAsync(d_sl, h_sl, (size_t)s->B * 4, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "host-to-device copy");
+    PKV_TRY(pkv_decode_step(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, d_o, d_lse, stream));
+    e = cudaMemcpyAsync(h_o, d_o, qbytes, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && h_lse && d_lse)
+        e = cudaMemcpyAsync(h_lse, d_lse, (size_t)s->B * s->Hq * 4, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device-to-host copy");
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    return PKV_OK;
+}
+
 int pkv_append(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *v_new,
                const int32_t *bt, int32_t *sl, void *k_cache, void *v_cache, void *stream)
 {

@@ -339,3 +339,24 @@ def test_append_writes_the_next_slot():
         n = int(tr.seq_lens[i])
         mask[tr.block_table[i, n // 16], n % 16] = False
     assert np.array_equal(kc[mask].view(np.uint16), k[mask].view(np.uint16))
+
+
+# ------------------------------------------------------------------ host-buffer step
+
+@pytest.mark.parametrize("cfg_id,path", [(1, BUCKETED), (3, WORKQUEUE), (3, SINGLE)])
+def test_host_buffer_step_matches_oracle(cfg_id, path):
+    tr = T.make_trace(cfg_id)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    kd, vd = dev(k), dev(v)
+    loop = api.HostDecodeLoop(kd, vd, tr.B, tr.Hq, tr.bt_stride, tr.n_max, path=path,
+                              split_tokens=tr.split_tokens)
+    hq = torch.from_numpy(q).pin_memory()
+    hbt = torch.from_numpy(tr.block_table).pin_memory()
+    hsl = torch.from_numpy(tr.seq_lens).pin_memory()
+    oref, lref = oracle_out(tr, q, k, v)
+    for _ in range(2):
+        o, lse = loop.step(hq, hbt, hsl)
+        close(o, oref)
+        close_lse(lse, lref)
+    check_error_free(loop.ws)
