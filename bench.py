@@ -104,6 +104,12 @@ def reduce_max(pg, x: float) -> float:
     return float(t.item())
 
 
+def whole_job_gbs(kv_bytes_per_rank: int, ms_per_step_max: float, world: int) -> float:
+    """Replicas: every rank streams its own step; the job's throughput is all
+    ranks' bytes over the slowest rank's time per step."""
+    return kv_bytes_per_rank * world / (ms_per_step_max * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -447,7 +453,7 @@ def run_pkv(args, rank, local, ws, pg):
                       appends, kn, vn, wsb)
 
     gbs = kv_step / (ms * 1e-3) / 1e9
-    total = kv_step * ws / (ms_max * 1e-3) / 1e9
+    total = whole_job_gbs(kv_step, ms_max, ws)
     cpu = None
     if rank == 0 and not args.no_cpu:
         if k_h is None:

@@ -1,0 +1,52 @@
+"""Multi-rank host logic of bench.py on CPU (gloo, world size 2, 127.0.0.1):
+the barrier, the max over ranks of the per-step time and the whole-job
+throughput.  The path itself runs replicas with no collective on the data
+path, so this is all the exchange there is."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank(rank, world, port, out):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import bench
+    r, local, ws, pg = bench.dist_setup(None)
+    assert (r, local, ws) == (rank, rank, world) and pg is not None
+    bench.barrier(pg)
+    ms = 1.0 + rank  # rank 1 is the slow one
+    ms_max = bench.reduce_max(pg, ms)
+    out.put((rank, ms_max, bench.whole_job_gbs(1000, ms_max, ws)))
+    pg.destroy_process_group()
+
+
+def test_two_rank_barrier_and_max_over_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs)
+    res = sorted(q.get(timeout=5) for _ in range(2))
+    assert [ms for _, ms, _ in res] == [2.0, 2.0]
+    # 1000 bytes per rank, 2 ranks, 2 ms per step -> 1e-3 GB/s
+    assert all(abs(g - 2000 / 2e-3 / 1e9) < 1e-12 for _, _, g in res)
+
+
+def test_single_rank_needs_no_process_group():
+    import bench
+    assert bench.reduce_max(None, 3.5) == 3.5
+    assert bench.whole_job_gbs(134217728, 0.0201, 1) == pytest.approx(6677.5, rel=1e-3)
