@@ -373,18 +373,25 @@ def run_pkv(args, rank, local, ws, pg):
     torch.cuda.synchronize()
     c = api.pkv_get_counters()
     launches_per_step = sum(c.values())
+    # graphs: one of R consecutive steps (pool 0..R-1), so that each step's
+    # kernels chain into the next step's by programmatic dependent launch, and
+    # single steps for a remainder of K mod R
     graphs = None
     if not args.no_graph:
         try:
-            graphs = []
+            loop_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(loop_graph, stream=stream):
+                for r in range(R):
+                    step(r)
+            singles = []
             for r in range(R):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
                     step(r)
-                graphs.append(g)
-            for r in range(R):
-                graphs[r].replay()
+                singles.append(g)
+            loop_graph.replay()
             torch.cuda.synchronize()
+            graphs = (loop_graph, singles)
         except Exception as e:  # capture unsupported: eager launches
             print(f"# graph capture failed ({e}); timing eager launches", file=sys.stderr)
             graphs = None
@@ -405,10 +412,13 @@ def run_pkv(args, rank, local, ws, pg):
     e1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     e0.record(stream)
-    for s in range(steps):
-        if graphs:
-            graphs[s % R].replay()
-        else:
+    if graphs:
+        for _ in range(steps // R):
+            graphs[0].replay()
+        for r in range(steps % R):
+            graphs[1][r].replay()
+    else:
+        for s in range(steps):
             step(s % R)
     e1.record(stream)
     torch.cuda.synchronize()

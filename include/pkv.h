@@ -90,7 +90,9 @@ typedef struct {
 /* ---------------------------------------------------------------- sizes */
 
 /* Bytes of the plan workspace: a 64-byte header (error word, task count),
- * offsets[B+1] and, for WORKQUEUE, the task list (16 bytes per task).  Every
+ * offsets[B+1] and, for WORKQUEUE, the task list (16 bytes per task) followed
+ * by internal scheduling data (a balance-ordered copy of the list and one int
+ * per row).  Every
  * launching entry point takes this workspace (it holds the error word).  It
  * needs no initialisation except that pkv_get_error() reads and clears the
  * error word; zero it once after allocation. */

@@ -248,7 +248,8 @@ int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_
             ntasks = (int64_t)s->B * s->Hkv * p.S_b;
         } else {
             ntasks = max_tasks(s, c);
-            p.tasks = reinterpret_cast<const int4 *>(static_cast<char *>(d_ws) + ws_tasks_off(s->B));
+            p.tasks = reinterpret_cast<const int4 *>(static_cast<char *>(d_ws) +
+                                                     ws_ordered_off(s->B, ntasks));
         }
     }
     if (ntasks > 0x7fffffffLL)
@@ -274,7 +275,7 @@ size_t pkv_plan_workspace_size(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
         return 0;
     size_t n = ws_tasks_off(s->B);
     if (c->path == PKV_PATH_WORKQUEUE)
-        n += 16 * (size_t)max_tasks(s, c);
+        n = ws_short_off(s->B, max_tasks(s, c)) + sizeof(int32_t) * (size_t)s->B;
     return n;
 }
 
@@ -298,14 +299,17 @@ int pkv_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, const int32_t *d_seq
     p.seq_lens = d_seq_lens;
     p.ws = ws_hdr(d_ws);
     p.offsets = reinterpret_cast<int32_t *>(static_cast<char *>(d_ws) + ws_offsets_off());
+    const int64_t cap = max_tasks(s, c);
     p.tasks = reinterpret_cast<int4 *>(static_cast<char *>(d_ws) + ws_tasks_off(s->B));
+    p.tasks_ordered = reinterpret_cast<int4 *>(static_cast<char *>(d_ws) + ws_ordered_off(s->B, cap));
+    p.short_before = reinterpret_cast<int32_t *>(static_cast<char *>(d_ws) + ws_short_off(s->B, cap));
     p.B = s->B;
     p.Hq = s->Hq;
     p.Hkv = s->Hkv;
     p.G = s->Hq / s->Hkv;
     p.C = c->split_tokens;
     p.len_cap = len_cap(s);
-    p.max_tasks = max_tasks(s, c);
+    p.max_tasks = cap;
     cudaError_t e = launch_plan(p, static_cast<cudaStream_t>(stream), true);
     if (e != cudaSuccess)
         return cuda_fail(e, "plan launch");

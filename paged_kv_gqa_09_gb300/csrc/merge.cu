@@ -27,7 +27,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
     __shared__ float s_max[kMergeWarps];
     __shared__ float s_l[kMergeWarps];
     __shared__ __align__(16) float s_acc[kMergeWarps][D];
+    // every libpkv kernel waits for its predecessor before touching global
+    // memory, so the next one may be scheduled as soon as this one runs
     pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int wg = blockIdx.x;
     if (wg >= p.B * p.Hq)
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p)
 {
     pdl_wait();
+    pdl_trigger();
     const int i = blockIdx.x;
     if (i >= p.B)
         return;

@@ -21,12 +21,18 @@ inline size_t ws_tasks_off(int B)
     size_t o = kWsHeaderBytes + sizeof(int32_t) * (size_t)(B + 1);
     return (o + 15) & ~(size_t)15;
 }
+// Workqueue-only regions after the canonical task list (max_tasks records):
+// the balance-ordered copy, then short_before[B].
+inline size_t ws_ordered_off(int B, int64_t max_tasks) { return ws_tasks_off(B) + 16 * (size_t)max_tasks; }
+inline size_t ws_short_off(int B, int64_t max_tasks) { return ws_ordered_off(B, max_tasks) + 16 * (size_t)max_tasks; }
 
 struct PlanParams {
     const int32_t *seq_lens;
     WsHeader *ws;
-    int32_t *offsets;  // [B+1]
-    int4 *tasks;       // [max_tasks]
+    int32_t *offsets;       // [B+1]
+    int32_t *short_before;  // [B]: rows before i whose last split is shorter than C
+    int4 *tasks;            // [max_tasks], canonical order
+    int4 *tasks_ordered;    // [max_tasks], balance order
     int B, Hq, Hkv, G, C;
     int len_cap;       // bt_stride * page_size: lengths are clamped to it
     int64_t max_tasks;

@@ -12,6 +12,9 @@
 //   Hkv*offsets[i+1]) is {i, g, j, (offsets[i] + j)*Hq + g*G} with
 //   g = (k - Hkv*offsets[i]) / n_i, j = ... % n_i -- the lexicographic
 //   (row, kv-head, split) order.  The host never reads T back.
+// A second copy of the same records, in balance order (every full-length
+// split first, then each row's shorter last split), is what the decode
+// kernel's CTAs stride over: the launch then ends on short tasks.
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
 
@@ -20,51 +23,71 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
+// Block-wide exclusive scan of one int per thread; returns the exclusive prefix
+// and sets *total to the block sum.
+__device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int *total)
 {
-    __shared__ int warp_tot[32];
-    __shared__ int chunk_tot;
-    pdl_wait();
-    pdl_trigger();
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    int carry = 0;
-    for (int base = 0; base < p.B; base += kPlanThreads) {
-        const int i = base + tid;
-        int n = 0;
-        if (i < p.B) {
-            int N = p.seq_lens[i];
-            N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);
-            n = (N + p.C - 1) / p.C;
-        }
-        int x = n;  // inclusive warp scan
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int t = warp_tot[lane];
+        int sc = t;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            const int y = __shfl_up_sync(0xffffffffu, sc, o);
             if (lane >= o)
-                x += y;
+                sc += y;
         }
+        warp_tot[lane] = sc - t;
         if (lane == 31)
-            warp_tot[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            int t = warp_tot[lane];
-            int s = t;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o)
-                    s += y;
-            }
-            warp_tot[lane] = s - t;  // exclusive prefix of warp totals
-            if (lane == 31)
-                chunk_tot = s;
+            warp_tot[32] = sc;
+    }
+    __syncthreads();
+    const int ex = warp_tot[warp] + incl - x;
+    *total = warp_tot[32];
+    __syncthreads();
+    return ex;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
+{
+    __shared__ int warp_tot[33];
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x;
+
+    // n_i = ceil(N_i / C) and r_i = 1 when row i ends in a shorter split; both
+    // scanned over the rows (in chunks of one block)
+    int carry = 0, carry_r = 0;
+    for (int base = 0; base < p.B; base += kPlanThreads) {
+        const int i = base + tid;
+        int n = 0, r = 0;
+        if (i < p.B) {
+            int N = p.seq_lens[i];
+            if (N < 0 || N > p.len_cap)
+                report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.len_cap);
+            N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);
+            n = (N + p.C - 1) / p.C;
+            r = (N % p.C) != 0 ? 1 : 0;
         }
-        __syncthreads();
-        if (i < p.B)
-            p.offsets[i] = carry + warp_tot[warp] + x - n;
-        carry += chunk_tot;
-        __syncthreads();
+        int tot, tot_r;
+        const int ex = block_exclusive_scan(n, warp_tot, &tot);
+        const int ex_r = block_exclusive_scan(r, warp_tot, &tot_r);
+        if (i < p.B) {
+            p.offsets[i] = carry + ex;
+            p.short_before[i] = carry_r + ex_r;
+        }
+        carry += tot;
+        carry_r += tot_r;
     }
     const int64_t T = (int64_t)carry * p.Hkv;
     const bool overflow = T > p.max_tasks;
@@ -80,6 +103,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
     __syncthreads();
     if (overflow)
         return;
+    // full-length tasks of the balance order come first, the rows' shorter last
+    // splits after them
+    const int64_t n_full = T - (int64_t)carry_r * p.Hkv;
     for (int64_t k = tid; k < T; k += kPlanThreads) {
         // last row i in [0, B-1] with Hkv * offsets[i] <= k
         int lo = 0, hi = p.B - 1;
@@ -94,7 +120,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
         const int ni = __ldcg(p.offsets + lo + 1) - oi;
         const int kk = (int)(k - (int64_t)oi * p.Hkv);
         const int g = kk / ni, j = kk - g * ni;
-        p.tasks[k] = make_int4(lo, g, j, (oi + j) * p.Hq + g * p.G);
+        const int4 rec = make_int4(lo, g, j, (oi + j) * p.Hq + g * p.G);
+        p.tasks[k] = rec;
+        // balance order: shorter splits before this task = Hkv * (rows before
+        // with one) + g * (this row has one)
+        const int sb = __ldcg(p.short_before + lo);
+        const int has_short = (lo + 1 < p.B ? __ldcg(p.short_before + lo + 1) : carry_r) - sb;
+        const bool is_short = has_short && j == ni - 1;
+        const int64_t pos = is_short ? n_full + (int64_t)sb * p.Hkv + g
+                                     : k - ((int64_t)sb * p.Hkv + (int64_t)g * has_short);
+        p.tasks_ordered[pos] = rec;
     }
 }
 

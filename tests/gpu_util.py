@@ -76,13 +76,18 @@ def close_lse(lse_gpu: torch.Tensor, lse_ref: np.ndarray):
         assert err <= LSE_ATOL, f"lse max abs err {err}"
 
 
-def read_plan(ws: torch.Tensor, B: int):
+def read_plan(ws: torch.Tensor, B: int, with_order: bool = False):
     h = ws[:64].view(torch.int32).cpu().numpy()
     count = int(h[4])
     off = ws[64:64 + 4 * (B + 1)].view(torch.int32).cpu().numpy()
     t0 = (64 + 4 * (B + 1) + 15) // 16 * 16
     tasks = ws[t0:t0 + 16 * count].view(torch.int32).cpu().numpy().reshape(-1, 4)
-    return count, off, tasks, h
+    if not with_order:
+        return count, off, tasks, h
+    cap = (ws.numel() - t0 - 4 * B) // 32
+    o0 = t0 + 16 * cap
+    ordered = ws[o0:o0 + 16 * count].view(torch.int32).cpu().numpy().reshape(-1, 4)
+    return count, off, tasks, h, ordered
 
 
 def oracle_out(tr, q, k, v):

@@ -101,7 +101,8 @@ def test_workspace_and_partial_sizes(L):
     c = cfg(C=256)
     tasks_off = (64 + 4 * 4 + 15) // 16 * 16
     cap = 8 * 3 * 4
-    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(c)) == tasks_off + 16 * cap
+    # canonical list, its balance-ordered copy, one int per row
+    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(c)) == tasks_off + 32 * cap + 4 * 3
     assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(c)) == cap * 4 * (128 + 2) * 4
     c = cfg(C=256, max_tasks=10)
     assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(c)) == 10 * 4 * 130 * 4

@@ -55,13 +55,21 @@ def test_plan_matches_oracle_bit_exact(lens, C):
     ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
     api.pkv_plan(shape, cfg, dev(tr.seq_lens), ws)
     torch.cuda.synchronize()
-    count, off, tasks, h = read_plan(ws, tr.B)
+    count, off, tasks, h, ordered = read_plan(ws, tr.B, with_order=True)
     want, want_off = oracle.plan_compact(tr.seq_lens, Hq, Hkv, C)
     assert count == want.shape[0]
     assert np.array_equal(off, want_off)
     assert np.array_equal(tasks, want)
     assert h[0] == 0 and h[6] == 0
     check_error_free(ws)
+    # the decode walks a balance-ordered copy: the same records, every
+    # full-length split first, then the rows' shorter last splits, each group
+    # in canonical order
+    lens = np.asarray(lens)
+    n = -(-lens // C)
+    short = [(lens[r[0]] % C != 0) and r[2] == n[r[0]] - 1 for r in want]
+    expect = np.concatenate([want[[not x for x in short]], want[short]]) if count else want
+    assert np.array_equal(ordered, expect)
 
 
 @pytest.mark.parametrize("cfg_id", [3, 5])
