@@ -191,6 +191,20 @@ int pkv_append(const pkv_shape_t *shape, void *d_ws, const void *d_k_new,
                const void *d_v_new, const int32_t *d_block_table, int32_t *d_seq_lens,
                void *d_k_cache, void *d_v_cache, void *stream);
 
+/* pkv_decode_step_rows -- the launch group of the exact-length-bucket scheme
+ * (Results, "Scheduling overhead": the scheme the compact workqueue replaces
+ * launches one group per exact row length): pkv_decode + pkv_merge on the
+ * BUCKETED_SPLIT path over the rows d_rows[0..n_rows) of the batch only
+ * (distinct indices in [0, B); an entry outside is a device error and that
+ * row is skipped).  bucket_len must cover the group's longest row; d_partials
+ * holds n_rows*S_b*Hq states (pkv_partials_size with B = n_rows).  Two kernel
+ * launches; o and lse rows outside the list are left untouched. */
+int pkv_decode_step_rows(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
+                         const int32_t *d_rows, int32_t n_rows,
+                         const void *d_q, const void *d_k_cache, const void *d_v_cache,
+                         const int32_t *d_block_table, const int32_t *d_seq_lens,
+                         float *d_partials, void *d_o, float *d_lse, void *stream);
+
 /* pkv_decode_step_noalloc -- pkv_decode_step for callers that cannot
  * allocate device memory.  No counterpart in the paper: it serves callers that
  * must not call cudaMalloc -- code running inside an allocator's callbacks,
@@ -243,6 +257,36 @@ void pkv_policy_default(pkv_policy_cfg_t *cfg);
  * cfg may be NULL (defaults).  Host only, deterministic, no CUDA call. */
 int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg,
                pkv_path_t *out_path, int32_t *out_split_tokens);
+
+/* Learned cost model (technical summary, Significance: the authors name a
+ * learned cost model for the thresholds as future work).  For route r
+ * (a path and a split size) log(t_r) = w_r . f with
+ *   f = [1, lb, ln, ls, lb*ln, lb^2, ln^2, fill, fill*lb, ls^2],
+ *   lb = log2 B, ln = log2 N_max, ls = log2 max(N_sum, 1), fill = N_sum / (B N_max),
+ * N_sum being the batch's total tokens.  Defaults are fitted by least squares
+ * on GB300 step times of the calibration seed (paged_kv_gqa_09_gb300/calibrate.py). */
+#define PKV_COST_FEATURES 10
+#define PKV_COST_MAX_ROUTES 16
+
+typedef struct {
+    int32_t path;          /* a pkv_path_t */
+    int32_t split_tokens;  /* C of the route (ignored by SINGLE_PASS) */
+    float w[PKV_COST_FEATURES];
+} pkv_cost_route_t;
+
+typedef struct {
+    int32_t n_routes;
+    pkv_cost_route_t route[PKV_COST_MAX_ROUTES];
+} pkv_cost_model_t;
+
+/* Fill `model` with the GB300-fitted routes. */
+void pkv_cost_model_default(pkv_cost_model_t *model);
+
+/* Pick the route of smallest predicted step time for B rows with longest
+ * row n_max and total tokens n_sum (host only, deterministic).  model may be
+ * NULL (defaults).  B = 0 or n_max = 0 gives SINGLE_PASS. */
+int pkv_policy_learned(int32_t B, int32_t n_max, int64_t n_sum, const pkv_cost_model_t *model,
+                       pkv_path_t *out_path, int32_t *out_split_tokens);
 
 /* ----------------------------------------------------------- counters */
 

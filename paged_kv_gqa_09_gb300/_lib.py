@@ -35,8 +35,10 @@ STATUS_NAMES = {
 # every symbol include/pkv.h declares
 EXPORTS = [
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
-    "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc", "pkv_decode_step_host",
+    "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_rows", "pkv_decode_step_noalloc",
+    "pkv_decode_step_host",
     "pkv_append", "pkv_policy_default", "pkv_policy",
+    "pkv_cost_model_default", "pkv_policy_learned",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error",
     "pkv_last_error_string", "pkv_version",
 ]
@@ -68,6 +70,19 @@ class PolicyCfg(ctypes.Structure):
     _fields_ = [("bucketed_min_tokens", ctypes.c_int32), ("bucketed_max_batch", ctypes.c_int32),
                 ("workqueue_min_tokens", ctypes.c_int32), ("workqueue_min_batch", ctypes.c_int32),
                 ("split_tokens", ctypes.c_int32), ("bucketed_split_tokens", ctypes.c_int32)]
+
+
+COST_FEATURES = 10
+COST_MAX_ROUTES = 16
+
+
+class CostRoute(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("split_tokens", ctypes.c_int32),
+                ("w", ctypes.c_float * COST_FEATURES)]
+
+
+class CostModel(ctypes.Structure):
+    _fields_ = [("n_routes", ctypes.c_int32), ("route", CostRoute * COST_MAX_ROUTES)]
 
 
 class Counters(ctypes.Structure):
@@ -115,10 +130,15 @@ def load() -> ctypes.CDLL:
             "pkv_decode_step": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_decode_step_noalloc": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_decode_step_host": (ctypes.c_int, [S, C] + [vp] * 15),
+            "pkv_decode_step_rows": (ctypes.c_int, [S, C, vp, vp, i32] + [vp] * 9),
             "pkv_append": (ctypes.c_int, [S, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_policy_default": (None, [PC]),
             "pkv_policy": (ctypes.c_int, [i32, i32, PC, ctypes.POINTER(ctypes.c_int32),
                                           ctypes.POINTER(ctypes.c_int32)]),
+            "pkv_cost_model_default": (None, [ctypes.POINTER(CostModel)]),
+            "pkv_policy_learned": (ctypes.c_int, [i32, i32, ctypes.c_int64, ctypes.POINTER(CostModel),
+                                                  ctypes.POINTER(ctypes.c_int32),
+                                                  ctypes.POINTER(ctypes.c_int32)]),
             "pkv_get_counters": (ctypes.c_int, [ctypes.POINTER(Counters)]),
             "pkv_reset_counters": (ctypes.c_int, []),
             "pkv_step_model": (ctypes.c_int, [i32, S, i32, i32, vp, ctypes.POINTER(StepModel)]),

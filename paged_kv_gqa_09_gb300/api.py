@@ -23,7 +23,8 @@ __all__ = [
     "Shape", "PlanCfg", "PolicyCfg", "make_shape", "make_cfg",
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
     "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc",
-    "pkv_decode_step_host", "pkv_append", "pkv_policy", "pkv_policy_default",
+    "pkv_decode_step_host", "pkv_decode_step_rows", "exact_length_buckets_step", "pkv_append", "pkv_policy", "pkv_policy_default",
+    "pkv_cost_model_default", "pkv_policy_learned",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error", "pkv_version",
     "PagedDecoder", "HostDecodeLoop",
 ]
@@ -163,6 +164,60 @@ def pkv_decode_step_noalloc(shape, cfg, q, k_cache, v_cache, block_table, seq_le
                                     _stream(stream)), "pkv_decode_step_noalloc")
 
 
+def pkv_decode_step_rows(shape, cfg, ws, rows, q, k_cache, v_cache, block_table, seq_lens,
+                         partials, o, lse=None, stream=None) -> None:
+    """Bucketed split step over the batch rows listed in `rows` (int32, device)."""
+    L = _lib.load()
+    check(L.pkv_decode_step_rows(ctypes.byref(shape), ctypes.byref(cfg), _ws(ws),
+                                 _dev(rows, "rows", torch.int32), int(rows.numel()),
+                                 _dev(q, "q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
+                                 _dev(v_cache, "v_cache", torch.float16),
+                                 _dev(block_table, "block_table", torch.int32),
+                                 _dev(seq_lens, "seq_lens", torch.int32),
+                                 _dev(partials, "partials", torch.float32), _dev(o, "o", torch.float16),
+                                 _dev(lse, "lse", torch.float32, nullable=True), _stream(stream)),
+          "pkv_decode_step_rows")
+
+
+def exact_length_buckets_step(q, k_cache, v_cache, block_table, seq_lens, seq_lens_host,
+                              split_tokens: int, o, lse=None, ws=None, partials=None,
+                              rows_cache: Optional[dict] = None, stream=None):
+    """The exact-length-bucket scheme the compact workqueue replaces (Results,
+    "Scheduling overhead"): one bucketed split + merge launch pair per distinct
+    non-zero row length, each over the rows of that length.  Rows of length 0
+    get o = 0, lse = -inf.  `seq_lens_host` is the host copy of the lengths
+    (the host groups the rows).  Returns the number of launch groups."""
+    shape = make_shape(q, k_cache, block_table)
+    lens = np.asarray(seq_lens_host)
+    groups = {}
+    for i, n in enumerate(lens.tolist()):
+        groups.setdefault(int(n), []).append(i)
+    dev = q.device
+    if 0 in groups:
+        z = torch.tensor(groups.pop(0), dtype=torch.long, device=dev)
+        o.index_fill_(0, z, 0)
+        if lse is not None:
+            lse.index_fill_(0, z, float("-inf"))
+    for n, rows in sorted(groups.items()):
+        cfg = make_cfg(PKV_PATH_BUCKETED_SPLIT, split_tokens, n)
+        key = (n, tuple(rows))
+        if rows_cache is not None and key in rows_cache:
+            rows_t = rows_cache[key]
+        else:
+            rows_t = torch.tensor(rows, dtype=torch.int32, device=dev)
+            if rows_cache is not None:
+                rows_cache[key] = rows_t
+        sub = Shape(len(rows), shape.Hq, shape.Hkv, shape.d, shape.page_size, shape.num_pages,
+                    shape.bt_stride, shape.scale)
+        need_p = pkv_partials_size(sub, cfg) // 4
+        part = partials if partials is not None and partials.numel() >= need_p else \
+            torch.empty(max(need_p, 4), dtype=torch.float32, device=dev)
+        w = ws if ws is not None else torch.zeros(64, dtype=torch.uint8, device=dev)
+        pkv_decode_step_rows(shape, cfg, w, rows_t, q, k_cache, v_cache, block_table, seq_lens,
+                             part, o, lse, stream)
+    return len(groups)
+
+
 def _host(t: Optional[torch.Tensor], name: str, dtype: torch.dtype, nullable: bool = False) -> int:
     if t is None:
         if nullable:
@@ -213,6 +268,22 @@ def pkv_policy(B: int, n_max: int, cfg: Optional[PolicyCfg] = None) -> tuple[int
     path, split = ctypes.c_int32(), ctypes.c_int32()
     check(_lib.load().pkv_policy(int(B), int(n_max), ctypes.byref(cfg) if cfg is not None else None,
                                  ctypes.byref(path), ctypes.byref(split)), "pkv_policy")
+    return int(path.value), int(split.value)
+
+
+def pkv_cost_model_default() -> _lib.CostModel:
+    m = _lib.CostModel()
+    _lib.load().pkv_cost_model_default(ctypes.byref(m))
+    return m
+
+
+def pkv_policy_learned(B: int, n_max: int, n_sum: int,
+                       model: Optional[_lib.CostModel] = None) -> tuple[int, int]:
+    path, split = ctypes.c_int32(), ctypes.c_int32()
+    check(_lib.load().pkv_policy_learned(int(B), int(n_max), int(n_sum),
+                                         ctypes.byref(model) if model is not None else None,
+                                         ctypes.byref(path), ctypes.byref(split)),
+          "pkv_policy_learned")
     return int(path.value), int(split.value)
 
 

@@ -166,14 +166,75 @@ def fit(results):
     return best_params, best_score
 
 
+# ----------------------------------------------------------- learned model
+# The pages' future work: a learned cost model in place of hand thresholds.
+# Per route, log(step time) is fitted by least squares on features of the
+# batch the host knows: B, N_max and the total tokens sum_i N_i.  The policy
+# picks the route with the smallest predicted time.  The same feature map is
+# written in C in pkv_policy_learned (api.cu); keep the two in step.
+
+N_FEATURES = 10
+
+
+def features(B: int, n_max: int, n_sum: int) -> np.ndarray:
+    lb, ln = math.log2(B), math.log2(n_max)
+    ls = math.log2(max(n_sum, 1))
+    fill = n_sum / (B * n_max)
+    return np.array([1.0, lb, ln, ls, lb * ln, lb * lb, ln * ln, fill, fill * lb, ls * ls])
+
+
+def trace_features(res) -> np.ndarray:
+    return features(res["B"], res["n_max"], res["kv_bytes"] // (HKV * D * 4))
+
+
+def fit_cost_model(results):
+    X = np.array([trace_features(r) for r in results])
+    model = {}
+    for name, c in routes():
+        key = f"{name}:{c}"
+        y = np.log([r["us"][key] for r in results])
+        model[key] = np.linalg.lstsq(X, y, rcond=None)[0]
+    return model
+
+
+def model_choice(model, res):
+    f = trace_features(res)
+    return min(model, key=lambda k: float(f @ model[k]))
+
+
+def model_regret(model, results):
+    r = [res["us"][model_choice(model, res)] / min(res["us"].values()) for res in results]
+    return float(np.mean(r)), float(np.max(r))
+
+
+def model_c_table(model) -> str:
+    """C initializer rows {path, split_tokens, {w0..w9}} for pkv_policy_learned."""
+    path_id = {"bucketed": 0, "workqueue": 1, "single": 2}
+    rows = []
+    for key, w in model.items():
+        name, c = key.split(":")
+        ws = ", ".join(f"{x:.9g}f" for x in w)
+        rows.append(f"    {{{path_id[name]}, {int(c) or 1024}, {{{ws}}}}},")
+    return "\n".join(rows)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default="policy_calibration.json")
     ap.add_argument("--reps", type=int, default=7)
+    ap.add_argument("--from-json", default=None,
+                    help="refit from an earlier run's measurements instead of timing")
     a = ap.parse_args(argv)
-    cal = measure(T.CALIBRATION_SEED, a.reps)
+    if a.from_json:
+        old = json.load(open(a.from_json))
+        cal, held = old["calibration"], old["heldout"]
+    else:
+        cal = measure(T.CALIBRATION_SEED, a.reps)
+        held = None
     params, score = fit(cal)
-    held = measure(T.HELDOUT_SEED, a.reps)
+    model = fit_cost_model(cal)
+    if held is None:
+        held = measure(T.HELDOUT_SEED, a.reps)
     pages_default = (4096, 1, 4096, 8, 1024, 1024)  # the pages' routing, RTX 3060-era cut-offs
     out = {
         "params": dict(zip(["bucketed_min_tokens", "bucketed_max_batch", "workqueue_min_tokens",
@@ -181,10 +242,14 @@ def main(argv=None):
         "calibration_mean_regret": score,
         "heldout_mean_max_regret": regret(params, held),
         "pages_structure_default_heldout_regret": regret(pages_default, held),
+        "learned_model_calibration_regret": model_regret(model, cal),
+        "learned_model_heldout_regret": model_regret(model, held),
+        "learned_model": {k: [float(x) for x in w] for k, w in model.items()},
         "calibration": cal, "heldout": held,
     }
+    print(model_c_table(model))
     json.dump(out, open(a.out, "w"), indent=1)
-    print(json.dumps({k: out[k] for k in list(out)[:4]}))
+    print(json.dumps({k: out[k] for k in list(out)[:6]}))
     return 0
 
 

@@ -108,10 +108,10 @@ int64_t max_tasks(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
     return (int64_t)s->Hkv * s->B * per_row;
 }
 
-int64_t partial_slots(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
+int64_t partial_slots(const pkv_shape_t *s, const pkv_plan_cfg_t *c, int64_t rows = -1)
 {
     if (c->path == PKV_PATH_BUCKETED_SPLIT)
-        return (int64_t)s->B * s_b(s, c) * s->Hq;
+        return (rows >= 0 ? rows : (int64_t)s->B) * s_b(s, c) * s->Hq;
     if (c->path == PKV_PATH_WORKQUEUE)
         return max_tasks(s, c) * (s->Hq / s->Hkv);
     return 0;
@@ -209,7 +209,8 @@ WsHeader *ws_hdr(void *ws) { return reinterpret_cast<WsHeader *>(ws); }
 
 int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_ws, const void *q,
                const void *k, const void *v, const int32_t *bt, const int32_t *sl, float *part,
-               void *o, float *lse, cudaStream_t st)
+               void *o, float *lse, cudaStream_t st, const int32_t *rows = nullptr,
+               int n_rows = -1)
 {
     int slots = 0;
     PKV_TRY(device_slots(s->d, &slots));
@@ -238,14 +239,15 @@ int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_
         p.lse = lse;
         ntasks = (int64_t)s->B * s->Hkv;
     } else {
-        const int64_t slots = partial_slots(s, c);
+        const int64_t slots = partial_slots(s, c, rows ? n_rows : -1);
         p.part_acc = part;
         p.part_m = part + slots * s->d;
         p.part_l = p.part_m + slots;
         p.C = c->split_tokens;
         p.S_b = s_b(s, c);
         if (mode == kModeRect) {
-            ntasks = (int64_t)s->B * s->Hkv * p.S_b;
+            p.rows = rows;
+            ntasks = (int64_t)(rows ? n_rows : s->B) * s->Hkv * p.S_b;
         } else {
             ntasks = max_tasks(s, c);
             p.tasks = reinterpret_cast<const int4 *>(static_cast<char *>(d_ws) +
@@ -336,20 +338,18 @@ int pkv_decode(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const 
                       static_cast<cudaStream_t>(stream));
 }
 
-int pkv_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const int32_t *sl,
-              const float *part, void *o, float *lse, void *stream)
+}  // extern "C"
+
+namespace {
+
+int run_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const int32_t *sl,
+              const float *part, void *o, float *lse, void *stream, const int32_t *rows,
+              int n_rows)
 {
-    PKV_TRY(check_shape(s));
-    PKV_TRY(check_cfg(s, c));
-    if (c->path == PKV_PATH_SINGLE_PASS)
-        return fail(PKV_EINVAL, "pkv_merge takes a split path");
-    PKV_TRY(check_ptr(d_ws, "workspace"));
-    PKV_TRY(check_ptr(sl, "seq_lens"));
-    PKV_TRY(check_ptr(part, "partials"));
-    PKV_TRY(check_ptr(o, "o"));
-    PKV_TRY(check_ptr(lse, "lse", true));
-    const int64_t slots = partial_slots(s, c);
+    const int64_t slots = partial_slots(s, c, rows ? n_rows : -1);
     MergeParams p = {};
+    p.rows = rows;
+    p.n_rows = rows ? n_rows : s->B;
     p.seq_lens = sl;
     p.ws = ws_hdr(d_ws);
     p.offsets = reinterpret_cast<const int32_t *>(static_cast<char *>(d_ws) + ws_offsets_off());
@@ -370,6 +370,51 @@ int pkv_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const i
         return cuda_fail(e, "merge launch");
     g_cnt.merge++;
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const int32_t *sl,
+              const float *part, void *o, float *lse, void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    if (c->path == PKV_PATH_SINGLE_PASS)
+        return fail(PKV_EINVAL, "pkv_merge takes a split path");
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PKV_TRY(check_ptr(sl, "seq_lens"));
+    PKV_TRY(check_ptr(part, "partials"));
+    PKV_TRY(check_ptr(o, "o"));
+    PKV_TRY(check_ptr(lse, "lse", true));
+    return run_merge(s, c, d_ws, sl, part, o, lse, stream, nullptr, -1);
+}
+
+int pkv_decode_step_rows(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws,
+                         const int32_t *d_rows, int32_t n_rows, const void *q, const void *k,
+                         const void *v, const int32_t *bt, const int32_t *sl, float *part, void *o,
+                         float *lse, void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    if (c->path != PKV_PATH_BUCKETED_SPLIT)
+        return fail(PKV_EINVAL, "pkv_decode_step_rows runs the BUCKETED_SPLIT path");
+    if (n_rows < 1 || n_rows > s->B)
+        return fail(PKV_EINVAL, "n_rows=%d must be in [1, B=%d]", n_rows, s->B);
+    PKV_TRY(check_ptr(d_rows, "rows"));
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PKV_TRY(check_ptr(q, "q"));
+    PKV_TRY(check_ptr(k, "k_cache"));
+    PKV_TRY(check_ptr(v, "v_cache"));
+    PKV_TRY(check_ptr(bt, "block_table"));
+    PKV_TRY(check_ptr(sl, "seq_lens"));
+    PKV_TRY(check_ptr(part, "partials"));
+    PKV_TRY(check_ptr(o, "o"));
+    PKV_TRY(check_ptr(lse, "lse", true));
+    PKV_TRY(run_decode(s, kModeRect, c, d_ws, q, k, v, bt, sl, part, nullptr, nullptr,
+                       static_cast<cudaStream_t>(stream), d_rows, n_rows));
+    return run_merge(s, c, d_ws, sl, part, o, lse, stream, d_rows, n_rows);
 }
 
 int pkv_single_pass(const pkv_shape_t *s, void *d_ws, const void *q, const void *k, const void *v,
@@ -518,6 +563,74 @@ int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t
     return PKV_OK;
 }
 
+// ------------------------------------------------------------ learned model
+
+// Routes and weights fitted by paged_kv_gqa_09_gb300/calibrate.py (least
+// squares of log step time, calibration seed 20260622, 224 GB300 traces);
+// held-out seed 20260623 mean regret 1.025 (worst 1.21x).
+static const pkv_cost_route_t kGb300Routes[] = {
+    {0, 128, {6.01822514f, 0.225079554f, 0.132225077f, -0.866300992f, -0.00286177224f, 0.0058537269f, 0.00381505922f, 0.392748749f, -0.0617887688f, 0.0346332006f}},
+    {0, 256, {6.37411087f, 0.126295736f, 0.104974546f, -0.852834268f, 0.00314028221f, 0.00308314744f, 0.00140758789f, 0.286179883f, -0.0621945571f, 0.0358782873f}},
+    {0, 512, {6.51785164f, -0.0564157854f, 0.0411683298f, -0.757304027f, 0.0134233371f, 0.00614057083f, 0.00134051404f, 0.161679818f, -0.0385851328f, 0.0332204809f}},
+    {0, 1024, {6.11387729f, -0.195668953f, 0.0786745573f, -0.67649932f, 0.0198199544f, 0.0101223915f, -0.00181196784f, 0.0586858502f, -0.0166309652f, 0.0306631533f}},
+    {0, 2048, {4.85739656f, -0.207377429f, 0.346906155f, -0.695155704f, 0.0167757827f, 0.0138003383f, -0.0123387416f, -0.00828948804f, -0.0047865178f, 0.0308990192f}},
+    {1, 256, {7.32733405f, 0.117223956f, 0.0193178352f, -0.878072865f, -0.00711632172f, -0.00045299104f, 0.00102104609f, 0.0447541912f, -0.0302528511f, 0.0408652389f}},
+    {1, 512, {6.96231729f, 0.125164353f, 0.141260129f, -0.90587617f, -0.00623116616f, -0.00385944783f, -0.00568025893f, 0.064981471f, -0.0510164257f, 0.042248377f}},
+    {1, 1024, {6.0076199f, 0.13822289f, 0.387047891f, -0.958177046f, -0.00769329818f, -0.00210724119f, -0.015380889f, 0.0727217225f, -0.0477712252f, 0.0431791278f}},
+    {1, 2048, {4.40811257f, 0.145833777f, 0.72000109f, -0.989956553f, -0.0102229642f, 0.00229557149f, -0.0274439559f, 0.03919701f, -0.0324846557f, 0.0428150806f}},
+    {2, 1024, {5.56172397f, -0.140274517f, -0.261910814f, -0.390119342f, -0.00961258517f, 0.0369471378f, 0.0313995807f, -0.396241805f, 0.162715669f, 0.0142896572f}},
+};
+
+void pkv_cost_model_default(pkv_cost_model_t *m)
+{
+    if (!m)
+        return;
+    std::memset(m, 0, sizeof *m);
+    m->n_routes = (int32_t)(sizeof kGb300Routes / sizeof kGb300Routes[0]);
+    for (int r = 0; r < m->n_routes; ++r)
+        m->route[r] = kGb300Routes[r];
+}
+
+int pkv_policy_learned(int32_t B, int32_t n_max, int64_t n_sum, const pkv_cost_model_t *model,
+                       pkv_path_t *out_path, int32_t *out_split)
+{
+    if (!out_path || !out_split)
+        return fail(PKV_EINVAL, "policy outputs are NULL");
+    if (B < 0 || n_max < 0 || n_sum < 0)
+        return fail(PKV_EINVAL, "negative B, n_max or n_sum");
+    pkv_cost_model_t d;
+    if (!model) {
+        pkv_cost_model_default(&d);
+        model = &d;
+    }
+    if (model->n_routes < 1 || model->n_routes > PKV_COST_MAX_ROUTES)
+        return fail(PKV_EINVAL, "cost model has %d routes", model->n_routes);
+    *out_path = PKV_PATH_SINGLE_PASS;
+    *out_split = 1024;
+    if (B == 0 || n_max == 0)
+        return PKV_OK;
+    const double lb = std::log2((double)B), ln = std::log2((double)n_max);
+    const double ls = std::log2((double)(n_sum > 1 ? n_sum : 1));
+    const double fill = (double)n_sum / ((double)B * (double)n_max);
+    const double f[PKV_COST_FEATURES] = {1.0, lb, ln, ls, lb * ln, lb * lb, ln * ln, fill, fill * lb,
+                                          ls * ls};
+    double best = INFINITY;
+    for (int r = 0; r < model->n_routes; ++r) {
+        const pkv_cost_route_t &rt = model->route[r];
+        if (rt.path < 0 || rt.path > 2 || (rt.path != 2 && rt.split_tokens <= 0))
+            return fail(PKV_EINVAL, "cost model route %d is invalid", r);
+        double t = 0.0;
+        for (int k = 0; k < PKV_COST_FEATURES; ++k)
+            t += (double)rt.w[k] * f[k];
+        if (t < best) {
+            best = t;
+            *out_path = (pkv_path_t)rt.path;
+            *out_split = rt.split_tokens;
+        }
+    }
+    return PKV_OK;
+}
+
 // ---------------------------------------------------------------- counters
 
 int pkv_get_counters(pkv_counters_t *out)
@@ -625,6 +738,8 @@ int pkv_get_error(void *d_ws, void *stream)
         return fail(PKV_EDEVICE, "row %d has length %d beyond its limit %d", h[1], h[2], h[3]);
     case kErrNegLen:
         return fail(PKV_EDEVICE, "row %d has negative length %d", h[1], h[2]);
+    case kErrBadRow:
+        return fail(PKV_EDEVICE, "row list entry %d is %d, outside [0, %d)", h[1], h[2], h[3]);
     case kErrTimeout:
         return fail(PKV_ETIMEOUT, "a barrier wait timed out (CTA %d, stage %d, site %d)", h[1], h[2],
                     h[3]);

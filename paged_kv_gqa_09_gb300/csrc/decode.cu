@@ -100,11 +100,18 @@ __device__ __forceinline__ TaskInfo load_task(const DecodeParams &p, int k, int 
         ti.sbase = r.w;
     } else if (MODE == kModeRect) {
         const int per_row = p.Hkv * p.S_b;
-        ti.i = k / per_row;
-        const int r = k - ti.i * per_row;
+        const int lr = k / per_row;  // row of the launch (index into rows[] when given)
+        const int r = k - lr * per_row;
         ti.g = r / p.S_b;
         j = r - ti.g * p.S_b;
-        ti.sbase = (ti.i * p.S_b + j) * p.Hq + ti.g * p.G;
+        ti.sbase = (lr * p.S_b + j) * p.Hq + ti.g * p.G;
+        ti.i = p.rows ? p.rows[lr] : lr;
+        if (ti.i < 0 || ti.i >= p.B) {
+            report_error(p.ws, kErrBadRow, lr, ti.i, p.B);
+            ti.i = 0;
+            ti.t0 = ti.t1 = 0;  // an empty task: neutral state, no KV read
+            return ti;
+        }
     } else {
         ti.i = k / p.Hkv;
         ti.g = k - ti.i * p.Hkv;
@@ -211,6 +218,9 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
         } else if (MODE == kModeRect) {
             i0 = (int)blockIdx.x / (p.Hkv * p.S_b);
             j0 = (int)blockIdx.x % p.S_b;
+            if (p.rows)
+                i0 = p.rows[i0];
+            i0 = min(max(i0, 0), p.B - 1);  // a bad row id is reported by load_task
         } else {
             i0 = (int)blockIdx.x / p.Hkv;
             j0 = 0;

@@ -32,10 +32,13 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int wg = blockIdx.x;
-    if (wg >= p.B * p.Hq)
+    const int lr = blockIdx.x / p.Hq, h = blockIdx.x - lr * p.Hq;
+    if (lr >= p.n_rows)
         return;
-    const int i = wg / p.Hq, h = wg - (wg / p.Hq) * p.Hq;
+    const int i = p.rows ? p.rows[lr] : lr;  // row of the batch
+    if (i < 0 || i >= p.B)
+        return;  // reported by the decode kernel
+    const int64_t wg = (int64_t)i * p.Hq + h;  // (row, head) of o and lse
     int N = p.seq_lens[i];
     N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);
     int n = (N + p.C - 1) / p.C;
@@ -45,7 +48,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
         base = p.offsets[i];
         bad = p.ws->overflow != 0 || base + n > p.state_rows_cap;
     } else {
-        base = (int64_t)i * p.S_b;
+        base = (int64_t)lr * p.S_b;
         n = min(n, p.S_b);
     }
     if (bad || n == 0) {
@@ -186,7 +189,7 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAtt
 
 cudaError_t launch_merge(int d, const MergeParams &p, cudaStream_t s, bool pdl)
 {
-    const int blocks = p.B * p.Hq > 0 ? p.B * p.Hq : 1;
+    const int blocks = p.n_rows * p.Hq > 0 ? p.n_rows * p.Hq : 1;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = make_cfg(dim3(blocks), dim3(32 * kMergeWarps), s, attr, pdl);
     if (d == 128)

@@ -20,6 +20,7 @@ enum DevErr : int32_t {
     kErrTimeout = 3,   // a bounded barrier wait gave up
     kErrCapacity = 4,  // workqueue larger than max_tasks: nothing decoded
     kErrNegLen = 5,    // negative length: row treated as empty
+    kErrBadRow = 6,    // a row list entry outside [0, B): that row skipped
 };
 
 // First 64 bytes of the plan workspace.

@@ -43,6 +43,7 @@ struct DecodeParams {
     const int32_t *bt;
     const int32_t *seq_lens;
     const int4 *tasks;  // workqueue mode
+    const int32_t *rows;  // rect mode: the launch covers rows[0..n_rows) (nullptr: rows 0..B)
     WsHeader *ws;
     float *part_acc, *part_m, *part_l;  // split modes
     __half *o;                           // single-pass mode
@@ -58,6 +59,8 @@ struct DecodeParams {
 };
 
 struct MergeParams {
+    const int32_t *rows;  // rect mode: merge rows[0..n_rows) (nullptr: rows 0..B)
+    int n_rows;
     const int32_t *seq_lens;
     const int32_t *offsets;  // workqueue mode
     const WsHeader *ws;

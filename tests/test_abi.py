@@ -150,3 +150,42 @@ def test_step_model_matches_oracle_counters(L, cfg_id):
 def test_counters_start_at_zero_and_reset(L):
     api.pkv_reset_counters()
     assert set(api.pkv_get_counters().values()) == {0}
+
+
+def test_learned_policy_matches_the_fitted_feature_map(L):
+    """pkv_policy_learned (C) against the calibration script's feature map
+    (Python) on the default GB300 model: same route on a grid of batches."""
+    from paged_kv_gqa_09_gb300 import calibrate
+    m = api.pkv_cost_model_default()
+    assert m.n_routes == 10
+    routes = [(m.route[r].path, m.route[r].split_tokens, np.array(m.route[r].w[:], np.float64))
+              for r in range(m.n_routes)]
+    assert {p for p, _, _ in routes} == {0, 1, 2}
+    rng = np.random.default_rng(3)
+    for _ in range(400):
+        B = int(rng.integers(1, 129))
+        n_max = int(rng.integers(1, 70000))
+        n_sum = int(rng.integers(n_max, B * n_max + 1))
+        f = calibrate.features(B, n_max, n_sum)
+        t = [float(f @ w) for _, _, w in routes]
+        best = int(np.argmin(t))
+        if sorted(t)[1] - t[best] < 1e-4:   # a near tie: float32 weights may pick either
+            continue
+        got = api.pkv_policy_learned(B, n_max, n_sum)
+        assert got == (routes[best][0], routes[best][1]), (B, n_max, n_sum)
+    assert api.pkv_policy_learned(0, 100, 0)[0] == _lib.PKV_PATH_SINGLE_PASS
+    assert api.pkv_policy_learned(4, 0, 0)[0] == _lib.PKV_PATH_SINGLE_PASS
+    with pytest.raises(_lib.PkvError):
+        api.pkv_policy_learned(-1, 5, 5)
+    bad = api.pkv_cost_model_default()
+    bad.n_routes = 0
+    with pytest.raises(_lib.PkvError):
+        api.pkv_policy_learned(1, 5, 5, bad)
+
+
+def test_learned_policy_prefers_workqueue_for_ragged_and_split_for_b1(L):
+    # B=1 long context -> a split path; B=64 uniform long -> not the bucketed grid
+    p1, _ = api.pkv_policy_learned(1, 32768, 32768)
+    assert p1 in (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_PATH_WORKQUEUE)
+    p2, _ = api.pkv_policy_learned(16, 32768, 16 * 900)       # one long row, the rest short
+    assert p2 == _lib.PKV_PATH_WORKQUEUE

@@ -368,3 +368,56 @@ def test_host_buffer_step_matches_oracle(cfg_id, path):
         close(o, oref)
         close_lse(lse, lref)
     check_error_free(loop.ws)
+
+
+# ------------------------------------------------------------------ exact-length buckets
+
+def test_exact_length_buckets_match_oracle_and_launch_twice_per_length():
+    """The scheme the pages compare against: one split + merge launch pair per
+    distinct length; 8 distinct lengths on the bimodal B=8 trace -> 16
+    launches, where the workqueue needs 2 (plus the plan)."""
+    tr = T.make_trace(3)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    d = upload(tr, q, k, v)
+    o = torch.full((tr.B, tr.Hq, tr.d), float("nan"), dtype=torch.float16, device="cuda")
+    lse = torch.full((tr.B, tr.Hq), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    api.pkv_reset_counters()
+    groups = api.exact_length_buckets_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], tr.seq_lens,
+                                           tr.split_tokens, o, lse, ws=ws)
+    torch.cuda.synchronize()
+    check_error_free(ws)
+    c = api.pkv_get_counters()
+    assert groups == 8
+    assert c["decode_launches"] + c["merge_launches"] == 16 and c["plan_launches"] == 0
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o, oref)
+    close_lse(lse, lref)
+
+
+def test_row_list_step_leaves_other_rows_untouched():
+    tr, q, k, v = case([300, 50, 300, 0, 128], Hq=8, Hkv=2, C=64)
+    d = upload(tr, q, k, v)
+    o = torch.full((tr.B, tr.Hq, tr.d), 7.0, dtype=torch.float16, device="cuda")
+    lse = torch.full((tr.B, tr.Hq), 7.0, dtype=torch.float32, device="cuda")
+    rows = torch.tensor([2, 0], dtype=torch.int32, device="cuda")
+    shape = shape_of(tr)
+    cfg = api.make_cfg(BUCKETED, 64, 300)
+    sub = _lib.Shape(2, tr.Hq, tr.Hkv, tr.d, tr.page_size, tr.num_pages, tr.bt_stride, tr.scale)
+    part = torch.empty(api.pkv_partials_size(sub, cfg) // 4, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    api.pkv_decode_step_rows(shape, cfg, ws, rows, d["q"], d["k"], d["v"], d["bt"], d["sl"], part,
+                             o, lse)
+    torch.cuda.synchronize()
+    check_error_free(ws)
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o[[0, 2]], oref[[0, 2]])
+    close_lse(lse[[0, 2]], lref[[0, 2]])
+    assert torch.all(o[[1, 3, 4]] == 7.0) and torch.all(lse[[1, 3, 4]] == 7.0)
+    # a row id outside the batch is reported, not faulted
+    bad = torch.tensor([0, 9], dtype=torch.int32, device="cuda")
+    api.pkv_decode_step_rows(shape, cfg, ws, bad, d["q"], d["k"], d["v"], d["bt"], d["sl"], part,
+                             o, lse)
+    st, msg = api.pkv_get_error(ws)
+    assert st == _lib.PKV_EDEVICE and "row list" in msg, msg
