@@ -48,6 +48,8 @@ constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any barrier wait
 constexpr uint64_t kDrainNs = 20000000ull;   // bound when draining after a timeout
 constexpr float kLn2 = 0.6931471805599453f;
 
+constexpr int kPrefetchTiles = 4;  // tiles of the first task prefetched into L2 early
+
 constexpr int kFirst = 1 << 16;  // stage flags (low 16 bits: valid tokens)
 constexpr int kLast = 1 << 17;
 constexpr int kEnd = 1 << 18;
@@ -344,6 +346,52 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
         for (int s = 0; s < L::kStages; ++s)
             if (pend & (1u << s))
                 mbar_wait(bar_full0 + s * 8, (pend_par >> s) & 1u, kDrainNs);
+    }
+}
+
+// Before the kernel may read its inputs (griddepcontrol.wait), warm L2 with
+// the first tiles of this CTA's first task: block-table entries are read
+// L2-only (they may still be changing, so they must not land in L1) and only
+// drive TMA prefetches, which cannot change any result.  The real loads after
+// the wait re-read everything.  Rectangular and single modes only: the
+// workqueue's task list is being written by the plan kernel right before.
+template <int D, int MODE>
+__device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                                     const DecodeParams &p)
+{
+    if (MODE == kModeQueue || (int)blockIdx.x >= p.n_tasks)
+        return;
+    const int lane = threadIdx.x & 31;
+    const int log2P = p.log2P, btl = p.box_log2;
+    int i0, g0, j0;
+    if (MODE == kModeRect) {
+        const int per_row = p.Hkv * p.S_b;
+        const int lr = (int)blockIdx.x / per_row, r = (int)blockIdx.x - lr * per_row;
+        g0 = r / p.S_b;
+        j0 = r - g0 * p.S_b;
+        i0 = p.rows ? __ldcg(p.rows + lr) : lr;
+    } else {
+        i0 = (int)blockIdx.x / p.Hkv;
+        g0 = (int)blockIdx.x - i0 * p.Hkv;
+        j0 = 0;
+    }
+    if (i0 < 0 || i0 >= p.B)
+        return;
+    const int t0 = MODE == kModeSingle ? 0 : j0 * p.C;
+    const int span = MODE == kModeSingle ? kPrefetchTiles * kTile : min(p.C, kPrefetchTiles * kTile);
+    const int n_pages = ((span - 1) >> log2P) + 1;
+    const int64_t row = (int64_t)i0 * p.bt_stride;
+    // lane l prefetches page s0 + l of the range (tiles hold whole pages when P <= 64)
+    const int s0 = t0 >> log2P;
+    if (lane < n_pages && s0 + lane < p.bt_stride) {
+        const int pg = __ldcg(p.bt + row + s0 + lane);
+        if (pg >= 0 && pg < p.num_pages) {
+            // one box per page when P <= 64, else the page's boxes inside the span
+            for (int b = 0; (b << btl) < (1 << log2P) && (b << btl) < span; ++b) {
+                tma_prefetch_5d(tmK, 0, b << btl, 0, g0, pg);
+                tma_prefetch_5d(tmV, 0, b << btl, 0, g0, pg);
+            }
+        }
     }
 }
 
@@ -644,6 +692,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
     }
+    if (warp == kCW)
+        prefetch_first_tiles<D, MODE>(&tmK, &tmV, p);
     __syncthreads();
     // everything above overlaps the previous kernel; nothing below runs before
     // it has finished and its writes are visible
