@@ -348,18 +348,43 @@ def run_pkv(args, rank, local, ws, pg):
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
     kn = torch.from_numpy(T.gen_append_tokens(tr, 0)[0]).to(dev)
     vn = torch.from_numpy(T.gen_append_tokens(tr, 0)[1]).to(dev)
+    if appends:
+        # on the workqueue, pages are allocated on the device as rows grow: each
+        # row starts with the pages its tokens fill and the rest of the shuffled
+        # pool is the free list; other paths use the pre-assigned table
+        bt_alloc, free_np = T.allocation_split(tr) if path == 1 else (tr.block_table, np.zeros(1, np.int32))
+        bt_init = torch.from_numpy(np.ascontiguousarray(bt_alloc)).to(dev)
+        bt.copy_(bt_init)
+        free_pages = torch.from_numpy(free_np).to(dev)
+        free_count = torch.tensor([free_np.size], dtype=torch.int32, device=dev)
+        free_init = free_count.clone()
     sp = stream.cuda_stream
     P = lambda t: t.data_ptr() if t is not None else None
     sref, cref = _ctypes_refs(shape, cfg)
 
     def step(r):
         kk, vv = pools[r]
+        if appends and path == 1:
+            # append + page allocation + plan in one launch, then decode and merge
+            rc = L.pkv_append_plan(sref, cref, P(wsb), P(kn), P(vn), P(bt), P(sl), P(free_pages),
+                                   P(free_count), P(kk), P(vv), sp)
+            _lib.check(rc, "pkv_append_plan")
+            _lib.check(L.pkv_decode(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(part), sp),
+                       "pkv_decode")
+            _lib.check(L.pkv_merge(sref, cref, P(wsb), P(sl), P(part), P(o), P(lse), sp), "pkv_merge")
+            return
         if appends:
             rc = L.pkv_append(sref, P(wsb), P(kn), P(vn), P(bt), P(sl), P(kk), P(vv), sp)
             _lib.check(rc, "pkv_append")
         rc = L.pkv_decode_step(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl),
                                P(part) if npart else None, P(o), P(lse), sp)
         _lib.check(rc, "pkv_decode_step")
+
+    def reset_lengths():
+        sl.copy_(sl_init)
+        if appends:
+            bt.copy_(bt_init)
+            free_count.copy_(free_init)
 
     # ---- warm-up (eager), then capture one graph per pool
     for w in range(warm):
@@ -396,7 +421,7 @@ def run_pkv(args, rank, local, ws, pg):
             print(f"# graph capture failed ({e}); timing eager launches", file=sys.stderr)
             graphs = None
     if appends:
-        sl.copy_(sl_init)
+        reset_lengths()
         torch.cuda.synchronize()
 
     kv_step = tr.kv_bytes()
@@ -433,7 +458,7 @@ def run_pkv(args, rank, local, ws, pg):
 
     # ---- the decode kernel alone (roofline): events around each launch
     if appends:
-        sl.copy_(sl_init)
+        reset_lengths()
     kern_steps = min(steps, 2000)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(kern_steps)]
@@ -458,7 +483,7 @@ def run_pkv(args, rank, local, ws, pg):
     e2e = None
     if not args.no_e2e:
         if appends:
-            sl.copy_(sl_init)
+            reset_lengths()
         e2e = run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps if not appends else steps,
                       appends, kn, vn, wsb)
 

@@ -179,6 +179,23 @@ int pkv_decode_step_host(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, vo
                          const void *d_k_cache, const void *d_v_cache,
                          void *d_o, void *h_o, float *d_lse, float *h_lse, void *stream);
 
+/* pkv_append_plan -- the step's KV write fused into the workqueue plan: one
+ * kernel launch that appends one token per row exactly as pkv_append does and
+ * then builds pkv_plan's task list from the advanced lengths.  With
+ * d_free_pages != NULL a token that starts a new page (N % page_size == 0)
+ * takes a page from the device free list d_free_pages[0 .. *d_free_count)
+ * (the top of the stack is the end): rows needing one are served in row order
+ * from the top, block_table[i][N / page_size] is set to it and *d_free_count
+ * drops by the pages taken.  A row with no free page left, no room in its
+ * block table or a bad page id keeps its length and the error word records it.
+ * cfg->path must be WORKQUEUE.  (Not a step of the pages' method: the per-step
+ * KV write and page allocation of a serving loop, folded into the launch the
+ * workqueue path makes anyway.) */
+int pkv_append_plan(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
+                    const void *d_k_new, const void *d_v_new, int32_t *d_block_table,
+                    int32_t *d_seq_lens, const int32_t *d_free_pages, int32_t *d_free_count,
+                    void *d_k_cache, void *d_v_cache, void *stream);
+
 /* pkv_append -- write one new token per row into the paged cache.
  * (Not a step of the pages' method: the per-step KV write of a serving loop.)
  * One kernel launch.  For every row i with N = seq_lens[i]: copies

@@ -37,7 +37,7 @@ EXPORTS = [
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
     "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_rows", "pkv_decode_step_noalloc",
     "pkv_decode_step_host",
-    "pkv_append", "pkv_policy_default", "pkv_policy",
+    "pkv_append", "pkv_append_plan", "pkv_policy_default", "pkv_policy",
     "pkv_cost_model_default", "pkv_policy_learned",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error",
     "pkv_last_error_string", "pkv_version",
@@ -132,6 +132,7 @@ def load() -> ctypes.CDLL:
             "pkv_decode_step_host": (ctypes.c_int, [S, C] + [vp] * 15),
             "pkv_decode_step_rows": (ctypes.c_int, [S, C, vp, vp, i32] + [vp] * 9),
             "pkv_append": (ctypes.c_int, [S, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "pkv_append_plan": (ctypes.c_int, [S, C] + [vp] * 10),
             "pkv_policy_default": (None, [PC]),
             "pkv_policy": (ctypes.c_int, [i32, i32, PC, ctypes.POINTER(ctypes.c_int32),
                                           ctypes.POINTER(ctypes.c_int32)]),

@@ -23,7 +23,8 @@ __all__ = [
     "Shape", "PlanCfg", "PolicyCfg", "make_shape", "make_cfg",
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
     "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc",
-    "pkv_decode_step_host", "pkv_decode_step_rows", "exact_length_buckets_step", "pkv_append", "pkv_policy", "pkv_policy_default",
+    "pkv_decode_step_host", "pkv_decode_step_rows", "exact_length_buckets_step", "pkv_append",
+    "pkv_append_plan", "pkv_policy", "pkv_policy_default",
     "pkv_cost_model_default", "pkv_policy_learned",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error", "pkv_version",
     "PagedDecoder", "HostDecodeLoop",
@@ -256,6 +257,22 @@ def pkv_append(shape, ws, k_new, v_new, block_table, seq_lens, k_cache, v_cache,
                        _dev(seq_lens, "seq_lens", torch.int32),
                        _dev(k_cache, "k_cache", torch.float16),
                        _dev(v_cache, "v_cache", torch.float16), _stream(stream)), "pkv_append")
+
+
+def pkv_append_plan(shape, cfg, ws, k_new, v_new, block_table, seq_lens, k_cache, v_cache,
+                    free_pages=None, free_count=None, stream=None) -> None:
+    """Append one token per row (allocating pages from the free list when
+    given), then build the workqueue plan -- one launch."""
+    L = _lib.load()
+    check(L.pkv_append_plan(ctypes.byref(shape), ctypes.byref(cfg), _ws(ws),
+                            _dev(k_new, "k_new", torch.float16), _dev(v_new, "v_new", torch.float16),
+                            _dev(block_table, "block_table", torch.int32),
+                            _dev(seq_lens, "seq_lens", torch.int32),
+                            _dev(free_pages, "free_pages", torch.int32, nullable=True),
+                            _dev(free_count, "free_count", torch.int32, nullable=True),
+                            _dev(k_cache, "k_cache", torch.float16),
+                            _dev(v_cache, "v_cache", torch.float16), _stream(stream)),
+          "pkv_append_plan")
 
 
 def pkv_policy_default() -> PolicyCfg:

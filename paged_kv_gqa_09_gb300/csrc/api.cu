@@ -288,15 +288,13 @@ size_t pkv_partials_size(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
     return (size_t)partial_slots(s, c) * (size_t)(s->d + 2) * sizeof(float);
 }
 
-int pkv_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, const int32_t *d_seq_lens, void *d_ws,
-             void *stream)
+}  // extern "C"
+
+namespace {
+
+PlanParams plan_params(const pkv_shape_t *s, const pkv_plan_cfg_t *c, const int32_t *d_seq_lens,
+                       void *d_ws)
 {
-    PKV_TRY(check_shape(s));
-    PKV_TRY(check_cfg(s, c));
-    if (c->path != PKV_PATH_WORKQUEUE)
-        return PKV_OK;
-    PKV_TRY(check_ptr(d_seq_lens, "seq_lens"));
-    PKV_TRY(check_ptr(d_ws, "workspace"));
     PlanParams p = {};
     p.seq_lens = d_seq_lens;
     p.ws = ws_hdr(d_ws);
@@ -312,6 +310,65 @@ int pkv_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, const int32_t *d_seq
     p.C = c->split_tokens;
     p.len_cap = len_cap(s);
     p.max_tasks = cap;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, const int32_t *d_seq_lens, void *d_ws,
+             void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    if (c->path != PKV_PATH_WORKQUEUE)
+        return PKV_OK;
+    PKV_TRY(check_ptr(d_seq_lens, "seq_lens"));
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    const PlanParams p = plan_params(s, c, d_seq_lens, d_ws);
+    cudaError_t e = launch_plan(p, static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "plan launch");
+    g_cnt.plan++;
+    return PKV_OK;
+}
+
+int pkv_append_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const void *k_new,
+                    const void *v_new, int32_t *bt, int32_t *sl, const int32_t *free_pages,
+                    int32_t *free_count, void *k_cache, void *v_cache, void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    if (c->path != PKV_PATH_WORKQUEUE)
+        return fail(PKV_EINVAL, "pkv_append_plan builds the WORKQUEUE plan");
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PKV_TRY(check_ptr(k_new, "k_new"));
+    PKV_TRY(check_ptr(v_new, "v_new"));
+    PKV_TRY(check_ptr(bt, "block_table"));
+    PKV_TRY(check_ptr(sl, "seq_lens"));
+    PKV_TRY(check_ptr(k_cache, "k_cache"));
+    PKV_TRY(check_ptr(v_cache, "v_cache"));
+    if ((free_pages == nullptr) != (free_count == nullptr))
+        return fail(PKV_EINVAL, "free_pages and free_count go together");
+    if (free_pages) {
+        PKV_TRY(check_ptr(free_pages, "free_pages"));
+        if (reinterpret_cast<uintptr_t>(free_count) & 3u)
+            return fail(PKV_EINVAL, "free_count is not 4-byte aligned");
+    }
+    PlanParams p = plan_params(s, c, sl, d_ws);
+    p.k_new = static_cast<const __half *>(k_new);
+    p.v_new = static_cast<const __half *>(v_new);
+    p.k_cache = static_cast<__half *>(k_cache);
+    p.v_cache = static_cast<__half *>(v_cache);
+    p.bt = bt;
+    p.seq_lens_rw = sl;
+    p.free_pages = free_pages;
+    p.free_count = free_count;
+    p.d = s->d;
+    p.log2P = ilog2(s->page_size);
+    p.num_pages = s->num_pages;
+    p.bt_stride = s->bt_stride;
     cudaError_t e = launch_plan(p, static_cast<cudaStream_t>(stream), true);
     if (e != cudaSuccess)
         return cuda_fail(e, "plan launch");
@@ -738,6 +795,9 @@ int pkv_get_error(void *d_ws, void *stream)
         return fail(PKV_EDEVICE, "row %d has length %d beyond its limit %d", h[1], h[2], h[3]);
     case kErrNegLen:
         return fail(PKV_EDEVICE, "row %d has negative length %d", h[1], h[2]);
+    case kErrNoPage:
+        return fail(PKV_EDEVICE, "no free page for row %d at length %d (%d pages were free)", h[1],
+                    h[2], h[3]);
     case kErrBadRow:
         return fail(PKV_EDEVICE, "row list entry %d is %d, outside [0, %d)", h[1], h[2], h[3]);
     case kErrTimeout:

@@ -21,6 +21,7 @@ enum DevErr : int32_t {
     kErrCapacity = 4,  // workqueue larger than max_tasks: nothing decoded
     kErrNegLen = 5,    // negative length: row treated as empty
     kErrBadRow = 6,    // a row list entry outside [0, B): that row skipped
+    kErrNoPage = 7,    // the free list ran out: that row's token not appended
 };
 
 // First 64 bytes of the plan workspace.

@@ -36,6 +36,16 @@ struct PlanParams {
     int B, Hq, Hkv, G, C;
     int len_cap;       // bt_stride * page_size: lengths are clamped to it
     int64_t max_tasks;
+    // fused append (k_new != nullptr): before planning, write one new token per
+    // row and advance its length; with free_pages, a token that starts a page
+    // takes one from the free list
+    const __half *k_new, *v_new;
+    __half *k_cache, *v_cache;
+    int32_t *bt;                // written when a page is allocated
+    int32_t *seq_lens_rw;       // the lengths, advanced in place
+    const int32_t *free_pages;  // free page ids, top of the stack at the end
+    int32_t *free_count;        // entries of free_pages in use
+    int d, log2P, num_pages, bt_stride;
 };
 
 struct DecodeParams {

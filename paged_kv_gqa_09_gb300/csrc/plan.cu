@@ -58,21 +58,109 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int *t
     return ex;
 }
 
+// The fused append: for every row i with length N, write k_new[i], v_new[i]
+// into page block_table[i][N / P], slot N % P, and set the length to N + 1.
+// With a free list, a row whose new token starts a page (N % P == 0) takes
+// free_pages[count - 1 - rank], rank = the row's place among such rows (a
+// block scan, so the assignment is deterministic), and the table names it.
+// A row that cannot append (no room in its table, no free page, a bad page
+// id) keeps its length and the error is recorded.  Rows are processed in
+// chunks of one block: each thread settles its row's destination, then the
+// whole block copies the chunk's tokens 16 bytes at a time.
+__device__ void append_tokens(const PlanParams &p, int *warp_tot, long long *s_dst)
+{
+    const int tid = threadIdx.x;
+    const int P = 1 << p.log2P;
+    const int chunks = p.Hkv * p.d / 8;  // 16-byte chunks of one token's K (or V)
+    const int avail = p.free_pages ? *p.free_count : 0;
+    int taken = 0;
+    for (int base = 0; base < p.B; base += kPlanThreads) {
+        const int i = base + tid;
+        int N = 0, need = 0;
+        if (i < p.B) {
+            N = p.seq_lens_rw[i];
+            need = (p.free_pages && N >= 0 && (N & (P - 1)) == 0 && N < p.len_cap) ? 1 : 0;
+        }
+        int tot;
+        const int rank = block_exclusive_scan(need, warp_tot, &tot);
+        int page = -1;
+        bool ok = i < p.B && N >= 0 && N < p.len_cap;
+        if (i < p.B && !ok)
+            report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.len_cap);
+        if (ok && need) {
+            const int slot = avail - 1 - (taken + rank);
+            if (slot < 0) {
+                report_error(p.ws, kErrNoPage, i, N, avail);
+                ok = false;
+            } else {
+                page = p.free_pages[slot];
+                p.bt[(int64_t)i * p.bt_stride + (N >> p.log2P)] = page;
+            }
+        } else if (ok) {
+            page = p.bt[(int64_t)i * p.bt_stride + (N >> p.log2P)];
+        }
+        if (ok && (page < 0 || page >= p.num_pages)) {
+            report_error(p.ws, kErrBadPage, i, N >> p.log2P, page);
+            ok = false;
+        }
+        s_dst[tid] = ok ? (long long)(((size_t)page * P + (N & (P - 1))) * (size_t)chunks) : -1ll;
+        if (ok)
+            p.seq_lens_rw[i] = N + 1;
+        __syncthreads();
+        const int rows = min(kPlanThreads, p.B - base);
+        const int total = rows * chunks;
+        constexpr int U = 4;
+        for (int e0 = tid; e0 < total; e0 += kPlanThreads * U) {
+            int4 a[U], b[U];
+            long long dst[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int e = e0 + u * kPlanThreads;
+                dst[u] = -1;
+                if (e < total) {
+                    const int r = e / chunks, c = e - r * chunks;
+                    if (s_dst[r] >= 0) {
+                        dst[u] = s_dst[r] + c;
+                        const size_t src = (size_t)(base + r) * chunks + c;
+                        a[u] = reinterpret_cast<const int4 *>(p.k_new)[src];
+                        b[u] = reinterpret_cast<const int4 *>(p.v_new)[src];
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (dst[u] >= 0) {
+                    reinterpret_cast<int4 *>(p.k_cache)[dst[u]] = a[u];
+                    reinterpret_cast<int4 *>(p.v_cache)[dst[u]] = b[u];
+                }
+            }
+        }
+        taken += tot;
+        __syncthreads();
+    }
+    if (tid == 0 && p.free_pages)
+        *p.free_count = avail - (taken < avail ? taken : avail);
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
 {
     __shared__ int warp_tot[33];
+    __shared__ long long s_dst[kPlanThreads];
     pdl_wait();
     pdl_trigger();
     const int tid = threadIdx.x;
 
     // n_i = ceil(N_i / C) and r_i = 1 when row i ends in a shorter split; both
     // scanned over the rows (in chunks of one block)
+    if (p.k_new)
+        append_tokens(p, warp_tot, s_dst);
     int carry = 0, carry_r = 0;
     for (int base = 0; base < p.B; base += kPlanThreads) {
         const int i = base + tid;
         int n = 0, r = 0;
         if (i < p.B) {
-            int N = p.seq_lens[i];
+            int N = p.k_new ? p.seq_lens_rw[i] : p.seq_lens[i];  // the same thread wrote it
             if (N < 0 || N > p.len_cap)
                 report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.len_cap);
             N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);

@@ -266,3 +266,18 @@ def gen_step_q(tr: Trace, step: int) -> np.ndarray:
         return gen_q(tr)
     rng = np.random.default_rng([tr.seed, tr.cfg_id, 11, step])
     return rng.standard_normal((tr.B, tr.Hq, tr.d), dtype=np.float32).astype(np.float16)
+
+
+def allocation_split(tr: Trace) -> tuple[np.ndarray, np.ndarray]:
+    """For decode loops that allocate pages on the device: the block table with
+    only the pages each row's current tokens fill (the rest set to -1), and the
+    remaining pool pages as a free list in the shuffled order the table gave
+    them (returned reversed, so the first page a row would take is on top)."""
+    bt = tr.block_table.copy()
+    free = []
+    for i in range(tr.B):
+        n = _pages(int(tr.seq_lens[i]), tr.page_size)
+        row = bt[i]
+        free.extend(row[n:][row[n:] >= 0].tolist())
+        row[n:] = -1
+    return bt, np.array(free[::-1], dtype=np.int32)

@@ -1,0 +1,106 @@
+"""The step's KV write fused into the workqueue plan (pkv_append_plan), with
+pages allocated on the device from a free list, over a multi-step decode
+loop.  A host mirror applies the documented rule (rows whose new token starts
+a page take free_pages[count - 1 - rank] in row order) to its own copy of the
+cache, block table and lengths; the oracle runs on that mirror."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pkv_traces as T
+from paged_kv_gqa_09_gb300 import _lib, api
+
+from gpu_util import check_error_free, close, close_lse, dev, shape_of
+
+pytestmark = pytest.mark.gpu
+
+P, HQ, HKV, D, C = 16, 8, 2, 128, 64
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_loaded():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_gqa_09_gb300 import build
+    build.build()
+    _lib.load()
+
+
+def setup(lens0, steps, spare_pages):
+    tr = T.custom_trace(lens0, HQ, HKV, D, P, C, extra_pages=spare_pages,
+                        extra_cols=steps // P + 2, tag=700)
+    k, v = T.gen_kv(tr)
+    used = set(tr.block_table[tr.block_table >= 0].tolist())
+    rng = np.random.default_rng([T.HELDOUT_SEED, 701])
+    free = [int(x) for x in rng.permutation(tr.num_pages) if int(x) not in used]
+    return tr, k, v, free
+
+
+def mirror_append(tr, k_h, v_h, bt_h, lens_h, free_h, count, kn, vn):
+    cap = tr.bt_stride * P
+    need = [i for i in range(tr.B) if lens_h[i] % P == 0 and lens_h[i] < cap]
+    for rank, i in enumerate(need):
+        bt_h[i, lens_h[i] // P] = free_h[count - 1 - rank]
+    count -= len(need)
+    for i in range(tr.B):
+        pg, sl = bt_h[i, lens_h[i] // P], lens_h[i] % P
+        k_h[pg, sl], v_h[pg, sl] = kn[i], vn[i]
+        lens_h[i] += 1
+    return count
+
+
+def test_fused_append_allocates_pages_and_matches_oracle():
+    steps = 40
+    tr, k, v, free = setup([15, 16, 40, 0, 33, 64, 1], steps, spare_pages=30)
+    k_h, v_h = k.copy(), v.copy()
+    bt_h, lens_h, count = tr.block_table.copy(), tr.seq_lens.astype(np.int64).copy(), len(free)
+    kd, vd, btd, sld = dev(k), dev(v), dev(tr.block_table), dev(tr.seq_lens)
+    freed = dev(np.array(free, np.int32))
+    cnt = torch.tensor([len(free)], dtype=torch.int32, device="cuda")
+    shape = shape_of(tr)
+    cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, C)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    part = torch.empty(api.pkv_partials_size(shape, cfg) // 4, dtype=torch.float32, device="cuda")
+    o = torch.empty((tr.B, HQ, D), dtype=torch.float16, device="cuda")
+    lse = torch.empty((tr.B, HQ), dtype=torch.float32, device="cuda")
+    api.pkv_reset_counters()
+    for step in range(steps):
+        kn, vn = T.gen_append_tokens(tr, step)
+        q = T.gen_step_q(tr, step)
+        count = mirror_append(tr, k_h, v_h, bt_h, lens_h, free, count, kn, vn)
+        api.pkv_append_plan(shape, cfg, ws, dev(kn), dev(vn), btd, sld, kd, vd, freed, cnt)
+        api.pkv_decode(shape, cfg, ws, dev(q), kd, vd, btd, sld, part)
+        api.pkv_merge(shape, cfg, ws, sld, part, o, lse)
+        if step in (0, 7, 23, steps - 1):
+            torch.cuda.synchronize()
+            check_error_free(ws)
+            assert np.array_equal(btd.cpu().numpy(), bt_h)
+            assert np.array_equal(sld.cpu().numpy(), lens_h)
+            assert int(cnt.item()) == count
+            oref, lref = oracle.attention(q, k_h, v_h, bt_h, lens_h.astype(np.int32), tr.scale)
+            close(o, oref, f"o at step {step}")
+            close_lse(lse, lref)
+    c = api.pkv_get_counters()
+    assert c["plan_launches"] == steps and c["append_launches"] == 0      # one launch per step
+    assert c["decode_launches"] == steps and c["merge_launches"] == steps
+    used = bt_h[bt_h >= 0]
+    assert len(np.unique(used)) == used.size                               # no page handed out twice
+
+
+def test_fused_append_reports_an_empty_free_list():
+    tr, k, v, free = setup([16, 32, 5], steps=4, spare_pages=1)
+    kd, vd, btd, sld = dev(k), dev(v), dev(tr.block_table), dev(tr.seq_lens)
+    freed = dev(np.array(free, np.int32))
+    cnt = torch.tensor([len(free)], dtype=torch.int32, device="cuda")
+    shape = shape_of(tr)
+    cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, C)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    kn, vn = T.gen_append_tokens(tr, 0)
+    api.pkv_append_plan(shape, cfg, ws, dev(kn), dev(vn), btd, sld, kd, vd, freed, cnt)
+    st, msg = api.pkv_get_error(ws)
+    # rows 0 and 1 both start a page, only one page is free: row 0 gets it
+    assert st == _lib.PKV_EDEVICE and "no free page" in msg, msg
+    assert sld.cpu().numpy().tolist() == [17, 32, 6]
+    assert int(cnt.item()) == 0
+    assert btd.cpu().numpy()[0, 1] == free[len(free) - 1]
