@@ -409,13 +409,32 @@ class HostDecodeLoop:
                  max_tasks: int = 0):
         dev = k_cache.device
         d = int(k_cache.shape[3])
-        self.q = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
-        self.bt = torch.empty((B, bt_stride), dtype=torch.int32, device=dev)
-        self.sl = torch.empty((B,), dtype=torch.int32, device=dev)
-        self.o = torch.empty_like(self.q)
-        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-        self.h_o = torch.empty(self.q.shape, dtype=torch.float16).pin_memory()
-        self.h_lse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        # the step's inputs (q | block table | lengths) and outputs (o | lse) each
+        # live in one buffer, on the device and pinned on the host, so that a
+        # step moves them with one copy each way
+        a16 = lambda n: (n + 15) // 16 * 16
+        qb, btb, slb = B * Hq * d * 2, B * bt_stride * 4, B * 4
+        ob, lb = qb, B * Hq * 4
+        in_sizes, out_sizes = [a16(qb), a16(btb), a16(slb)], [a16(ob), a16(lb)]
+        self.d_in = torch.empty(sum(in_sizes), dtype=torch.uint8, device=dev)
+        self.h_in = torch.empty(sum(in_sizes), dtype=torch.uint8).pin_memory()
+        self.d_out = torch.empty(sum(out_sizes), dtype=torch.uint8, device=dev)
+        self.h_out = torch.empty(sum(out_sizes), dtype=torch.uint8).pin_memory()
+
+        def views(buf, sizes, specs):
+            out, off = [], 0
+            for size, (n, dtype, shape) in zip(sizes, specs):
+                out.append(buf[off:off + n].view(dtype).view(shape))
+                off += size
+            return out
+
+        in_specs = [(qb, torch.float16, (B, Hq, d)), (btb, torch.int32, (B, bt_stride)),
+                    (slb, torch.int32, (B,))]
+        out_specs = [(ob, torch.float16, (B, Hq, d)), (lb, torch.float32, (B, Hq))]
+        self.q, self.bt, self.sl = views(self.d_in, in_sizes, in_specs)
+        self.h_q, self.h_bt, self.h_sl = views(self.h_in, in_sizes, in_specs)
+        self.o, self.lse = views(self.d_out, out_sizes, out_specs)
+        self.h_o, self.h_lse = views(self.h_out, out_sizes, out_specs)
         self.shape = make_shape(self.q, k_cache, self.bt, scale)
         p, c = pkv_policy(B, n_max, policy)
         if path is not None:
@@ -430,6 +449,8 @@ class HostDecodeLoop:
         self.k, self.v = k_cache, v_cache
         self._fn = _lib.load().pkv_decode_step_host
         self._refs = (ctypes.byref(self.shape), ctypes.byref(self.cfg))
+        self._graph = None
+        self._graph_stream = None
 
     def step(self, h_q: torch.Tensor, h_block_table: Optional[torch.Tensor] = None,
              h_seq_lens: Optional[torch.Tensor] = None, stream=None):
@@ -444,4 +465,40 @@ class HostDecodeLoop:
                       self.k.data_ptr(), self.v.data_ptr(), self.o.data_ptr(), self.h_o.data_ptr(),
                       self.lse.data_ptr(), self.h_lse.data_ptr(), st)
         check(rc, "pkv_decode_step_host")
+        return self.h_o, self.h_lse
+
+    def capture(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        """Capture one whole host step as a CUDA graph: one copy of the pinned
+        inputs `h_q`, `h_bt`, `h_sl` (views of one buffer) to the device, the
+        decode step, one copy of o and lse back into `h_o`, `h_lse`.  Afterwards each
+        step is `step_graph()`: write the inputs into the staging tensors, one
+        graph launch, one synchronize.  Capture needs a non-default stream."""
+        st = stream if stream is not None else torch.cuda.current_stream()
+        if st.cuda_stream == torch.cuda.default_stream(st.device).cuda_stream:
+            raise ValueError("capture needs a non-default stream")
+        L = _lib.load()
+        part = self.partials.data_ptr() if self.partials is not None else None
+
+        def body():
+            self.d_in.copy_(self.h_in, non_blocking=True)
+            check(L.pkv_decode_step(self._refs[0], self._refs[1], self.ws.data_ptr(),
+                                    self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                    self.bt.data_ptr(), self.sl.data_ptr(), part, self.o.data_ptr(),
+                                    self.lse.data_ptr(), st.cuda_stream), "pkv_decode_step")
+            self.h_out.copy_(self.d_out, non_blocking=True)
+
+        with torch.cuda.stream(st):
+            body()  # an eager step first (binds lazily-created state)
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                body()
+        self._graph, self._graph_stream = g, st
+
+    def step_graph(self):
+        """Replay the captured step and wait for it; returns the pinned (o, lse)."""
+        if self._graph is None:
+            raise RuntimeError("capture() first")
+        self._graph.replay()
+        self._graph_stream.synchronize()
         return self.h_o, self.h_lse

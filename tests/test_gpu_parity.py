@@ -421,3 +421,22 @@ def test_row_list_step_leaves_other_rows_untouched():
                              o, lse)
     st, msg = api.pkv_get_error(ws)
     assert st == _lib.PKV_EDEVICE and "row list" in msg, msg
+
+
+def test_host_loop_graph_step_matches_oracle():
+    tr = T.make_trace(2)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    loop = api.HostDecodeLoop(dev(k), dev(v), tr.B, tr.Hq, tr.bt_stride, tr.n_max,
+                              path=BUCKETED, split_tokens=tr.split_tokens)
+    loop.h_q.copy_(torch.from_numpy(q))
+    loop.h_bt.copy_(torch.from_numpy(tr.block_table))
+    loop.h_sl.copy_(torch.from_numpy(tr.seq_lens))
+    s = torch.cuda.Stream()
+    loop.capture(s)
+    oref, lref = oracle_out(tr, q, k, v)
+    for _ in range(3):
+        o, lse = loop.step_graph()
+        close(o, oref)
+        close_lse(lse, lref)
+    check_error_free(loop.ws)
