@@ -353,6 +353,13 @@ int pkv_step_model(int32_t path_or_exact, const pkv_shape_t *shape, int32_t spli
  * pkv_last_error_string()). */
 int pkv_get_error(void *d_ws, void *stream);
 
+/* Test hook for the bounded-wait path: the next n decode or single-pass
+ * launches run with CTA 0 leaving its first pipeline stage unfilled, so the
+ * consumer warps' wait on it runs out (after about 1 s); the kernel records
+ * PKV_ETIMEOUT, drains its own copies and returns.  Nothing faults, traps or
+ * hangs; the outputs of such a launch are meaningless.  0 switches it off. */
+int pkv_test_starve_next_decodes(int32_t n);
+
 /* Description of the last failure on the calling thread ("" if none). */
 const char *pkv_last_error_string(void);
 

@@ -40,7 +40,7 @@ EXPORTS = [
     "pkv_append", "pkv_append_plan", "pkv_policy_default", "pkv_policy",
     "pkv_cost_model_default", "pkv_policy_learned",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error",
-    "pkv_last_error_string", "pkv_version",
+    "pkv_test_starve_next_decodes", "pkv_last_error_string", "pkv_version",
 ]
 
 
@@ -144,6 +144,7 @@ def load() -> ctypes.CDLL:
             "pkv_reset_counters": (ctypes.c_int, []),
             "pkv_step_model": (ctypes.c_int, [i32, S, i32, i32, vp, ctypes.POINTER(StepModel)]),
             "pkv_get_error": (ctypes.c_int, [vp, vp]),
+            "pkv_test_starve_next_decodes": (ctypes.c_int, [i32]),
             "pkv_last_error_string": (ctypes.c_char_p, []),
             "pkv_version": (ctypes.c_int, []),
         }

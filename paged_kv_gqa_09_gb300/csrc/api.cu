@@ -40,6 +40,8 @@ struct Counters {
     std::atomic<int64_t> plan{0}, decode{0}, merge{0}, single{0}, append{0};
 } g_cnt;
 
+std::atomic<int32_t> g_starve{0};  // decode launches left to run with the test hook
+
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 int ilog2(int x)
 {
@@ -233,6 +235,11 @@ int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_
     p.box_log2 = ilog2(box_tok);
     p.len_cap = len_cap(s);
     p.scale_log2 = s->scale * 1.4426950408889634f;
+    for (int32_t n = g_starve.load(); n > 0;)
+        if (g_starve.compare_exchange_weak(n, n - 1)) {
+            p.starve_first_stage = 1;
+            break;
+        }
     int64_t ntasks = 0;
     if (mode == kModeSingle) {
         p.o = static_cast<__half *>(o);
@@ -808,6 +815,14 @@ int pkv_get_error(void *d_ws, void *stream)
     default:
         return fail(PKV_EDEVICE, "device error code %d", h[0]);
     }
+}
+
+int pkv_test_starve_next_decodes(int32_t n)
+{
+    if (n < 0)
+        return fail(PKV_EINVAL, "negative count");
+    g_starve = n;
+    return PKV_OK;
 }
 
 const char *pkv_last_error_string(void) { return g_err.c_str(); }

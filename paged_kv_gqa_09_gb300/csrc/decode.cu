@@ -286,6 +286,17 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                         break;
                     }
                     pend &= ~(1u << stage);
+                    if (p.starve_first_stage && blockIdx.x == 0 && stage == 0 && ph == 0) {
+                        // test hook: leave the consumers' first full barrier
+                        // without arrival or copies, so their bounded wait runs out
+                        if (lane == 0)
+                            meta[stage] = make_int4(cur.i, cur.g, cur.sbase, flags);
+                        if (++stage == L::kStages) {
+                            stage = 0;
+                            ph ^= 1;
+                        }
+                        continue;
+                    }
                     const int nb = (nv + (1 << btl) - 1) >> btl;
                     const uint32_t kdst = sbase + stage * L::kStageBytes;
                     const uint32_t vdst = kdst + L::kTileBytes;

@@ -66,6 +66,7 @@ struct DecodeParams {
     int n_tasks;       // rect/single: tasks in the grid; queue: capacity
     int len_cap;       // bt_stride * page_size
     float scale_log2;  // scale * log2(e)
+    int starve_first_stage;  // test hook: CTA 0 never fills its first stage
 };
 
 struct MergeParams {

@@ -440,3 +440,27 @@ def test_host_loop_graph_step_matches_oracle():
         close(o, oref)
         close_lse(lse, lref)
     check_error_free(loop.ws)
+
+
+# ------------------------------------------------------------------ bounded waits
+
+def test_a_starved_barrier_times_out_and_the_context_stays_usable():
+    """A barrier wait that nothing completes (test hook) runs out after its
+    bound; the kernel reports PKV_ETIMEOUT and returns, and the next launch on
+    the same context is correct."""
+    tr = T.make_trace(1)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    d = upload(tr, q, k, v)
+    L = _lib.load()
+    assert L.pkv_test_starve_next_decodes(1) == 0
+    try:
+        o, lse, ws, _ = run_path(tr, d, BUCKETED)
+    finally:
+        L.pkv_test_starve_next_decodes(0)
+    st, msg = api.pkv_get_error(ws)
+    assert st == _lib.PKV_ETIMEOUT, msg
+    o, lse, ws, _ = run_path(tr, d, BUCKETED)
+    check_error_free(ws)
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o, oref)
