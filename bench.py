@@ -68,6 +68,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--merge", default="separate", choices=["fused", "separate"],
+                    help="split paths: merge on the decode's tail, or in a second kernel")
     return ap.parse_args()
 
 
@@ -340,7 +342,8 @@ def run_pkv(args, rank, local, ws, pg):
         C = tr.split_tokens  # the workload fixes its split size (S splits)
     n_max_run = tr.n_max + (tr.steps if appends else 0)
     bucket = n_max_run if path == 0 else 0
-    cfg = api.make_cfg(path, C, bucket)
+    fused = args.merge == "fused" and path != 2
+    cfg = api.make_cfg(path, C, bucket, 0, api.PKV_MERGE_FUSED if fused else api.PKV_MERGE_SEPARATE)
     wsb = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device=dev)
     npart = api.pkv_partials_size(shape, cfg)
     part = torch.empty(max(npart // 4, 4), dtype=torch.float32, device=dev)
@@ -369,6 +372,10 @@ def run_pkv(args, rank, local, ws, pg):
             rc = L.pkv_append_plan(sref, cref, P(wsb), P(kn), P(vn), P(bt), P(sl), P(free_pages),
                                    P(free_count), P(kk), P(vv), sp)
             _lib.check(rc, "pkv_append_plan")
+            if fused:
+                _lib.check(L.pkv_decode_merge(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl),
+                                              P(part), P(o), P(lse), sp), "pkv_decode_merge")
+                return
             _lib.check(L.pkv_decode(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(part), sp),
                        "pkv_decode")
             _lib.check(L.pkv_merge(sref, cref, P(wsb), P(sl), P(part), P(o), P(lse), sp), "pkv_merge")
@@ -470,7 +477,9 @@ def run_pkv(args, rank, local, ws, pg):
         if path == 2:
             rc = L.pkv_single_pass(sref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(o), P(lse), sp)
         else:
-            rc = L.pkv_decode(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(part), sp)
+            rc = (L.pkv_decode_merge(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(part),
+                                     P(o), P(lse), sp) if fused else
+                  L.pkv_decode(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(part), sp))
         evs[s][1].record(stream)
         _lib.check(rc, "decode")
     torch.cuda.synchronize()
@@ -485,7 +494,7 @@ def run_pkv(args, rank, local, ws, pg):
         if appends:
             reset_lengths()
         e2e = run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps if not appends else steps,
-                      appends, kn, vn, wsb)
+                      appends, kn, vn, wsb, cfg.merge)
 
     gbs = kv_step / (ms * 1e-3) / 1e9
     total = whole_job_gbs(kv_step, ms_max, ws)
@@ -506,13 +515,15 @@ def run_pkv(args, rank, local, ws, pg):
         "data": "synthetic",
         "config": {
             "workload": WORKLOADS[cfg_id], "path": ["bucketed-split", "workqueue", "single-pass"][path],
+            "merge": ("fused" if fused else "separate") if path != 2 else None,
             "split_tokens": C, "kv_bytes_per_step": kv_step, "seed": tr.seed,
             "l2": (f"{R} KV pools rotated ({R * pool_bytes / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB)"
                    if R > 1 else f"inputs ({pool_bytes / 2**30:.1f} GiB) larger than L2"),
             "graph": bool(graphs), "parallelism": f"replicas x{ws}",
         },
         "hbm_frac": total / ws / peak,
-        "roofline": {"bound": "hbm", "kernel": "decode" if path != 2 else "single_pass",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("decode_merge" if fused else "decode") if path != 2 else "single_pass",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src, "traffic": profiled_traffic(cfg_id),
                      "us_per_launch": kms * 1e3, "bytes_per_launch": kv_launch},
@@ -538,7 +549,7 @@ def _ctypes_refs(shape, cfg):
     return ctypes.byref(shape), ctypes.byref(cfg)
 
 
-def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, wsb):
+def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, wsb, merge):
     """Public-API steps with host buffers (HostDecodeLoop -> pkv_decode_step_host):
     every step copies q, the block table and the lengths in from pinned memory
     (and, when the workload appends, the new K/V token), decodes, copies o and
@@ -546,7 +557,8 @@ def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, ws
     from paged_kv_gqa_09_gb300 import _lib
     R = len(pools)
     n_max = int(tr.seq_lens.max()) + (tr.steps if appends else 0)
-    loops = [api.HostDecodeLoop(kk, vv, tr.B, tr.Hq, tr.bt_stride, n_max, path=path, split_tokens=C)
+    loops = [api.HostDecodeLoop(kk, vv, tr.B, tr.Hq, tr.bt_stride, n_max, path=path, split_tokens=C,
+                                merge=merge)
              for kk, vv in pools]
     q_pin = torch.from_numpy(q_h).pin_memory()
     sl0 = torch.from_numpy(tr.seq_lens.copy())

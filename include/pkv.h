@@ -85,17 +85,28 @@ typedef struct {
                              A row longer than the bucket is a device error. */
     int32_t max_tasks;    /* WORKQUEUE: task capacity of the workspace;
                              0 = Hkv * B * ceil(bt_stride*page_size / C) */
+    int32_t merge;        /* split paths, for the step calls (pkv_decode_step
+                             and its variants): PKV_MERGE_SEPARATE or
+                             PKV_MERGE_FUSED (see pkv_decode_merge) */
 } pkv_plan_cfg_t;
+
+/* How a step combines the split states.  SEPARATE is the pages' structure
+ * (Methodology 1, "Sequence splitting": a second kernel merges the states);
+ * FUSED runs the same exact merge on the decode kernel's tail, one launch
+ * fewer per step.  A zero-filled cfg selects SEPARATE. */
+#define PKV_MERGE_SEPARATE 0
+#define PKV_MERGE_FUSED 1
 
 /* ---------------------------------------------------------------- sizes */
 
 /* Bytes of the plan workspace: a 64-byte header (error word, task count),
  * offsets[B+1] and, for WORKQUEUE, the task list (16 bytes per task) followed
  * by internal scheduling data (a balance-ordered copy of the list and one int
- * per row).  Every
- * launching entry point takes this workspace (it holds the error word).  It
- * needs no initialisation except that pkv_get_error() reads and clears the
- * error word; zero it once after allocation. */
+ * per row); split paths end with B*Hkv int32 arrival counters of the fused
+ * merge.  Every launching entry point takes this workspace (it holds the
+ * error word).  Zero it once after allocation: the error word and the
+ * counters must start at zero, and both are back at zero after every call
+ * (pkv_get_error clears the error word, and the counters a timeout left). */
 size_t pkv_plan_workspace_size(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg);
 
 /* Bytes of the fp32 partial-state buffer for split paths: acc[slots][d] then
@@ -154,10 +165,25 @@ int pkv_single_pass(const pkv_shape_t *shape, void *d_ws,
                     const int32_t *d_block_table, const int32_t *d_seq_lens,
                     void *d_o, float *d_lse, void *stream);
 
+/* pkv_decode_merge -- pkv_decode with the exact merge of pkv_merge on its
+ * tail (cfg->merge is not consulted).  One kernel launch.  Every split writes
+ * its state as pkv_decode does, then takes a ticket from an arrival counter
+ * of its (row, kv head) in d_ws; the split drawing the last ticket merges the
+ * row's n_i states of its G heads into o / lse with pkv_merge's formulas and
+ * resets the counter.  A row with one split writes o / lse directly; a row
+ * with N*_i = 0 gets o = 0, lse = -inf; a workqueue overflow writes NaN as
+ * pkv_merge does.  Results equal pkv_decode + pkv_merge up to the order of
+ * the fp32 sums.  Launches on one workspace must not overlap on the GPU. */
+int pkv_decode_merge(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
+                     const void *d_q, const void *d_k_cache, const void *d_v_cache,
+                     const int32_t *d_block_table, const int32_t *d_seq_lens,
+                     float *d_partials, void *d_o, float *d_lse, void *stream);
+
 /* pkv_decode_step -- one whole decode step on the path cfg->path:
  * WORKQUEUE = pkv_plan + pkv_decode + pkv_merge, BUCKETED_SPLIT = pkv_decode +
- * pkv_merge, SINGLE_PASS = pkv_single_pass.  Same arguments and errors as
- * those calls; d_partials may be NULL for SINGLE_PASS. */
+ * pkv_merge, SINGLE_PASS = pkv_single_pass; with cfg->merge == PKV_MERGE_FUSED
+ * pkv_decode_merge replaces pkv_decode + pkv_merge.  Same arguments and
+ * errors as those calls; d_partials may be NULL for SINGLE_PASS. */
 int pkv_decode_step(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
                     const void *d_q, const void *d_k_cache, const void *d_v_cache,
                     const int32_t *d_block_table, const int32_t *d_seq_lens,
@@ -215,7 +241,8 @@ int pkv_append(const pkv_shape_t *shape, void *d_ws, const void *d_k_new,
  * (distinct indices in [0, B); an entry outside is a device error and that
  * row is skipped).  bucket_len must cover the group's longest row; d_partials
  * holds n_rows*S_b*Hq states (pkv_partials_size with B = n_rows).  Two kernel
- * launches; o and lse rows outside the list are left untouched. */
+ * launches (one with PKV_MERGE_FUSED); o and lse rows outside the list are
+ * left untouched. */
 int pkv_decode_step_rows(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
                          const int32_t *d_rows, int32_t n_rows,
                          const void *d_q, const void *d_k_cache, const void *d_v_cache,
@@ -236,9 +263,9 @@ int pkv_decode_step_rows(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, vo
  * - The first call on each device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  * - Every call shares the one array and it keeps the last call's contents:
- *   the call clears the error word and task count itself, but calls that
- *   overlap on the GPU (different streams, or other host threads) race --
- *   serialize them.  Device-side check results stay in the array and are not
+ *   the call clears the error word, task count and merge counters itself,
+ *   but calls that overlap on the GPU (different streams, or other host
+ *   threads) race -- serialize them.  Device-side check results stay in the array and are not
  *   reported; callers needing pkv_get_error use pkv_decode_step. */
 #define PKV_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
 

@@ -22,6 +22,9 @@ PKV_ECAPACITY = -6
 PKV_PATH_BUCKETED_SPLIT = 0
 PKV_PATH_WORKQUEUE = 1
 PKV_PATH_SINGLE_PASS = 2
+
+PKV_MERGE_SEPARATE = 0  # the split states are merged by a second kernel
+PKV_MERGE_FUSED = 1     # merged on the decode kernel's tail
 PATH_EXACT_BUCKETS = 3  # step-model only
 
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # PKV_NOALLOC_SCRATCH_BYTES in include/pkv.h
@@ -35,6 +38,7 @@ STATUS_NAMES = {
 # every symbol include/pkv.h declares
 EXPORTS = [
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
+    "pkv_decode_merge",
     "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_rows", "pkv_decode_step_noalloc",
     "pkv_decode_step_host",
     "pkv_append", "pkv_append_plan", "pkv_policy_default", "pkv_policy",
@@ -63,7 +67,8 @@ class Shape(ctypes.Structure):
 
 class PlanCfg(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("split_tokens", ctypes.c_int32),
-                ("bucket_len", ctypes.c_int32), ("max_tasks", ctypes.c_int32)]
+                ("bucket_len", ctypes.c_int32), ("max_tasks", ctypes.c_int32),
+                ("merge", ctypes.c_int32)]
 
 
 class PolicyCfg(ctypes.Structure):
@@ -125,6 +130,7 @@ def load() -> ctypes.CDLL:
             "pkv_partials_size": (sz, [S, C]),
             "pkv_plan": (ctypes.c_int, [S, C, vp, vp, vp]),
             "pkv_decode": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "pkv_decode_merge": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_merge": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp]),
             "pkv_single_pass": (ctypes.c_int, [S, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_decode_step": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),

@@ -16,13 +16,14 @@ import numpy as np
 import torch
 
 from . import _lib
-from ._lib import (PKV_PATH_BUCKETED_SPLIT, PKV_PATH_SINGLE_PASS, PKV_PATH_WORKQUEUE, Counters,
+from ._lib import (PKV_MERGE_FUSED, PKV_MERGE_SEPARATE, PKV_PATH_BUCKETED_SPLIT,
+                   PKV_PATH_SINGLE_PASS, PKV_PATH_WORKQUEUE, Counters,
                    PlanCfg, PolicyCfg, Shape, StepModel, check)
 
 __all__ = [
     "Shape", "PlanCfg", "PolicyCfg", "make_shape", "make_cfg",
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
-    "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc",
+    "pkv_decode_merge", "PKV_MERGE_SEPARATE", "PKV_MERGE_FUSED", "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc",
     "pkv_decode_step_host", "pkv_decode_step_rows", "exact_length_buckets_step", "pkv_append",
     "pkv_append_plan", "pkv_policy", "pkv_policy_default",
     "pkv_cost_model_default", "pkv_policy_learned",
@@ -76,8 +77,9 @@ def make_shape(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Tensor
                  float(1.0 / math.sqrt(d) if scale is None else scale))
 
 
-def make_cfg(path: int, split_tokens: int = 1024, bucket_len: int = 0, max_tasks: int = 0) -> PlanCfg:
-    return PlanCfg(int(path), int(split_tokens), int(bucket_len), int(max_tasks))
+def make_cfg(path: int, split_tokens: int = 1024, bucket_len: int = 0, max_tasks: int = 0,
+             merge: int = PKV_MERGE_SEPARATE) -> PlanCfg:
+    return PlanCfg(int(path), int(split_tokens), int(bucket_len), int(max_tasks), int(merge))
 
 
 # ------------------------------------------------------------------ C ABI
@@ -120,6 +122,19 @@ def pkv_merge(shape, cfg, ws, seq_lens, partials, o, lse=None, stream=None) -> N
                       _dev(seq_lens, "seq_lens", torch.int32),
                       _dev(partials, "partials", torch.float32), _dev(o, "o", torch.float16),
                       _dev(lse, "lse", torch.float32, nullable=True), _stream(stream)), "pkv_merge")
+
+
+def pkv_decode_merge(shape, cfg, ws, q, k_cache, v_cache, block_table, seq_lens, partials, o,
+                     lse=None, stream=None) -> None:
+    L = _lib.load()
+    check(L.pkv_decode_merge(ctypes.byref(shape), ctypes.byref(cfg), _ws(ws),
+                             _dev(q, "q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
+                             _dev(v_cache, "v_cache", torch.float16),
+                             _dev(block_table, "block_table", torch.int32),
+                             _dev(seq_lens, "seq_lens", torch.int32),
+                             _dev(partials, "partials", torch.float32), _dev(o, "o", torch.float16),
+                             _dev(lse, "lse", torch.float32, nullable=True), _stream(stream)),
+          "pkv_decode_merge")
 
 
 def pkv_single_pass(shape, ws, q, k_cache, v_cache, block_table, seq_lens, o, lse=None,
@@ -339,13 +354,20 @@ class PagedDecoder:
 
     Buffers come from the torch caching allocator on the current device and are
     reused across steps; they are resized when a larger configuration arrives.
+    `merge` picks how split states are combined (a second kernel by default,
+    or PKV_MERGE_FUSED: on the decode's tail); the workspace is zeroed whenever
+    the configuration changes, since the fused merge's counters sit at a place
+    that depends on it.
     """
 
-    def __init__(self, policy: Optional[PolicyCfg] = None, max_split_tasks: int = 0):
+    def __init__(self, policy: Optional[PolicyCfg] = None, max_split_tasks: int = 0,
+                 merge: int = PKV_MERGE_SEPARATE):
         self.policy = policy
         self.max_split_tasks = max_split_tasks
+        self.merge = merge
         self._ws: dict = {}
         self._part: dict = {}
+        self._key: dict = {}
 
     def plan_cfg(self, B: int, n_max: int, path: Optional[int] = None,
                  split_tokens: Optional[int] = None) -> PlanCfg:
@@ -355,15 +377,21 @@ class PagedDecoder:
         if split_tokens is not None:
             c = split_tokens
         bucket = n_max if p == PKV_PATH_BUCKETED_SPLIT else 0
-        return make_cfg(p, c, bucket, self.max_split_tasks if p == PKV_PATH_WORKQUEUE else 0)
+        return make_cfg(p, c, bucket, self.max_split_tasks if p == PKV_PATH_WORKQUEUE else 0,
+                        self.merge)
 
     def buffers(self, shape: Shape, cfg: PlanCfg, device) -> tuple[torch.Tensor, Optional[torch.Tensor]]:
         nws = pkv_plan_workspace_size(shape, cfg)
         npart = pkv_partials_size(shape, cfg)
         ws = self._ws.get(device)
+        key = (tuple(getattr(shape, f) for f, _ in shape._fields_),
+               tuple(getattr(cfg, f) for f, _ in cfg._fields_))
         if ws is None or ws.numel() < nws:
             ws = torch.zeros(max(nws, 64), dtype=torch.uint8, device=device)
             self._ws[device] = ws
+        elif self._key.get(device) != key:
+            ws.zero_()
+        self._key[device] = key
         part = None
         if npart:
             part = self._part.get(device)
@@ -406,7 +434,7 @@ class HostDecodeLoop:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, B: int, Hq: int, bt_stride: int,
                  n_max: int, path: Optional[int] = None, split_tokens: Optional[int] = None,
                  policy: Optional[PolicyCfg] = None, scale: Optional[float] = None,
-                 max_tasks: int = 0):
+                 max_tasks: int = 0, merge: int = PKV_MERGE_SEPARATE):
         dev = k_cache.device
         d = int(k_cache.shape[3])
         # the step's inputs (q | block table | lengths) and outputs (o | lse) each
@@ -442,7 +470,7 @@ class HostDecodeLoop:
         if split_tokens is not None:
             c = split_tokens
         self.cfg = make_cfg(p, c, n_max if p == PKV_PATH_BUCKETED_SPLIT else 0,
-                            max_tasks if p == PKV_PATH_WORKQUEUE else 0)
+                            max_tasks if p == PKV_PATH_WORKQUEUE else 0, merge)
         self.ws = torch.zeros(pkv_plan_workspace_size(self.shape, self.cfg), dtype=torch.uint8, device=dev)
         npart = pkv_partials_size(self.shape, self.cfg)
         self.partials = torch.empty(max(npart // 4, 4), dtype=torch.float32, device=dev) if npart else None

@@ -91,6 +91,8 @@ int check_cfg(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
                     c->split_tokens, s->page_size);
     if (c->bucket_len < 0 || c->max_tasks < 0)
         return fail(PKV_EINVAL, "negative bucket_len or max_tasks");
+    if (c->merge != PKV_MERGE_SEPARATE && c->merge != PKV_MERGE_FUSED)
+        return fail(PKV_EINVAL, "unknown merge mode %d", (int)c->merge);
     return PKV_OK;
 }
 
@@ -212,7 +214,7 @@ WsHeader *ws_hdr(void *ws) { return reinterpret_cast<WsHeader *>(ws); }
 int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_ws, const void *q,
                const void *k, const void *v, const int32_t *bt, const int32_t *sl, float *part,
                void *o, float *lse, cudaStream_t st, const int32_t *rows = nullptr,
-               int n_rows = -1)
+               int n_rows = -1, bool fuse = false)
 {
     int slots = 0;
     PKV_TRY(device_slots(s->d, &slots));
@@ -260,6 +262,19 @@ int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_
             p.tasks = reinterpret_cast<const int4 *>(static_cast<char *>(d_ws) +
                                                      ws_ordered_off(s->B, ntasks));
         }
+        if (fuse) {
+            const size_t co = ws_ctr_off(s->B, mode == kModeQueue, max_tasks(s, c));
+            p.fuse = 1;
+            p.o = static_cast<__half *>(o);
+            p.lse = lse;
+            p.ctr = reinterpret_cast<int32_t *>(static_cast<char *>(d_ws) + co);
+            p.offsets = reinterpret_cast<const int32_t *>(static_cast<char *>(d_ws) + ws_offsets_off());
+            p.n_rows = rows ? n_rows : s->B;
+            if (co / 16 > 0x7fffffffull)
+                return fail(PKV_EUNSUPPORTED, "workspace too large for the counter record");
+            p.ctr_off16 = (int)(co / 16);
+            p.ctr_words = p.n_rows * s->Hkv;
+        }
     }
     if (ntasks > 0x7fffffffLL)
         return fail(PKV_EUNSUPPORTED, "%lld tasks exceed int32", (long long)ntasks);
@@ -282,10 +297,11 @@ size_t pkv_plan_workspace_size(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
 {
     if (check_shape(s) || check_cfg(s, c))
         return 0;
-    size_t n = ws_tasks_off(s->B);
-    if (c->path == PKV_PATH_WORKQUEUE)
-        n = ws_short_off(s->B, max_tasks(s, c)) + sizeof(int32_t) * (size_t)s->B;
-    return n;
+    if (c->path == PKV_PATH_SINGLE_PASS)
+        return ws_tasks_off(s->B);
+    // split paths end with the fused merge's arrival counters
+    return ws_ctr_off(s->B, c->path == PKV_PATH_WORKQUEUE, max_tasks(s, c)) +
+           sizeof(int32_t) * (size_t)s->B * s->Hkv;
 }
 
 size_t pkv_partials_size(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
@@ -402,6 +418,28 @@ int pkv_decode(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const 
                       static_cast<cudaStream_t>(stream));
 }
 
+int pkv_decode_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const void *q,
+                     const void *k, const void *v, const int32_t *bt, const int32_t *sl, float *part,
+                     void *o, float *lse, void *stream)
+{
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    if (c->path == PKV_PATH_SINGLE_PASS)
+        return fail(PKV_EINVAL, "pkv_decode_merge takes a split path; use pkv_single_pass");
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PKV_TRY(check_ptr(q, "q"));
+    PKV_TRY(check_ptr(k, "k_cache"));
+    PKV_TRY(check_ptr(v, "v_cache"));
+    PKV_TRY(check_ptr(bt, "block_table"));
+    PKV_TRY(check_ptr(sl, "seq_lens"));
+    PKV_TRY(check_ptr(part, "partials"));
+    PKV_TRY(check_ptr(o, "o"));
+    PKV_TRY(check_ptr(lse, "lse", true));
+    const int mode = c->path == PKV_PATH_WORKQUEUE ? kModeQueue : kModeRect;
+    return run_decode(s, mode, c, d_ws, q, k, v, bt, sl, part, o, lse,
+                      static_cast<cudaStream_t>(stream), nullptr, -1, true);
+}
+
 }  // extern "C"
 
 namespace {
@@ -476,6 +514,9 @@ int pkv_decode_step_rows(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_
     PKV_TRY(check_ptr(part, "partials"));
     PKV_TRY(check_ptr(o, "o"));
     PKV_TRY(check_ptr(lse, "lse", true));
+    if (c->merge == PKV_MERGE_FUSED)
+        return run_decode(s, kModeRect, c, d_ws, q, k, v, bt, sl, part, o, lse,
+                          static_cast<cudaStream_t>(stream), d_rows, n_rows, true);
     PKV_TRY(run_decode(s, kModeRect, c, d_ws, q, k, v, bt, sl, part, nullptr, nullptr,
                        static_cast<cudaStream_t>(stream), d_rows, n_rows));
     return run_merge(s, c, d_ws, sl, part, o, lse, stream, d_rows, n_rows);
@@ -508,6 +549,8 @@ int pkv_decode_step(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, c
     PKV_TRY(check_ptr(o, "o"));
     PKV_TRY(check_ptr(lse, "lse", true));
     PKV_TRY(pkv_plan(s, c, sl, d_ws, stream));
+    if (c->merge == PKV_MERGE_FUSED)
+        return pkv_decode_merge(s, c, d_ws, q, k, v, bt, sl, part, o, lse, stream);
     PKV_TRY(pkv_decode(s, c, d_ws, q, k, v, bt, sl, part, stream));
     return pkv_merge(s, c, d_ws, sl, part, o, lse, stream);
 }
@@ -785,15 +828,23 @@ int pkv_get_error(void *d_ws, void *stream)
     cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaStreamSynchronize");
-    int32_t h[4] = {0, 0, 0, 0};
-    e = cudaMemcpy(h, d_ws, sizeof h, cudaMemcpyDeviceToHost);
+    WsHeader hd;
+    e = cudaMemcpy(&hd, d_ws, sizeof hd, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMemcpy (error word)");
+    const int32_t h[4] = {hd.err, hd.err_a, hd.err_b, hd.err_c};
     if (h[0] == kErrNone)
         return PKV_OK;
     e = cudaMemset(d_ws, 0, sizeof h);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMemset (error word)");
+    if (h[0] == kErrTimeout && hd.ctr_words > 0) {
+        // a CTA that gave up left its splits' arrival counters mid-count
+        e = cudaMemset(static_cast<char *>(d_ws) + (size_t)hd.ctr_off16 * 16, 0,
+                       (size_t)hd.ctr_words * sizeof(int32_t));
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemset (merge counters)");
+    }
     switch (h[0]) {
     case kErrBadPage:
         return fail(PKV_EDEVICE, "block-table entry out of range: row %d, logical page %d, value %d",

@@ -63,9 +63,10 @@ struct Layout {
     static constexpr int kStages = (D == 128) ? 3 : 6;
     static constexpr int kMetaOff = kStages * kStageBytes;           // int4 per stage
     static constexpr int kRedOff = kMetaOff + kStages * 16;          // [stage][warp 1..3][m 8, l 8]
-    static constexpr int kBarOff = kRedOff + kStages * (kCW - 1) * 2 * kMaxG * 4;
-    // barriers: full[S], empty[S], merge[S]
-    static constexpr int kBytes = kBarOff + 3 * kStages * 8;
+    static constexpr int kDecOff = kRedOff + kStages * (kCW - 1) * 2 * kMaxG * 4;  // int4 per stage
+    static constexpr int kBarOff = kDecOff + kStages * 16;
+    // barriers: full[S], empty[S], merge[S], decision[S]
+    static constexpr int kBytes = kBarOff + 4 * kStages * 8;
     static constexpr int kAlloc = kBytes + 1024;                     // slack for alignment
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
     static_assert(2 * (kAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
@@ -150,6 +151,169 @@ __device__ __forceinline__ uint32_t row_base(int t, int btl)
     return (uint32_t)(((b << btl) * Layout<D>::kDch + s) * 128);
 }
 
+// ---------------------------------------------------------------- fused merge
+//
+// With p.fuse the exact log-sum-exp merge ("Sequence splitting": the split
+// states are combined exactly) runs on the decode's tail instead of in a
+// second kernel.  Every split of (row i, kv head g) publishes its state and
+// takes a ticket from that pair's arrival counter; the split that draws the
+// last ticket merges the row's n_i states of the G heads and writes o / lse,
+// then resets the counter for the next launch.  Nothing waits on another CTA.
+// A row with one split writes o / lse from registers, and rows without
+// tokens are filled by the producer warps after their tasks.
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Splits of batch row i that hold tokens: ceil(N*_i / C), the length clamped
+// as load_task clamps it (a rectangular grid holds at most S_b of them).
+template <int MODE>
+__device__ __forceinline__ int split_count(const DecodeParams &p, int i)
+{
+    int N = p.seq_lens[i];
+    N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);
+    const int n = (N + p.C - 1) / p.C;
+    return MODE == kModeRect ? min(n, p.S_b) : n;
+}
+
+// Consumer warp w's share of the merge of (row i, kv head g): query heads
+// h = w, w + 4, ... of the group, over states base .. base + n - 1:
+//   M = max_j m_j, L = sum_j l_j e^{m_j - M}, o = sum_j acc_j e^{m_j - M} / L,
+//   lse = M + ln L.
+// The states were written by other CTAs, so they are read L2-only.  The merge
+// sits on the launch's tail, so it is latency-bound: each lane keeps up to
+// kMergeBatch state loads in flight, and the first batch is issued before
+// the maximum is known.
+constexpr int kMergeBatch = 8;
+
+template <int VPL>
+__device__ __forceinline__ void load_states(const float *a, int64_t js, int j, int cnt,
+                                            float (&x)[kMergeBatch][VPL])
+{
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+        if (u < cnt) {
+            const float *aj = a + (int64_t)(j + u) * js;
+            if constexpr (VPL == 4) {
+                const float4 t = __ldcg(reinterpret_cast<const float4 *>(aj));
+                x[u][0] = t.x;
+                x[u][1] = t.y;
+                x[u][2] = t.z;
+                x[u][3] = t.w;
+            } else {
+                const float2 t = __ldcg(reinterpret_cast<const float2 *>(aj));
+                x[u][0] = t.x;
+                x[u][1] = t.y;
+            }
+        }
+    }
+}
+
+// acc += sum over the batch of e^{m_j - M} acc_j, the weights held by lanes
+// lane0 .. lane0 + cnt - 1 of wj
+template <int VPL>
+__device__ __forceinline__ void fold_states(float (&acc)[VPL], const float (&x)[kMergeBatch][VPL],
+                                            float wj, int lane0, int cnt)
+{
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+        const float wt = __shfl_sync(0xffffffffu, wj, (lane0 + u) & 31);
+        if (u < cnt) {
+#pragma unroll
+            for (int v = 0; v < VPL; ++v)
+                acc[v] += wt * x[u][v];
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void merge_heads(const float *part_acc, const float *part_m,
+                                         const float *part_l, __half *o, float *lse, int Hq, int G,
+                                         int i, int g, int base, int n, int w)
+{
+    constexpr int VPL = D / 32;  // values of d per lane
+    const int lane = threadIdx.x & 31;
+    const int64_t js = (int64_t)Hq * D;  // floats between consecutive splits' vectors
+    for (int h = w; h < G; h += kCW) {
+        const int64_t s0 = (int64_t)base * Hq + g * G + h;  // split j's state slot: s0 + j * Hq
+        const float *a = part_acc + s0 * D + lane * VPL;
+        float mj = -INFINITY, lj = 0.f;
+        if (lane < n) {
+            mj = __ldcg(part_m + s0 + (int64_t)lane * Hq);
+            lj = __ldcg(part_l + s0 + (int64_t)lane * Hq);
+        }
+        float x[kMergeBatch][VPL];
+        load_states<VPL>(a, js, 0, min(n, kMergeBatch), x);  // in flight during the reduction
+        float M = mj;
+        for (int j = lane + 32; j < n; j += 32)
+            M = fmaxf(M, __ldcg(part_m + s0 + (int64_t)j * Hq));
+#pragma unroll
+        for (int t = 16; t > 0; t >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, t));
+        float Ls = 0.f, acc[VPL];
+#pragma unroll
+        for (int v = 0; v < VPL; ++v)
+            acc[v] = 0.f;
+        for (int j0 = 0; j0 < n; j0 += 32) {
+            if (j0 > 0) {
+                mj = -INFINITY;
+                lj = 0.f;
+                if (j0 + lane < n) {
+                    mj = __ldcg(part_m + s0 + (int64_t)(j0 + lane) * Hq);
+                    lj = __ldcg(part_l + s0 + (int64_t)(j0 + lane) * Hq);
+                }
+            }
+            const float wj = ex2((mj - M) * kLog2e);  // 0 past the row's states
+            Ls += wj * lj;
+            const int cnt = min(32, n - j0);
+            for (int b = 0; b < cnt; b += kMergeBatch) {
+                if (j0 + b > 0)
+                    load_states<VPL>(a, js, j0 + b, min(kMergeBatch, cnt - b), x);
+                fold_states<VPL>(acc, x, wj, b, min(kMergeBatch, cnt - b));
+            }
+        }
+#pragma unroll
+        for (int t = 16; t > 0; t >>= 1)
+            Ls += __shfl_xor_sync(0xffffffffu, Ls, t);
+        const float inv = 1.f / Ls;
+        const int64_t oh = (int64_t)i * Hq + g * G + h;
+        __half *out = o + oh * D + lane * VPL;
+        if constexpr (VPL == 4)
+            *reinterpret_cast<uint2 *>(out) =
+                make_uint2(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv));
+        else
+            *reinterpret_cast<uint32_t *>(out) = pack_half2(acc[0] * inv, acc[1] * inv);
+        if (lse && lane == 0)
+            lse[oh] = M + logf(Ls);
+    }
+}
+
+// Rows of the launch that no task covers: o = 0 and lse = -inf for a row
+// without tokens; after a workqueue overflow (no tasks ran) every row gets
+// NaN, as the merge kernel writes.  CTAs stride over the rows.
+template <int D, int MODE>
+__device__ void fill_uncovered_rows(const DecodeParams &p, int lane)
+{
+    const bool bad = MODE == kModeQueue && p.ws->overflow != 0;
+    const uint32_t w2 = bad ? 0x7e007e00u : 0u;  // two fp16 NaNs, or zeros
+    const int4 fill = make_int4((int)w2, (int)w2, (int)w2, (int)w2);
+    for (int lr = blockIdx.x; lr < p.n_rows; lr += gridDim.x) {
+        int i = lr;
+        if (MODE == kModeRect && p.rows) {
+            i = p.rows[lr];
+            if (i < 0 || i >= p.B)
+                continue;  // reported by load_task
+        }
+        if (!bad && split_count<MODE>(p, i) > 0)
+            continue;
+        int4 *out = reinterpret_cast<int4 *>(p.o + (size_t)i * p.Hq * D);
+        for (int x = lane; x < p.Hq * D / 8; x += 32)
+            out[x] = fill;
+        if (p.lse)
+            for (int h = lane; h < p.Hq; h += 32)
+                p.lse[(size_t)i * p.Hq + h] = bad ? NAN : -INFINITY;
+    }
+}
+
 // ---------------------------------------------------------------- producer
 
 // Block-table entries of pages [s0, s0 + kSeg) of row i, clipped to pg_end:
@@ -187,7 +351,7 @@ __device__ __forceinline__ void load_pages(const DecodeParams &p, int i, int s0,
     check_pages(p, i, s0, pg_end, lane, pid);
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool FUSE>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUtensorMap *tmV,
                                              const DecodeParams &p, int ntasks, uint32_t sbase,
                                              int4 *meta, uint32_t bar_full0, uint32_t bar_empty0)
@@ -260,7 +424,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                     reinterpret_cast<int4 *>(p.o + (size_t)cur.sbase * D)[x] = make_int4(0, 0, 0, 0);
                 if (p.lse && lane < G)
                     p.lse[cur.sbase + lane] = -INFINITY;
-            } else {
+            } else if (!FUSE) {  // the fused merge reads only the splits that hold tokens
                 for (int x = lane; x < G * D / 4; x += 32)
                     reinterpret_cast<float4 *>(p.part_acc + (size_t)cur.sbase * D)[x] =
                         make_float4(0.f, 0.f, 0.f, 0.f);
@@ -347,6 +511,8 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                 meta[stage] = make_int4(0, 0, 0, kEnd);
                 mbar_arrive(bar_full0 + stage * 8);
             }
+            if (FUSE)
+                fill_uncovered_rows<D, MODE>(p, lane);
         } else {
             report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 1);
             ok = false;
@@ -422,7 +588,7 @@ __device__ __forceinline__ uint32_t park_addr(uint32_t ktile, int w, int lane, i
            (uint32_t)(((c & 7) ^ (r & 7)) << 4);
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool FUSE>
 __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sbase, uint8_t *basep,
                                              const int4 *meta, uint32_t bar_full0,
                                              uint32_t bar_empty0, uint32_t bar_merge0)
@@ -456,6 +622,8 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
 
     int stage = 0;
     uint32_t ph = 0, mpar = 0;  // ring lap parity; per-stage merge-barrier parities
+    uint32_t dpar = 0;          // per-stage decision-barrier parities (fused merge)
+    const uint32_t bar_dec0 = bar_merge0 + L::kStages * 8;
     for (;;) {
         const uint32_t full = bar_full0 + stage * 8;
         const bool got = __all_sync(0xffffffffu, mbar_wait(full, ph, kWaitNs));
@@ -558,6 +726,8 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
                 l1 += __shfl_xor_sync(0xffffffffu, l1, o);
             }
             float *rs = red + stage * (kCW - 1) * 2 * kMaxG;  // [warp 1..3][m 8 | l 8]
+            // fused merge: splits of this task's row (a row with one writes o directly)
+            const int nsp = FUSE ? split_count<MODE>(p, mt.x) : 0;
             const uint32_t mbar = bar_merge0 + stage * 8;
             const uint32_t mp = (mpar >> stage) & 1u;
             mpar ^= 1u << stage;
@@ -576,6 +746,21 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
                 fence_proxy_async_smem();  // these K rows are refilled by TMA later
                 mbar_arrive(mbar);
                 // warp 0 releases the stage once it has read the parked states
+                if (nsp > 1) {
+                    // warp 0 publishes whether this split arrived last; if so,
+                    // every consumer warp takes its heads of the merge
+                    const uint32_t dp = (dpar >> stage) & 1u;
+                    dpar ^= 1u << stage;
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_dec0 + stage * 8, dp, kWaitNs))) {
+                        report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 4);
+                        return;
+                    }
+                    const int4 dec = *reinterpret_cast<const int4 *>(basep + L::kDecOff + stage * 16);
+                    if (dec.x) {  // ordered after lane 0's acquire by the barrier
+                        merge_heads<D>(p.part_acc, p.part_m, p.part_l, p.o, p.lse, p.Hq, G, mt.x, mt.y,
+                                       dec.y, nsp, w);
+                    }
+                }
             } else {
                 if (!__all_sync(0xffffffffu, mbar_wait(mbar, mp, kWaitNs))) {
                     report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 3);
@@ -617,25 +802,28 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
                     mbar_arrive_n(bar_empty0 + stage * 8, kCW);  // release for all four warps
                 const int sb0 = mt.z;
                 const bool ok0 = h0 < G, ok1 = h0 + 1 < G;
-                if (MODE == kModeSingle) {
+                if (MODE == kModeSingle || nsp == 1) {
+                    // o / lse from registers: the whole row (single pass), or a
+                    // row of one split (fused merge)
+                    const int ob = MODE == kModeSingle ? sb0 : mt.x * p.Hq + mt.y * G;
                     const float i0 = 1.f / L0, i1 = 1.f / L1;
 #pragma unroll
                     for (int x = 0; x < KS; ++x) {
                         const int d0 = 16 * x + r0;
                         if (ok0) {
-                            p.o[(size_t)(sb0 + h0) * D + d0] = __float2half_rn(O[x][0] * i0);
-                            p.o[(size_t)(sb0 + h0) * D + d0 + 8] = __float2half_rn(O[x][2] * i0);
+                            p.o[(size_t)(ob + h0) * D + d0] = __float2half_rn(O[x][0] * i0);
+                            p.o[(size_t)(ob + h0) * D + d0 + 8] = __float2half_rn(O[x][2] * i0);
                         }
                         if (ok1) {
-                            p.o[(size_t)(sb0 + h0 + 1) * D + d0] = __float2half_rn(O[x][1] * i1);
-                            p.o[(size_t)(sb0 + h0 + 1) * D + d0 + 8] = __float2half_rn(O[x][3] * i1);
+                            p.o[(size_t)(ob + h0 + 1) * D + d0] = __float2half_rn(O[x][1] * i1);
+                            p.o[(size_t)(ob + h0 + 1) * D + d0 + 8] = __float2half_rn(O[x][3] * i1);
                         }
                     }
                     if (lane < 4 && p.lse) {
                         if (ok0)
-                            p.lse[sb0 + h0] = (M0 + log2f(L0)) * kLn2;
+                            p.lse[ob + h0] = (M0 + log2f(L0)) * kLn2;
                         if (ok1)
-                            p.lse[sb0 + h0 + 1] = (M1 + log2f(L1)) * kLn2;
+                            p.lse[ob + h0 + 1] = (M1 + log2f(L1)) * kLn2;
                     }
                 } else {
 #pragma unroll
@@ -660,6 +848,36 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
                             p.part_l[sb0 + h0 + 1] = L1;
                         }
                     }
+                    if (nsp > 1) {
+                        // fused merge: publish this state, then take a ticket; the
+                        // warp barrier orders every lane's state stores before
+                        // lane 0's release, and its acquire orders the merge's reads
+                        __syncwarp();
+                        int base, cidx;
+                        if (MODE == kModeQueue) {
+                            base = p.offsets[mt.x];
+                            cidx = mt.x * p.Hkv + mt.y;
+                        } else {
+                            const int lr = (sb0 / p.Hq) / p.S_b;  // row of the launch
+                            base = lr * p.S_b;
+                            cidx = lr * p.Hkv + mt.y;
+                        }
+                        int last = 0;
+                        if (lane == 0) {
+                            last = atom_add_acq_rel_gpu(p.ctr + cidx, 1) == nsp - 1 ? 1 : 0;
+                            if (last)
+                                p.ctr[cidx] = 0;  // all splits are in: ready for the next launch
+                            *reinterpret_cast<int4 *>(basep + L::kDecOff + stage * 16) =
+                                make_int4(last, base, 0, 0);
+                            mbar_arrive(bar_dec0 + stage * 8);
+                        }
+                        last = __shfl_sync(0xffffffffu, last, 0);
+                        __syncwarp();
+                        if (last) {
+                            merge_heads<D>(p.part_acc, p.part_m, p.part_l, p.o, p.lse, p.Hq, G, mt.x,
+                                           mt.y, base, nsp, 0);
+                        }
+                    }
                 }
             }
             m0 = m1 = -INFINITY;
@@ -675,7 +893,7 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
     }
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p)
@@ -696,6 +914,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(bar_full0 + s * 8, 1);
             mbar_init(bar_empty0 + s * 8, kCW);
             mbar_init(bar_merge0 + s * 8, (kCW - 1) * 32);
+            mbar_init(bar_merge0 + (L::kStages + s) * 8, 1);  // decision (fused merge)
         }
         fence_mbar_init();
     }
@@ -710,18 +929,23 @@ __global__ void __launch_bounds__(kThreads, 2)
     // it has finished and its writes are visible
     pdl_wait();
     pdl_trigger();
+    if (FUSE && blockIdx.x == 0 && threadIdx.x == 0) {
+        p.ws->ctr_off16 = p.ctr_off16;
+        p.ws->ctr_words = p.ctr_words;
+    }
     const int ntasks = (MODE == kModeQueue) ? min(p.ws->task_count, p.n_tasks) : p.n_tasks;
     if (warp == kCW)
-        run_producer<D, MODE>(&tmK, &tmV, p, ntasks, sbase, meta, bar_full0, bar_empty0);
+        run_producer<D, MODE, FUSE>(&tmK, &tmV, p, ntasks, sbase, meta, bar_full0, bar_empty0);
     else
-        run_consumer<D, MODE>(p, sbase, basep, meta, bar_full0, bar_empty0, bar_merge0);
+        run_consumer<D, MODE, FUSE>(p, sbase, basep, meta, bar_full0, bar_empty0, bar_merge0);
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool FUSE>
 cudaError_t launch_one(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
                        cudaStream_t s, bool pdl)
 {
-    auto kern = decode_kernel<D, MODE>;
+    static_assert(!FUSE || MODE != kModeSingle, "the single pass has no merge");
+    auto kern = decode_kernel<D, MODE, FUSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout<D>::kAlloc);
     if (e != cudaSuccess)
@@ -742,7 +966,7 @@ cudaError_t launch_one(const CUtensorMap &tk, const CUtensorMap &tv, const Decod
 template <int D>
 cudaError_t occupancy(int *out)
 {
-    auto kern = decode_kernel<D, kModeQueue>;
+    auto kern = decode_kernel<D, kModeQueue, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout<D>::kAlloc);
     if (e != cudaSuccess)
@@ -759,21 +983,26 @@ cudaError_t decode_ctas_per_sm(int d, int *out)
     return d == 64 ? occupancy<64>(out) : occupancy<128>(out);
 }
 
+template <int D>
+cudaError_t launch_d(int mode, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
+                     int grid, cudaStream_t s, bool pdl)
+{
+    // the fused merge is a separate instance, so the split kernels without it
+    // carry none of its code or registers
+    if (mode == kModeRect)
+        return p.fuse ? launch_one<D, kModeRect, true>(tk, tv, p, grid, s, pdl)
+                      : launch_one<D, kModeRect, false>(tk, tv, p, grid, s, pdl);
+    if (mode == kModeQueue)
+        return p.fuse ? launch_one<D, kModeQueue, true>(tk, tv, p, grid, s, pdl)
+                      : launch_one<D, kModeQueue, false>(tk, tv, p, grid, s, pdl);
+    return launch_one<D, kModeSingle, false>(tk, tv, p, grid, s, pdl);
+}
+
 cudaError_t launch_decode(int d, int mode, const CUtensorMap &tk, const CUtensorMap &tv,
                           const DecodeParams &p, int grid, cudaStream_t s, bool pdl)
 {
-    if (d == 128) {
-        if (mode == kModeRect)
-            return launch_one<128, kModeRect>(tk, tv, p, grid, s, pdl);
-        if (mode == kModeQueue)
-            return launch_one<128, kModeQueue>(tk, tv, p, grid, s, pdl);
-        return launch_one<128, kModeSingle>(tk, tv, p, grid, s, pdl);
-    }
-    if (mode == kModeRect)
-        return launch_one<64, kModeRect>(tk, tv, p, grid, s, pdl);
-    if (mode == kModeQueue)
-        return launch_one<64, kModeQueue>(tk, tv, p, grid, s, pdl);
-    return launch_one<64, kModeSingle>(tk, tv, p, grid, s, pdl);
+    return d == 128 ? launch_d<128>(mode, tk, tv, p, grid, s, pdl)
+                    : launch_d<64>(mode, tk, tv, p, grid, s, pdl);
 }
 
 }  // namespace pkv

@@ -31,7 +31,11 @@ struct WsHeader {
     int32_t task_count;   // tasks written by the plan (0 after an overflow)
     int32_t state_rows;   // sum_i n_i
     int32_t overflow;     // 1 when the plan exceeded max_tasks
-    int32_t pad[9];
+    // arrival counters of the fused merge (written by the decode kernel so
+    // that the host can clear them after a timeout left some mid-count)
+    int32_t ctr_off16;    // byte offset / 16 of the counter array in the workspace
+    int32_t ctr_words;    // int32 counters in it
+    int32_t pad[7];
 };
 static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
 
@@ -69,6 +73,17 @@ __device__ __forceinline__ float ex2(float x)
 
 // Programmatic dependent launch: wait for the preceding grid (and its memory),
 // and allow the next grid in the stream to be scheduled early.
+// Atomic add at GPU scope with acquire-release ordering: the caller's earlier
+// writes (and those it observed, e.g. through a warp barrier) are visible to a
+// thread that later reads the new value, and the caller's later reads see
+// what the writers before it published.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -31,14 +31,18 @@ def shape_of(tr: T.Trace):
 
 
 def run_path(tr: T.Trace, d: dict, path: int, C: int | None = None, bucket: int | None = None,
-             max_tasks: int = 0, want_lse: bool = True):
-    """One decode step through pkv_decode_step; returns (o, lse, ws, partials)."""
+             max_tasks: int = 0, want_lse: bool = True, merge: int = _lib.PKV_MERGE_SEPARATE,
+             ws: torch.Tensor | None = None):
+    """One decode step through pkv_decode_step; returns (o, lse, ws, partials).
+    A given workspace `ws` is reused (it must be zeroed once before first use)."""
     shape = shape_of(tr)
     C = tr.split_tokens if C is None else C
     if bucket is None:
         bucket = tr.n_max if path == _lib.PKV_PATH_BUCKETED_SPLIT else 0
-    cfg = api.make_cfg(path, C, bucket, max_tasks)
-    ws = torch.zeros(max(64, api.pkv_plan_workspace_size(shape, cfg)), dtype=torch.uint8, device="cuda")
+    cfg = api.make_cfg(path, C, bucket, max_tasks, merge)
+    if ws is None:
+        ws = torch.zeros(max(64, api.pkv_plan_workspace_size(shape, cfg)), dtype=torch.uint8,
+                         device="cuda")
     npart = api.pkv_partials_size(shape, cfg)
     part = torch.full((max(npart // 4, 4),), float("nan"), dtype=torch.float32, device="cuda")
     o = torch.full((tr.B, tr.Hq, tr.d), float("nan"), dtype=torch.float16, device="cuda")
@@ -76,7 +80,12 @@ def close_lse(lse_gpu: torch.Tensor, lse_ref: np.ndarray):
         assert err <= LSE_ATOL, f"lse max abs err {err}"
 
 
-def read_plan(ws: torch.Tensor, B: int, with_order: bool = False):
+def merge_counters(ws: torch.Tensor, B: int, Hkv: int) -> np.ndarray:
+    """The fused merge's arrival counters: the workspace's last B*Hkv int32."""
+    return ws[ws.numel() - 4 * B * Hkv:].view(torch.int32).cpu().numpy()
+
+
+def read_plan(ws: torch.Tensor, B: int, with_order: bool = False, Hkv: int = 0):
     h = ws[:64].view(torch.int32).cpu().numpy()
     count = int(h[4])
     off = ws[64:64 + 4 * (B + 1)].view(torch.int32).cpu().numpy()
@@ -84,7 +93,8 @@ def read_plan(ws: torch.Tensor, B: int, with_order: bool = False):
     tasks = ws[t0:t0 + 16 * count].view(torch.int32).cpu().numpy().reshape(-1, 4)
     if not with_order:
         return count, off, tasks, h
-    cap = (ws.numel() - t0 - 4 * B) // 32
+    # workspace = t0 + 32 * cap + short_before[B] (16-byte aligned) + B*Hkv counters
+    cap = (ws.numel() - 4 * B * Hkv - t0 - (4 * B + 15) // 16 * 16) // 32
     o0 = t0 + 16 * cap
     ordered = ws[o0:o0 + 16 * count].view(torch.int32).cpu().numpy().reshape(-1, 4)
     return count, off, tasks, h, ordered

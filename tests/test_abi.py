@@ -42,8 +42,8 @@ def shape(**kw):
     return _lib.Shape(*[base[k] for k, _ in _lib.Shape._fields_])
 
 
-def cfg(path=_lib.PKV_PATH_WORKQUEUE, C=256, bucket=0, max_tasks=0):
-    return _lib.PlanCfg(path, C, bucket, max_tasks)
+def cfg(path=_lib.PKV_PATH_WORKQUEUE, C=256, bucket=0, max_tasks=0, merge=0):
+    return _lib.PlanCfg(path, C, bucket, max_tasks, merge)
 
 
 FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation fails first
@@ -89,6 +89,17 @@ def test_bad_cfg_and_pointers_are_rejected(L):
     assert L.pkv_get_error(None, None) == _lib.PKV_EINVAL
 
 
+def test_unknown_merge_mode_is_rejected(L):
+    s = shape()
+    for bad in (-1, 2):
+        c = cfg(merge=bad)
+        assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(c)) == 0
+        assert L.pkv_decode_merge(ctypes.byref(s), ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, FAKE, FAKE, None, None) == _lib.PKV_EINVAL
+    ok = cfg(merge=_lib.PKV_MERGE_FUSED)
+    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(ok)) > 0
+
+
 def test_plan_is_a_noop_off_the_workqueue(L):
     s = shape()
     for p in (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_PATH_SINGLE_PASS):
@@ -101,15 +112,18 @@ def test_workspace_and_partial_sizes(L):
     c = cfg(C=256)
     tasks_off = (64 + 4 * 4 + 15) // 16 * 16
     cap = 8 * 3 * 4
-    # canonical list, its balance-ordered copy, one int per row
-    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(c)) == tasks_off + 32 * cap + 4 * 3
+    # canonical list, its balance-ordered copy, one int per row, then (16-byte
+    # aligned) one arrival counter of the fused merge per (row, kv head)
+    ctr_off = (tasks_off + 32 * cap + 4 * 3 + 15) // 16 * 16
+    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(c)) == ctr_off + 4 * 3 * 8
     assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(c)) == cap * 4 * (128 + 2) * 4
     c = cfg(C=256, max_tasks=10)
     assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(c)) == 10 * 4 * 130 * 4
     r = cfg(path=_lib.PKV_PATH_BUCKETED_SPLIT, C=256, bucket=600)
-    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(r)) == tasks_off
+    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(r)) == tasks_off + 4 * 3 * 8
     assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(r)) == 3 * 3 * 32 * 130 * 4
     one = cfg(path=_lib.PKV_PATH_SINGLE_PASS)
+    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(one)) == tasks_off
     assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(one)) == 0
 
 

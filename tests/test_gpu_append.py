@@ -50,7 +50,10 @@ def mirror_append(tr, k_h, v_h, bt_h, lens_h, free_h, count, kn, vn):
     return count
 
 
-def test_fused_append_allocates_pages_and_matches_oracle():
+@pytest.mark.parametrize("merge", [_lib.PKV_MERGE_SEPARATE, _lib.PKV_MERGE_FUSED])
+def test_fused_append_allocates_pages_and_matches_oracle(merge):
+    """With merge == FUSED the loop runs two launches per step: append + plan,
+    then the decode with the merge on its tail (pkv_decode_merge)."""
     steps = 40
     tr, k, v, free = setup([15, 16, 40, 0, 33, 64, 1], steps, spare_pages=30)
     k_h, v_h = k.copy(), v.copy()
@@ -70,8 +73,11 @@ def test_fused_append_allocates_pages_and_matches_oracle():
         q = T.gen_step_q(tr, step)
         count = mirror_append(tr, k_h, v_h, bt_h, lens_h, free, count, kn, vn)
         api.pkv_append_plan(shape, cfg, ws, dev(kn), dev(vn), btd, sld, kd, vd, freed, cnt)
-        api.pkv_decode(shape, cfg, ws, dev(q), kd, vd, btd, sld, part)
-        api.pkv_merge(shape, cfg, ws, sld, part, o, lse)
+        if merge == _lib.PKV_MERGE_FUSED:
+            api.pkv_decode_merge(shape, cfg, ws, dev(q), kd, vd, btd, sld, part, o, lse)
+        else:
+            api.pkv_decode(shape, cfg, ws, dev(q), kd, vd, btd, sld, part)
+            api.pkv_merge(shape, cfg, ws, sld, part, o, lse)
         if step in (0, 7, 23, steps - 1):
             torch.cuda.synchronize()
             check_error_free(ws)
@@ -83,7 +89,8 @@ def test_fused_append_allocates_pages_and_matches_oracle():
             close_lse(lse, lref)
     c = api.pkv_get_counters()
     assert c["plan_launches"] == steps and c["append_launches"] == 0      # one launch per step
-    assert c["decode_launches"] == steps and c["merge_launches"] == steps
+    assert c["decode_launches"] == steps
+    assert c["merge_launches"] == (0 if merge == _lib.PKV_MERGE_FUSED else steps)
     used = bt_h[bt_h >= 0]
     assert len(np.unique(used)) == used.size                               # no page handed out twice
 

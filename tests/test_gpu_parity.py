@@ -55,7 +55,7 @@ def test_plan_matches_oracle_bit_exact(lens, C):
     ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
     api.pkv_plan(shape, cfg, dev(tr.seq_lens), ws)
     torch.cuda.synchronize()
-    count, off, tasks, h, ordered = read_plan(ws, tr.B, with_order=True)
+    count, off, tasks, h, ordered = read_plan(ws, tr.B, with_order=True, Hkv=Hkv)
     want, want_off = oracle.plan_compact(tr.seq_lens, Hq, Hkv, C)
     assert count == want.shape[0]
     assert np.array_equal(off, want_off)

@@ -48,15 +48,19 @@ def _noalloc(L, tr, d, cfg):
     return o, lse
 
 
-@pytest.mark.parametrize("path", PATHS)
-def test_noalloc_matches_decode_step_twice(lib, path):
+@pytest.mark.parametrize("path,merge", [(p, _lib.PKV_MERGE_SEPARATE) for p in PATHS] +
+                         [(p, _lib.PKV_MERGE_FUSED) for p in PATHS[:2]])
+def test_noalloc_matches_decode_step_twice(lib, path, merge):
+    """With the fused merge the array also holds the arrival counters, which
+    the call zeroes: their place moves with the shape, over whatever the
+    previous call left there."""
     tr = T.make_trace(3)  # B=8 bimodal, ~491 MB of K+V
     q = T.gen_q(tr)
     k, v = T.gen_kv(tr)
     d = upload(tr, q, k, v)
     o_ref, lse_ref, _, _ = run_path(tr, d, path)
     C = tr.split_tokens
-    cfg = api.make_cfg(path, C, tr.n_max if path == _lib.PKV_PATH_BUCKETED_SPLIT else 0)
+    cfg = api.make_cfg(path, C, tr.n_max if path == _lib.PKV_PATH_BUCKETED_SPLIT else 0, 0, merge)
     ref = o_ref.float().cpu().numpy()
     lref = lse_ref.cpu().numpy()
     for call in range(2):
