@@ -167,10 +167,11 @@ int pkv_single_pass(const pkv_shape_t *shape, void *d_ws,
 
 /* pkv_decode_merge -- pkv_decode with the exact merge of pkv_merge on its
  * tail (cfg->merge is not consulted).  One kernel launch.  Every split writes
- * its state as pkv_decode does, then takes a ticket from an arrival counter
- * of its (row, kv head) in d_ws; the split drawing the last ticket merges the
- * row's n_i states of its G heads into o / lse with pkv_merge's formulas and
- * resets the counter.  A row with one split writes o / lse directly; a row
+ * its state as pkv_decode does; once a CTA has finished its splits it takes a
+ * ticket per split from the arrival counter of that split's (row, kv head) in
+ * d_ws, and the CTA drawing a group's last ticket merges the row's n_i states
+ * of its G heads into o / lse with pkv_merge's formulas and resets the
+ * counter.  A row with one split writes o / lse directly; a row
  * with N*_i = 0 gets o = 0, lse = -inf; a workqueue overflow writes NaN as
  * pkv_merge does.  Results equal pkv_decode + pkv_merge up to the order of
  * the fp32 sums.  Launches on one workspace must not overlap on the GPU. */

@@ -63,10 +63,16 @@ struct Layout {
     static constexpr int kStages = (D == 128) ? 3 : 6;
     static constexpr int kMetaOff = kStages * kStageBytes;           // int4 per stage
     static constexpr int kRedOff = kMetaOff + kStages * 16;          // [stage][warp 1..3][m 8, l 8]
-    static constexpr int kDecOff = kRedOff + kStages * (kCW - 1) * 2 * kMaxG * 4;  // int4 per stage
-    static constexpr int kBarOff = kDecOff + kStages * 16;
-    // barriers: full[S], empty[S], merge[S], decision[S]
-    static constexpr int kBytes = kBarOff + 4 * kStages * 8;
+    static constexpr int kBarOff = kRedOff + kStages * (kCW - 1) * 2 * kMaxG * 4;
+    // barriers: full[S], empty[S], merge[S]
+    static constexpr int kBytes = kBarOff + 3 * kStages * 8;
+    // fused merge, once the CTA's tasks are done and the ring is idle: the
+    // states being merged, their m and l, and the list of groups to merge
+    static constexpr int kMrgListOff = kMetaOff - 4096;  // int4 per group (<= kThreads per round)
+    static constexpr int kMrgMOff = kMetaOff - 8192;     // kMrgML floats of m, then of l
+    static constexpr int kMrgML = 512;
+    static constexpr int kMrgBufFloats = kMrgMOff / 4;   // acc vectors
+    static_assert(kThreads * 16 <= 4096, "merge list fits");
     static constexpr int kAlloc = kBytes + 1024;                     // slack for alignment
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
     static_assert(2 * (kAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
@@ -175,115 +181,143 @@ __device__ __forceinline__ int split_count(const DecodeParams &p, int i)
     return MODE == kModeRect ? min(n, p.S_b) : n;
 }
 
-// Consumer warp w's share of the merge of (row i, kv head g): query heads
-// h = w, w + 4, ... of the group, over states base .. base + n - 1:
+// The merge of (row i, kv head g) over states base .. base + n - 1 by the
+// whole CTA, once its own tasks are done and its stage ring is idle:
 //   M = max_j m_j, L = sum_j l_j e^{m_j - M}, o = sum_j acc_j e^{m_j - M} / L,
 //   lse = M + ln L.
-// The states were written by other CTAs, so they are read L2-only.  The merge
-// sits on the launch's tail, so it is latency-bound: each lane keeps up to
-// kMergeBatch state loads in flight, and the first batch is issued before
-// the maximum is known.
-constexpr int kMergeBatch = 8;
-
-template <int VPL>
-__device__ __forceinline__ void load_states(const float *a, int64_t js, int j, int cnt,
-                                            float (&x)[kMergeBatch][VPL])
+// The states were written by other CTAs; they are copied into the ring with
+// cp.async (no register held per copy, so all are in flight at once), in
+// chunks of splits that fit, and every thread folds its (head, 4 values of d)
+// items over each chunk with a running maximum.
+template <int D>
+__device__ void merge_group(const DecodeParams &p, uint8_t *basep, uint32_t sbase, int i, int g,
+                            int base, int n)
 {
+    using L = Layout<D>;
+    constexpr int kItems = (kMaxG * D / 4 + kThreads - 1) / kThreads;  // items per thread
+    const int tid = threadIdx.x, G = p.G, Hq = p.Hq;
+    const int vec = G * D;        // floats of one split's G consecutive states
+    const int nitems = vec / 4;   // (head, 4 values of d) items
+    const int per = min(L::kMrgBufFloats / vec, L::kMrgML / G);
+    const float *buf = reinterpret_cast<const float *>(basep);
+    float *sm = reinterpret_cast<float *>(basep + L::kMrgMOff);
+    float *sl = sm + L::kMrgML;
+    float M[kItems], Ls[kItems], acc[kItems][4];
 #pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
-        if (u < cnt) {
-            const float *aj = a + (int64_t)(j + u) * js;
-            if constexpr (VPL == 4) {
-                const float4 t = __ldcg(reinterpret_cast<const float4 *>(aj));
-                x[u][0] = t.x;
-                x[u][1] = t.y;
-                x[u][2] = t.z;
-                x[u][3] = t.w;
-            } else {
-                const float2 t = __ldcg(reinterpret_cast<const float2 *>(aj));
-                x[u][0] = t.x;
-                x[u][1] = t.y;
+    for (int u = 0; u < kItems; ++u) {
+        M[u] = -INFINITY;
+        Ls[u] = 0.f;
+        acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+    }
+    for (int c0 = 0; c0 < n; c0 += per) {
+        const int cnt = min(per, n - c0);
+        const int64_t s0 = (int64_t)(base + c0) * Hq + g * G;  // slot of split c0, head 0
+        for (int e = tid; e < cnt * nitems; e += kThreads) {
+            const int j = e / nitems, o = e - j * nitems;
+            cp_async_16(sbase + (uint32_t)(j * vec + o * 4) * 4u,
+                        p.part_acc + (s0 + (int64_t)j * Hq) * D + o * 4);
+        }
+        for (int e = tid; e < cnt * G; e += kThreads) {
+            const int j = e / G, h = e - j * G;
+            sm[e] = __ldcg(p.part_m + s0 + (int64_t)j * Hq + h);
+            sl[e] = __ldcg(p.part_l + s0 + (int64_t)j * Hq + h);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kItems; ++u) {
+            const int it = tid + u * kThreads;
+            if (it < nitems) {
+                const int h = it / (D / 4), d4 = it - h * (D / 4);
+                float mc = M[u];
+                for (int j = 0; j < cnt; ++j)
+                    mc = fmaxf(mc, sm[j * G + h]);
+                const float sc = ex2((M[u] - mc) * kLog2e);  // 0 on the first chunk
+                Ls[u] *= sc;
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    acc[u][v] *= sc;
+                for (int j = 0; j < cnt; ++j) {
+                    const float w = ex2((sm[j * G + h] - mc) * kLog2e);
+                    Ls[u] += w * sl[j * G + h];
+                    const float4 x = *reinterpret_cast<const float4 *>(buf + j * vec + h * D + d4 * 4);
+                    acc[u][0] += w * x.x;
+                    acc[u][1] += w * x.y;
+                    acc[u][2] += w * x.z;
+                    acc[u][3] += w * x.w;
+                }
+                M[u] = mc;
             }
         }
+        __syncthreads();  // the ring is refilled by the next chunk
     }
-}
-
-// acc += sum over the batch of e^{m_j - M} acc_j, the weights held by lanes
-// lane0 .. lane0 + cnt - 1 of wj
-template <int VPL>
-__device__ __forceinline__ void fold_states(float (&acc)[VPL], const float (&x)[kMergeBatch][VPL],
-                                            float wj, int lane0, int cnt)
-{
 #pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
-        const float wt = __shfl_sync(0xffffffffu, wj, (lane0 + u) & 31);
-        if (u < cnt) {
-#pragma unroll
-            for (int v = 0; v < VPL; ++v)
-                acc[v] += wt * x[u][v];
+    for (int u = 0; u < kItems; ++u) {
+        const int it = tid + u * kThreads;
+        if (it < nitems) {
+            const int h = it / (D / 4), d4 = it - h * (D / 4);
+            const float inv = 1.f / Ls[u];
+            const int64_t oh = (int64_t)i * Hq + g * G + h;
+            *reinterpret_cast<uint2 *>(p.o + oh * D + d4 * 4) =
+                make_uint2(pack_half2(acc[u][0] * inv, acc[u][1] * inv),
+                           pack_half2(acc[u][2] * inv, acc[u][3] * inv));
+            if (d4 == 0 && p.lse)
+                p.lse[oh] = M[u] + logf(Ls[u]);
         }
     }
 }
 
-template <int D>
-__device__ __forceinline__ void merge_heads(const float *part_acc, const float *part_m,
-                                         const float *part_l, __half *o, float *lse, int Hq, int G,
-                                         int i, int g, int base, int n, int w)
+// End of a fused launch, all warps: every split this CTA decoded has written
+// its state (warp 0, before the CTA barrier); now take a ticket per split of
+// a multi-split row from its (row, kv head) arrival counter -- an acquire-
+// release add at GPU scope, so the barrier-ordered state stores are published
+// before it and the other CTAs' states are visible after it -- and merge the
+// groups whose last ticket this CTA drew, resetting their counters.  Tickets
+// are taken here rather than at each task's end so that no CTA stalls its
+// pipeline for them.  A CTA in which a wait timed out takes none (the error is
+// recorded; pkv_get_error then clears the counters).
+template <int D, int MODE>
+__device__ void finish_merges(const DecodeParams &p, int ntasks, uint8_t *basep, uint32_t sbase,
+                              volatile int *ctl)
 {
-    constexpr int VPL = D / 32;  // values of d per lane
-    const int lane = threadIdx.x & 31;
-    const int64_t js = (int64_t)Hq * D;  // floats between consecutive splits' vectors
-    for (int h = w; h < G; h += kCW) {
-        const int64_t s0 = (int64_t)base * Hq + g * G + h;  // split j's state slot: s0 + j * Hq
-        const float *a = part_acc + s0 * D + lane * VPL;
-        float mj = -INFINITY, lj = 0.f;
-        if (lane < n) {
-            mj = __ldcg(part_m + s0 + (int64_t)lane * Hq);
-            lj = __ldcg(part_l + s0 + (int64_t)lane * Hq);
-        }
-        float x[kMergeBatch][VPL];
-        load_states<VPL>(a, js, 0, min(n, kMergeBatch), x);  // in flight during the reduction
-        float M = mj;
-        for (int j = lane + 32; j < n; j += 32)
-            M = fmaxf(M, __ldcg(part_m + s0 + (int64_t)j * Hq));
-#pragma unroll
-        for (int t = 16; t > 0; t >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, t));
-        float Ls = 0.f, acc[VPL];
-#pragma unroll
-        for (int v = 0; v < VPL; ++v)
-            acc[v] = 0.f;
-        for (int j0 = 0; j0 < n; j0 += 32) {
-            if (j0 > 0) {
-                mj = -INFINITY;
-                lj = 0.f;
-                if (j0 + lane < n) {
-                    mj = __ldcg(part_m + s0 + (int64_t)(j0 + lane) * Hq);
-                    lj = __ldcg(part_l + s0 + (int64_t)(j0 + lane) * Hq);
+    using L = Layout<D>;
+    const int tid = threadIdx.x;
+    __syncthreads();
+    if (ctl[0])
+        return;
+    const int nloc = ntasks > (int)blockIdx.x ? (ntasks - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    int4 *list = reinterpret_cast<int4 *>(basep + L::kMrgListOff);
+    for (int r0 = 0; r0 < nloc; r0 += kThreads) {
+        if (tid == 0)
+            ctl[1] = 0;
+        __syncthreads();
+        const int t = r0 + tid;
+        if (t < nloc) {
+            const TaskInfo ti = load_task<MODE>(p, (int)blockIdx.x + t * (int)gridDim.x, ntasks);
+            const int n = ti.t0 < ti.t1 ? split_count<MODE>(p, ti.i) : 0;
+            if (n > 1) {
+                int base, cidx;
+                if (MODE == kModeQueue) {
+                    base = p.offsets[ti.i];
+                    cidx = ti.i * p.Hkv + ti.g;
+                } else {
+                    const int lr = (ti.sbase / p.Hq) / p.S_b;  // row of the launch
+                    base = lr * p.S_b;
+                    cidx = lr * p.Hkv + ti.g;
+                }
+                if (atom_add_acq_rel_gpu(p.ctr + cidx, 1) == n - 1) {
+                    p.ctr[cidx] = 0;  // every split is in: ready for the next launch
+                    list[atomicAdd(const_cast<int *>(ctl + 1), 1)] = make_int4(ti.i, ti.g, base, n);
                 }
             }
-            const float wj = ex2((mj - M) * kLog2e);  // 0 past the row's states
-            Ls += wj * lj;
-            const int cnt = min(32, n - j0);
-            for (int b = 0; b < cnt; b += kMergeBatch) {
-                if (j0 + b > 0)
-                    load_states<VPL>(a, js, j0 + b, min(kMergeBatch, cnt - b), x);
-                fold_states<VPL>(acc, x, wj, b, min(kMergeBatch, cnt - b));
-            }
         }
-#pragma unroll
-        for (int t = 16; t > 0; t >>= 1)
-            Ls += __shfl_xor_sync(0xffffffffu, Ls, t);
-        const float inv = 1.f / Ls;
-        const int64_t oh = (int64_t)i * Hq + g * G + h;
-        __half *out = o + oh * D + lane * VPL;
-        if constexpr (VPL == 4)
-            *reinterpret_cast<uint2 *>(out) =
-                make_uint2(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv));
-        else
-            *reinterpret_cast<uint32_t *>(out) = pack_half2(acc[0] * inv, acc[1] * inv);
-        if (lse && lane == 0)
-            lse[oh] = M + logf(Ls);
+        __syncthreads();
+        const int cnt = ctl[1];
+        for (int e = 0; e < cnt; ++e) {
+            const int4 m = list[e];
+            merge_group<D>(p, basep, sbase, m.x, m.y, m.z, m.w);
+        }
+        __syncthreads();
     }
 }
 
@@ -354,7 +388,8 @@ __device__ __forceinline__ void load_pages(const DecodeParams &p, int i, int s0,
 template <int D, int MODE, bool FUSE>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUtensorMap *tmV,
                                              const DecodeParams &p, int ntasks, uint32_t sbase,
-                                             int4 *meta, uint32_t bar_full0, uint32_t bar_empty0)
+                                             int4 *meta, uint32_t bar_full0, uint32_t bar_empty0,
+                                             volatile int *fail)
 {
     using L = Layout<D>;
     const int lane = threadIdx.x & 31;
@@ -446,6 +481,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                     const uint32_t full = bar_full0 + stage * 8, empty = bar_empty0 + stage * 8;
                     if (!__all_sync(0xffffffffu, mbar_wait(empty, ph ^ 1, kWaitNs))) {
                         report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 0);
+                        *fail = 1;
                         ok = false;
                         break;
                     }
@@ -515,6 +551,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                 fill_uncovered_rows<D, MODE>(p, lane);
         } else {
             report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 1);
+            *fail = 1;
             ok = false;
         }
     }
@@ -591,7 +628,8 @@ __device__ __forceinline__ uint32_t park_addr(uint32_t ktile, int w, int lane, i
 template <int D, int MODE, bool FUSE>
 __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sbase, uint8_t *basep,
                                              const int4 *meta, uint32_t bar_full0,
-                                             uint32_t bar_empty0, uint32_t bar_merge0)
+                                             uint32_t bar_empty0, uint32_t bar_merge0,
+                                             volatile int *fail)
 {
     using L = Layout<D>;
     constexpr int KS = D / 16;  // k-steps of the QK product == m-blocks of the PV product
@@ -622,13 +660,12 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
 
     int stage = 0;
     uint32_t ph = 0, mpar = 0;  // ring lap parity; per-stage merge-barrier parities
-    uint32_t dpar = 0;          // per-stage decision-barrier parities (fused merge)
-    const uint32_t bar_dec0 = bar_merge0 + L::kStages * 8;
     for (;;) {
         const uint32_t full = bar_full0 + stage * 8;
         const bool got = __all_sync(0xffffffffu, mbar_wait(full, ph, kWaitNs));
         if (!got) {
             report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 2);
+            *fail = 1;
             return;
         }
         const int4 mt = meta[stage];
@@ -726,8 +763,8 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
                 l1 += __shfl_xor_sync(0xffffffffu, l1, o);
             }
             float *rs = red + stage * (kCW - 1) * 2 * kMaxG;  // [warp 1..3][m 8 | l 8]
-            // fused merge: splits of this task's row (a row with one writes o directly)
-            const int nsp = FUSE ? split_count<MODE>(p, mt.x) : 0;
+            // fused merge: a row of one split writes o / lse directly
+            const bool direct = FUSE && split_count<MODE>(p, mt.x) == 1;
             const uint32_t mbar = bar_merge0 + stage * 8;
             const uint32_t mp = (mpar >> stage) & 1u;
             mpar ^= 1u << stage;
@@ -746,24 +783,10 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
                 fence_proxy_async_smem();  // these K rows are refilled by TMA later
                 mbar_arrive(mbar);
                 // warp 0 releases the stage once it has read the parked states
-                if (nsp > 1) {
-                    // warp 0 publishes whether this split arrived last; if so,
-                    // every consumer warp takes its heads of the merge
-                    const uint32_t dp = (dpar >> stage) & 1u;
-                    dpar ^= 1u << stage;
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar_dec0 + stage * 8, dp, kWaitNs))) {
-                        report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 4);
-                        return;
-                    }
-                    const int4 dec = *reinterpret_cast<const int4 *>(basep + L::kDecOff + stage * 16);
-                    if (dec.x) {  // ordered after lane 0's acquire by the barrier
-                        merge_heads<D>(p.part_acc, p.part_m, p.part_l, p.o, p.lse, p.Hq, G, mt.x, mt.y,
-                                       dec.y, nsp, w);
-                    }
-                }
             } else {
                 if (!__all_sync(0xffffffffu, mbar_wait(mbar, mp, kWaitNs))) {
                     report_error(p.ws, kErrTimeout, (int)blockIdx.x, stage, 3);
+                    *fail = 1;
                     return;
                 }
                 float M0 = m0, M1 = m1;
@@ -802,7 +825,7 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
                     mbar_arrive_n(bar_empty0 + stage * 8, kCW);  // release for all four warps
                 const int sb0 = mt.z;
                 const bool ok0 = h0 < G, ok1 = h0 + 1 < G;
-                if (MODE == kModeSingle || nsp == 1) {
+                if (MODE == kModeSingle || direct) {
                     // o / lse from registers: the whole row (single pass), or a
                     // row of one split (fused merge)
                     const int ob = MODE == kModeSingle ? sb0 : mt.x * p.Hq + mt.y * G;
@@ -848,36 +871,6 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
                             p.part_l[sb0 + h0 + 1] = L1;
                         }
                     }
-                    if (nsp > 1) {
-                        // fused merge: publish this state, then take a ticket; the
-                        // warp barrier orders every lane's state stores before
-                        // lane 0's release, and its acquire orders the merge's reads
-                        __syncwarp();
-                        int base, cidx;
-                        if (MODE == kModeQueue) {
-                            base = p.offsets[mt.x];
-                            cidx = mt.x * p.Hkv + mt.y;
-                        } else {
-                            const int lr = (sb0 / p.Hq) / p.S_b;  // row of the launch
-                            base = lr * p.S_b;
-                            cidx = lr * p.Hkv + mt.y;
-                        }
-                        int last = 0;
-                        if (lane == 0) {
-                            last = atom_add_acq_rel_gpu(p.ctr + cidx, 1) == nsp - 1 ? 1 : 0;
-                            if (last)
-                                p.ctr[cidx] = 0;  // all splits are in: ready for the next launch
-                            *reinterpret_cast<int4 *>(basep + L::kDecOff + stage * 16) =
-                                make_int4(last, base, 0, 0);
-                            mbar_arrive(bar_dec0 + stage * 8);
-                        }
-                        last = __shfl_sync(0xffffffffu, last, 0);
-                        __syncwarp();
-                        if (last) {
-                            merge_heads<D>(p.part_acc, p.part_m, p.part_l, p.o, p.lse, p.Hq, G, mt.x,
-                                           mt.y, base, nsp, 0);
-                        }
-                    }
                 }
             }
             m0 = m1 = -INFINITY;
@@ -908,13 +901,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t bar_empty0 = bar_full0 + L::kStages * 8;
     const uint32_t bar_merge0 = bar_empty0 + L::kStages * 8;
     const int warp = threadIdx.x >> 5;
+    __shared__ int s_ctl[2];  // [0]: a wait timed out in this CTA; [1]: fused-merge list length
 
     if (threadIdx.x == 0) {
+        s_ctl[0] = s_ctl[1] = 0;
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(bar_full0 + s * 8, 1);
             mbar_init(bar_empty0 + s * 8, kCW);
             mbar_init(bar_merge0 + s * 8, (kCW - 1) * 32);
-            mbar_init(bar_merge0 + (L::kStages + s) * 8, 1);  // decision (fused merge)
         }
         fence_mbar_init();
     }
@@ -935,9 +929,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int ntasks = (MODE == kModeQueue) ? min(p.ws->task_count, p.n_tasks) : p.n_tasks;
     if (warp == kCW)
-        run_producer<D, MODE, FUSE>(&tmK, &tmV, p, ntasks, sbase, meta, bar_full0, bar_empty0);
+        run_producer<D, MODE, FUSE>(&tmK, &tmV, p, ntasks, sbase, meta, bar_full0, bar_empty0, s_ctl);
     else
-        run_consumer<D, MODE, FUSE>(p, sbase, basep, meta, bar_full0, bar_empty0, bar_merge0);
+        run_consumer<D, MODE, FUSE>(p, sbase, basep, meta, bar_full0, bar_empty0, bar_merge0, s_ctl);
+    if constexpr (FUSE)
+        finish_merges<D, MODE>(p, ntasks, basep, sbase, s_ctl);
 }
 
 template <int D, int MODE, bool FUSE>

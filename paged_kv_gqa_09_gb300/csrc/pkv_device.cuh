@@ -84,6 +84,14 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v)
     return old;
 }
 
+// 16-byte copy global -> shared that holds no register while in flight
+// (L2 only); cp_async_wait_all waits for all of this thread's copies.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void *gmem_src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -143,81 +143,123 @@ __device__ void append_tokens(const PlanParams &p, int *warp_tot, long long *s_d
     __syncthreads();
 }
 
+// n_i = ceil(N_i / C) of row i and r_i = 1 when it ends in a shorter split,
+// the length clamped to [0, len_cap] (reported when it was outside).
+__device__ __forceinline__ void row_splits(const PlanParams &p, int i, bool report, int &n, int &r)
+{
+    int N = p.k_new ? p.seq_lens_rw[i] : p.seq_lens[i];  // the same thread appended to it
+    if (report && (N < 0 || N > p.len_cap))
+        report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.len_cap);
+    N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);
+    n = (N + p.C - 1) / p.C;
+    r = (N % p.C) != 0 ? 1 : 0;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
 {
     __shared__ int warp_tot[33];
     __shared__ long long s_dst[kPlanThreads];
+    // offsets and short-split prefix of the current chunk's rows (+ the row after)
+    __shared__ int s_off[kPlanThreads + 1];
+    __shared__ int s_sb[kPlanThreads + 1];
     pdl_wait();
     pdl_trigger();
     const int tid = threadIdx.x;
 
-    // n_i = ceil(N_i / C) and r_i = 1 when row i ends in a shorter split; both
-    // scanned over the rows (in chunks of one block)
     if (p.k_new)
         append_tokens(p, warp_tot, s_dst);
+    // the balance order puts every full-length split before the shorter last
+    // splits, so the totals are needed before the first task is written: one
+    // extra pass over the lengths when the rows span several chunks
+    int total = 0, total_r = 0;
+    const bool chunks = p.B > kPlanThreads;
+    if (chunks) {
+        for (int base = 0; base < p.B; base += kPlanThreads) {
+            int n = 0, r = 0, tot, tot_r;
+            if (base + tid < p.B)
+                row_splits(p, base + tid, false, n, r);
+            block_exclusive_scan(n, warp_tot, &tot);
+            block_exclusive_scan(r, warp_tot, &tot_r);
+            total += tot;
+            total_r += tot_r;
+        }
+    }
     int carry = 0, carry_r = 0;
-    for (int base = 0; base < p.B; base += kPlanThreads) {
+    bool overflow = false;
+    int64_t n_full = 0;
+    for (int base = 0; base < p.B || base == 0; base += kPlanThreads) {
         const int i = base + tid;
         int n = 0, r = 0;
-        if (i < p.B) {
-            int N = p.k_new ? p.seq_lens_rw[i] : p.seq_lens[i];  // the same thread wrote it
-            if (N < 0 || N > p.len_cap)
-                report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.len_cap);
-            N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);
-            n = (N + p.C - 1) / p.C;
-            r = (N % p.C) != 0 ? 1 : 0;
-        }
+        if (i < p.B)
+            row_splits(p, i, true, n, r);
         int tot, tot_r;
         const int ex = block_exclusive_scan(n, warp_tot, &tot);
         const int ex_r = block_exclusive_scan(r, warp_tot, &tot_r);
+        const int rows = min(kPlanThreads, p.B - base);
         if (i < p.B) {
             p.offsets[i] = carry + ex;
             p.short_before[i] = carry_r + ex_r;
+            s_off[tid] = carry + ex;
+            s_sb[tid] = carry_r + ex_r;
+        }
+        if (tid == 0) {
+            s_off[rows] = carry + tot;
+            s_sb[rows] = carry_r + tot_r;
+        }
+        if (base == 0) {
+            if (!chunks) {
+                total = tot;
+                total_r = tot_r;
+            }
+            const int64_t T = (int64_t)total * p.Hkv;
+            overflow = T > p.max_tasks;
+            n_full = T - (int64_t)total_r * p.Hkv;
+            if (tid == 0) {
+                p.offsets[p.B] = total;
+                p.ws->task_count = overflow ? 0 : (int32_t)T;
+                p.ws->state_rows = total;
+                p.ws->overflow = overflow ? 1 : 0;
+                if (overflow)
+                    report_error(p.ws, kErrCapacity, (int32_t)(T > 0x7fffffff ? 0x7fffffff : T),
+                                 (int32_t)p.max_tasks, 0);
+            }
+        }
+        __syncthreads();
+        if (!overflow) {
+            // this chunk's tasks: k in [Hkv * carry, Hkv * (carry + tot)), lexicographic
+            const int64_t k1 = (int64_t)(carry + tot) * p.Hkv;
+            for (int64_t k = (int64_t)carry * p.Hkv + tid; k < k1; k += kPlanThreads) {
+                // last chunk row lo with Hkv * offsets <= k (rows without splits share
+                // the next row's offset, so the search lands on the row holding k)
+                int lo = 0, hi = rows - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if ((int64_t)s_off[mid] * p.Hkv <= k)
+                        lo = mid;
+                    else
+                        hi = mid - 1;
+                }
+                const int oi = s_off[lo];
+                const int ni = s_off[lo + 1] - oi;
+                const int kk = (int)(k - (int64_t)oi * p.Hkv);
+                const int g = kk / ni, j = kk - g * ni;
+                const int4 rec = make_int4(base + lo, g, j, (oi + j) * p.Hq + g * p.G);
+                p.tasks[k] = rec;
+                // balance order: shorter splits before this task = Hkv * (rows
+                // before with one) + g * (this row has one)
+                const int sb = s_sb[lo];
+                const int has_short = s_sb[lo + 1] - sb;
+                const bool is_short = has_short && j == ni - 1;
+                const int64_t pos = is_short ? n_full + (int64_t)sb * p.Hkv + g
+                                             : k - ((int64_t)sb * p.Hkv + (int64_t)g * has_short);
+                p.tasks_ordered[pos] = rec;
+            }
         }
         carry += tot;
         carry_r += tot_r;
-    }
-    const int64_t T = (int64_t)carry * p.Hkv;
-    const bool overflow = T > p.max_tasks;
-    if (tid == 0) {
-        p.offsets[p.B] = carry;
-        p.ws->task_count = overflow ? 0 : (int32_t)T;
-        p.ws->state_rows = carry;
-        p.ws->overflow = overflow ? 1 : 0;
-        if (overflow)
-            report_error(p.ws, kErrCapacity, (int32_t)(T > 0x7fffffff ? 0x7fffffff : T),
-                         (int32_t)p.max_tasks, 0);
-    }
-    __syncthreads();
-    if (overflow)
-        return;
-    // full-length tasks of the balance order come first, the rows' shorter last
-    // splits after them
-    const int64_t n_full = T - (int64_t)carry_r * p.Hkv;
-    for (int64_t k = tid; k < T; k += kPlanThreads) {
-        // last row i in [0, B-1] with Hkv * offsets[i] <= k
-        int lo = 0, hi = p.B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)__ldcg(p.offsets + mid) * p.Hkv <= k)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        const int oi = __ldcg(p.offsets + lo);
-        const int ni = __ldcg(p.offsets + lo + 1) - oi;
-        const int kk = (int)(k - (int64_t)oi * p.Hkv);
-        const int g = kk / ni, j = kk - g * ni;
-        const int4 rec = make_int4(lo, g, j, (oi + j) * p.Hq + g * p.G);
-        p.tasks[k] = rec;
-        // balance order: shorter splits before this task = Hkv * (rows before
-        // with one) + g * (this row has one)
-        const int sb = __ldcg(p.short_before + lo);
-        const int has_short = (lo + 1 < p.B ? __ldcg(p.short_before + lo + 1) : carry_r) - sb;
-        const bool is_short = has_short && j == ni - 1;
-        const int64_t pos = is_short ? n_full + (int64_t)sb * p.Hkv + g
-                                     : k - ((int64_t)sb * p.Hkv + (int64_t)g * has_short);
-        p.tasks_ordered[pos] = rec;
+        __syncthreads();  // the chunk's shared offsets are rewritten next
+        if (base + kPlanThreads >= p.B)
+            break;
     }
 }
 

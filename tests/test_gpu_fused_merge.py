@@ -2,8 +2,8 @@
 the float64 oracle, and its bookkeeping.
 
 The fused step computes what pkv_decode + pkv_merge compute -- the exact
-log-sum-exp merge of "Sequence splitting" -- with the merge run by the
-last-arriving split of each (row, kv head) on the decode's tail.  Besides the
+log-sum-exp merge of "Sequence splitting" -- with the merge run on the decode's
+tail by the CTA that draws the last arrival ticket of each (row, kv head).  Besides the
 outputs (spec tolerance |x - y| <= 3e-3 + 1e-2 |y|), these tests check
 that the arrival counters are back at zero after every launch (also after a
 timeout, through pkv_get_error), that rows without tokens and workqueue
@@ -87,15 +87,16 @@ def test_fused_boundary_lengths(P, C, path):
                                        (12, 4, 128), (6, 2, 64)])
 @pytest.mark.parametrize("path", [BUCKETED, WORKQUEUE])
 def test_fused_group_sizes_and_head_dims(Hq, Hkv, dd, path):
-    """G = 1..8 query heads per KV head: the merge's heads are spread over the
-    four consumer warps (two each at G = 8, some idle below 4)."""
+    """G = 1..8 query heads per KV head: the merging CTA's threads take
+    (head, 4 values of d) items, two each at G = 8 and d = 128."""
     tr, q, k, v = case([333, 17, 1000, 64], Hq=Hq, Hkv=Hkv, d=dd, P=16, C=128, seed=Hq * 7 + dd)
     against_oracle(tr, q, k, v, path)
 
 
 @pytest.mark.parametrize("path", [BUCKETED, WORKQUEUE])
 def test_fused_rows_with_more_splits_than_a_warp(path):
-    """n_i above 32: the merge walks the states in chunks of one per lane."""
+    """Many splits: at G = 8 and d = 128 a chunk of states that fits the idle
+    stage ring holds 23 splits, so these rows are merged in several chunks."""
     tr, q, k, v = case([100 * 64 + 5, 33 * 64, 32 * 64, 31 * 64 + 1, 64], Hq=16, Hkv=2, C=64,
                        seed=11)
     against_oracle(tr, q, k, v, path)

@@ -45,6 +45,9 @@ def case(lens, Hq=8, Hkv=2, d=128, P=16, C=64, seed=3, **kw):
     ([0, 0, 0], 64),
     ([5000, 3, 64, 64, 100000, 7, 0, 2048], 1024),
     (list(range(1, 300, 7)), 16),
+    # more rows than one plan block: a totals pass, then chunk by chunk
+    (np.random.default_rng(7).integers(0, 600, 2500).tolist(), 64),
+    ([64] * 1024 + [65], 64),
 ])
 def test_plan_matches_oracle_bit_exact(lens, C):
     Hq, Hkv = 32, 8
