@@ -204,7 +204,8 @@ def profiled_traffic(cfg_id: int):
 def cpu_baseline_run(tr, q, k, v, seconds: float):
     """The oracle, as it stands, on this host's cores: repeated whole decode
     steps of the workload (or, for large workloads, a row-prefix sample) for
-    about `seconds`; returns (GB/s of K+V processed, cores, description)."""
+    about `seconds` on all cores, then a quarter of that on one thread; returns
+    (GB/s of K+V processed on all cores, cores, description, one-thread GB/s)."""
     import oracle
     cores = oracle.max_threads()
     lens = tr.seq_lens
@@ -223,14 +224,19 @@ def cpu_baseline_run(tr, q, k, v, seconds: float):
         sample_q, sample_bt = q[:1], tr.block_table[:1]
         desc = f"row 0, first {n} tokens, all {tr.Hq} query heads, repeated"
     bytes_per = int(sample_lens.astype(np.int64).sum()) * tr.Hkv * tr.d * 4
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.attention(sample_q, k, v, sample_bt, sample_lens, tr.scale)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return bytes_per * reps / el / 1e9, cores, f"{desc}; {reps} reps in {el:.1f} s"
+
+    def timed(budget, nthreads):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.attention(sample_q, k, v, sample_bt, sample_lens, tr.scale, nthreads=nthreads)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget:
+                return bytes_per * reps / el / 1e9, reps, el
+
+    gbs, reps, el = timed(seconds, 0)
+    one, reps1, el1 = timed(seconds / 4, 1)
+    return gbs, cores, f"{desc}; {reps} reps in {el:.1f} s ({reps1} in {el1:.1f} s on one thread)", one
 
 
 # ------------------------------------------------------------------ reference arm
@@ -523,8 +529,9 @@ def run_pkv(args, rank, local, ws, pg):
             tr_s, qb, k_s, v_s = _row0_sample(tr)
         else:
             tr_s, qb, k_s, v_s = tr, q_h, k_h, v_h
-        val, cores, desc = cpu_baseline_run(tr_s, qb, k_s, v_s, args.cpu_seconds)
-        cpu = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        val, cores, desc, one = cpu_baseline_run(tr_s, qb, k_s, v_s, args.cpu_seconds)
+        cpu = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+               "single_thread_value": one}
     if rank != 0:
         return
     line = {

@@ -440,17 +440,31 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
     uint32_t pend = 0, pend_par = 0;  // stages with copies in flight, and their parity
     bool ok = true;
 
-    for (int t = 0; t < nloc && ok; ++t) {
-        if (t > 0 && (t & 31) == 0) {
-            wa = wb;
-            wb = task_of(t + 32 + lane);
+    // The workqueue's CTAs (without the fused merge, whose end phase re-walks a
+    // CTA's strided tasks) claim tasks dynamically: the first round is static,
+    // then each CTA takes the next balance-order task from a counter once it
+    // has issued the copies of its current one, so the longest tasks go first
+    // and the short ones fill in wherever a CTA runs free.  The claim, the task
+    // record and its block-table entries arrive while the consumers drain the
+    // stages in flight.  Other modes stride statically over their tasks.
+    constexpr bool kDyn = MODE == kModeQueue && !FUSE;
+    int k_cur = (int)blockIdx.x;  // kDyn: balance-order index of cur
+    for (int t = 0; (kDyn ? k_cur < ntasks : t < nloc) && ok; ++t) {
+        TaskInfo nxt{0, 0, 0, 0, 0};
+        bool nxt_live = false;
+        if (!kDyn) {
+            if (t > 0 && (t & 31) == 0) {
+                wa = wb;
+                wb = task_of(t + 32 + lane);
+            }
+            // the next task's first block-table entries load while this one streams
+            const int tn = t + 1;
+            nxt = shfl_task(((tn & 31) != 0) ? wa : wb, tn & 31);
+            nxt_live = tn < nloc && nxt.t0 < nxt.t1;
+            if (nxt_live)
+                load_pages(p, nxt.i, nxt.t0 >> log2P, min(seg_end(nxt), (nxt.t0 >> log2P) + kSeg), lane,
+                           pnx);
         }
-        // the next task's first block-table entries load while this one streams
-        const int tn = t + 1;
-        const TaskInfo nxt = shfl_task(((tn & 31) != 0) ? wa : wb, tn & 31);
-        const bool nxt_live = tn < nloc && nxt.t0 < nxt.t1;
-        if (nxt_live)
-            load_pages(p, nxt.i, nxt.t0 >> log2P, min(seg_end(nxt), (nxt.t0 >> log2P) + kSeg), lane, pnx);
 
         if (cur.t0 >= cur.t1) {
             // empty task: neutral state (split modes) or o = 0, lse = -inf (single)
@@ -534,10 +548,33 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                 }
             }
         }
+        if (kDyn && ok) {
+            int kn = 0;
+            if (lane == 0)
+                kn = (int)gridDim.x + atomicAdd(&p.ws->next_task, 1);
+            kn = __shfl_sync(0xffffffffu, kn, 0);
+            if (kn < ntasks) {
+                nxt = load_task<MODE>(p, kn, ntasks);
+                nxt_live = nxt.t0 < nxt.t1;
+                if (nxt_live)
+                    load_pages(p, nxt.i, nxt.t0 >> log2P, min(seg_end(nxt), (nxt.t0 >> log2P) + kSeg),
+                               lane, pnx);
+            }
+            k_cur = kn;
+        }
         cur = nxt;
 #pragma unroll
         for (int r = 0; r < kSegRegs; ++r)
             pid[r] = pnx[r];
+    }
+    if (kDyn && lane == 0) {
+        // this CTA claims no more; the last one to get here resets the counters
+        // for the next launch on this workspace (every claim precedes the fence)
+        __threadfence();
+        if (atomicAdd(&p.ws->done_ctas, 1) == (int)gridDim.x - 1) {
+            p.ws->next_task = 0;
+            p.ws->done_ctas = 0;
+        }
     }
     if (ok) {
         // end-of-work sentinel

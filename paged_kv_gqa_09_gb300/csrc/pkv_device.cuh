@@ -35,7 +35,12 @@ struct WsHeader {
     // that the host can clear them after a timeout left some mid-count)
     int32_t ctr_off16;    // byte offset / 16 of the counter array in the workspace
     int32_t ctr_words;    // int32 counters in it
-    int32_t pad[7];
+    // dynamic task claims of the workqueue decode: next balance-order index to
+    // hand out (beyond the first round) and CTAs finished; the last CTA to
+    // finish zeroes both for the next launch
+    int32_t next_task;
+    int32_t done_ctas;
+    int32_t pad[5];
 };
 static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
 

@@ -50,3 +50,15 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.reduce_max(None, 3.5) == 3.5
     assert bench.whole_job_gbs(134217728, 0.0201, 1) == pytest.approx(6677.5, rel=1e-3)
+
+
+def test_cpu_baseline_times_all_cores_and_one_thread():
+    """The cpu_baseline leg: the oracle as it stands on the small case, timed
+    on all cores and on one thread, in GB/s of K+V."""
+    import bench
+    import pkv_traces as T
+    tr = T.make_trace(1)
+    k, v = T.gen_kv(tr)
+    gbs, cores, desc, one = bench.cpu_baseline_run(tr, T.gen_q(tr), k, v, 0.2)
+    assert gbs > 0 and one > 0 and cores >= 1
+    assert "whole decode steps" in desc and "one thread" in desc
