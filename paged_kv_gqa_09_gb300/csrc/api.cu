@@ -638,10 +638,10 @@ void pkv_policy_default(pkv_policy_cfg_t *c)
     if (!c)
         return;
     c->bucketed_min_tokens = 1024;
-    c->bucketed_max_batch = 8;
-    c->workqueue_min_tokens = 4096;
+    c->bucketed_max_batch = 4;
+    c->workqueue_min_tokens = 2048;
     c->workqueue_min_batch = 1;
-    c->split_tokens = 1024;
+    c->split_tokens = 512;
     c->bucketed_split_tokens = 512;
 }
 
@@ -676,16 +676,16 @@ int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t
 // squares of log step time, calibration seed 20260622, 224 GB300 traces);
 // held-out seed 20260623 mean regret 1.025 (worst 1.21x).
 static const pkv_cost_route_t kGb300Routes[] = {
-    {0, 128, {6.01822514f, 0.225079554f, 0.132225077f, -0.866300992f, -0.00286177224f, 0.0058537269f, 0.00381505922f, 0.392748749f, -0.0617887688f, 0.0346332006f}},
-    {0, 256, {6.37411087f, 0.126295736f, 0.104974546f, -0.852834268f, 0.00314028221f, 0.00308314744f, 0.00140758789f, 0.286179883f, -0.0621945571f, 0.0358782873f}},
-    {0, 512, {6.51785164f, -0.0564157854f, 0.0411683298f, -0.757304027f, 0.0134233371f, 0.00614057083f, 0.00134051404f, 0.161679818f, -0.0385851328f, 0.0332204809f}},
-    {0, 1024, {6.11387729f, -0.195668953f, 0.0786745573f, -0.67649932f, 0.0198199544f, 0.0101223915f, -0.00181196784f, 0.0586858502f, -0.0166309652f, 0.0306631533f}},
-    {0, 2048, {4.85739656f, -0.207377429f, 0.346906155f, -0.695155704f, 0.0167757827f, 0.0138003383f, -0.0123387416f, -0.00828948804f, -0.0047865178f, 0.0308990192f}},
-    {1, 256, {7.32733405f, 0.117223956f, 0.0193178352f, -0.878072865f, -0.00711632172f, -0.00045299104f, 0.00102104609f, 0.0447541912f, -0.0302528511f, 0.0408652389f}},
-    {1, 512, {6.96231729f, 0.125164353f, 0.141260129f, -0.90587617f, -0.00623116616f, -0.00385944783f, -0.00568025893f, 0.064981471f, -0.0510164257f, 0.042248377f}},
-    {1, 1024, {6.0076199f, 0.13822289f, 0.387047891f, -0.958177046f, -0.00769329818f, -0.00210724119f, -0.015380889f, 0.0727217225f, -0.0477712252f, 0.0431791278f}},
-    {1, 2048, {4.40811257f, 0.145833777f, 0.72000109f, -0.989956553f, -0.0102229642f, 0.00229557149f, -0.0274439559f, 0.03919701f, -0.0324846557f, 0.0428150806f}},
-    {2, 1024, {5.56172397f, -0.140274517f, -0.261910814f, -0.390119342f, -0.00961258517f, 0.0369471378f, 0.0313995807f, -0.396241805f, 0.162715669f, 0.0142896572f}},
+    {0, 128, {6.3911511f, 0.18869681f, 0.113038967f, -0.872334747f, -0.00111166821f, 0.00570620828f, 0.00389673768f, 0.333247013f, -0.0526887548f, 0.0348977711f}},
+    {0, 256, {6.73588227f, 0.101975149f, 0.110912851f, -0.880277407f, 0.00430088841f, 0.00318768111f, 0.000633300328f, 0.250103107f, -0.0582065134f, 0.0366974999f}},
+    {0, 512, {6.85069008f, -0.0199633378f, 0.0875755601f, -0.832104671f, 0.0120954918f, 0.00404960658f, -0.000342222623f, 0.192960041f, -0.0448385477f, 0.0352934669f}},
+    {0, 1024, {6.43892679f, -0.14679993f, 0.132516769f, -0.760243062f, 0.0178044681f, 0.00758829307f, -0.00362695527f, 0.0932693563f, -0.0234600053f, 0.0330072711f}},
+    {0, 2048, {5.21789607f, -0.151656726f, 0.372049944f, -0.765199027f, 0.0147380797f, 0.0106726982f, -0.0127868016f, 0.0473664272f, -0.0113390157f, 0.0326924f}},
+    {1, 256, {7.46433045f, 0.142281247f, 0.0415647499f, -0.915908375f, -0.00786971047f, -0.00235486857f, 0.00101025077f, 0.0779131574f, -0.0216318039f, 0.0413073873f}},
+    {1, 512, {7.1416581f, 0.149791916f, 0.16981438f, -0.958581609f, -0.00814656145f, -0.00358729065f, -0.00534764157f, 0.0836702774f, -0.0296661475f, 0.0428970791f}},
+    {1, 1024, {6.12978505f, 0.17430816f, 0.437913689f, -1.01776603f, -0.0103437813f, -0.00389283438f, -0.016456589f, 0.062021911f, -0.026802004f, 0.0444890352f}},
+    {1, 2048, {4.59033968f, 0.20436047f, 0.770685133f, -1.05846004f, -0.0152960465f, -0.0008797314f, -0.0288815227f, 0.0112963283f, -0.0141198967f, 0.0449685579f}},
+    {2, 1024, {5.85305682f, -0.101661956f, -0.248880265f, -0.436635689f, -0.0105043141f, 0.0333611675f, 0.0308085814f, -0.359093353f, 0.151939249f, 0.0157091673f}},
 };
 
 void pkv_cost_model_default(pkv_cost_model_t *m)
