@@ -467,3 +467,65 @@ def test_a_starved_barrier_times_out_and_the_context_stays_usable():
     check_error_free(ws)
     oref, lref = oracle_out(tr, q, k, v)
     close(o, oref)
+
+
+# ------------------------------------------------------------------ dynamic task claims
+
+def _claim_counters(ws):
+    h = ws[:64].view(torch.int32).cpu().numpy()
+    return int(h[9]), int(h[10])  # next_task, done_ctas
+
+
+def test_workqueue_claims_reset_between_launches():
+    """The workqueue decode hands tasks out from a counter in the workspace
+    header; the last CTA of a launch zeroes it, so repeated decodes on one
+    plan and workspace each process every task (bit-identical outputs)."""
+    tr = T.make_trace(3)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    d = upload(tr, q, k, v)
+    shape = shape_of(tr)
+    cfg = api.make_cfg(WORKQUEUE, tr.split_tokens)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    part = torch.empty(api.pkv_partials_size(shape, cfg) // 4, dtype=torch.float32, device="cuda")
+    api.pkv_plan(shape, cfg, d["sl"], ws)
+    outs = []
+    for _ in range(4):
+        part.fill_(float("nan"))
+        o = torch.empty((tr.B, tr.Hq, tr.d), dtype=torch.float16, device="cuda")
+        lse = torch.empty((tr.B, tr.Hq), dtype=torch.float32, device="cuda")
+        api.pkv_decode(shape, cfg, ws, d["q"], d["k"], d["v"], d["bt"], d["sl"], part)
+        api.pkv_merge(shape, cfg, ws, d["sl"], part, o, lse)
+        torch.cuda.synchronize()
+        assert _claim_counters(ws) == (0, 0)
+        outs.append((o, lse))
+    check_error_free(ws)
+    oref, lref = oracle_out(tr, q, k, v)
+    close(outs[0][0], oref)
+    close_lse(outs[0][1], lref)
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+
+
+def test_a_starved_workqueue_launch_resets_its_claims():
+    """A CTA that times out stops claiming; the others take the remaining
+    tasks, every CTA still counts itself done, and the next launch on the same
+    workspace starts from a zeroed counter."""
+    tr = T.make_trace(3)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    d = upload(tr, q, k, v)
+    L = _lib.load()
+    assert L.pkv_test_starve_next_decodes(1) == 0
+    try:
+        o, lse, ws, _ = run_path(tr, d, WORKQUEUE)
+    finally:
+        L.pkv_test_starve_next_decodes(0)
+    st, msg = api.pkv_get_error(ws)
+    assert st == _lib.PKV_ETIMEOUT, msg
+    assert _claim_counters(ws) == (0, 0)
+    o, lse, ws, _ = run_path(tr, d, WORKQUEUE, ws=ws)
+    check_error_free(ws)
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o, oref)
+    close_lse(lse, lref)
