@@ -661,7 +661,7 @@ def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, ws
     return {"value": kv_total[0] / el / 1e9, "unit": UNIT, "us_per_step": el / steps * 1e6,
             "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "timing": "synchronized wall clock per step" + (
-                " (HostDecodeLoop graph: H2D q/bt/lengths, decode step writing o/lse into pinned host memory)" if graph_mode
+                " (HostDecodeLoop graph: the step's kernels read q/bt/lengths from pinned host memory and write o/lse there)" if graph_mode
                 else " (pkv_append + pkv_decode_step_host)")}
 
 

@@ -496,13 +496,13 @@ class HostDecodeLoop:
         return self.h_o, self.h_lse
 
     def capture(self, stream: Optional[torch.cuda.Stream] = None) -> None:
-        """Capture one whole host step as a CUDA graph: one copy of the pinned
-        inputs `h_q`, `h_bt`, `h_sl` (views of one buffer) to the device, then
-        the decode step, whose last kernel writes o and lse straight into the
-        pinned `h_o`, `h_lse` (page-locked host memory is addressable from
-        kernels under unified addressing, so no copy back is needed).  Afterwards
-        each step is `step_graph()`: write the inputs into the staging tensors,
-        one graph launch, one synchronize.  Capture needs a non-default stream."""
+        """Capture one whole host step as a CUDA graph of the step's kernels
+        alone: they read the pinned inputs `h_q`, `h_bt`, `h_sl` in place and the
+        last one writes o and lse straight into the pinned `h_o`, `h_lse`
+        (page-locked host memory is addressable from kernels under unified
+        addressing, so no copy in or out is needed).  Afterwards each step is
+        `step_graph()`: write the inputs into the staging tensors, one graph
+        launch, one synchronize.  Capture needs a non-default stream."""
         st = stream if stream is not None else torch.cuda.current_stream()
         if st.cuda_stream == torch.cuda.default_stream(st.device).cuda_stream:
             raise ValueError("capture needs a non-default stream")
@@ -510,10 +510,9 @@ class HostDecodeLoop:
         part = self.partials.data_ptr() if self.partials is not None else None
 
         def body():
-            self.d_in.copy_(self.h_in, non_blocking=True)
             check(L.pkv_decode_step(self._refs[0], self._refs[1], self.ws.data_ptr(),
-                                    self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
-                                    self.bt.data_ptr(), self.sl.data_ptr(), part,
+                                    self.h_q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                    self.h_bt.data_ptr(), self.h_sl.data_ptr(), part,
                                     self.h_o.data_ptr(), self.h_lse.data_ptr(), st.cuda_stream),
                   "pkv_decode_step")
 

@@ -388,8 +388,8 @@ __device__ __forceinline__ void load_pages(const DecodeParams &p, int i, int s0,
 template <int D, int MODE, bool FUSE>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUtensorMap *tmV,
                                              const DecodeParams &p, int ntasks, uint32_t sbase,
-                                             int4 *meta, uint32_t bar_full0, uint32_t bar_empty0,
-                                             volatile int *fail)
+                                             uint8_t *basep, int4 *meta, uint32_t bar_full0,
+                                             uint32_t bar_empty0, volatile int *fail)
 {
     using L = Layout<D>;
     const int lane = threadIdx.x & 31;
@@ -516,13 +516,12 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                     const uint32_t vdst = kdst + L::kTileBytes;
                     if (lane == 0) {
                         meta[stage] = make_int4(cur.i, cur.g, cur.sbase, flags);
-                        const uint32_t bytes =
-                            2u * nb * box_bytes + ((flags & kFirst) ? (uint32_t)(G * D * 2) : 0u);
-                        mbar_arrive_expect_tx(full, bytes);
+                        // a task's first tile also carries its q rows, stored below:
+                        // its arrival then comes after them
                         if (flags & kFirst)
-                            bulk_load(kdst + 2 * L::kTileBytes,
-                                      p.q + ((size_t)cur.i * p.Hq + (size_t)cur.g * G) * D,
-                                      (uint32_t)(G * D * 2), full);
+                            mbar_expect_tx(full, 2u * nb * box_bytes);
+                        else
+                            mbar_arrive_expect_tx(full, 2u * nb * box_bytes);
                     }
                     __syncwarp();
                     // box b of the tile is page rel0 + b of the segment; the lane
@@ -538,6 +537,20 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                         const int slot = (tt + (b << btl)) & ((1 << log2P) - 1);
                         tma_load_5d(kdst + b * box_bytes, tmK, full, 0, slot, 0, cur.g, pg, pol);
                         tma_load_5d(vdst + b * box_bytes, tmV, full, 0, slot, 0, cur.g, pg, pol);
+                    }
+                    if (flags & kFirst) {
+                        // the G query rows of the task, copied with plain 16-byte loads
+                        // (q may live in page-locked host memory, which kernels can
+                        // address) while the K/V copies are in flight; lane 0's
+                        // arrival then publishes them to the consumers
+                        const int4 *qsrc = reinterpret_cast<const int4 *>(
+                            p.q + ((size_t)cur.i * p.Hq + (size_t)cur.g * G) * D);
+                        int4 *qdst = reinterpret_cast<int4 *>(basep + (kdst - sbase) + 2 * L::kTileBytes);
+                        for (int x = lane; x < G * D / 8; x += 32)
+                            qdst[x] = qsrc[x];
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(full);
                     }
                     pend |= 1u << stage;
                     pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
@@ -966,7 +979,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int ntasks = (MODE == kModeQueue) ? min(p.ws->task_count, p.n_tasks) : p.n_tasks;
     if (warp == kCW)
-        run_producer<D, MODE, FUSE>(&tmK, &tmV, p, ntasks, sbase, meta, bar_full0, bar_empty0, s_ctl);
+        run_producer<D, MODE, FUSE>(&tmK, &tmV, p, ntasks, sbase, basep, meta, bar_full0, bar_empty0,
+                                    s_ctl);
     else
         run_consumer<D, MODE, FUSE>(p, sbase, basep, meta, bar_full0, bar_empty0, bar_merge0, s_ctl);
     if constexpr (FUSE)

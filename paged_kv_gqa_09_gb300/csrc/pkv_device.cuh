@@ -123,6 +123,14 @@ __device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t count)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Raise the barrier's expected transaction bytes without arriving (the
+// arrival follows separately, e.g. after the thread's own shared stores).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -193,17 +201,6 @@ __device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap *m, int c0, in
                      reinterpret_cast<uint64_t>(m)),
                  "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
                  : "memory");
-}
-
-// Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
-                                          uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
 }
 
 // Order this thread's generic-proxy shared-memory writes before later
