@@ -426,22 +426,33 @@ def test_row_list_step_leaves_other_rows_untouched():
     assert st == _lib.PKV_EDEVICE and "row list" in msg, msg
 
 
-def test_host_loop_graph_step_matches_oracle():
-    tr = T.make_trace(2)
+@pytest.mark.parametrize("cfg_id,path", [(2, BUCKETED), (3, WORKQUEUE), (1, SINGLE)])
+def test_host_loop_graph_step_matches_oracle(cfg_id, path):
+    """The captured host step: its kernels read q, the block table and the
+    lengths from pinned host memory in place (the plan too, on the workqueue)
+    and write o / lse there."""
+    tr = T.make_trace(cfg_id)
     q = T.gen_q(tr)
     k, v = T.gen_kv(tr)
     loop = api.HostDecodeLoop(dev(k), dev(v), tr.B, tr.Hq, tr.bt_stride, tr.n_max,
-                              path=BUCKETED, split_tokens=tr.split_tokens)
+                              path=path, split_tokens=tr.split_tokens)
     loop.h_q.copy_(torch.from_numpy(q))
     loop.h_bt.copy_(torch.from_numpy(tr.block_table))
     loop.h_sl.copy_(torch.from_numpy(tr.seq_lens))
     s = torch.cuda.Stream()
     loop.capture(s)
     oref, lref = oracle_out(tr, q, k, v)
-    for _ in range(3):
+    for _ in range(2):
         o, lse = loop.step_graph()
         close(o, oref)
         close_lse(lse, lref)
+    # the next step's query, written into the pinned input, is what the kernels read
+    q2 = T.gen_step_q(tr, 1)
+    loop.h_q.copy_(torch.from_numpy(q2))
+    o, lse = loop.step_graph()
+    oref2, lref2 = oracle_out(tr, q2, k, v)
+    close(o, oref2)
+    close_lse(lse, lref2)
     check_error_free(loop.ws)
 
 
