@@ -434,8 +434,9 @@ class HostDecodeLoop:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, B: int, Hq: int, bt_stride: int,
                  n_max: int, path: Optional[int] = None, split_tokens: Optional[int] = None,
                  policy: Optional[PolicyCfg] = None, scale: Optional[float] = None,
-                 max_tasks: int = 0, merge: int = PKV_MERGE_SEPARATE):
+                 max_tasks: int = 0, merge: int = PKV_MERGE_SEPARATE, inputs_in_place: bool = True):
         dev = k_cache.device
+        self.inputs_in_place = inputs_in_place
         d = int(k_cache.shape[3])
         # the step's inputs (q | block table | lengths) and outputs (o | lse) each
         # live in one buffer, on the device and pinned on the host, so that a
@@ -496,11 +497,15 @@ class HostDecodeLoop:
         return self.h_o, self.h_lse
 
     def capture(self, stream: Optional[torch.cuda.Stream] = None) -> None:
-        """Capture one whole host step as a CUDA graph of the step's kernels
-        alone: they read the pinned inputs `h_q`, `h_bt`, `h_sl` in place and the
-        last one writes o and lse straight into the pinned `h_o`, `h_lse`
+        """Capture one whole host step as a CUDA graph: the step's kernels, the
+        last of which writes o and lse straight into the pinned `h_o`, `h_lse`
         (page-locked host memory is addressable from kernels under unified
-        addressing, so no copy in or out is needed).  Afterwards each step is
+        addressing, so no copy back is needed).  With `inputs_in_place` the
+        kernels also read the pinned inputs `h_q`, `h_bt`, `h_sl` where they are;
+        otherwise one copy moves them to the device first.  In place every split
+        of a row re-reads its q rows, and every kv head its block-table entries,
+        over the host link; those reads overlap the KV stream (on GB300 in place
+        measured no slower than the copy from B=1 to B=64).  Afterwards each step is
         `step_graph()`: write the inputs into the staging tensors, one graph
         launch, one synchronize.  Capture needs a non-default stream."""
         st = stream if stream is not None else torch.cuda.current_stream()
@@ -509,10 +514,14 @@ class HostDecodeLoop:
         L = _lib.load()
         part = self.partials.data_ptr() if self.partials is not None else None
 
+        src = (self.h_q, self.h_bt, self.h_sl) if self.inputs_in_place else (self.q, self.bt, self.sl)
+
         def body():
+            if not self.inputs_in_place:
+                self.d_in.copy_(self.h_in, non_blocking=True)
             check(L.pkv_decode_step(self._refs[0], self._refs[1], self.ws.data_ptr(),
-                                    self.h_q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
-                                    self.h_bt.data_ptr(), self.h_sl.data_ptr(), part,
+                                    src[0].data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                    src[1].data_ptr(), src[2].data_ptr(), part,
                                     self.h_o.data_ptr(), self.h_lse.data_ptr(), st.cuda_stream),
                   "pkv_decode_step")
 
@@ -528,6 +537,9 @@ class HostDecodeLoop:
         """Replay the captured step and wait for it; returns the pinned (o, lse)."""
         if self._graph is None:
             raise RuntimeError("capture() first")
-        self._graph.replay()
+        # a graph replays on the current stream: make it the capture stream, so
+        # that the synchronize below waits for this very replay
+        with torch.cuda.stream(self._graph_stream):
+            self._graph.replay()
         self._graph_stream.synchronize()
         return self.h_o, self.h_lse

@@ -426,16 +426,17 @@ def test_row_list_step_leaves_other_rows_untouched():
     assert st == _lib.PKV_EDEVICE and "row list" in msg, msg
 
 
-@pytest.mark.parametrize("cfg_id,path", [(2, BUCKETED), (3, WORKQUEUE), (1, SINGLE)])
-def test_host_loop_graph_step_matches_oracle(cfg_id, path):
+@pytest.mark.parametrize("cfg_id,path,in_place", [(2, BUCKETED, True), (3, WORKQUEUE, True),
+                                                  (1, SINGLE, True), (3, WORKQUEUE, False)])
+def test_host_loop_graph_step_matches_oracle(cfg_id, path, in_place):
     """The captured host step: its kernels read q, the block table and the
-    lengths from pinned host memory in place (the plan too, on the workqueue)
-    and write o / lse there."""
+    lengths from pinned host memory in place (the plan too, on the workqueue),
+    or from one copy of them, and write o / lse into pinned host memory."""
     tr = T.make_trace(cfg_id)
     q = T.gen_q(tr)
     k, v = T.gen_kv(tr)
     loop = api.HostDecodeLoop(dev(k), dev(v), tr.B, tr.Hq, tr.bt_stride, tr.n_max,
-                              path=path, split_tokens=tr.split_tokens)
+                              path=path, split_tokens=tr.split_tokens, inputs_in_place=in_place)
     loop.h_q.copy_(torch.from_numpy(q))
     loop.h_bt.copy_(torch.from_numpy(tr.block_table))
     loop.h_sl.copy_(torch.from_numpy(tr.seq_lens))
@@ -540,3 +541,54 @@ def test_a_starved_workqueue_launch_resets_its_claims():
     oref, lref = oracle_out(tr, q, k, v)
     close(o, oref)
     close_lse(lse, lref)
+
+
+# ------------------------------------------------------------------ the timed launch configuration
+
+@pytest.mark.parametrize("cfg_id,path,merge", [(2, BUCKETED, _lib.PKV_MERGE_SEPARATE),
+                                               (3, WORKQUEUE, _lib.PKV_MERGE_SEPARATE),
+                                               (1, SINGLE, _lib.PKV_MERGE_SEPARATE),
+                                               (2, BUCKETED, _lib.PKV_MERGE_FUSED),
+                                               (3, WORKQUEUE, _lib.PKV_MERGE_FUSED)])
+def test_chained_graph_steps_match_oracle(cfg_id, path, merge):
+    """bench.py times CUDA graphs of consecutive steps whose kernels chain by
+    programmatic dependent launch: a step's decode may start while the previous
+    step's merge still reads the partial states.  Replaying such a graph (four
+    steps on the same workspace, partials and outputs) must give the oracle's
+    result every time."""
+    tr = T.make_trace(cfg_id)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    d = upload(tr, q, k, v)
+    shape = shape_of(tr)
+    cfg = api.make_cfg(path, tr.split_tokens, tr.n_max if path == BUCKETED else 0, 0, merge)
+    ws = torch.zeros(max(64, api.pkv_plan_workspace_size(shape, cfg)), dtype=torch.uint8,
+                     device="cuda")
+    npart = api.pkv_partials_size(shape, cfg)
+    part = torch.empty(max(npart // 4, 4), dtype=torch.float32, device="cuda") if npart else None
+    o = torch.empty((tr.B, tr.Hq, tr.d), dtype=torch.float16, device="cuda")
+    lse = torch.empty((tr.B, tr.Hq), dtype=torch.float32, device="cuda")
+    k2, v2 = d["k"].clone(), d["v"].clone()  # a second pool, as the bench rotates them
+    st = torch.cuda.Stream()
+
+    def steps():
+        for r in range(4):
+            kk, vv = (d["k"], d["v"]) if r % 2 == 0 else (k2, v2)
+            api.pkv_decode_step(shape, cfg, ws, d["q"], kk, vv, d["bt"], d["sl"], part, o, lse,
+                                stream=st)
+
+    with torch.cuda.stream(st):
+        steps()
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            steps()
+    oref, lref = oracle_out(tr, q, k, v)
+    for _ in range(3):
+        with torch.cuda.stream(st):
+            o.fill_(float("nan"))
+            g.replay()
+        st.synchronize()
+        check_error_free(ws)
+        close(o, oref)
+        close_lse(lse, lref)
