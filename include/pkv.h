@@ -99,14 +99,13 @@ typedef struct {
 
 /* ---------------------------------------------------------------- sizes */
 
-/* Bytes of the plan workspace: a 64-byte header (error word, task count),
- * offsets[B+1] and, for WORKQUEUE, the task list (16 bytes per task) followed
- * by internal scheduling data (a balance-ordered copy of the list and one int
- * per row); split paths end with B*Hkv int32 arrival counters of the fused
- * merge.  Every launching entry point takes this workspace (it holds the
- * error word).  Zero it once after allocation: the error word and the
- * counters must start at zero, and both are back at zero after every call
- * (pkv_get_error clears the error word, and the counters a timeout left). */
+/* Bytes of the plan workspace: a 64-byte header (error word, task count, the
+ * decode's task-claim and barrier counters), offsets[B+1] and, for WORKQUEUE,
+ * the task list (16 bytes per task) followed by internal scheduling data (a
+ * balance-ordered copy of the list and one int per row).  Every launching
+ * entry point takes this workspace (it holds the error word).  Zero it once
+ * after allocation: the header must start at zero; its counters are back at
+ * zero after every launch and pkv_get_error() clears the error word. */
 size_t pkv_plan_workspace_size(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg);
 
 /* Bytes of the fp32 partial-state buffer for split paths: acc[slots][d] then
@@ -167,14 +166,14 @@ int pkv_single_pass(const pkv_shape_t *shape, void *d_ws,
 
 /* pkv_decode_merge -- pkv_decode with the exact merge of pkv_merge on its
  * tail (cfg->merge is not consulted).  One kernel launch.  Every split writes
- * its state as pkv_decode does; once a CTA has finished its splits it takes a
- * ticket per split from the arrival counter of that split's (row, kv head) in
- * d_ws, and the CTA drawing a group's last ticket merges the row's n_i states
- * of its G heads into o / lse with pkv_merge's formulas and resets the
- * counter.  A row with one split writes o / lse directly; a row
- * with N*_i = 0 gets o = 0, lse = -inf; a workqueue overflow writes NaN as
- * pkv_merge does.  Results equal pkv_decode + pkv_merge up to the order of
- * the fp32 sums.  Launches on one workspace must not overlap on the GPU. */
+ * its state as pkv_decode does; the kernel's CTAs then meet at a grid-wide
+ * barrier (counters in d_ws; every CTA is resident at once, and the wait is
+ * bounded: a CTA that gives up reports PKV_ETIMEOUT) and share out the
+ * (row, query head) merges, computed with pkv_merge's formulas.  A row with
+ * one split writes o / lse directly; a row with N*_i = 0 gets o = 0,
+ * lse = -inf; a workqueue overflow writes NaN as pkv_merge does.  Results
+ * equal pkv_decode + pkv_merge up to the order of the fp32 sums.  Launches on
+ * one workspace must not overlap on the GPU. */
 int pkv_decode_merge(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
                      const void *d_q, const void *d_k_cache, const void *d_v_cache,
                      const int32_t *d_block_table, const int32_t *d_seq_lens,
@@ -264,7 +263,7 @@ int pkv_decode_step_rows(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, vo
  * - The first call on each device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  * - Every call shares the one array and it keeps the last call's contents:
- *   the call clears the error word, task count and merge counters itself,
+ *   the call clears the workspace header (error word, task count, counters),
  *   but calls that overlap on the GPU (different streams, or other host
  *   threads) race -- serialize them.  Device-side check results stay in the array and are not
  *   reported; callers needing pkv_get_error use pkv_decode_step. */

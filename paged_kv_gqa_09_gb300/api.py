@@ -356,8 +356,8 @@ class PagedDecoder:
     reused across steps; they are resized when a larger configuration arrives.
     `merge` picks how split states are combined (a second kernel by default,
     or PKV_MERGE_FUSED: on the decode's tail); the workspace is zeroed whenever
-    the configuration changes, since the fused merge's counters sit at a place
-    that depends on it.
+    the configuration changes, so that each configuration starts from a clean
+    header.
     """
 
     def __init__(self, policy: Optional[PolicyCfg] = None, max_split_tasks: int = 0,

@@ -263,17 +263,11 @@ int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_
                                                      ws_ordered_off(s->B, ntasks));
         }
         if (fuse) {
-            const size_t co = ws_ctr_off(s->B, mode == kModeQueue, max_tasks(s, c));
             p.fuse = 1;
             p.o = static_cast<__half *>(o);
             p.lse = lse;
-            p.ctr = reinterpret_cast<int32_t *>(static_cast<char *>(d_ws) + co);
             p.offsets = reinterpret_cast<const int32_t *>(static_cast<char *>(d_ws) + ws_offsets_off());
             p.n_rows = rows ? n_rows : s->B;
-            if (co / 16 > 0x7fffffffull)
-                return fail(PKV_EUNSUPPORTED, "workspace too large for the counter record");
-            p.ctr_off16 = (int)(co / 16);
-            p.ctr_words = p.n_rows * s->Hkv;
         }
     }
     if (ntasks > 0x7fffffffLL)
@@ -297,11 +291,9 @@ size_t pkv_plan_workspace_size(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
 {
     if (check_shape(s) || check_cfg(s, c))
         return 0;
-    if (c->path == PKV_PATH_SINGLE_PASS)
+    if (c->path != PKV_PATH_WORKQUEUE)
         return ws_tasks_off(s->B);
-    // split paths end with the fused merge's arrival counters
-    return ws_ctr_off(s->B, c->path == PKV_PATH_WORKQUEUE, max_tasks(s, c)) +
-           sizeof(int32_t) * (size_t)s->B * s->Hkv;
+    return ws_short_off(s->B, max_tasks(s, c)) + sizeof(int32_t) * (size_t)s->B;
 }
 
 size_t pkv_partials_size(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
@@ -838,13 +830,6 @@ int pkv_get_error(void *d_ws, void *stream)
     e = cudaMemset(d_ws, 0, sizeof h);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMemset (error word)");
-    if (h[0] == kErrTimeout && hd.ctr_words > 0) {
-        // a CTA that gave up left its splits' arrival counters mid-count
-        e = cudaMemset(static_cast<char *>(d_ws) + (size_t)hd.ctr_off16 * 16, 0,
-                       (size_t)hd.ctr_words * sizeof(int32_t));
-        if (e != cudaSuccess)
-            return cuda_fail(e, "cudaMemset (merge counters)");
-    }
     switch (h[0]) {
     case kErrBadPage:
         return fail(PKV_EDEVICE, "block-table entry out of range: row %d, logical page %d, value %d",

@@ -66,13 +66,6 @@ struct Layout {
     static constexpr int kBarOff = kRedOff + kStages * (kCW - 1) * 2 * kMaxG * 4;
     // barriers: full[S], empty[S], merge[S]
     static constexpr int kBytes = kBarOff + 3 * kStages * 8;
-    // fused merge, once the CTA's tasks are done and the ring is idle: the
-    // states being merged, their m and l, and the list of groups to merge
-    static constexpr int kMrgListOff = kMetaOff - 4096;  // int4 per group (<= kThreads per round)
-    static constexpr int kMrgMOff = kMetaOff - 8192;     // kMrgML floats of m, then of l
-    static constexpr int kMrgML = 512;
-    static constexpr int kMrgBufFloats = kMrgMOff / 4;   // acc vectors
-    static_assert(kThreads * 16 <= 4096, "merge list fits");
     static constexpr int kAlloc = kBytes + 1024;                     // slack for alignment
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
     static_assert(2 * (kAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
@@ -161,12 +154,10 @@ __device__ __forceinline__ uint32_t row_base(int t, int btl)
 //
 // With p.fuse the exact log-sum-exp merge ("Sequence splitting": the split
 // states are combined exactly) runs on the decode's tail instead of in a
-// second kernel.  Every split of (row i, kv head g) publishes its state and
-// takes a ticket from that pair's arrival counter; the split that draws the
-// last ticket merges the row's n_i states of the G heads and writes o / lse,
-// then resets the counter for the next launch.  Nothing waits on another CTA.
-// A row with one split writes o / lse from registers, and rows without
-// tokens are filled by the producer warps after their tasks.
+// second kernel: every split writes its state, the CTAs meet at a grid-wide
+// barrier, then share the (row, query head) merges out (grid_merge).  A row
+// with one split writes o / lse from registers at its task's end, and rows
+// without tokens are filled by the producer warps after their tasks.
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -181,143 +172,130 @@ __device__ __forceinline__ int split_count(const DecodeParams &p, int i)
     return MODE == kModeRect ? min(n, p.S_b) : n;
 }
 
-// The merge of (row i, kv head g) over states base .. base + n - 1 by the
-// whole CTA, once its own tasks are done and its stage ring is idle:
-//   M = max_j m_j, L = sum_j l_j e^{m_j - M}, o = sum_j acc_j e^{m_j - M} / L,
-//   lse = M + ln L.
-// The states were written by other CTAs; they are copied into the ring with
-// cp.async (no register held per copy, so all are in flight at once), in
-// chunks of splits that fit, and every thread folds its (head, 4 values of d)
-// items over each chunk with a running maximum.
-template <int D>
-__device__ void merge_group(const DecodeParams &p, uint8_t *basep, uint32_t sbase, int i, int g,
-                            int base, int n)
-{
-    using L = Layout<D>;
-    constexpr int kItems = (kMaxG * D / 4 + kThreads - 1) / kThreads;  // items per thread
-    const int tid = threadIdx.x, G = p.G, Hq = p.Hq;
-    const int vec = G * D;        // floats of one split's G consecutive states
-    const int nitems = vec / 4;   // (head, 4 values of d) items
-    const int per = min(L::kMrgBufFloats / vec, L::kMrgML / G);
-    const float *buf = reinterpret_cast<const float *>(basep);
-    float *sm = reinterpret_cast<float *>(basep + L::kMrgMOff);
-    float *sl = sm + L::kMrgML;
-    float M[kItems], Ls[kItems], acc[kItems][4];
-#pragma unroll
-    for (int u = 0; u < kItems; ++u) {
-        M[u] = -INFINITY;
-        Ls[u] = 0.f;
-        acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
-    }
-    for (int c0 = 0; c0 < n; c0 += per) {
-        const int cnt = min(per, n - c0);
-        const int64_t s0 = (int64_t)(base + c0) * Hq + g * G;  // slot of split c0, head 0
-        for (int e = tid; e < cnt * nitems; e += kThreads) {
-            const int j = e / nitems, o = e - j * nitems;
-            cp_async_16(sbase + (uint32_t)(j * vec + o * 4) * 4u,
-                        p.part_acc + (s0 + (int64_t)j * Hq) * D + o * 4);
-        }
-        for (int e = tid; e < cnt * G; e += kThreads) {
-            const int j = e / G, h = e - j * G;
-            sm[e] = __ldcg(p.part_m + s0 + (int64_t)j * Hq + h);
-            sl[e] = __ldcg(p.part_l + s0 + (int64_t)j * Hq + h);
-        }
-        cp_async_wait_all();
-        __syncthreads();
-#pragma unroll
-        for (int u = 0; u < kItems; ++u) {
-            const int it = tid + u * kThreads;
-            if (it < nitems) {
-                const int h = it / (D / 4), d4 = it - h * (D / 4);
-                float mc = M[u];
-                for (int j = 0; j < cnt; ++j)
-                    mc = fmaxf(mc, sm[j * G + h]);
-                const float sc = ex2((M[u] - mc) * kLog2e);  // 0 on the first chunk
-                Ls[u] *= sc;
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    acc[u][v] *= sc;
-                for (int j = 0; j < cnt; ++j) {
-                    const float w = ex2((sm[j * G + h] - mc) * kLog2e);
-                    Ls[u] += w * sl[j * G + h];
-                    const float4 x = *reinterpret_cast<const float4 *>(buf + j * vec + h * D + d4 * 4);
-                    acc[u][0] += w * x.x;
-                    acc[u][1] += w * x.y;
-                    acc[u][2] += w * x.z;
-                    acc[u][3] += w * x.w;
-                }
-                M[u] = mc;
-            }
-        }
-        __syncthreads();  // the ring is refilled by the next chunk
-    }
-#pragma unroll
-    for (int u = 0; u < kItems; ++u) {
-        const int it = tid + u * kThreads;
-        if (it < nitems) {
-            const int h = it / (D / 4), d4 = it - h * (D / 4);
-            const float inv = 1.f / Ls[u];
-            const int64_t oh = (int64_t)i * Hq + g * G + h;
-            *reinterpret_cast<uint2 *>(p.o + oh * D + d4 * 4) =
-                make_uint2(pack_half2(acc[u][0] * inv, acc[u][1] * inv),
-                           pack_half2(acc[u][2] * inv, acc[u][3] * inv));
-            if (d4 == 0 && p.lse)
-                p.lse[oh] = M[u] + logf(Ls[u]);
-        }
-    }
-}
+// The fused merge: once every CTA has finished its tasks
+// (a grid-wide barrier; the grid never exceeds the CTAs the GPU holds at once,
+// and dependents launch only after all of them have started, so all of them
+// become resident), each CTA merges (row, query head) units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ... the way the merge kernel does: consumer warp w
+// folds states j = w, w + 4, ... with its own running maximum, all loads in
+// flight, and the four warp results meet in shared memory.  The barrier's wait
+// is bounded; a CTA that gives up records a timeout and merges nothing.
 
-// End of a fused launch, all warps: every split this CTA decoded has written
-// its state (warp 0, before the CTA barrier); now take a ticket per split of
-// a multi-split row from its (row, kv head) arrival counter -- an acquire-
-// release add at GPU scope, so the barrier-ordered state stores are published
-// before it and the other CTAs' states are visible after it -- and merge the
-// groups whose last ticket this CTA drew, resetting their counters.  Tickets
-// are taken here rather than at each task's end so that no CTA stalls its
-// pipeline for them.  A CTA in which a wait timed out takes none (the error is
-// recorded; pkv_get_error then clears the counters).
 template <int D, int MODE>
-__device__ void finish_merges(const DecodeParams &p, int ntasks, uint8_t *basep, uint32_t sbase,
-                              volatile int *ctl)
+__device__ void grid_merge(const DecodeParams &p, uint8_t *basep, volatile int *ctl)
 {
-    using L = Layout<D>;
-    const int tid = threadIdx.x;
-    __syncthreads();
-    if (ctl[0])
-        return;
-    const int nloc = ntasks > (int)blockIdx.x ? (ntasks - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    int4 *list = reinterpret_cast<int4 *>(basep + L::kMrgListOff);
-    for (int r0 = 0; r0 < nloc; r0 += kThreads) {
-        if (tid == 0)
-            ctl[1] = 0;
-        __syncthreads();
-        const int t = r0 + tid;
-        if (t < nloc) {
-            const TaskInfo ti = load_task<MODE>(p, (int)blockIdx.x + t * (int)gridDim.x, ntasks);
-            const int n = ti.t0 < ti.t1 ? split_count<MODE>(p, ti.i) : 0;
-            if (n > 1) {
-                int base, cidx;
-                if (MODE == kModeQueue) {
-                    base = p.offsets[ti.i];
-                    cidx = ti.i * p.Hkv + ti.g;
-                } else {
-                    const int lr = (ti.sbase / p.Hq) / p.S_b;  // row of the launch
-                    base = lr * p.S_b;
-                    cidx = lr * p.Hkv + ti.g;
+    constexpr int VPL = D / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __syncthreads();  // this CTA's states are written and all of its waits have ended
+    if (tid == 0) {
+        // every CTA arrives, also after a timeout, so that no other waits on it
+        int ok = 1;
+        const int gen = ld_acquire_gpu(&p.ws->bar_gen);
+        __threadfence();  // the CTA's state stores, ordered by the barrier above, go first
+        if (atomicAdd(&p.ws->bar_count, 1) == (int)gridDim.x - 1) {
+            p.ws->bar_count = 0;  // ready for the next launch
+            st_release_gpu(&p.ws->bar_gen, gen + 1);
+        } else {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(&p.ws->bar_gen) == gen) {
+                if (globaltimer_ns() - t0 > kWaitNs) {
+                    report_error(p.ws, kErrTimeout, (int)blockIdx.x, 0, 5);
+                    ok = 0;
+                    break;
                 }
-                if (atom_add_acq_rel_gpu(p.ctr + cidx, 1) == n - 1) {
-                    p.ctr[cidx] = 0;  // every split is in: ready for the next launch
-                    list[atomicAdd(const_cast<int *>(ctl + 1), 1)] = make_int4(ti.i, ti.g, base, n);
-                }
+                __nanosleep(64);
             }
         }
-        __syncthreads();
-        const int cnt = ctl[1];
-        for (int e = 0; e < cnt; ++e) {
-            const int4 m = list[e];
-            merge_group<D>(p, basep, sbase, m.x, m.y, m.z, m.w);
+        ctl[1] = ok;
+    }
+    __syncthreads();
+    if (!ctl[1] || ctl[0])
+        return;
+    float *s_m = reinterpret_cast<float *>(basep);  // [kCW] maxima, [kCW] sums, [kCW][D] acc
+    float *s_l = s_m + kCW;
+    float *s_acc = s_m + 4 * kCW;
+    const int U = p.n_rows * p.Hq;
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        const int lr = u / p.Hq, h = u - lr * p.Hq;
+        int i = lr;
+        if (MODE == kModeRect && p.rows) {
+            i = p.rows[lr];
+            if (i < 0 || i >= p.B)
+                continue;
+        }
+        const int n = split_count<MODE>(p, i);
+        if (n <= 1)
+            continue;  // written at its task's end, or by the producers' fill pass
+        const int base = MODE == kModeQueue ? p.offsets[i] : lr * p.S_b;
+        if (warp < kCW) {
+            float Mw = -INFINITY, Lw = 0.f, acc[VPL];
+#pragma unroll
+            for (int v = 0; v < VPL; ++v)
+                acc[v] = 0.f;
+#pragma unroll 8
+            for (int j = warp; j < n; j += kCW) {
+                const int64_t slot = (int64_t)(base + j) * p.Hq + h;
+                const float mj = __ldcg(p.part_m + slot), lj = __ldcg(p.part_l + slot);
+                float x[VPL];
+                if constexpr (VPL == 4) {
+                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(p.part_acc + slot * D) + lane);
+                    x[0] = t.x;
+                    x[1] = t.y;
+                    x[2] = t.z;
+                    x[3] = t.w;
+                } else {
+                    const float2 t = __ldcg(reinterpret_cast<const float2 *>(p.part_acc + slot * D) + lane);
+                    x[0] = t.x;
+                    x[1] = t.y;
+                }
+                const float mn = fmaxf(Mw, mj);
+                const float so = ex2((Mw - mn) * kLog2e), sj = ex2((mj - mn) * kLog2e);
+                Lw = Lw * so + lj * sj;
+#pragma unroll
+                for (int v = 0; v < VPL; ++v)
+                    acc[v] = acc[v] * so + x[v] * sj;
+                Mw = mn;
+            }
+            if (lane == 0) {
+                s_m[warp] = Mw;
+                s_l[warp] = Lw;
+            }
+#pragma unroll
+            for (int v = 0; v < VPL; ++v)
+                s_acc[warp * D + lane * VPL + v] = acc[v];
         }
         __syncthreads();
+        if (warp == 0) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w2 = 0; w2 < kCW; ++w2)
+                M = fmaxf(M, s_m[w2]);
+            float sc[kCW], L = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < kCW; ++w2) {
+                sc[w2] = ex2((s_m[w2] - M) * kLog2e);  // 0 for a warp that saw no state
+                L += s_l[w2] * sc[w2];
+            }
+            const float inv = 1.f / L;
+            float o[VPL];
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                float t = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < kCW; ++w2)
+                    t += s_acc[w2 * D + lane * VPL + v] * sc[w2];
+                o[v] = t * inv;
+            }
+            const int64_t oh = (int64_t)i * p.Hq + h;
+            __half *out = p.o + oh * D + lane * VPL;
+            if constexpr (VPL == 4)
+                *reinterpret_cast<uint2 *>(out) = make_uint2(pack_half2(o[0], o[1]), pack_half2(o[2], o[3]));
+            else
+                *reinterpret_cast<uint32_t *>(out) = pack_half2(o[0], o[1]);
+            if (p.lse && lane == 0)
+                p.lse[oh] = M + logf(L);
+        }
+        __syncthreads();  // the shared scratch is reused by the next unit
     }
 }
 
@@ -447,7 +425,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
     // and the short ones fill in wherever a CTA runs free.  The claim, the task
     // record and its block-table entries arrive while the consumers drain the
     // stages in flight.  Other modes stride statically over their tasks.
-    constexpr bool kDyn = MODE == kModeQueue && !FUSE;
+    constexpr bool kDyn = MODE == kModeQueue;
     int k_cur = (int)blockIdx.x;  // kDyn: balance-order index of cur
     for (int t = 0; (kDyn ? k_cur < ntasks : t < nloc) && ok; ++t) {
         TaskInfo nxt{0, 0, 0, 0, 0};
@@ -951,7 +929,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t bar_empty0 = bar_full0 + L::kStages * 8;
     const uint32_t bar_merge0 = bar_empty0 + L::kStages * 8;
     const int warp = threadIdx.x >> 5;
-    __shared__ int s_ctl[2];  // [0]: a wait timed out in this CTA; [1]: fused-merge list length
+    __shared__ int s_ctl[2];  // [0]: a wait timed out in this CTA; [1]: fused merge may proceed
 
     if (threadIdx.x == 0) {
         s_ctl[0] = s_ctl[1] = 0;
@@ -973,10 +951,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     // it has finished and its writes are visible
     pdl_wait();
     pdl_trigger();
-    if (FUSE && blockIdx.x == 0 && threadIdx.x == 0) {
-        p.ws->ctr_off16 = p.ctr_off16;
-        p.ws->ctr_words = p.ctr_words;
-    }
     const int ntasks = (MODE == kModeQueue) ? min(p.ws->task_count, p.n_tasks) : p.n_tasks;
     if (warp == kCW)
         run_producer<D, MODE, FUSE>(&tmK, &tmV, p, ntasks, sbase, basep, meta, bar_full0, bar_empty0,
@@ -984,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     else
         run_consumer<D, MODE, FUSE>(p, sbase, basep, meta, bar_full0, bar_empty0, bar_merge0, s_ctl);
     if constexpr (FUSE)
-        finish_merges<D, MODE>(p, ntasks, basep, sbase, s_ctl);
+        grid_merge<D, MODE>(p, basep, s_ctl);
 }
 
 template <int D, int MODE, bool FUSE>

@@ -82,17 +82,10 @@ extern "C" int pkv_decode_step_noalloc(const pkv_shape_t *shape, const pkv_plan_
     const int rc = scratch_address(&base);
     if (rc != PKV_OK)
         return rc;
-    // the array keeps the previous call's contents: clear the error word and
-    // task count, and the fused merge's arrival counters at the workspace's
-    // end (their place moves with the shape), which must start at zero; the
-    // rest is written before it is read
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    size_t ctr_bytes = 0;
-    if (cfg->path != PKV_PATH_SINGLE_PASS)
-        ctr_bytes = sizeof(int32_t) * (size_t)shape->B * shape->Hkv;
-    if (cudaMemsetAsync(base, 0, 64, st) != cudaSuccess ||
-        (ctr_bytes && cudaMemsetAsync(static_cast<unsigned char *>(base) + ws - ctr_bytes, 0,
-                                      ctr_bytes, st) != cudaSuccess))
+    // the array keeps the previous call's contents: clear the workspace header
+    // (error word, task count, the decode's task-claim and barrier counters),
+    // which must start at zero; the rest is written before it is read
+    if (cudaMemsetAsync(base, 0, 64, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return pkv::record_error(PKV_ECUDA, "pkv_decode_step_noalloc: cudaMemsetAsync failed");
     float *partials = part ? reinterpret_cast<float *>(static_cast<unsigned char *>(base) + ws_slot)
                            : nullptr;

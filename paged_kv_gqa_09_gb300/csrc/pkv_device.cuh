@@ -31,15 +31,15 @@ struct WsHeader {
     int32_t task_count;   // tasks written by the plan (0 after an overflow)
     int32_t state_rows;   // sum_i n_i
     int32_t overflow;     // 1 when the plan exceeded max_tasks
-    // arrival counters of the fused merge (written by the decode kernel so
-    // that the host can clear them after a timeout left some mid-count)
-    int32_t ctr_off16;    // byte offset / 16 of the counter array in the workspace
-    int32_t ctr_words;    // int32 counters in it
     // dynamic task claims of the workqueue decode: next balance-order index to
     // hand out (beyond the first round) and CTAs finished; the last CTA to
     // finish zeroes both for the next launch
     int32_t next_task;
     int32_t done_ctas;
+    // grid-wide barrier of the fused merge: CTAs arrived, and a generation the
+    // last arrival advances (the count is back at zero after every launch)
+    int32_t bar_count;
+    int32_t bar_gen;
     int32_t pad[5];
 };
 static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
@@ -78,24 +78,17 @@ __device__ __forceinline__ float ex2(float x)
 
 // Programmatic dependent launch: wait for the preceding grid (and its memory),
 // and allow the next grid in the stream to be scheduled early.
-// Atomic add at GPU scope with acquire-release ordering: the caller's earlier
-// writes (and those it observed, e.g. through a warp barrier) are visible to a
-// thread that later reads the new value, and the caller's later reads see
-// what the writers before it published.
-__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v)
+// GPU-scope acquire load / release store of one int (grid-wide barrier words).
+__device__ __forceinline__ int ld_acquire_gpu(const int *p)
 {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
-
-// 16-byte copy global -> shared that holds no register while in flight
-// (L2 only); cp_async_wait_all waits for all of this thread's copies.
-__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void *gmem_src)
+__device__ __forceinline__ void st_release_gpu(int *p, int v)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gmem_src) : "memory");
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

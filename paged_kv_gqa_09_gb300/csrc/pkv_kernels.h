@@ -25,13 +25,6 @@ inline size_t ws_tasks_off(int B)
 // the balance-ordered copy, then short_before[B].
 inline size_t ws_ordered_off(int B, int64_t max_tasks) { return ws_tasks_off(B) + 16 * (size_t)max_tasks; }
 inline size_t ws_short_off(int B, int64_t max_tasks) { return ws_ordered_off(B, max_tasks) + 16 * (size_t)max_tasks; }
-// Split paths end with the fused merge's arrival counters, one int32 per
-// (row, kv head): after offsets (rectangular) or after short_before (workqueue).
-inline size_t ws_ctr_off(int B, bool queue, int64_t max_tasks)
-{
-    const size_t o = queue ? ws_short_off(B, max_tasks) + sizeof(int32_t) * (size_t)B : ws_tasks_off(B);
-    return (o + 15) & ~(size_t)15;
-}
 
 struct PlanParams {
     const int32_t *seq_lens;
@@ -65,13 +58,11 @@ struct DecodeParams {
     float *part_acc, *part_m, *part_l;  // split modes
     __half *o;                           // single-pass and fused-merge modes
     float *lse;                          // single-pass and fused-merge modes (nullable)
-    // fused merge (split modes): the last-arriving split of a (row, kv head)
-    // merges the row's states into o / lse
+    // fused merge (split modes): after a grid-wide barrier the CTAs merge the
+    // rows' states into o / lse
     int fuse;
-    int32_t *ctr;            // [launch rows][Hkv] arrival counters, zero between launches
     const int32_t *offsets;  // workqueue: first state row of each batch row
     int n_rows;              // rows of the launch (rect: rows[] entries, else B)
-    int ctr_off16, ctr_words;
     int B, Hq, Hkv, G, num_pages, bt_stride;
     int log2P;         // page size = 1 << log2P
     int box_log2;      // tokens per TMA box = 1 << box_log2 (min(P, 64))

@@ -80,12 +80,14 @@ def close_lse(lse_gpu: torch.Tensor, lse_ref: np.ndarray):
         assert err <= LSE_ATOL, f"lse max abs err {err}"
 
 
-def merge_counters(ws: torch.Tensor, B: int, Hkv: int) -> np.ndarray:
-    """The fused merge's arrival counters: the workspace's last B*Hkv int32."""
-    return ws[ws.numel() - 4 * B * Hkv:].view(torch.int32).cpu().numpy()
+def header_counters(ws: torch.Tensor) -> dict:
+    """The decode's counters in the workspace header, all zero between launches:
+    the workqueue's task claims and the fused merge's grid-barrier count."""
+    h = ws[:64].view(torch.int32).cpu().numpy()
+    return {"next_task": int(h[7]), "done_ctas": int(h[8]), "bar_count": int(h[9])}
 
 
-def read_plan(ws: torch.Tensor, B: int, with_order: bool = False, Hkv: int = 0):
+def read_plan(ws: torch.Tensor, B: int, with_order: bool = False):
     h = ws[:64].view(torch.int32).cpu().numpy()
     count = int(h[4])
     off = ws[64:64 + 4 * (B + 1)].view(torch.int32).cpu().numpy()
@@ -93,8 +95,7 @@ def read_plan(ws: torch.Tensor, B: int, with_order: bool = False, Hkv: int = 0):
     tasks = ws[t0:t0 + 16 * count].view(torch.int32).cpu().numpy().reshape(-1, 4)
     if not with_order:
         return count, off, tasks, h
-    # workspace = t0 + 32 * cap + short_before[B] (16-byte aligned) + B*Hkv counters
-    cap = (ws.numel() - 4 * B * Hkv - t0 - (4 * B + 15) // 16 * 16) // 32
+    cap = (ws.numel() - t0 - 4 * B) // 32  # workspace = t0 + 32 * cap + short_before[B]
     o0 = t0 + 16 * cap
     ordered = ws[o0:o0 + 16 * count].view(torch.int32).cpu().numpy().reshape(-1, 4)
     return count, off, tasks, h, ordered

@@ -112,15 +112,13 @@ def test_workspace_and_partial_sizes(L):
     c = cfg(C=256)
     tasks_off = (64 + 4 * 4 + 15) // 16 * 16
     cap = 8 * 3 * 4
-    # canonical list, its balance-ordered copy, one int per row, then (16-byte
-    # aligned) one arrival counter of the fused merge per (row, kv head)
-    ctr_off = (tasks_off + 32 * cap + 4 * 3 + 15) // 16 * 16
-    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(c)) == ctr_off + 4 * 3 * 8
+    # canonical list, its balance-ordered copy, one int per row
+    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(c)) == tasks_off + 32 * cap + 4 * 3
     assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(c)) == cap * 4 * (128 + 2) * 4
     c = cfg(C=256, max_tasks=10)
     assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(c)) == 10 * 4 * 130 * 4
     r = cfg(path=_lib.PKV_PATH_BUCKETED_SPLIT, C=256, bucket=600)
-    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(r)) == tasks_off + 4 * 3 * 8
+    assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(r)) == tasks_off
     assert L.pkv_partials_size(ctypes.byref(s), ctypes.byref(r)) == 3 * 3 * 32 * 130 * 4
     one = cfg(path=_lib.PKV_PATH_SINGLE_PASS)
     assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(one)) == tasks_off

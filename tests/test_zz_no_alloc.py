@@ -51,8 +51,8 @@ def _noalloc(L, tr, d, cfg):
 @pytest.mark.parametrize("path,merge", [(p, _lib.PKV_MERGE_SEPARATE) for p in PATHS] +
                          [(p, _lib.PKV_MERGE_FUSED) for p in PATHS[:2]])
 def test_noalloc_matches_decode_step_twice(lib, path, merge):
-    """With the fused merge the array also holds the arrival counters, which
-    the call zeroes: their place moves with the shape, over whatever the
+    """With the fused merge the header also holds the grid barrier's counters,
+    which the call zeroes with the rest of the header, over whatever the
     previous call left there."""
     tr = T.make_trace(3)  # B=8 bimodal, ~491 MB of K+V
     q = T.gen_q(tr)
