@@ -537,9 +537,13 @@ class HostDecodeLoop:
         """Replay the captured step and wait for it; returns the pinned (o, lse)."""
         if self._graph is None:
             raise RuntimeError("capture() first")
-        # a graph replays on the current stream: make it the capture stream, so
-        # that the synchronize below waits for this very replay
-        with torch.cuda.stream(self._graph_stream):
+        # a graph replays on the current stream: it must be the capture stream,
+        # so that the synchronize below waits for this very replay (switching
+        # costs a few microseconds, so only when needed)
+        if torch.cuda.current_stream().cuda_stream == self._graph_stream.cuda_stream:
             self._graph.replay()
+        else:
+            with torch.cuda.stream(self._graph_stream):
+                self._graph.replay()
         self._graph_stream.synchronize()
         return self.h_o, self.h_lse
