@@ -582,76 +582,65 @@ def _ctypes_refs(shape, cfg):
 
 
 def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, wsb, merge):
-    """Public-API steps with host buffers (HostDecodeLoop -> pkv_decode_step_host):
-    every step copies q, the block table and the lengths in from pinned memory
-    (and, when the workload appends, the new K/V token), decodes, copies o and
-    lse out and synchronizes; timed on the wall clock."""
-    from paged_kv_gqa_09_gb300 import _lib
+    """Public-API steps with host buffers (HostDecodeLoop, one captured graph per
+    step): the step's kernels read q, the block table and the lengths (or, when
+    the workload appends, q and the new K/V token, the table and lengths being
+    device state the step advances) from pinned host memory and write o and lse
+    there; every step is synchronized; timed on the wall clock."""
+    import pkv_traces as T
     R = len(pools)
     n_max = int(tr.seq_lens.max()) + (tr.steps if appends else 0)
-    loops = [api.HostDecodeLoop(kk, vv, tr.B, tr.Hq, tr.bt_stride, n_max, path=path, split_tokens=C,
-                                merge=merge)
-             for kk, vv in pools]
     q_pin = torch.from_numpy(q_h).pin_memory()
-    sl0 = torch.from_numpy(tr.seq_lens.copy())
-    sl_pin = sl0.clone().pin_memory()
-    bt_pin = torch.from_numpy(tr.block_table).pin_memory()
-    kn_pin, vn_pin = kn.cpu().pin_memory(), vn.cpu().pin_memory()
-    h2d = q_pin.numel() * 2 + sl_pin.numel() * 4 + bt_pin.numel() * 4
-    if appends:
-        h2d += (kn_pin.numel() + vn_pin.numel()) * 2
-    d2h = q_pin.numel() * 2 + q_pin.shape[0] * q_pin.shape[1] * 4
+    sl0 = tr.seq_lens.astype(np.int64)
+    qb = q_pin.numel() * 2
+    d2h = qb + q_pin.shape[0] * q_pin.shape[1] * 4
     steps = min(steps, 4000 if not appends else tr.steps - 4)
-    L = _lib.load()
     stream = torch.cuda.current_stream(dev)
+    per_tok = tr.Hkv * tr.d * 4
+    loops = []
+    for kk, vv in pools:
+        if appends:
+            # as in the device loop: on the workqueue the rows' pages are taken
+            # from a device free list as they grow
+            bt0, free_np = T.allocation_split(tr) if path == 1 else (tr.block_table, None)
+            fp = torch.from_numpy(free_np).to(dev) if free_np is not None else None
+            fc = torch.tensor([free_np.size], dtype=torch.int32, device=dev) if fp is not None else None
+            lp = api.HostDecodeLoop(kk, vv, tr.B, tr.Hq, tr.bt_stride, n_max, path=path,
+                                    split_tokens=C, merge=merge, append=True, free_pages=fp,
+                                    free_count=fc)
+            lp.set_state(torch.from_numpy(np.ascontiguousarray(bt0)), torch.from_numpy(tr.seq_lens))
+            lp.h_kn.copy_(kn.cpu())
+            lp.h_vn.copy_(vn.cpu())
+        else:
+            lp = api.HostDecodeLoop(kk, vv, tr.B, tr.Hq, tr.bt_stride, n_max, path=path,
+                                    split_tokens=C, merge=merge)
+            lp.h_bt.copy_(torch.from_numpy(tr.block_table))
+            lp.h_sl.copy_(torch.from_numpy(tr.seq_lens))
+        lp.h_q.copy_(q_pin)
+        lp.capture(stream)  # with appends, this runs the first step (one token)
+        loops.append(lp)
+    h2d = qb + (2 * kn.numel() * 2 if appends else tr.block_table.size * 4 + tr.B * 4)
+    # host views of the pinned staging, so that refreshing a step's inputs costs
+    # a memcpy and not a framework call
+    q_np = q_pin.numpy().view(np.uint16)
+    stage = [lp.h_q.numpy().view(np.uint16) for lp in loops]
+    sl_np = tr.seq_lens
+    stage_sl = [lp.h_sl.numpy() for lp in loops]
+    appended = [1 if appends else 0]  # tokens each row has gained so far
     kv_total = [0]
-
-    graph_mode = not appends
-    if graph_mode:
-        for lp in loops:
-            lp.h_q.copy_(q_pin)
-            lp.h_bt.copy_(bt_pin)
-            lp.h_sl.copy_(sl_pin)
-            lp.capture(stream)
-        # host views of the pinned staging, so that refreshing a step's inputs
-        # costs a memcpy and not a framework call; lengths are fixed here, so
-        # the K+V bytes per step are too
-        stage = [(lp.h_q.numpy().view(np.uint16), lp.h_sl.numpy()) for lp in loops]
-        q_np, sl_np = q_pin.numpy().view(np.uint16), sl_pin.numpy()
-        kv_fixed = int(sl_np.astype(np.int64).sum()) * tr.Hkv * tr.d * 4
 
     def one(s):
         lp = loops[s % R]
-        if graph_mode:
-            # the step's inputs go through the loop's pinned staging: refresh them
-            hq, hsl = stage[s % R]
-            hq[...] = q_np
-            hsl[...] = sl_np
-            lp.step_graph()
-            kv_total[0] += kv_fixed
-            return
+        stage[s % R][...] = q_np
+        if not appends:
+            stage_sl[s % R][...] = sl_np
+        lp.step_graph()
         if appends:
-            # the new token's K/V come from the host too; the append kernel writes
-            # them into their pages and advances the device lengths
-            kn.copy_(kn_pin, non_blocking=True)
-            vn.copy_(vn_pin, non_blocking=True)
-            lp.sl.copy_(sl_pin, non_blocking=True)
-            rc = L.pkv_append(ctypes.byref(lp.shape), lp.ws.data_ptr(), kn.data_ptr(), vn.data_ptr(),
-                              lp.bt.data_ptr(), lp.sl.data_ptr(), lp.k.data_ptr(), lp.v.data_ptr(),
-                              stream.cuda_stream)
-            _lib.check(rc, "pkv_append")
-            lp.step(q_pin, bt_pin if s == 0 else None, None)
-            sl_pin.add_(1)  # after the synchronized step: the copy above has read it
-        else:
-            lp.step(q_pin, bt_pin, sl_pin)
-        kv_total[0] += int(sl_pin.numpy().astype(np.int64).sum()) * tr.Hkv * tr.d * 4
+            appended[0] += 1
+        kv_total[0] += (int(sl0.sum()) + tr.B * appended[0]) * per_tok
 
-    if appends:  # the append needs the block table on the device before the first step
-        for lp in loops:
-            lp.bt.copy_(bt_pin)
     for s in range(3):
         one(s)
-    sl_pin.copy_(sl0)
     kv_total[0] = 0
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -660,9 +649,9 @@ def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, ws
     el = time.perf_counter() - t0
     return {"value": kv_total[0] / el / 1e9, "unit": UNIT, "us_per_step": el / steps * 1e6,
             "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "timing": "synchronized wall clock per step" + (
-                " (HostDecodeLoop graph: the step's kernels read q/bt/lengths from pinned host memory and write o/lse there)" if graph_mode
-                else " (pkv_append + pkv_decode_step_host)")}
+            "timing": "synchronized wall clock per step (HostDecodeLoop graph: the step's kernels "
+                      + ("append the staged token, then " if appends else "")
+                      + "read their host inputs from pinned memory and write o/lse there)"}
 
 
 def main():

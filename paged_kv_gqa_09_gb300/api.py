@@ -429,14 +429,28 @@ class HostDecodeLoop:
     B and n_max unless `path` is given); device staging buffers, the workspace
     and the partial-state buffer are allocated once; outputs land in pinned
     host tensors `h_o` and `h_lse`, reused across steps.
+
+    With `append`, every captured step first writes one new K/V token per row
+    (pinned staging `h_kn`, `h_vn` [B, Hkv, d]) into its page and advances the
+    lengths, then decodes: the block table and lengths are device-resident
+    state, loaded once by `set_state()` and advanced by the step's kernels.  On
+    the workqueue the append is fused into the plan launch, and with
+    `free_pages` / `free_count` (device int32) a token that starts a page takes
+    one from that free list.  `n_max` must then cover the lengths the loop will
+    reach.
     """
 
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, B: int, Hq: int, bt_stride: int,
                  n_max: int, path: Optional[int] = None, split_tokens: Optional[int] = None,
                  policy: Optional[PolicyCfg] = None, scale: Optional[float] = None,
-                 max_tasks: int = 0, merge: int = PKV_MERGE_SEPARATE, inputs_in_place: bool = True):
+                 max_tasks: int = 0, merge: int = PKV_MERGE_SEPARATE, inputs_in_place: bool = True,
+                 append: bool = False, free_pages: Optional[torch.Tensor] = None,
+                 free_count: Optional[torch.Tensor] = None):
         dev = k_cache.device
         self.inputs_in_place = inputs_in_place
+        self.append = append
+        if (free_pages is None) != (free_count is None):
+            raise ValueError("free_pages and free_count go together")
         d = int(k_cache.shape[3])
         # the step's inputs (q | block table | lengths) and outputs (o | lse) each
         # live in one buffer, on the device and pinned on the host, so that a
@@ -476,6 +490,16 @@ class HostDecodeLoop:
         npart = pkv_partials_size(self.shape, self.cfg)
         self.partials = torch.empty(max(npart // 4, 4), dtype=torch.float32, device=dev) if npart else None
         self.k, self.v = k_cache, v_cache
+        if append:
+            if free_pages is not None and p != PKV_PATH_WORKQUEUE:
+                raise ValueError("device page allocation comes with the workqueue's fused append")
+            hkv = int(k_cache.shape[2])
+            self.h_new = torch.empty((2, B, hkv, d), dtype=torch.float16).pin_memory()
+            self.d_new = torch.empty((2, B, hkv, d), dtype=torch.float16, device=dev)
+            self.h_kn, self.h_vn = self.h_new[0], self.h_new[1]
+            self.free_pages = _dev(free_pages, "free_pages", torch.int32, nullable=True)
+            self.free_count = _dev(free_count, "free_count", torch.int32, nullable=True)
+            self._free = (free_pages, free_count)  # keeps them alive
         self._fn = _lib.load().pkv_decode_step_host
         self._refs = (ctypes.byref(self.shape), ctypes.byref(self.cfg))
         self._graph = None
@@ -496,6 +520,13 @@ class HostDecodeLoop:
         check(rc, "pkv_decode_step_host")
         return self.h_o, self.h_lse
 
+    def set_state(self, h_block_table: torch.Tensor, h_seq_lens: torch.Tensor) -> None:
+        """Append mode: load the block table and lengths the step's kernels then
+        advance on the device (synchronous)."""
+        self.bt.copy_(h_block_table)
+        self.sl.copy_(h_seq_lens)
+        torch.cuda.synchronize(self.bt.device)
+
     def capture(self, stream: Optional[torch.cuda.Stream] = None) -> None:
         """Capture one whole host step as a CUDA graph: the step's kernels, the
         last of which writes o and lse straight into the pinned `h_o`, `h_lse`
@@ -507,7 +538,9 @@ class HostDecodeLoop:
         over the host link; those reads overlap the KV stream (on GB300 in place
         measured no slower than the copy from B=1 to B=64).  Afterwards each step is
         `step_graph()`: write the inputs into the staging tensors, one graph
-        launch, one synchronize.  Capture needs a non-default stream."""
+        launch, one synchronize.  Capture needs a non-default stream.  The
+        capture runs the step once eagerly first: in append mode that is a real
+        step, appending the token staged in `h_kn`, `h_vn`."""
         st = stream if stream is not None else torch.cuda.current_stream()
         if st.cuda_stream == torch.cuda.default_stream(st.device).cuda_stream:
             raise ValueError("capture needs a non-default stream")
@@ -515,14 +548,41 @@ class HostDecodeLoop:
         part = self.partials.data_ptr() if self.partials is not None else None
 
         src = (self.h_q, self.h_bt, self.h_sl) if self.inputs_in_place else (self.q, self.bt, self.sl)
+        if self.append:  # table and lengths are device state; q and the new tokens come in
+            new = self.h_new if self.inputs_in_place else self.d_new
+            src = (self.h_q if self.inputs_in_place else self.q, self.bt, self.sl)
+        sref, cref = self._refs
+        ho, hl = self.h_o.data_ptr(), self.h_lse.data_ptr()
 
         def body():
             if not self.inputs_in_place:
-                self.d_in.copy_(self.h_in, non_blocking=True)
-            check(L.pkv_decode_step(self._refs[0], self._refs[1], self.ws.data_ptr(),
-                                    src[0].data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
-                                    src[1].data_ptr(), src[2].data_ptr(), part,
-                                    self.h_o.data_ptr(), self.h_lse.data_ptr(), st.cuda_stream),
+                if self.append:
+                    self.q.copy_(self.h_q, non_blocking=True)
+                    self.d_new.copy_(self.h_new, non_blocking=True)
+                else:
+                    self.d_in.copy_(self.h_in, non_blocking=True)
+            q_, bt_, sl_ = (t.data_ptr() for t in src)
+            if self.append and self.cfg.path == PKV_PATH_WORKQUEUE:
+                check(L.pkv_append_plan(sref, cref, self.ws.data_ptr(), new[0].data_ptr(),
+                                        new[1].data_ptr(), bt_, sl_, self.free_pages,
+                                        self.free_count, self.k.data_ptr(), self.v.data_ptr(),
+                                        st.cuda_stream), "pkv_append_plan")
+                if self.cfg.merge == PKV_MERGE_FUSED:
+                    check(L.pkv_decode_merge(sref, cref, self.ws.data_ptr(), q_, self.k.data_ptr(),
+                                             self.v.data_ptr(), bt_, sl_, part, ho, hl, st.cuda_stream),
+                          "pkv_decode_merge")
+                else:
+                    check(L.pkv_decode(sref, cref, self.ws.data_ptr(), q_, self.k.data_ptr(),
+                                       self.v.data_ptr(), bt_, sl_, part, st.cuda_stream), "pkv_decode")
+                    check(L.pkv_merge(sref, cref, self.ws.data_ptr(), sl_, part, ho, hl,
+                                      st.cuda_stream), "pkv_merge")
+                return
+            if self.append:
+                check(L.pkv_append(sref, self.ws.data_ptr(), new[0].data_ptr(), new[1].data_ptr(),
+                                   bt_, sl_, self.k.data_ptr(), self.v.data_ptr(), st.cuda_stream),
+                      "pkv_append")
+            check(L.pkv_decode_step(sref, cref, self.ws.data_ptr(), q_, self.k.data_ptr(),
+                                    self.v.data_ptr(), bt_, sl_, part, ho, hl, st.cuda_stream),
                   "pkv_decode_step")
 
         with torch.cuda.stream(st):

@@ -111,3 +111,59 @@ def test_fused_append_reports_an_empty_free_list():
     assert sld.cpu().numpy().tolist() == [17, 32, 6]
     assert int(cnt.item()) == 0
     assert btd.cpu().numpy()[0, 1] == free[len(free) - 1]
+
+
+@pytest.mark.parametrize("path,alloc", [(_lib.PKV_PATH_WORKQUEUE, True),
+                                        (_lib.PKV_PATH_BUCKETED_SPLIT, False)])
+def test_host_loop_append_graph_matches_mirror(path, alloc):
+    """HostDecodeLoop in append mode: each captured step appends the staged
+    token (on the workqueue fused into the plan, with device page allocation)
+    and decodes, reading q and the token from pinned memory and writing o / lse
+    there; the block table and lengths stay on the device.  Checked against the
+    host mirror of the append rule and the oracle."""
+    steps = 24
+    tr, k, v, free = setup([15, 16, 40, 0, 33, 64, 1], steps, spare_pages=30)
+    k_h, v_h = k.copy(), v.copy()
+    bt_h, lens_h, count = tr.block_table.copy(), tr.seq_lens.astype(np.int64).copy(), len(free)
+    if not alloc:
+        # the bucketed path writes into pages the table already names
+        for i in range(tr.B):
+            for col in range(tr.bt_stride):
+                if bt_h[i, col] < 0:
+                    bt_h[i, col] = free[count - 1]
+                    count -= 1
+    kd, vd = dev(k), dev(v)
+    freed = dev(np.array(free, np.int32)) if alloc else None
+    cnt = torch.tensor([count], dtype=torch.int32, device="cuda") if alloc else None
+    loop = api.HostDecodeLoop(kd, vd, tr.B, HQ, tr.bt_stride, int(lens_h.max()) + steps + 1, path=path,
+                              split_tokens=C, append=True, free_pages=freed, free_count=cnt)
+    loop.set_state(torch.from_numpy(bt_h.astype(np.int32)), torch.from_numpy(lens_h.astype(np.int32)))
+    st = torch.cuda.Stream()
+    for step in range(steps):
+        kn, vn = T.gen_append_tokens(tr, step)
+        q = T.gen_step_q(tr, step)
+        loop.h_q.copy_(torch.from_numpy(q))
+        loop.h_kn.copy_(torch.from_numpy(kn))
+        loop.h_vn.copy_(torch.from_numpy(vn))
+        if alloc:
+            count = mirror_append(tr, k_h, v_h, bt_h, lens_h, free, count, kn, vn)
+        else:  # the page is already in the table
+            for i in range(tr.B):
+                pg, sl = bt_h[i, lens_h[i] // P], lens_h[i] % P
+                k_h[pg, sl], v_h[pg, sl] = kn[i], vn[i]
+                lens_h[i] += 1
+        if step == 0:
+            loop.capture(st)  # runs step 0 eagerly
+            torch.cuda.synchronize()
+            o, lse = loop.h_o, loop.h_lse
+        else:
+            o, lse = loop.step_graph()
+        if step in (0, 1, 9, steps - 1):
+            check_error_free(loop.ws)
+            assert np.array_equal(loop.sl.cpu().numpy(), lens_h)
+            if alloc:
+                assert np.array_equal(loop.bt.cpu().numpy(), bt_h)
+                assert int(cnt.item()) == count
+            oref, lref = oracle.attention(q, k_h, v_h, bt_h, lens_h.astype(np.int32), tr.scale)
+            close(o, oref, f"o at step {step}")
+            close_lse(lse, lref)
