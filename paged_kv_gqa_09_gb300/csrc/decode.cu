@@ -211,6 +211,8 @@ __device__ void grid_merge(const DecodeParams &p, uint8_t *basep, volatile int *
     __syncthreads();
     if (!ctl[1] || ctl[0])
         return;
+    if (MODE == kModeQueue && p.ws->overflow)
+        return;  // no task ran: the producers' fill pass wrote NaN, as the merge kernel does
     float *s_m = reinterpret_cast<float *>(basep);  // [kCW] maxima, [kCW] sums, [kCW][D] acc
     float *s_l = s_m + kCW;
     float *s_acc = s_m + 4 * kCW;

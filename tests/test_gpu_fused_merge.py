@@ -116,9 +116,17 @@ def test_fused_empty_rows_get_zero_and_minus_inf(path):
 
 
 def test_fused_workqueue_overflow_writes_nan_and_reports():
+    """No task runs after an overflow: every row gets NaN, and the merge phase
+    must not combine the (here zero-filled) states no task wrote."""
     tr, q, k, v = case([300, 700], Hq=8, Hkv=2)
     d = upload(tr, q, k, v)
-    o, lse, ws, _ = run_path(tr, d, WORKQUEUE, C=64, max_tasks=5, merge=FUSED)
+    shape = shape_of(tr)
+    cfg = api.make_cfg(WORKQUEUE, 64, 0, 5, FUSED)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    part = torch.zeros(api.pkv_partials_size(shape, cfg) // 4, dtype=torch.float32, device="cuda")
+    o = torch.zeros((tr.B, tr.Hq, tr.d), dtype=torch.float16, device="cuda")
+    lse = torch.zeros((tr.B, tr.Hq), dtype=torch.float32, device="cuda")
+    api.pkv_decode_step(shape, cfg, ws, d["q"], d["k"], d["v"], d["bt"], d["sl"], part, o, lse)
     st, msg = api.pkv_get_error(ws)
     assert st == _lib.PKV_ECAPACITY, msg
     assert torch.isnan(o.float()).all() and torch.isnan(lse).all()
@@ -126,8 +134,8 @@ def test_fused_workqueue_overflow_writes_nan_and_reports():
 
 
 def test_fused_equals_separate_and_reruns_bit_identically():
-    """The merging split reads every state from memory in split order, so the
-    result does not depend on which CTA arrived last."""
+    """Each (row, head) is merged by one CTA reading its states in a fixed
+    order, so reruns are bit-identical whichever CTAs ran which tasks."""
     for cfg_id, path in ((3, WORKQUEUE), (1, BUCKETED), (2, BUCKETED)):
         tr = T.make_trace(cfg_id)
         q = T.gen_q(tr)
