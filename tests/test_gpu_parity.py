@@ -89,14 +89,22 @@ def test_plan_matches_oracle_on_workloads(cfg_id):
 
 
 def test_plan_capacity_overflow_is_reported():
+    """A plan that exceeds its capacity writes no task, reports PKV_ECAPACITY,
+    and the merge writes NaN (outputs and partial states start at zero here, so
+    a missing write would show)."""
     tr = T.custom_trace([300, 700], 8, 2, 128, 16, 64)
     shape = shape_of(tr)
     cfg = api.make_cfg(WORKQUEUE, 64, 0, max_tasks=5)
     d = upload(tr, T.gen_q(tr), *T.gen_kv(tr))
-    o, lse, ws, _ = run_path(tr, d, WORKQUEUE, C=64, max_tasks=5)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    part = torch.zeros(api.pkv_partials_size(shape, cfg) // 4, dtype=torch.float32, device="cuda")
+    o = torch.zeros((tr.B, tr.Hq, tr.d), dtype=torch.float16, device="cuda")
+    lse = torch.zeros((tr.B, tr.Hq), dtype=torch.float32, device="cuda")
+    api.pkv_decode_step(shape, cfg, ws, d["q"], d["k"], d["v"], d["bt"], d["sl"], part, o, lse)
     st, msg = api.pkv_get_error(ws)
     assert st == _lib.PKV_ECAPACITY, msg
-    assert torch.isnan(o.float()).all()
+    assert torch.isnan(o.float()).all() and torch.isnan(lse).all()
+    assert read_plan(ws, tr.B)[0] == 0  # no task count
 
 
 # ------------------------------------------------------------------ partials
