@@ -173,7 +173,10 @@ int pkv_single_pass(const pkv_shape_t *shape, void *d_ws,
  * one split writes o / lse directly; a row with N*_i = 0 gets o = 0,
  * lse = -inf; a workqueue overflow writes NaN as pkv_merge does.  Results
  * equal pkv_decode + pkv_merge up to the order of the fp32 sums.  Launches on
- * one workspace must not overlap on the GPU. */
+ * one workspace must not overlap on the GPU.  The barrier needs the whole grid
+ * (at most the CTAs the GPU holds at once) resident together: kernels of other
+ * streams that keep SMs busy delay it, and if it cannot fill within 1 s the
+ * CTAs give up and report PKV_ETIMEOUT rather than wait on. */
 int pkv_decode_merge(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
                      const void *d_q, const void *d_k_cache, const void *d_v_cache,
                      const int32_t *d_block_table, const int32_t *d_seq_lens,
