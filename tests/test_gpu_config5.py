@@ -1,9 +1,12 @@
 """Full-size uniform workload (B=64, Hq=64, Hkv=8, G=8, lengths U[128, 65536],
 256 decode steps each appending one token per row), in the launch
-configuration the benchmark times: append + plan + decode + merge per step on
-the compact workqueue.  The ~8.6 GB pool is drawn on the GPU by torch's seeded
+configuration the benchmark times: one captured CUDA graph per step holding
+the fused append + page allocation + plan launch, the decode and the merge on
+the compact workqueue, the step's q and new token copied into fixed buffers
+before each replay.  The ~8.6 GB pool is drawn on the GPU by torch's seeded
 generator; the oracle checks sampled rows (all 64 heads each) at steps 0, 1
-and 255 from host copies of exactly those rows' pages."""
+and 255 from host copies of exactly those rows' pages, found through the block
+table as the device allocated it."""
 import numpy as np
 import pytest
 import torch
@@ -42,28 +45,49 @@ def test_uniform_b64_decode_loop_matches_oracle():
         pytest.skip("no CUDA device")
     tr = T.make_trace(5)
     k, v = T.gen_kv_torch(tr, "cuda")
-    bt = dev(tr.block_table)
+    bt_alloc, free_np = T.allocation_split(tr)  # rows start with the pages their tokens fill
+    bt = dev(np.ascontiguousarray(bt_alloc))
     sl = dev(tr.seq_lens)
+    free = dev(free_np)
+    cnt = torch.tensor([free_np.size], dtype=torch.int32, device="cuda")
     shape = shape_of(tr)
     cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, tr.split_tokens)
     ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
     part = torch.empty(api.pkv_partials_size(shape, cfg) // 4, dtype=torch.float32, device="cuda")
     o = torch.empty((tr.B, tr.Hq, tr.d), dtype=torch.float16, device="cuda")
     lse = torch.empty((tr.B, tr.Hq), dtype=torch.float32, device="cuda")
+    q_buf = torch.empty((tr.B, tr.Hq, tr.d), dtype=torch.float16, device="cuda")
+    kn_buf = torch.empty((tr.B, tr.Hkv, tr.d), dtype=torch.float16, device="cuda")
+    vn_buf = torch.empty_like(kn_buf)
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):  # captured, not run
+            api.pkv_append_plan(shape, cfg, ws, kn_buf, vn_buf, bt, sl, k, v, free, cnt, stream=st)
+            api.pkv_decode(shape, cfg, ws, q_buf, k, v, bt, sl, part, stream=st)
+            api.pkv_merge(shape, cfg, ws, sl, part, o, lse, stream=st)
     lens = tr.seq_lens.copy()
     checked = 0
     for step in range(tr.steps):
         kn, vn = T.gen_append_tokens(tr, step)
         q = T.gen_step_q(tr, step)
-        api.pkv_append(shape, ws, dev(kn), dev(vn), bt, sl, k, v)
+        with torch.cuda.stream(st):
+            q_buf.copy_(torch.from_numpy(q), non_blocking=False)
+            kn_buf.copy_(torch.from_numpy(kn), non_blocking=False)
+            vn_buf.copy_(torch.from_numpy(vn), non_blocking=False)
+            g.replay()
         lens += 1
-        api.pkv_decode_step(shape, cfg, ws, dev(q), k, v, bt, sl, part, o, lse)
         if step in CHECK_STEPS:
-            torch.cuda.synchronize()
+            st.synchronize()
             check_error_free(ws)
             assert np.array_equal(sl.cpu().numpy(), lens)
-            oref, lref = row_oracle(tr, q, k, v, tr.block_table, lens, SAMPLE_ROWS)
+            bt_now = bt.cpu().numpy()
+            oref, lref = row_oracle(tr, q, k, v, bt_now, lens, SAMPLE_ROWS)
             close(o[SAMPLE_ROWS], oref, f"o at step {step}")
             close_lse(lse[SAMPLE_ROWS], lref)
             checked += 1
+    st.synchronize()
     assert checked == len(CHECK_STEPS)
+    used = bt.cpu().numpy()
+    used = used[used >= 0]
+    assert len(np.unique(used)) == used.size  # no page handed out twice
