@@ -65,6 +65,8 @@ typedef enum {
     PKV_PATH_SINGLE_PASS = 2     /* one task per (row, kv-head), no split, no merge */
 } pkv_path_t;
 
+/* A shape with B = 0 is accepted by every launching call, which then does
+ * nothing and returns PKV_OK (its pointers are not examined). */
 typedef struct {
     int32_t B;          /* batch rows, one query token each */
     int32_t Hq;         /* query heads */

@@ -23,7 +23,8 @@ from ._lib import (PKV_MERGE_FUSED, PKV_MERGE_SEPARATE, PKV_PATH_BUCKETED_SPLIT,
 __all__ = [
     "Shape", "PlanCfg", "PolicyCfg", "make_shape", "make_cfg",
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
-    "pkv_decode_merge", "PKV_MERGE_SEPARATE", "PKV_MERGE_FUSED", "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_noalloc",
+    "pkv_decode_merge", "PKV_MERGE_SEPARATE", "PKV_MERGE_FUSED", "pkv_single_pass",
+    "pkv_decode_step", "pkv_decode_step_noalloc",
     "pkv_decode_step_host", "pkv_decode_step_rows", "exact_length_buckets_step", "pkv_append",
     "pkv_append_plan", "pkv_policy", "pkv_policy_default",
     "pkv_cost_model_default", "pkv_policy_learned",
@@ -108,31 +109,33 @@ def pkv_plan(shape, cfg, seq_lens, ws, stream=None) -> None:
 def pkv_decode(shape, cfg, ws, q, k_cache, v_cache, block_table, seq_lens, partials,
                stream=None) -> None:
     L = _lib.load()
+    part = _dev(partials, "partials", torch.float32, nullable=shape.B == 0)
     check(L.pkv_decode(ctypes.byref(shape), ctypes.byref(cfg), _ws(ws),
                        _dev(q, "q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
                        _dev(v_cache, "v_cache", torch.float16),
                        _dev(block_table, "block_table", torch.int32),
                        _dev(seq_lens, "seq_lens", torch.int32),
-                       _dev(partials, "partials", torch.float32), _stream(stream)), "pkv_decode")
+                       part, _stream(stream)), "pkv_decode")
 
 
 def pkv_merge(shape, cfg, ws, seq_lens, partials, o, lse=None, stream=None) -> None:
     L = _lib.load()
+    part = _dev(partials, "partials", torch.float32, nullable=shape.B == 0)
     check(L.pkv_merge(ctypes.byref(shape), ctypes.byref(cfg), _ws(ws),
-                      _dev(seq_lens, "seq_lens", torch.int32),
-                      _dev(partials, "partials", torch.float32), _dev(o, "o", torch.float16),
+                      _dev(seq_lens, "seq_lens", torch.int32), part, _dev(o, "o", torch.float16),
                       _dev(lse, "lse", torch.float32, nullable=True), _stream(stream)), "pkv_merge")
 
 
 def pkv_decode_merge(shape, cfg, ws, q, k_cache, v_cache, block_table, seq_lens, partials, o,
                      lse=None, stream=None) -> None:
     L = _lib.load()
+    part = _dev(partials, "partials", torch.float32, nullable=shape.B == 0)
     check(L.pkv_decode_merge(ctypes.byref(shape), ctypes.byref(cfg), _ws(ws),
                              _dev(q, "q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
                              _dev(v_cache, "v_cache", torch.float16),
                              _dev(block_table, "block_table", torch.int32),
                              _dev(seq_lens, "seq_lens", torch.int32),
-                             _dev(partials, "partials", torch.float32), _dev(o, "o", torch.float16),
+                             part, _dev(o, "o", torch.float16),
                              _dev(lse, "lse", torch.float32, nullable=True), _stream(stream)),
           "pkv_decode_merge")
 
@@ -152,7 +155,8 @@ def pkv_single_pass(shape, ws, q, k_cache, v_cache, block_table, seq_lens, o, ls
 def pkv_decode_step(shape, cfg, ws, q, k_cache, v_cache, block_table, seq_lens, partials, o,
                     lse=None, stream=None) -> None:
     L = _lib.load()
-    part = _dev(partials, "partials", torch.float32, nullable=(cfg.path == PKV_PATH_SINGLE_PASS))
+    part = _dev(partials, "partials", torch.float32,
+                nullable=cfg.path == PKV_PATH_SINGLE_PASS or shape.B == 0)
     check(L.pkv_decode_step(ctypes.byref(shape), ctypes.byref(cfg), _ws(ws),
                             _dev(q, "q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
                             _dev(v_cache, "v_cache", torch.float16),
@@ -190,7 +194,8 @@ def pkv_decode_step_rows(shape, cfg, ws, rows, q, k_cache, v_cache, block_table,
                                  _dev(v_cache, "v_cache", torch.float16),
                                  _dev(block_table, "block_table", torch.int32),
                                  _dev(seq_lens, "seq_lens", torch.int32),
-                                 _dev(partials, "partials", torch.float32), _dev(o, "o", torch.float16),
+                                 _dev(partials, "partials", torch.float32, nullable=shape.B == 0),
+                                 _dev(o, "o", torch.float16),
                                  _dev(lse, "lse", torch.float32, nullable=True), _stream(stream)),
           "pkv_decode_step_rows")
 
@@ -251,7 +256,8 @@ def pkv_decode_step_host(shape, cfg, ws, partials, h_q, q, h_block_table, block_
                          stream=None) -> None:
     """One synchronized decode step with host inputs/outputs (see include/pkv.h)."""
     L = _lib.load()
-    part = _dev(partials, "partials", torch.float32, nullable=(cfg.path == PKV_PATH_SINGLE_PASS))
+    part = _dev(partials, "partials", torch.float32,
+                nullable=cfg.path == PKV_PATH_SINGLE_PASS or shape.B == 0)
     check(L.pkv_decode_step_host(
         ctypes.byref(shape), ctypes.byref(cfg), _ws(ws), part, _host(h_q, "h_q", torch.float16),
         _dev(q, "q", torch.float16), _host(h_block_table, "h_block_table", torch.int32, True),

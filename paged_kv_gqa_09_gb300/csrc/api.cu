@@ -337,6 +337,8 @@ int pkv_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, const int32_t *d_seq
 {
     PKV_TRY(check_shape(s));
     PKV_TRY(check_cfg(s, c));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     if (c->path != PKV_PATH_WORKQUEUE)
         return PKV_OK;
     PKV_TRY(check_ptr(d_seq_lens, "seq_lens"));
@@ -355,6 +357,8 @@ int pkv_append_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, c
 {
     PKV_TRY(check_shape(s));
     PKV_TRY(check_cfg(s, c));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     if (c->path != PKV_PATH_WORKQUEUE)
         return fail(PKV_EINVAL, "pkv_append_plan builds the WORKQUEUE plan");
     PKV_TRY(check_ptr(d_ws, "workspace"));
@@ -396,6 +400,8 @@ int pkv_decode(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const 
 {
     PKV_TRY(check_shape(s));
     PKV_TRY(check_cfg(s, c));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     if (c->path == PKV_PATH_SINGLE_PASS)
         return fail(PKV_EINVAL, "pkv_decode takes a split path; use pkv_single_pass");
     PKV_TRY(check_ptr(d_ws, "workspace"));
@@ -416,6 +422,8 @@ int pkv_decode_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, 
 {
     PKV_TRY(check_shape(s));
     PKV_TRY(check_cfg(s, c));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     if (c->path == PKV_PATH_SINGLE_PASS)
         return fail(PKV_EINVAL, "pkv_decode_merge takes a split path; use pkv_single_pass");
     PKV_TRY(check_ptr(d_ws, "workspace"));
@@ -475,6 +483,8 @@ int pkv_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const i
 {
     PKV_TRY(check_shape(s));
     PKV_TRY(check_cfg(s, c));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     if (c->path == PKV_PATH_SINGLE_PASS)
         return fail(PKV_EINVAL, "pkv_merge takes a split path");
     PKV_TRY(check_ptr(d_ws, "workspace"));
@@ -492,6 +502,8 @@ int pkv_decode_step_rows(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_
 {
     PKV_TRY(check_shape(s));
     PKV_TRY(check_cfg(s, c));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     if (c->path != PKV_PATH_BUCKETED_SPLIT)
         return fail(PKV_EINVAL, "pkv_decode_step_rows runs the BUCKETED_SPLIT path");
     if (n_rows < 1 || n_rows > s->B)
@@ -518,6 +530,8 @@ int pkv_single_pass(const pkv_shape_t *s, void *d_ws, const void *q, const void 
                     const int32_t *bt, const int32_t *sl, void *o, float *lse, void *stream)
 {
     PKV_TRY(check_shape(s));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     PKV_TRY(check_ptr(d_ws, "workspace"));
     PKV_TRY(check_ptr(q, "q"));
     PKV_TRY(check_ptr(k, "k_cache"));
@@ -536,6 +550,8 @@ int pkv_decode_step(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, c
 {
     PKV_TRY(check_shape(s));
     PKV_TRY(check_cfg(s, c));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     if (c->path == PKV_PATH_SINGLE_PASS)
         return pkv_single_pass(s, d_ws, q, k, v, bt, sl, o, lse, stream);
     PKV_TRY(check_ptr(o, "o"));
@@ -554,6 +570,8 @@ int pkv_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_
 {
     PKV_TRY(check_shape(s));
     PKV_TRY(check_cfg(s, c));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     PKV_TRY(check_ptr(d_ws, "workspace"));
     PKV_TRY(check_ptr(d_q, "q"));
     PKV_TRY(check_ptr(k, "k_cache"));
@@ -591,6 +609,8 @@ int pkv_append(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *
                const int32_t *bt, int32_t *sl, void *k_cache, void *v_cache, void *stream)
 {
     PKV_TRY(check_shape(s));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     PKV_TRY(check_ptr(d_ws, "workspace"));
     PKV_TRY(check_ptr(k_new, "k_new"));
     PKV_TRY(check_ptr(v_new, "v_new"));

@@ -68,6 +68,8 @@ extern "C" int pkv_decode_step_noalloc(const pkv_shape_t *shape, const pkv_plan_
     if (ws == 0)
         return pkv_decode_step(shape, cfg, nullptr, d_q, d_k_cache, d_v_cache, d_block_table,
                                d_seq_lens, nullptr, d_o, d_lse, stream);
+    if (shape->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
     const size_t part = pkv_partials_size(shape, cfg);
     const size_t ws_slot = round_up(ws, 256);
     if (ws_slot + part > (size_t)PKV_NOALLOC_SCRATCH_BYTES) {

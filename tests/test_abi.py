@@ -89,6 +89,33 @@ def test_bad_cfg_and_pointers_are_rejected(L):
     assert L.pkv_get_error(None, None) == _lib.PKV_EINVAL
 
 
+def test_empty_batch_is_a_no_op(L):
+    """B = 0: every launching call returns PKV_OK without looking at its
+    pointers (NULL here) or the GPU."""
+    s = shape(B=0)
+    for path in (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_PATH_WORKQUEUE, _lib.PKV_PATH_SINGLE_PASS):
+        for merge in (0, 1):
+            c = cfg(path=path, merge=merge)
+            args = (ctypes.byref(s), ctypes.byref(c))
+            assert L.pkv_decode_step(*args, None, None, None, None, None, None, None, None, None,
+                                     None) == 0
+            assert L.pkv_decode_step_noalloc(*args, None, None, None, None, None, None, None,
+                                             None) == 0
+            assert L.pkv_decode_step_host(*args, None, None, None, None, None, None, None, None,
+                                          None, None, None, None, None, None, None) == 0
+            if path != _lib.PKV_PATH_SINGLE_PASS:
+                assert L.pkv_plan(*args, None, None, None) == 0
+                assert L.pkv_decode(*args, None, None, None, None, None, None, None, None) == 0
+                assert L.pkv_decode_merge(*args, None, None, None, None, None, None, None, None,
+                                          None, None) == 0
+                assert L.pkv_merge(*args, None, None, None, None, None, None) == 0
+    assert L.pkv_single_pass(ctypes.byref(s), None, None, None, None, None, None, None, None,
+                             None) == 0
+    assert L.pkv_append(ctypes.byref(s), None, None, None, None, None, None, None, None) == 0
+    wq = cfg()
+    assert L.pkv_append_plan(ctypes.byref(s), ctypes.byref(wq), *([None] * 10)) == 0
+
+
 def test_unknown_merge_mode_is_rejected(L):
     s = shape()
     for bad in (-1, 2):

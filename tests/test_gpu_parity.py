@@ -251,6 +251,22 @@ def test_empty_batch_rows_and_zero_lengths():
         close(o, oref)
 
 
+def test_empty_batch_through_the_python_api():
+    """B = 0 through PagedDecoder on every route: no launch, empty outputs."""
+    k = torch.zeros((4, 16, 2, 128), dtype=torch.float16, device="cuda")
+    q = torch.zeros((0, 8, 128), dtype=torch.float16, device="cuda")
+    bt = torch.zeros((0, 4), dtype=torch.int32, device="cuda")
+    sl = torch.zeros((0,), dtype=torch.int32, device="cuda")
+    api.pkv_reset_counters()
+    for path in (BUCKETED, WORKQUEUE, SINGLE):
+        for merge in (_lib.PKV_MERGE_SEPARATE, _lib.PKV_MERGE_FUSED):
+            o, lse = api.PagedDecoder(merge=merge).step(q, k, k, bt, sl, 0, path=path,
+                                                        split_tokens=16)
+            assert o.shape == (0, 8, 128) and lse.shape == (0, 8)
+    torch.cuda.synchronize()
+    assert sum(api.pkv_get_counters().values()) == 0
+
+
 def test_outputs_are_deterministic():
     tr = T.make_trace(3)
     q = T.gen_q(tr)
