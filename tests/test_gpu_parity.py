@@ -267,6 +267,22 @@ def test_empty_batch_through_the_python_api():
     assert sum(api.pkv_get_counters().values()) == 0
 
 
+def test_one_very_long_row():
+    """N = 262144 tokens in one row (16384 pages): 256 splits for the merge to
+    combine on the split paths (also fused), 128 block-table segments per
+    task on the single pass."""
+    tr, q, k, v = case([262144], Hq=8, Hkv=2, P=16, C=1024, seed=41)
+    d = upload(tr, q, k, v)
+    oref, lref = oracle_out(tr, q, k, v)
+    for path, merge in ((BUCKETED, _lib.PKV_MERGE_SEPARATE), (WORKQUEUE, _lib.PKV_MERGE_SEPARATE),
+                        (SINGLE, _lib.PKV_MERGE_SEPARATE), (BUCKETED, _lib.PKV_MERGE_FUSED),
+                        (WORKQUEUE, _lib.PKV_MERGE_FUSED)):
+        o, lse, ws, _ = run_path(tr, d, path, merge=merge)
+        check_error_free(ws)
+        close(o, oref, f"o on path {path} merge {merge}")
+        close_lse(lse, lref)
+
+
 def test_outputs_are_deterministic():
     tr = T.make_trace(3)
     q = T.gen_q(tr)
