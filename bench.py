@@ -14,11 +14,13 @@ One JSON line on rank 0:
                step reads is not in L2)
   roofline     the decode kernel alone: algorithmic K+V bytes per launch /
                its average CUDA-event duration, against the measured HBM peak
-  e2e          the same metric through the public API (PagedDecoder.step) with
-               pinned host buffers: q, seq_lens and block table copied in and
-               o, lse copied out every step, synchronized wall clock
+  e2e          the same metric through the public API (HostDecodeLoop, one
+               captured graph per step) with the step's inputs and outputs in
+               pinned host memory, synchronized wall clock per step
   cpu_baseline the float64 oracle on the host cores on a bounded sample
-`--impl reference` times the oracle alone (the reference arm).
+`--merge fused` merges on the decode kernel's tail; `--plan in-decode` lets the
+workqueue's decode build its own plan (no plan launch).  `--impl reference`
+times the oracle alone (the reference arm).
 Multi-GPU (torchrun): every rank runs an independent replica (no collective
 on the data path); value sums the ranks' bytes over the slowest rank's time.
 """
@@ -70,6 +72,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--merge", default="separate", choices=["fused", "separate"],
                     help="split paths: merge on the decode's tail, or in a second kernel")
+    ap.add_argument("--plan", default="separate", choices=["in-decode", "separate"],
+                    help="workqueue without appends: the decode builds its own plan, or a plan kernel")
     return ap.parse_args()
 
 
@@ -181,7 +185,7 @@ def peaks():
 def decode_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_gqa_09_gb300", "csrc")
-    for f in ("decode.cu", "pkv_device.cuh", "pkv_kernels.h"):
+    for f in ("decode.cu", "pkv_device.cuh", "pkv_kernels.h", "plan_map.cuh"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -349,7 +353,12 @@ def run_pkv(args, rank, local, ws, pg):
     n_max_run = tr.n_max + (tr.steps if appends else 0)
     bucket = n_max_run if path == 0 else 0
     fused = args.merge == "fused" and path != 2
-    cfg = api.make_cfg(path, C, bucket, 0, api.PKV_MERGE_FUSED if fused else api.PKV_MERGE_SEPARATE)
+    # the appending workqueue builds its plan in the append launch already
+    self_plan = (args.plan == "in-decode" and path == 1 and not appends and not fused
+                 and tr.B <= api.PKV_SELF_PLAN_MAX_B)
+    plan_mode = api.PKV_PLAN_IN_DECODE if self_plan else api.PKV_PLAN_SEPARATE
+    cfg = api.make_cfg(path, C, bucket, 0, api.PKV_MERGE_FUSED if fused else api.PKV_MERGE_SEPARATE,
+                       plan_mode)
     wsb = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device=dev)
     npart = api.pkv_partials_size(shape, cfg)
     part = torch.empty(max(npart // 4, 4), dtype=torch.float32, device=dev)
@@ -519,7 +528,7 @@ def run_pkv(args, rank, local, ws, pg):
         if appends:
             reset_lengths()
         e2e = run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps if not appends else steps,
-                      appends, kn, vn, wsb, cfg.merge)
+                      appends, kn, vn, wsb, cfg.merge, cfg.plan)
 
     gbs = kv_step / (ms * 1e-3) / 1e9
     total = whole_job_gbs(kv_step, ms_max, ws)
@@ -542,6 +551,7 @@ def run_pkv(args, rank, local, ws, pg):
         "config": {
             "workload": WORKLOADS[cfg_id], "path": ["bucketed-split", "workqueue", "single-pass"][path],
             "merge": ("fused" if fused else "separate") if path != 2 else None,
+            "plan": ("in-decode" if self_plan else "plan kernel") if path == 1 else None,
             "split_tokens": C, "kv_bytes_per_step": kv_step, "seed": tr.seed,
             "l2": (f"{R} KV pools rotated ({R * pool_bytes / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB)"
                    if R > 1 else f"inputs ({pool_bytes / 2**30:.1f} GiB) larger than L2"),
@@ -581,7 +591,7 @@ def _ctypes_refs(shape, cfg):
     return ctypes.byref(shape), ctypes.byref(cfg)
 
 
-def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, wsb, merge):
+def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, wsb, merge, plan):
     """Public-API steps with host buffers (HostDecodeLoop, one captured graph per
     step): the step's kernels read q, the block table and the lengths (or, when
     the workload appends, q and the new K/V token, the table and lengths being
@@ -613,7 +623,7 @@ def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, ws
             lp.h_vn.copy_(vn.cpu())
         else:
             lp = api.HostDecodeLoop(kk, vv, tr.B, tr.Hq, tr.bt_stride, n_max, path=path,
-                                    split_tokens=C, merge=merge)
+                                    split_tokens=C, merge=merge, plan=plan)
             lp.h_bt.copy_(torch.from_numpy(tr.block_table))
             lp.h_sl.copy_(torch.from_numpy(tr.seq_lens))
         lp.h_q.copy_(q_pin)

@@ -90,6 +90,8 @@ typedef struct {
     int32_t merge;        /* split paths, for the step calls (pkv_decode_step
                              and its variants): PKV_MERGE_SEPARATE or
                              PKV_MERGE_FUSED (see pkv_decode_merge) */
+    int32_t plan;         /* WORKQUEUE: PKV_PLAN_SEPARATE or
+                             PKV_PLAN_IN_DECODE (see pkv_decode) */
 } pkv_plan_cfg_t;
 
 /* How a step combines the split states.  SEPARATE is the pages' structure
@@ -98,6 +100,14 @@ typedef struct {
  * fewer per step.  A zero-filled cfg selects SEPARATE. */
 #define PKV_MERGE_SEPARATE 0
 #define PKV_MERGE_FUSED 1
+
+/* Where the workqueue's plan is built.  SEPARATE: the plan kernel (pkv_plan),
+ * then the decode reads its task list.  IN_DECODE: for B <= PKV_SELF_PLAN_MAX_B
+ * the decode kernel builds the same plan itself, so a step needs no plan
+ * launch (pkv_decode documents it).  A zero-filled cfg selects SEPARATE. */
+#define PKV_PLAN_SEPARATE 0
+#define PKV_PLAN_IN_DECODE 1
+#define PKV_SELF_PLAN_MAX_B 512
 
 /* ---------------------------------------------------------------- sizes */
 
@@ -138,8 +148,13 @@ int pkv_plan(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg,
  * rectangular grid B x Hkv x S_b (state_base = (i*S_b + j)*Hq + g*G); an empty
  * split writes the neutral state (m=-inf, l=0, acc=0) and reads no KV.
  * WORKQUEUE walks the task list pkv_plan wrote into d_ws (enqueue pkv_plan
- * first on the same stream).  K/V pages are read in place through the block
- * table; no page is repacked. */
+ * first on the same stream) -- unless cfg->plan == PKV_PLAN_IN_DECODE and
+ * B <= PKV_SELF_PLAN_MAX_B: then every CTA derives the tasks from d_seq_lens
+ * itself (prefix sums of each row's full and shorter splits, in shared
+ * memory) and the launch also writes into d_ws the plan pkv_plan would have
+ * written (header, offsets, task list), so pkv_merge follows as usual and no
+ * pkv_plan is needed.  K/V pages are read in place through the block table;
+ * no page is repacked. */
 int pkv_decode(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
                const void *d_q, const void *d_k_cache, const void *d_v_cache,
                const int32_t *d_block_table, const int32_t *d_seq_lens,
@@ -187,8 +202,11 @@ int pkv_decode_merge(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *
 /* pkv_decode_step -- one whole decode step on the path cfg->path:
  * WORKQUEUE = pkv_plan + pkv_decode + pkv_merge, BUCKETED_SPLIT = pkv_decode +
  * pkv_merge, SINGLE_PASS = pkv_single_pass; with cfg->merge == PKV_MERGE_FUSED
- * pkv_decode_merge replaces pkv_decode + pkv_merge.  Same arguments and
- * errors as those calls; d_partials may be NULL for SINGLE_PASS. */
+ * pkv_decode_merge replaces pkv_decode + pkv_merge.  WORKQUEUE with
+ * cfg->plan == PKV_PLAN_IN_DECODE, the separate merge and
+ * B <= PKV_SELF_PLAN_MAX_B drops the pkv_plan launch (the decode plans for
+ * itself); otherwise the field has no effect.  Same arguments and errors as
+ * those calls; d_partials may be NULL for SINGLE_PASS. */
 int pkv_decode_step(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
                     const void *d_q, const void *d_k_cache, const void *d_v_cache,
                     const int32_t *d_block_table, const int32_t *d_seq_lens,

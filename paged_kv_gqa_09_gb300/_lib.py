@@ -25,6 +25,9 @@ PKV_PATH_SINGLE_PASS = 2
 
 PKV_MERGE_SEPARATE = 0  # the split states are merged by a second kernel
 PKV_MERGE_FUSED = 1     # merged on the decode kernel's tail
+PKV_PLAN_SEPARATE = 0   # the workqueue's plan is its own launch (pkv_plan)
+PKV_PLAN_IN_DECODE = 1  # the decode kernel builds the plan itself (B <= PKV_SELF_PLAN_MAX_B)
+PKV_SELF_PLAN_MAX_B = 512
 PATH_EXACT_BUCKETS = 3  # step-model only
 
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # PKV_NOALLOC_SCRATCH_BYTES in include/pkv.h
@@ -68,7 +71,7 @@ class Shape(ctypes.Structure):
 class PlanCfg(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("split_tokens", ctypes.c_int32),
                 ("bucket_len", ctypes.c_int32), ("max_tasks", ctypes.c_int32),
-                ("merge", ctypes.c_int32)]
+                ("merge", ctypes.c_int32), ("plan", ctypes.c_int32)]
 
 
 class PolicyCfg(ctypes.Structure):

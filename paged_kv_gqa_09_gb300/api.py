@@ -17,13 +17,15 @@ import torch
 
 from . import _lib
 from ._lib import (PKV_MERGE_FUSED, PKV_MERGE_SEPARATE, PKV_PATH_BUCKETED_SPLIT,
-                   PKV_PATH_SINGLE_PASS, PKV_PATH_WORKQUEUE, Counters,
+                   PKV_PATH_SINGLE_PASS, PKV_PATH_WORKQUEUE, PKV_PLAN_IN_DECODE,
+                   PKV_PLAN_SEPARATE, PKV_SELF_PLAN_MAX_B, Counters,
                    PlanCfg, PolicyCfg, Shape, StepModel, check)
 
 __all__ = [
     "Shape", "PlanCfg", "PolicyCfg", "make_shape", "make_cfg",
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
-    "pkv_decode_merge", "PKV_MERGE_SEPARATE", "PKV_MERGE_FUSED", "pkv_single_pass",
+    "pkv_decode_merge", "PKV_MERGE_SEPARATE", "PKV_MERGE_FUSED", "PKV_PLAN_SEPARATE",
+    "PKV_PLAN_IN_DECODE", "PKV_SELF_PLAN_MAX_B", "pkv_single_pass",
     "pkv_decode_step", "pkv_decode_step_noalloc",
     "pkv_decode_step_host", "pkv_decode_step_rows", "exact_length_buckets_step", "pkv_append",
     "pkv_append_plan", "pkv_policy", "pkv_policy_default",
@@ -79,8 +81,8 @@ def make_shape(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Tensor
 
 
 def make_cfg(path: int, split_tokens: int = 1024, bucket_len: int = 0, max_tasks: int = 0,
-             merge: int = PKV_MERGE_SEPARATE) -> PlanCfg:
-    return PlanCfg(int(path), int(split_tokens), int(bucket_len), int(max_tasks), int(merge))
+             merge: int = PKV_MERGE_SEPARATE, plan: int = PKV_PLAN_SEPARATE) -> PlanCfg:
+    return PlanCfg(int(path), int(split_tokens), int(bucket_len), int(max_tasks), int(merge), int(plan))
 
 
 # ------------------------------------------------------------------ C ABI
@@ -361,16 +363,18 @@ class PagedDecoder:
     Buffers come from the torch caching allocator on the current device and are
     reused across steps; they are resized when a larger configuration arrives.
     `merge` picks how split states are combined (a second kernel by default,
-    or PKV_MERGE_FUSED: on the decode's tail); the workspace is zeroed whenever
-    the configuration changes, so that each configuration starts from a clean
-    header.
+    or PKV_MERGE_FUSED: on the decode's tail) and `plan` where the workqueue's
+    plan is built (its own launch, or PKV_PLAN_IN_DECODE: by the decode kernel);
+    the workspace is zeroed whenever the configuration changes, so that each
+    configuration starts from a clean header.
     """
 
     def __init__(self, policy: Optional[PolicyCfg] = None, max_split_tasks: int = 0,
-                 merge: int = PKV_MERGE_SEPARATE):
+                 merge: int = PKV_MERGE_SEPARATE, plan: int = PKV_PLAN_SEPARATE):
         self.policy = policy
         self.max_split_tasks = max_split_tasks
         self.merge = merge
+        self.plan = plan
         self._ws: dict = {}
         self._part: dict = {}
         self._key: dict = {}
@@ -384,7 +388,7 @@ class PagedDecoder:
             c = split_tokens
         bucket = n_max if p == PKV_PATH_BUCKETED_SPLIT else 0
         return make_cfg(p, c, bucket, self.max_split_tasks if p == PKV_PATH_WORKQUEUE else 0,
-                        self.merge)
+                        self.merge, self.plan)
 
     def buffers(self, shape: Shape, cfg: PlanCfg, device) -> tuple[torch.Tensor, Optional[torch.Tensor]]:
         nws = pkv_plan_workspace_size(shape, cfg)
@@ -443,7 +447,7 @@ class HostDecodeLoop:
     the workqueue the append is fused into the plan launch, and with
     `free_pages` / `free_count` (device int32) a token that starts a page takes
     one from that free list.  `n_max` must then cover the lengths the loop will
-    reach.
+    reach.  `merge` and `plan` choose the step's launches as in PagedDecoder.
     """
 
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, B: int, Hq: int, bt_stride: int,
@@ -451,7 +455,7 @@ class HostDecodeLoop:
                  policy: Optional[PolicyCfg] = None, scale: Optional[float] = None,
                  max_tasks: int = 0, merge: int = PKV_MERGE_SEPARATE, inputs_in_place: bool = True,
                  append: bool = False, free_pages: Optional[torch.Tensor] = None,
-                 free_count: Optional[torch.Tensor] = None):
+                 free_count: Optional[torch.Tensor] = None, plan: int = PKV_PLAN_SEPARATE):
         dev = k_cache.device
         self.inputs_in_place = inputs_in_place
         self.append = append
@@ -491,7 +495,7 @@ class HostDecodeLoop:
         if split_tokens is not None:
             c = split_tokens
         self.cfg = make_cfg(p, c, n_max if p == PKV_PATH_BUCKETED_SPLIT else 0,
-                            max_tasks if p == PKV_PATH_WORKQUEUE else 0, merge)
+                            max_tasks if p == PKV_PATH_WORKQUEUE else 0, merge, plan)
         self.ws = torch.zeros(pkv_plan_workspace_size(self.shape, self.cfg), dtype=torch.uint8, device=dev)
         npart = pkv_partials_size(self.shape, self.cfg)
         self.partials = torch.empty(max(npart // 4, 4), dtype=torch.float32, device=dev) if npart else None

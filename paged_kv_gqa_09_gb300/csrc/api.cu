@@ -4,6 +4,7 @@
 #include "pkv.h"
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
+#include "plan_map.cuh"
 
 #include <atomic>
 #include <cmath>
@@ -93,7 +94,17 @@ int check_cfg(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
         return fail(PKV_EINVAL, "negative bucket_len or max_tasks");
     if (c->merge != PKV_MERGE_SEPARATE && c->merge != PKV_MERGE_FUSED)
         return fail(PKV_EINVAL, "unknown merge mode %d", (int)c->merge);
+    if (c->plan != PKV_PLAN_SEPARATE && c->plan != PKV_PLAN_IN_DECODE)
+        return fail(PKV_EINVAL, "unknown plan mode %d", (int)c->plan);
     return PKV_OK;
+}
+
+static_assert(pkv::kSelfPlanMaxB == PKV_SELF_PLAN_MAX_B, "one row limit for the self-planning decode");
+
+// The workqueue decode of this shape and cfg builds its own plan.
+bool self_plans(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
+{
+    return c->path == PKV_PATH_WORKQUEUE && c->plan == PKV_PLAN_IN_DECODE && s->B <= kSelfPlanMaxB;
 }
 
 int len_cap(const pkv_shape_t *s) { return s->bt_stride * s->page_size; }
@@ -259,8 +270,15 @@ int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_
             ntasks = (int64_t)(rows ? n_rows : s->B) * s->Hkv * p.S_b;
         } else {
             ntasks = max_tasks(s, c);
-            p.tasks = reinterpret_cast<const int4 *>(static_cast<char *>(d_ws) +
-                                                     ws_ordered_off(s->B, ntasks));
+            char *w = static_cast<char *>(d_ws);
+            p.tasks = reinterpret_cast<const int4 *>(w + ws_ordered_off(s->B, ntasks));
+            if (!fuse && self_plans(s, c)) {
+                p.self_plan = 1;
+                p.plan_offsets = reinterpret_cast<int32_t *>(w + ws_offsets_off());
+                p.plan_short_before = reinterpret_cast<int32_t *>(w + ws_short_off(s->B, ntasks));
+                p.plan_tasks = reinterpret_cast<int4 *>(w + ws_tasks_off(s->B));
+                p.plan_ordered = reinterpret_cast<int4 *>(w + ws_ordered_off(s->B, ntasks));
+            }
         }
         if (fuse) {
             p.fuse = 1;
@@ -556,9 +574,12 @@ int pkv_decode_step(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, c
         return pkv_single_pass(s, d_ws, q, k, v, bt, sl, o, lse, stream);
     PKV_TRY(check_ptr(o, "o"));
     PKV_TRY(check_ptr(lse, "lse", true));
-    PKV_TRY(pkv_plan(s, c, sl, d_ws, stream));
-    if (c->merge == PKV_MERGE_FUSED)
+    if (c->merge == PKV_MERGE_FUSED) {
+        PKV_TRY(pkv_plan(s, c, sl, d_ws, stream));
         return pkv_decode_merge(s, c, d_ws, q, k, v, bt, sl, part, o, lse, stream);
+    }
+    if (!self_plans(s, c))
+        PKV_TRY(pkv_plan(s, c, sl, d_ws, stream));
     PKV_TRY(pkv_decode(s, c, d_ws, q, k, v, bt, sl, part, stream));
     return pkv_merge(s, c, d_ws, sl, part, o, lse, stream);
 }

@@ -34,6 +34,7 @@
 // workspace header and the CTA drains its own copies and exits.
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
+#include "plan_map.cuh"
 
 namespace pkv {
 namespace {
@@ -86,16 +87,31 @@ __device__ __forceinline__ TaskInfo shfl_task(const TaskInfo &a, int src)
     return r;
 }
 
+// Prefix sums of a self-planning workqueue launch in shared memory: F[i] full
+// splits and R[i] shorter last splits in the rows before i (B + 1 entries
+// each); F == nullptr when the plan kernel wrote the task list.
+struct SelfPlan {
+    const int *F, *R;
+};
+
+// Workqueue task k (balance order) as {row, kv head, split, first state slot}.
+__device__ __forceinline__ int4 queue_record(const DecodeParams &p, const SelfPlan &sp, int k)
+{
+    if (sp.F)
+        return plan_task_at(k, sp.F, sp.R, p.B, p.Hkv, p.Hq, p.G, nullptr);
+    return p.tasks[k];
+}
+
 // Task k of this launch, with its row-local token range.
 template <int MODE>
-__device__ __forceinline__ TaskInfo load_task(const DecodeParams &p, int k, int ntasks)
+__device__ __forceinline__ TaskInfo load_task(const DecodeParams &p, const SelfPlan &sp, int k, int ntasks)
 {
     TaskInfo ti{0, 0, 0, 0, 0};
     if (k >= ntasks)
         return ti;
     int j = 0;
     if (MODE == kModeQueue) {
-        const int4 r = p.tasks[k];
+        const int4 r = queue_record(p, sp, k);
         ti.i = r.x;
         ti.g = r.y;
         j = r.z;
@@ -369,7 +385,7 @@ template <int D, int MODE, bool FUSE>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUtensorMap *tmV,
                                              const DecodeParams &p, int ntasks, uint32_t sbase,
                                              uint8_t *basep, int4 *meta, uint32_t bar_full0,
-                                             uint32_t bar_empty0, volatile int *fail)
+                                             uint32_t bar_empty0, volatile int *fail, const SelfPlan sp)
 {
     using L = Layout<D>;
     const int lane = threadIdx.x & 31;
@@ -382,7 +398,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
 
     // task infos of this CTA's local tasks t, lane-held in windows of 32
     auto task_of = [&](int t) {
-        return t < nloc ? load_task<MODE>(p, (int)blockIdx.x + t * (int)gridDim.x, ntasks)
+        return t < nloc ? load_task<MODE>(p, sp, (int)blockIdx.x + t * (int)gridDim.x, ntasks)
                         : TaskInfo{0, 0, 0, 0, 0};
     };
     auto seg_end = [&](const TaskInfo &ti) { return ((ti.t1 - 1) >> log2P) + 1; };
@@ -393,7 +409,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
     if (nloc > 0) {
         int i0, j0;
         if (MODE == kModeQueue) {
-            const int4 r = p.tasks[blockIdx.x];
+            const int4 r = queue_record(p, sp, (int)blockIdx.x);
             i0 = r.x;
             j0 = r.z;
         } else if (MODE == kModeRect) {
@@ -547,7 +563,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                 kn = (int)gridDim.x + atomicAdd(&p.ws->next_task, 1);
             kn = __shfl_sync(0xffffffffu, kn, 0);
             if (kn < ntasks) {
-                nxt = load_task<MODE>(p, kn, ntasks);
+                nxt = load_task<MODE>(p, sp, kn, ntasks);
                 nxt_live = nxt.t0 < nxt.t1;
                 if (nxt_live)
                     load_pages(p, nxt.i, nxt.t0 >> log2P, min(seg_end(nxt), (nxt.t0 >> log2P) + kSeg),
@@ -916,6 +932,127 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
     }
 }
 
+// ---------------------------------------------------------- self-planning workqueue
+
+// The plan of a workqueue launch, built by every CTA from the row lengths
+// ("Row-local bounds": n_i = ceil(N*_i / C), split i's states start at the
+// exclusive prefix of n): thread t sums the full and shorter splits of rows
+// [kPer t, kPer t + kPer), one block scan gives the prefixes, which land in
+// F and R (B + 1 entries each).  CTA 0 also writes what the merge and the
+// workspace's readers expect of the plan kernel: the header's task count,
+// state rows and overflow flag, offsets and short_before, and any bad length.
+// Returns the task count (0 after an overflow of the launch's capacity).
+// Every thread of the CTA calls it.
+__device__ __noinline__ int self_plan_build(const DecodeParams &p, int *F, int *R)
+{
+    constexpr int kWarps = kThreads / 32;
+    constexpr int kPer = (kSelfPlanMaxB + kThreads - 1) / kThreads;
+    __shared__ long long s_tot[2][kWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool cta0 = blockIdx.x == 0;
+    if (p.B > kSelfPlanMaxB) {  // the host never launches this; decode nothing, merge NaN
+        if (cta0 && tid == 0) {
+            p.ws->task_count = 0;
+            p.ws->overflow = 1;
+            report_error(p.ws, kErrCapacity, p.B, kSelfPlanMaxB, 1);
+        }
+        return 0;
+    }
+    int f[kPer], r[kPer];
+    long long sf = 0, sr = 0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i = tid * kPer + u;
+        f[u] = r[u] = 0;
+        if (i < p.B) {
+            int N = p.seq_lens[i];
+            if (N < 0 || N > p.len_cap) {
+                if (cta0)
+                    report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.len_cap);
+                N = N < 0 ? 0 : p.len_cap;
+            }
+            f[u] = N / p.C;
+            r[u] = (N % p.C) != 0 ? 1 : 0;
+        }
+        sf += f[u];
+        sr += r[u];
+    }
+    long long xf = sf, xr = sr;  // inclusive warp scans
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long yf = __shfl_up_sync(0xffffffffu, xf, o);
+        const long long yr = __shfl_up_sync(0xffffffffu, xr, o);
+        if (lane >= o) {
+            xf += yf;
+            xr += yr;
+        }
+    }
+    if (lane == 31) {
+        s_tot[0][warp] = xf;
+        s_tot[1][warp] = xr;
+    }
+    __syncthreads();
+    long long ef = xf - sf, er = xr - sr, tf = 0, tr = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) {
+            ef += s_tot[0][w];
+            er += s_tot[1][w];
+        }
+        tf += s_tot[0][w];
+        tr += s_tot[1][w];
+    }
+    const long long T = (tf + tr) * p.Hkv;
+    const bool over = T > p.n_tasks;  // the capacity, at most INT32_MAX: F and R fit in int
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i = tid * kPer + u;
+        if (i < p.B) {
+            if (!over) {
+                F[i] = (int)ef;
+                R[i] = (int)er;
+            }
+            if (cta0) {
+                p.plan_offsets[i] = (int)(ef + er);
+                p.plan_short_before[i] = (int)er;
+            }
+        }
+        ef += f[u];
+        er += r[u];
+    }
+    if (tid == 0) {
+        if (!over) {
+            F[p.B] = (int)tf;
+            R[p.B] = (int)tr;
+        }
+        if (cta0) {
+            p.plan_offsets[p.B] = (int)(tf + tr);
+            p.ws->task_count = over ? 0 : (int)T;
+            p.ws->state_rows = (int)(tf + tr);
+            p.ws->overflow = over ? 1 : 0;
+            if (over)
+                report_error(p.ws, kErrCapacity, (int)(T > 0x7fffffffLL ? 0x7fffffffLL : T), p.n_tasks, 0);
+        }
+    }
+    __syncthreads();
+    return over ? 0 : (int)T;
+}
+
+// Both task lists of the plan, written by the consumer warps of all CTAs
+// (task t of the balance order goes to position t of the balanced list and
+// to its lexicographic index in the canonical one) while the first tiles
+// are in flight; nothing in this launch reads them back.
+__device__ __forceinline__ void self_plan_write_tasks(const DecodeParams &p, const SelfPlan &sp, int ntasks)
+{
+    constexpr int kWriters = 32 * kCW;
+    for (int64_t t = (int64_t)blockIdx.x * kWriters + threadIdx.x; t < ntasks; t += (int64_t)gridDim.x * kWriters) {
+        int64_t lex;
+        const int4 rec = plan_task_at((int)t, sp.F, sp.R, p.B, p.Hkv, p.Hq, p.G, &lex);
+        p.plan_ordered[t] = rec;
+        p.plan_tasks[lex] = rec;
+    }
+}
+
 template <int D, int MODE, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -932,6 +1069,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t bar_merge0 = bar_empty0 + L::kStages * 8;
     const int warp = threadIdx.x >> 5;
     __shared__ int s_ctl[2];  // [0]: a wait timed out in this CTA; [1]: fused merge may proceed
+    // the self-planning workqueue's prefix sums F, R (the other instances keep one word)
+    constexpr bool kSelf = MODE == kModeQueue && !FUSE;
+    __shared__ int s_plan[kSelf ? 2 * (kSelfPlanMaxB + 1) : 1];
 
     if (threadIdx.x == 0) {
         s_ctl[0] = s_ctl[1] = 0;
@@ -953,12 +1093,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     // it has finished and its writes are visible
     pdl_wait();
     pdl_trigger();
-    const int ntasks = (MODE == kModeQueue) ? min(p.ws->task_count, p.n_tasks) : p.n_tasks;
-    if (warp == kCW)
+    SelfPlan sp{nullptr, nullptr};
+    int ntasks = p.n_tasks;
+    if constexpr (kSelf) {
+        if (p.self_plan) {
+            ntasks = self_plan_build(p, s_plan, s_plan + kSelfPlanMaxB + 1);
+            sp = SelfPlan{s_plan, s_plan + kSelfPlanMaxB + 1};
+        } else {
+            ntasks = min(p.ws->task_count, p.n_tasks);
+        }
+    } else if (MODE == kModeQueue) {
+        ntasks = min(p.ws->task_count, p.n_tasks);
+    }
+    if (warp == kCW) {
         run_producer<D, MODE, FUSE>(&tmK, &tmV, p, ntasks, sbase, basep, meta, bar_full0, bar_empty0,
-                                    s_ctl);
-    else
+                                    s_ctl, sp);
+    } else {
+        if constexpr (kSelf)
+            if (sp.F)
+                self_plan_write_tasks(p, sp, ntasks);
         run_consumer<D, MODE, FUSE>(p, sbase, basep, meta, bar_full0, bar_empty0, bar_merge0, s_ctl);
+    }
     if constexpr (FUSE)
         grid_merge<D, MODE>(p, basep, s_ctl);
 }

@@ -63,6 +63,13 @@ struct DecodeParams {
     int fuse;
     const int32_t *offsets;  // workqueue: first state row of each batch row
     int n_rows;              // rows of the launch (rect: rows[] entries, else B)
+    // self-planning workqueue (self_plan != 0, B <= kSelfPlanMaxB, no fused
+    // merge): every CTA derives the tasks from the lengths in shared memory,
+    // and the launch writes the plan -- header, offsets, short_before and both
+    // task lists -- exactly as the plan kernel would
+    int self_plan;
+    int32_t *plan_offsets, *plan_short_before;
+    int4 *plan_tasks, *plan_ordered;
     int B, Hq, Hkv, G, num_pages, bt_stride;
     int log2P;         // page size = 1 << log2P
     int box_log2;      // tokens per TMA box = 1 << box_log2 (min(P, 64))

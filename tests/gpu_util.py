@@ -32,14 +32,14 @@ def shape_of(tr: T.Trace):
 
 def run_path(tr: T.Trace, d: dict, path: int, C: int | None = None, bucket: int | None = None,
              max_tasks: int = 0, want_lse: bool = True, merge: int = _lib.PKV_MERGE_SEPARATE,
-             ws: torch.Tensor | None = None):
+             ws: torch.Tensor | None = None, plan: int = _lib.PKV_PLAN_SEPARATE):
     """One decode step through pkv_decode_step; returns (o, lse, ws, partials).
     A given workspace `ws` is reused (it must be zeroed once before first use)."""
     shape = shape_of(tr)
     C = tr.split_tokens if C is None else C
     if bucket is None:
         bucket = tr.n_max if path == _lib.PKV_PATH_BUCKETED_SPLIT else 0
-    cfg = api.make_cfg(path, C, bucket, max_tasks, merge)
+    cfg = api.make_cfg(path, C, bucket, max_tasks, merge, plan)
     if ws is None:
         ws = torch.zeros(max(64, api.pkv_plan_workspace_size(shape, cfg)), dtype=torch.uint8,
                          device="cuda")

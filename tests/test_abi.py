@@ -42,8 +42,8 @@ def shape(**kw):
     return _lib.Shape(*[base[k] for k, _ in _lib.Shape._fields_])
 
 
-def cfg(path=_lib.PKV_PATH_WORKQUEUE, C=256, bucket=0, max_tasks=0, merge=0):
-    return _lib.PlanCfg(path, C, bucket, max_tasks, merge)
+def cfg(path=_lib.PKV_PATH_WORKQUEUE, C=256, bucket=0, max_tasks=0, merge=0, plan=0):
+    return _lib.PlanCfg(path, C, bucket, max_tasks, merge, plan)
 
 
 FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation fails first
@@ -125,6 +125,21 @@ def test_unknown_merge_mode_is_rejected(L):
                                   FAKE, FAKE, FAKE, None, None) == _lib.PKV_EINVAL
     ok = cfg(merge=_lib.PKV_MERGE_FUSED)
     assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(ok)) > 0
+
+
+def test_unknown_plan_mode_is_rejected(L):
+    s = shape()
+    for bad in (-1, 2):
+        c = cfg(plan=bad)
+        assert L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(c)) == 0
+        assert L.pkv_decode_step(ctypes.byref(s), ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                 FAKE, FAKE, None, None) == _lib.PKV_EINVAL
+    for path in (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_PATH_BUCKETED_SPLIT):
+        ok = cfg(path=path, plan=_lib.PKV_PLAN_IN_DECODE)
+        # the workspace is the same whichever kernel builds the plan
+        same = cfg(path=path)
+        assert (L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(ok)) ==
+                L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(same)) > 0)
 
 
 def test_plan_is_a_noop_off_the_workqueue(L):
