@@ -18,8 +18,8 @@ One JSON line on rank 0:
                captured graph per step) with the step's inputs and outputs in
                pinned host memory, synchronized wall clock per step
   cpu_baseline the float64 oracle on the host cores on a bounded sample
-`--merge fused` merges on the decode kernel's tail; `--plan in-decode` lets the
-workqueue's decode build its own plan (no plan launch).  `--impl reference`
+`--merge fused` merges on the decode kernel's tail; on the workqueue the decode
+builds its own plan (no plan launch) unless `--plan separate`.  `--impl reference`
 times the oracle alone (the reference arm).
 Multi-GPU (torchrun): every rank runs an independent replica (no collective
 on the data path); value sums the ranks' bytes over the slowest rank's time.
@@ -72,7 +72,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--merge", default="separate", choices=["fused", "separate"],
                     help="split paths: merge on the decode's tail, or in a second kernel")
-    ap.add_argument("--plan", default="separate", choices=["in-decode", "separate"],
+    ap.add_argument("--plan", default="in-decode", choices=["in-decode", "separate"],
                     help="workqueue without appends: the decode builds its own plan, or a plan kernel")
     return ap.parse_args()
 
@@ -551,7 +551,8 @@ def run_pkv(args, rank, local, ws, pg):
         "config": {
             "workload": WORKLOADS[cfg_id], "path": ["bucketed-split", "workqueue", "single-pass"][path],
             "merge": ("fused" if fused else "separate") if path != 2 else None,
-            "plan": ("in-decode" if self_plan else "plan kernel") if path == 1 else None,
+            "plan": ("in-decode" if self_plan else "append+plan kernel" if appends else "plan kernel")
+                    if path == 1 else None,
             "split_tokens": C, "kv_bytes_per_step": kv_step, "seed": tr.seed,
             "l2": (f"{R} KV pools rotated ({R * pool_bytes / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB)"
                    if R > 1 else f"inputs ({pool_bytes / 2**30:.1f} GiB) larger than L2"),

@@ -364,13 +364,14 @@ class PagedDecoder:
     reused across steps; they are resized when a larger configuration arrives.
     `merge` picks how split states are combined (a second kernel by default,
     or PKV_MERGE_FUSED: on the decode's tail) and `plan` where the workqueue's
-    plan is built (its own launch, or PKV_PLAN_IN_DECODE: by the decode kernel);
-    the workspace is zeroed whenever the configuration changes, so that each
-    configuration starts from a clean header.
+    plan is built (by the decode kernel by default, for batches of up to
+    PKV_SELF_PLAN_MAX_B rows; PKV_PLAN_SEPARATE: its own launch); the workspace
+    is zeroed whenever the configuration changes, so that each configuration
+    starts from a clean header.
     """
 
     def __init__(self, policy: Optional[PolicyCfg] = None, max_split_tasks: int = 0,
-                 merge: int = PKV_MERGE_SEPARATE, plan: int = PKV_PLAN_SEPARATE):
+                 merge: int = PKV_MERGE_SEPARATE, plan: int = PKV_PLAN_IN_DECODE):
         self.policy = policy
         self.max_split_tasks = max_split_tasks
         self.merge = merge
@@ -447,7 +448,8 @@ class HostDecodeLoop:
     the workqueue the append is fused into the plan launch, and with
     `free_pages` / `free_count` (device int32) a token that starts a page takes
     one from that free list.  `n_max` must then cover the lengths the loop will
-    reach.  `merge` and `plan` choose the step's launches as in PagedDecoder.
+    reach.  `merge` and `plan` choose the step's launches as in PagedDecoder
+    (with `append` the workqueue's plan comes from the append launch).
     """
 
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, B: int, Hq: int, bt_stride: int,
@@ -455,7 +457,7 @@ class HostDecodeLoop:
                  policy: Optional[PolicyCfg] = None, scale: Optional[float] = None,
                  max_tasks: int = 0, merge: int = PKV_MERGE_SEPARATE, inputs_in_place: bool = True,
                  append: bool = False, free_pages: Optional[torch.Tensor] = None,
-                 free_count: Optional[torch.Tensor] = None, plan: int = PKV_PLAN_SEPARATE):
+                 free_count: Optional[torch.Tensor] = None, plan: int = PKV_PLAN_IN_DECODE):
         dev = k_cache.device
         self.inputs_in_place = inputs_in_place
         self.append = append
@@ -494,6 +496,8 @@ class HostDecodeLoop:
             p = path
         if split_tokens is not None:
             c = split_tokens
+        if append:
+            plan = PKV_PLAN_SEPARATE  # the fused append launch builds the workqueue's plan
         self.cfg = make_cfg(p, c, n_max if p == PKV_PATH_BUCKETED_SPLIT else 0,
                             max_tasks if p == PKV_PATH_WORKQUEUE else 0, merge, plan)
         self.ws = torch.zeros(pkv_plan_workspace_size(self.shape, self.cfg), dtype=torch.uint8, device=dev)

@@ -934,108 +934,99 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
 
 // ---------------------------------------------------------- self-planning workqueue
 
-// The plan of a workqueue launch, built by every CTA from the row lengths
-// ("Row-local bounds": n_i = ceil(N*_i / C), split i's states start at the
-// exclusive prefix of n): thread t sums the full and shorter splits of rows
-// [kPer t, kPer t + kPer), one block scan gives the prefixes, which land in
-// F and R (B + 1 entries each).  CTA 0 also writes what the merge and the
-// workspace's readers expect of the plan kernel: the header's task count,
-// state rows and overflow flag, offsets and short_before, and any bad length.
+// The plan of a workqueue launch, built by the producer warp of every CTA
+// from the row lengths ("Row-local bounds": n_i = ceil(N*_i / C), row i's
+// states start at the exclusive prefix of n).  Rows go 32 at a time, one per
+// lane (all lengths loaded at once); a warp scan per round plus a carry gives
+// the prefixes F (full splits) and R (shorter last splits) of every row,
+// B + 1 entries each, in shared memory.  CTA 0 also writes what the merge and
+// the workspace's readers expect of the plan kernel: offsets, short_before,
+// the header's task count, state rows and overflow flag, and any bad length.
 // Returns the task count (0 after an overflow of the launch's capacity).
-// Every thread of the CTA calls it.
-__device__ __noinline__ int self_plan_build(const DecodeParams &p, int *F, int *R)
+__device__ __forceinline__ int self_plan_warp(const DecodeParams &p, int *F, int *R)
 {
-    constexpr int kWarps = kThreads / 32;
-    constexpr int kPer = (kSelfPlanMaxB + kThreads - 1) / kThreads;
-    __shared__ long long s_tot[2][kWarps];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kRounds = kSelfPlanMaxB / 32;
+    const int lane = threadIdx.x & 31;
     const bool cta0 = blockIdx.x == 0;
     if (p.B > kSelfPlanMaxB) {  // the host never launches this; decode nothing, merge NaN
-        if (cta0 && tid == 0) {
+        if (cta0 && lane == 0) {
             p.ws->task_count = 0;
             p.ws->overflow = 1;
             report_error(p.ws, kErrCapacity, p.B, kSelfPlanMaxB, 1);
         }
         return 0;
     }
-    int f[kPer], r[kPer];
-    long long sf = 0, sr = 0;
+    int len[kRounds];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int i = tid * kPer + u;
-        f[u] = r[u] = 0;
-        if (i < p.B) {
-            int N = p.seq_lens[i];
-            if (N < 0 || N > p.len_cap) {
-                if (cta0)
-                    report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.len_cap);
-                N = N < 0 ? 0 : p.len_cap;
+    for (int u = 0; u < kRounds; ++u) {
+        const int i = u * 32 + lane;
+        len[u] = i < p.B ? p.seq_lens[i] : 0;
+    }
+    long long cf = 0, cr = 0;  // splits of the rows before this round
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+        if (u * 32 >= p.B)
+            break;
+        const int i = u * 32 + lane;
+        int N = len[u];
+        if (N < 0 || N > p.len_cap) {
+            if (cta0)
+                report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.len_cap);
+            N = N < 0 ? 0 : p.len_cap;
+        }
+        const int f = N / p.C, r = (N % p.C) != 0 ? 1 : 0;
+        long long xf = f, xr = r;  // inclusive warp scans
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long yf = __shfl_up_sync(0xffffffffu, xf, o);
+            const long long yr = __shfl_up_sync(0xffffffffu, xr, o);
+            if (lane >= o) {
+                xf += yf;
+                xr += yr;
             }
-            f[u] = N / p.C;
-            r[u] = (N % p.C) != 0 ? 1 : 0;
         }
-        sf += f[u];
-        sr += r[u];
-    }
-    long long xf = sf, xr = sr;  // inclusive warp scans
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const long long yf = __shfl_up_sync(0xffffffffu, xf, o);
-        const long long yr = __shfl_up_sync(0xffffffffu, xr, o);
-        if (lane >= o) {
-            xf += yf;
-            xr += yr;
-        }
-    }
-    if (lane == 31) {
-        s_tot[0][warp] = xf;
-        s_tot[1][warp] = xr;
-    }
-    __syncthreads();
-    long long ef = xf - sf, er = xr - sr, tf = 0, tr = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        if (w < warp) {
-            ef += s_tot[0][w];
-            er += s_tot[1][w];
-        }
-        tf += s_tot[0][w];
-        tr += s_tot[1][w];
-    }
-    const long long T = (tf + tr) * p.Hkv;
-    const bool over = T > p.n_tasks;  // the capacity, at most INT32_MAX: F and R fit in int
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int i = tid * kPer + u;
-        if (i < p.B) {
-            if (!over) {
-                F[i] = (int)ef;
-                R[i] = (int)er;
-            }
+        const long long ef = cf + xf - f, er = cr + xr - r;
+        if (i < p.B) {  // after an overflow F and R go unused
+            F[i] = (int)ef;
+            R[i] = (int)er;
             if (cta0) {
                 p.plan_offsets[i] = (int)(ef + er);
                 p.plan_short_before[i] = (int)er;
             }
         }
-        ef += f[u];
-        er += r[u];
+        cf += __shfl_sync(0xffffffffu, xf, 31);
+        cr += __shfl_sync(0xffffffffu, xr, 31);
     }
-    if (tid == 0) {
-        if (!over) {
-            F[p.B] = (int)tf;
-            R[p.B] = (int)tr;
-        }
+    const long long T = (cf + cr) * p.Hkv;
+    const bool over = T > p.n_tasks;  // the capacity, at most INT32_MAX: F and R fit in int
+    if (lane == 0) {
+        F[p.B] = (int)cf;
+        R[p.B] = (int)cr;
         if (cta0) {
-            p.plan_offsets[p.B] = (int)(tf + tr);
+            p.plan_offsets[p.B] = (int)(cf + cr);
             p.ws->task_count = over ? 0 : (int)T;
-            p.ws->state_rows = (int)(tf + tr);
+            p.ws->state_rows = (int)(cf + cr);
             p.ws->overflow = over ? 1 : 0;
             if (over)
                 report_error(p.ws, kErrCapacity, (int)(T > 0x7fffffffLL ? 0x7fffffffLL : T), p.n_tasks, 0);
         }
     }
-    __syncthreads();
+    __syncwarp();
     return over ? 0 : (int)T;
+}
+
+// Named barrier between the planning producer warp (arrives) and the
+// consumer warps (wait), so that only the consumers wait for the plan.
+constexpr int kPlanBarrier = 1;
+
+__device__ __forceinline__ void plan_barrier_arrive()
+{
+    asm volatile("bar.arrive %0, %1;" ::"n"(kPlanBarrier), "n"(kThreads) : "memory");
+}
+
+__device__ __forceinline__ void plan_barrier_sync()
+{
+    asm volatile("bar.sync %0, %1;" ::"n"(kPlanBarrier), "n"(kThreads) : "memory");
 }
 
 // Both task lists of the plan, written by the consumer warps of all CTAs
@@ -1071,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ int s_ctl[2];  // [0]: a wait timed out in this CTA; [1]: fused merge may proceed
     // the self-planning workqueue's prefix sums F, R (the other instances keep one word)
     constexpr bool kSelf = MODE == kModeQueue && !FUSE;
-    __shared__ int s_plan[kSelf ? 2 * (kSelfPlanMaxB + 1) : 1];
+    __shared__ int s_plan[kSelf ? 2 * (kSelfPlanMaxB + 1) + 1 : 1];  // + the task count
 
     if (threadIdx.x == 0) {
         s_ctl[0] = s_ctl[1] = 0;
@@ -1097,8 +1088,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     int ntasks = p.n_tasks;
     if constexpr (kSelf) {
         if (p.self_plan) {
-            ntasks = self_plan_build(p, s_plan, s_plan + kSelfPlanMaxB + 1);
             sp = SelfPlan{s_plan, s_plan + kSelfPlanMaxB + 1};
+            int *s_count = s_plan + 2 * (kSelfPlanMaxB + 1);
+            if (warp == kCW) {
+                ntasks = self_plan_warp(p, s_plan, s_plan + kSelfPlanMaxB + 1);
+                if ((threadIdx.x & 31) == 0)
+                    *s_count = ntasks;
+                plan_barrier_arrive();
+            } else {
+                plan_barrier_sync();
+                ntasks = *s_count;
+            }
         } else {
             ntasks = min(p.ws->task_count, p.n_tasks);
         }
