@@ -11,7 +11,8 @@ Procedure:
    B in {1..64}, N_max in {256..32768}, Hq=32, Hkv=8, d=128, page_size 16 --
    time every route (bucketed split and workqueue at several split sizes C,
    single pass) as synchronized wall-clock per decode step through the C ABI
-   (host planning and launches included, as the pages measure).
+   (host planning and launches included, as the pages measure; the workqueue
+   with its plan built inside the decode, as PagedDecoder runs it).
 2. Search the policy parameters (two long-context cut-offs, two batch cut-offs,
    one C per split route) minimising the mean ratio of the chosen route's time
    to the best route's time over the calibration traces.
@@ -98,7 +99,9 @@ def measure(seed: int, reps: int = 7, warm: int = 2, log=print):
         times = {}
         for name, C in routes():
             path = {"bucketed": 0, "workqueue": 1, "single": 2}[name]
-            cfg = api.make_cfg(path, C if C else 1024, n_max if path == 0 else 0)
+            # the workqueue as PagedDecoder runs it: its plan built by the decode
+            cfg = api.make_cfg(path, C if C else 1024, n_max if path == 0 else 0, 0,
+                               _lib.PKV_MERGE_SEPARATE, _lib.PKV_PLAN_IN_DECODE if path == 1 else 0)
             ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device=dev)
             npart = api.pkv_partials_size(shape, cfg)
             part = torch.empty(max(4, npart // 4), dtype=torch.float32, device=dev)
@@ -233,8 +236,9 @@ def render_markdown(out: dict) -> str:
              "--md policy_calibration.md", "",
              "Grid: families bucketed / bimodal / uniform / Zipf x B in {1,2,4,8,16,32,64} x N_max in",
              "{256..32768}; Hq=32, Hkv=8, d=128, page_size 16. Routes: bucketed split C in {128..2048},",
-             "workqueue C in {256..2048}, single pass. Time = median synchronized wall-clock per decode step",
-             "through the C ABI (launches and host planning included). Policy parameters searched to minimise",
+             "workqueue C in {256..2048} (its plan built inside the decode), single pass. Time = median",
+             "synchronized wall-clock per decode step through the C ABI (launches and host planning",
+             "included). Policy parameters searched to minimise",
              "the mean chosen/best time ratio on the calibration seed 20260622, then checked on held-out seed",
              "20260623.", "",
              f"Frozen in `pkv_policy_default`: {p}", "",

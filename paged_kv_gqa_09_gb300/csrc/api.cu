@@ -665,17 +665,18 @@ int pkv_append(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *
 // Thresholds calibrated on a GB300 (152 SMs) by paged_kv_gqa_09_gb300/calibrate.py:
 // 224 traces (bucketed, bimodal, uniform, Zipf; B 1..64; N_max 256..32768;
 // Hq=32, Hkv=8, d=128, P=16) drawn with the calibration seed 20260622, timed as
-// synchronized wall-clock per step; held-out seed 20260623 mean regret 1.047.
+// synchronized wall-clock per step (the workqueue with its plan built inside the
+// decode); held-out seed 20260623 mean regret 1.046 (worst 1.21x).
 void pkv_policy_default(pkv_policy_cfg_t *c)
 {
     if (!c)
         return;
-    c->bucketed_min_tokens = 1024;
-    c->bucketed_max_batch = 4;
-    c->workqueue_min_tokens = 2048;
+    c->bucketed_min_tokens = 16384;
+    c->bucketed_max_batch = 2;
+    c->workqueue_min_tokens = 1024;
     c->workqueue_min_batch = 1;
     c->split_tokens = 512;
-    c->bucketed_split_tokens = 512;
+    c->bucketed_split_tokens = 1024;
 }
 
 int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t *out_path,
@@ -706,19 +707,20 @@ int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t
 // ------------------------------------------------------------ learned model
 
 // Routes and weights fitted by paged_kv_gqa_09_gb300/calibrate.py (least
-// squares of log step time, calibration seed 20260622, 224 GB300 traces);
-// held-out seed 20260623 mean regret 1.025 (worst 1.21x).
+// squares of log step time, calibration seed 20260622, 224 GB300 traces, the
+// workqueue with its plan built inside the decode); held-out seed 20260623 mean
+// regret 1.026 (worst 1.21x).
 static const pkv_cost_route_t kGb300Routes[] = {
-    {0, 128, {6.3911511f, 0.18869681f, 0.113038967f, -0.872334747f, -0.00111166821f, 0.00570620828f, 0.00389673768f, 0.333247013f, -0.0526887548f, 0.0348977711f}},
-    {0, 256, {6.73588227f, 0.101975149f, 0.110912851f, -0.880277407f, 0.00430088841f, 0.00318768111f, 0.000633300328f, 0.250103107f, -0.0582065134f, 0.0366974999f}},
-    {0, 512, {6.85069008f, -0.0199633378f, 0.0875755601f, -0.832104671f, 0.0120954918f, 0.00404960658f, -0.000342222623f, 0.192960041f, -0.0448385477f, 0.0352934669f}},
-    {0, 1024, {6.43892679f, -0.14679993f, 0.132516769f, -0.760243062f, 0.0178044681f, 0.00758829307f, -0.00362695527f, 0.0932693563f, -0.0234600053f, 0.0330072711f}},
-    {0, 2048, {5.21789607f, -0.151656726f, 0.372049944f, -0.765199027f, 0.0147380797f, 0.0106726982f, -0.0127868016f, 0.0473664272f, -0.0113390157f, 0.0326924f}},
-    {1, 256, {7.46433045f, 0.142281247f, 0.0415647499f, -0.915908375f, -0.00786971047f, -0.00235486857f, 0.00101025077f, 0.0779131574f, -0.0216318039f, 0.0413073873f}},
-    {1, 512, {7.1416581f, 0.149791916f, 0.16981438f, -0.958581609f, -0.00814656145f, -0.00358729065f, -0.00534764157f, 0.0836702774f, -0.0296661475f, 0.0428970791f}},
-    {1, 1024, {6.12978505f, 0.17430816f, 0.437913689f, -1.01776603f, -0.0103437813f, -0.00389283438f, -0.016456589f, 0.062021911f, -0.026802004f, 0.0444890352f}},
-    {1, 2048, {4.59033968f, 0.20436047f, 0.770685133f, -1.05846004f, -0.0152960465f, -0.0008797314f, -0.0288815227f, 0.0112963283f, -0.0141198967f, 0.0449685579f}},
-    {2, 1024, {5.85305682f, -0.101661956f, -0.248880265f, -0.436635689f, -0.0105043141f, 0.0333611675f, 0.0308085814f, -0.359093353f, 0.151939249f, 0.0157091673f}},
+    {0, 128, {6.30381386f, 0.146490208f, 0.0766507722f, -0.817804401f, 0.00221713447f, 0.00773811571f, 0.005210673f, 0.344296909f, -0.0570552701f, 0.032716484f}},
+    {0, 256, {6.80283592f, 0.0684275072f, 0.0648224914f, -0.839746221f, 0.00700632318f, 0.00431572125f, 0.00229686144f, 0.258659391f, -0.0598971814f, 0.0350487925f}},
+    {0, 512, {6.81804098f, -0.0406811549f, 0.0664215198f, -0.803152733f, 0.0137774587f, 0.00563256323f, 0.000659806355f, 0.207581675f, -0.04293712f, 0.0338510971f}},
+    {0, 1024, {6.40653584f, -0.166238885f, 0.116008665f, -0.731888572f, 0.0191883576f, 0.00827006613f, -0.00325081398f, 0.0964632869f, -0.0286775284f, 0.0319785319f}},
+    {0, 2048, {5.2492311f, -0.202409639f, 0.333875118f, -0.719615545f, 0.0174190081f, 0.0127817358f, -0.0118381823f, 0.0226557524f, -0.011753664f, 0.0312219853f}},
+    {1, 256, {7.32420448f, 0.112937442f, 0.023359348f, -0.869745583f, -0.00706408591f, 7.99227637e-05f, 0.00136712949f, 0.0523260483f, -0.0168115665f, 0.0396993464f}},
+    {1, 512, {7.12917364f, 0.136180101f, 0.153859026f, -0.935766956f, -0.00738813911f, -0.00292030006f, -0.00495750755f, 0.0771535752f, -0.0287264073f, 0.0420219287f}},
+    {1, 1024, {6.05268677f, 0.154866756f, 0.430157638f, -0.992877683f, -0.00919112845f, -0.00266958781f, -0.0163468768f, 0.0599483139f, -0.0263472104f, 0.0435006428f}},
+    {1, 2048, {4.38967457f, 0.207614697f, 0.802688683f, -1.0557703f, -0.0152409556f, -0.00017741742f, -0.029851963f, 0.0251214756f, -0.0119293571f, 0.0444260996f}},
+    {2, 1024, {5.96752215f, -0.106514951f, -0.280153379f, -0.420131456f, -0.00988210887f, 0.0331434419f, 0.0320161238f, -0.345054899f, 0.147479276f, 0.0150444364f}},
 };
 
 void pkv_cost_model_default(pkv_cost_model_t *m)
