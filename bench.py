@@ -182,11 +182,21 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments, blank lines or trailing blanks: what the
+    compiler sees (these files hold no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def decode_source_hash() -> str:
+    """Identity of the decode kernel's code, so that an ncu summary taken on it
+    stays attached to it across comment edits and to nothing else."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_gqa_09_gb300", "csrc")
     for f in ("decode.cu", "pkv_device.cuh", "pkv_kernels.h", "plan_map.cuh"):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -182,7 +182,8 @@ int pkv_single_pass(const pkv_shape_t *shape, void *d_ws,
                     void *d_o, float *d_lse, void *stream);
 
 /* pkv_decode_merge -- pkv_decode with the exact merge of pkv_merge on its
- * tail (cfg->merge is not consulted).  One kernel launch.  Every split writes
+ * tail (cfg->merge is not consulted, nor cfg->plan: on the workqueue enqueue
+ * pkv_plan first).  One kernel launch.  Every split writes
  * its state as pkv_decode does; the kernel's CTAs then meet at a grid-wide
  * barrier (counters in d_ws; every CTA is resident at once, and the wait is
  * bounded: a CTA that gives up reports PKV_ETIMEOUT) and share out the

@@ -8,7 +8,10 @@
 //             ("Row-local bounds": an empty split writes the neutral state and
 //             reads no KV);
 //   queue  -- the compact 1D workqueue of non-empty (row, kv-head, split)
-//             tasks built by the plan kernel ("Compact workqueue");
+//             tasks ("Compact workqueue"), read from the plan kernel's list or,
+//             for batches of up to kSelfPlanMaxB rows, derived by the CTA's
+//             producer warp from the row lengths (the launch then writes the
+//             plan itself);
 //   single -- one task per (row, kv-head) over the whole row, writing o/lse
 //             directly (the policy's no-split route).
 //

@@ -48,19 +48,21 @@ def _noalloc(L, tr, d, cfg):
     return o, lse
 
 
-@pytest.mark.parametrize("path,merge", [(p, _lib.PKV_MERGE_SEPARATE) for p in PATHS] +
-                         [(p, _lib.PKV_MERGE_FUSED) for p in PATHS[:2]])
-def test_noalloc_matches_decode_step_twice(lib, path, merge):
+@pytest.mark.parametrize("path,merge,plan", [(p, _lib.PKV_MERGE_SEPARATE, 0) for p in PATHS] +
+                         [(p, _lib.PKV_MERGE_FUSED, 0) for p in PATHS[:2]] +
+                         [(_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_SEPARATE, _lib.PKV_PLAN_IN_DECODE)])
+def test_noalloc_matches_decode_step_twice(lib, path, merge, plan):
     """With the fused merge the header also holds the grid barrier's counters,
     which the call zeroes with the rest of the header, over whatever the
-    previous call left there."""
+    previous call left there; with the plan built in the decode, the decode
+    writes the plan into the same scratch."""
     tr = T.make_trace(3)  # B=8 bimodal, ~491 MB of K+V
     q = T.gen_q(tr)
     k, v = T.gen_kv(tr)
     d = upload(tr, q, k, v)
     o_ref, lse_ref, _, _ = run_path(tr, d, path)
     C = tr.split_tokens
-    cfg = api.make_cfg(path, C, tr.n_max if path == _lib.PKV_PATH_BUCKETED_SPLIT else 0, 0, merge)
+    cfg = api.make_cfg(path, C, tr.n_max if path == _lib.PKV_PATH_BUCKETED_SPLIT else 0, 0, merge, plan)
     ref = o_ref.float().cpu().numpy()
     lref = lse_ref.cpu().numpy()
     for call in range(2):
