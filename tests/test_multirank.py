@@ -62,3 +62,44 @@ def test_cpu_baseline_times_all_cores_and_one_thread():
     gbs, cores, desc, one = bench.cpu_baseline_run(tr, T.gen_q(tr), k, v, 0.2)
     assert gbs > 0 and one > 0 and cores >= 1
     assert "whole decode steps" in desc and "one thread" in desc
+
+
+# ------------------------------------------------------------------ the reference arm's line
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _reference_lines(nproc):
+    import subprocess
+    import sys
+    args = ["bench.py", "--impl", "reference", "--gpus", str(nproc), "--steps", "2", "--warmup", "1",
+            "--config", "1"]
+    if nproc > 1:
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={nproc}",
+               "--master-addr", "127.0.0.1", "--master-port", str(_free_port())] + args
+    else:
+        cmd = [sys.executable] + args
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [line for line in r.stdout.splitlines() if line.startswith("{")]
+
+
+@pytest.mark.parametrize("nproc", [1, 2])
+def test_reference_arm_prints_one_contract_line(nproc):
+    """The oracle timed on the host cores: one JSON line from rank 0 only, with
+    the base contract's keys, a cpu_baseline describing the run, and an e2e
+    that moves no bytes."""
+    import json
+    lines = _reference_lines(nproc)
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    metric = json.load(open(os.path.join(ROOT, "BASELINE.json")))["metric"]
+    assert d["impl"] == "reference" and d["metric"] == metric and d["unit"] == "GB/s"
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
+    assert (d["n_gpus"], d["steps"], d["warmup"]) == (nproc, 2, 1)
+    assert d["vs_baseline"] is None and d["data"] == "synthetic" and d["dtype"] == "f64"
+    assert d["scaling"] == "weak" and "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
