@@ -27,19 +27,35 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
     __shared__ float s_max[kMergeWarps];
     __shared__ float s_l[kMergeWarps];
     __shared__ __align__(16) float s_acc[kMergeWarps][D];
-    // every libpkv kernel waits for its predecessor before touching global
-    // memory, so the next one may be scheduled as soon as this one runs
-    pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int lr = blockIdx.x / p.Hq, h = blockIdx.x - lr * p.Hq;
+    // The rectangular grid's merge reads the row list and the lengths while
+    // the decode it follows is still running: both are inputs that no kernel
+    // writes between a step's decode and its merge (an append that advances
+    // the lengths finished before the decode started, and the next one waits
+    // for this merge), so the state loads below need not wait for them.  The
+    // workqueue's offsets come from the plan, which its decode may write.
+    const bool rect = p.mode != kModeQueue;
+    int i = -1, N = 0;
+    if (rect && lr < p.n_rows) {
+        i = p.rows ? p.rows[lr] : lr;
+        if (i >= 0 && i < p.B)
+            N = p.seq_lens[i];
+    }
+    // otherwise every libpkv kernel waits for its predecessor before touching
+    // global memory, so the next one may be scheduled as soon as this one runs
+    pdl_wait();
+    pdl_trigger();
     if (lr >= p.n_rows)
         return;
-    const int i = p.rows ? p.rows[lr] : lr;  // row of the batch
+    if (!rect) {
+        i = p.rows ? p.rows[lr] : lr;  // row of the batch
+        if (i >= 0 && i < p.B)
+            N = p.seq_lens[i];
+    }
     if (i < 0 || i >= p.B)
         return;  // reported by the decode kernel
     const int64_t wg = (int64_t)i * p.Hq + h;  // (row, head) of o and lse
-    int N = p.seq_lens[i];
     N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);
     int n = (N + p.C - 1) / p.C;
     int64_t base;
