@@ -418,7 +418,7 @@ def run_pkv(args, rank, local, ws, pg):
             bt.copy_(bt_init)
             free_count.copy_(free_init)
 
-    # ---- warm-up (eager), then capture one graph per pool
+    # ---- warm-up (eager), then capture the step graphs
     for w in range(warm):
         step(w % R)
     torch.cuda.synchronize()
@@ -430,16 +430,18 @@ def run_pkv(args, rank, local, ws, pg):
     torch.cuda.synchronize()
     c = api.pkv_get_counters()
     launches_per_step = sum(c.values())
-    # graphs: one of R consecutive steps (pool 0..R-1), so that each step's
-    # kernels chain into the next step's by programmatic dependent launch, and
-    # single steps for a remainder of K mod R
+    # graphs: one of G consecutive steps (pools 0..R-1 in turn, G a multiple of
+    # R and at least 8), so that each step's kernels chain into the next step's
+    # by programmatic dependent launch (which stops at a graph boundary), and
+    # single steps for a remainder of K mod G
+    G = R * -(-8 // R)
     graphs = None
     if not args.no_graph:
         try:
             loop_graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(loop_graph, stream=stream):
-                for r in range(R):
-                    step(r)
+                for r in range(G):
+                    step(r % R)
             singles = []
             for r in range(R):
                 g = torch.cuda.CUDAGraph()
@@ -470,10 +472,10 @@ def run_pkv(args, rank, local, ws, pg):
     t_wall0 = time.time()
     e0.record(stream)
     if graphs:
-        for _ in range(steps // R):
+        for _ in range(steps // G):
             graphs[0].replay()
-        for r in range(steps % R):
-            graphs[1][r].replay()
+        for r in range(steps % G):
+            graphs[1][r % R].replay()
     else:
         for s in range(steps):
             step(s % R)
@@ -566,7 +568,7 @@ def run_pkv(args, rank, local, ws, pg):
             "split_tokens": C, "kv_bytes_per_step": kv_step, "seed": tr.seed,
             "l2": (f"{R} KV pools rotated ({R * pool_bytes / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB)"
                    if R > 1 else f"inputs ({pool_bytes / 2**30:.1f} GiB) larger than L2"),
-            "graph": bool(graphs), "parallelism": f"replicas x{ws}",
+            "graph": bool(graphs), "graph_steps": G if graphs else 0, "parallelism": f"replicas x{ws}",
         },
         "hbm_frac": total / ws / peak,
         "roofline": {"bound": "hbm",
