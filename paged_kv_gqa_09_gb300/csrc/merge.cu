@@ -18,6 +18,9 @@ namespace pkv {
 namespace {
 
 constexpr int kMergeWarps = 4;
+// Batches up to this many rows: the workqueue's merge finds its row's first
+// state itself, from the lengths of the rows before it.
+constexpr int kEarlyBaseRows = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -29,18 +32,39 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
     __shared__ __align__(16) float s_acc[kMergeWarps][D];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int lr = blockIdx.x / p.Hq, h = blockIdx.x - lr * p.Hq;
-    // The rectangular grid's merge reads the row list and the lengths while
-    // the decode it follows is still running: both are inputs that no kernel
-    // writes between a step's decode and its merge (an append that advances
-    // the lengths finished before the decode started, and the next one waits
-    // for this merge), so the state loads below need not wait for them.  The
-    // workqueue's offsets come from the plan, which its decode may write.
+    // The merge reads the row list and the lengths while the decode it follows
+    // is still running: both are inputs that no kernel writes between a step's
+    // decode and its merge (an append that advances the lengths finished before
+    // the decode started, and the next one waits for this merge), so after the
+    // wait only the state loads remain.  The workqueue's offsets come from the
+    // plan, which its own decode may write: on batches of up to kEarlyBaseRows
+    // rows the CTA instead sums ceil(N / C) over the rows before its own (the
+    // plan's definition of offsets[i]); larger ones read offsets after the wait.
     const bool rect = p.mode != kModeQueue;
+    const bool early = rect || p.B <= kEarlyBaseRows;
     int i = -1, N = 0;
-    if (rect && lr < p.n_rows) {
+    int64_t base = 0;
+    if (early && lr < p.n_rows) {
         i = p.rows ? p.rows[lr] : lr;
         if (i >= 0 && i < p.B)
             N = p.seq_lens[i];
+    }
+    if (!rect && early && lr < p.n_rows) {  // the same branch for the whole CTA
+        __shared__ long long s_part[kMergeWarps];
+        long long sum = 0;
+        for (int r = threadIdx.x; r < i; r += 32 * kMergeWarps) {
+            int Nr = p.seq_lens[r];
+            Nr = Nr < 0 ? 0 : (Nr > p.len_cap ? p.len_cap : Nr);
+            sum += (Nr + p.C - 1) / p.C;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane == 0)
+            s_part[warp] = sum;
+        __syncthreads();
+        for (int w = 0; w < kMergeWarps; ++w)
+            base += s_part[w];
     }
     // otherwise every libpkv kernel waits for its predecessor before touching
     // global memory, so the next one may be scheduled as soon as this one runs
@@ -48,7 +72,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
     pdl_trigger();
     if (lr >= p.n_rows)
         return;
-    if (!rect) {
+    if (!early) {
         i = p.rows ? p.rows[lr] : lr;  // row of the batch
         if (i >= 0 && i < p.B)
             N = p.seq_lens[i];
@@ -58,10 +82,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
     const int64_t wg = (int64_t)i * p.Hq + h;  // (row, head) of o and lse
     N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);
     int n = (N + p.C - 1) / p.C;
-    int64_t base;
     bool bad = false;
     if (p.mode == kModeQueue) {
-        base = p.offsets[i];
+        if (!early)
+            base = p.offsets[i];
         bad = p.ws->overflow != 0 || base + n > p.state_rows_cap;
     } else {
         base = (int64_t)lr * p.S_b;
