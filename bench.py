@@ -510,7 +510,9 @@ def run_pkv(args, rank, local, ws, pg):
         evs[s][1].record(stream)
         _lib.check(rc, "decode")
     torch.cuda.synchronize()
-    kms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    launch_ms = sorted(a.elapsed_time(b) for a, b in evs)
+    kms = statistics.mean(launch_ms)
+    pct = lambda f: launch_ms[min(len(launch_ms) - 1, int(f * len(launch_ms)))] * 1e3
     # the same launches back to back with no event between them, so that each
     # overlaps the previous one's tail by programmatic dependent launch as in
     # the step loop: the kernel's per-launch time once its launch and ramp-up
@@ -576,6 +578,7 @@ def run_pkv(args, rank, local, ws, pg):
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src, "traffic": profiled_traffic(cfg_id),
                      "us_per_launch": kms * 1e3, "bytes_per_launch": kv_launch,
+                     "us_per_launch_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
                      "chained": {"us_per_launch": chained_ms * 1e3,
                                  "achieved": kv_launch / (chained_ms * 1e-3) / 1e9,
                                  "frac": kv_launch / (chained_ms * 1e-3) / 1e9 / peak,
