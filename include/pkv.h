@@ -122,7 +122,9 @@ size_t pkv_plan_workspace_size(const pkv_shape_t *shape, const pkv_plan_cfg_t *c
 
 /* Bytes of the fp32 partial-state buffer for split paths: acc[slots][d] then
  * m[slots] then l[slots], where slots = B*S_b*Hq (BUCKETED_SPLIT) or
- * max_tasks*G (WORKQUEUE).  0 for SINGLE_PASS. */
+ * max_tasks*G (WORKQUEUE).  0 for SINGLE_PASS.  Slots are 32-bit indices: the
+ * launching calls refuse a configuration with more than INT32_MAX of them
+ * (PKV_EUNSUPPORTED). */
 size_t pkv_partials_size(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg);
 
 /* ----------------------------------------------------------- the path */

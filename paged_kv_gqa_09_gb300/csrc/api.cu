@@ -222,11 +222,24 @@ int encode_kv_map(CUtensorMap *m, const void *base, const pkv_shape_t *s, int bo
 
 WsHeader *ws_hdr(void *ws) { return reinterpret_cast<WsHeader *>(ws); }
 
+// State slots are int32 in the task records and the kernels: a split path
+// whose partial-state buffer would hold more is refused before any launch.
+int check_slots(const pkv_shape_t *s, const pkv_plan_cfg_t *c, int64_t rows = -1)
+{
+    const int64_t slots = partial_slots(s, c, rows);
+    if (slots > 0x7fffffffLL)
+        return fail(PKV_EUNSUPPORTED, "%lld partial-state slots exceed int32 (lower max_tasks, "
+                    "bucket_len or B)", (long long)slots);
+    return PKV_OK;
+}
+
 int run_decode(const pkv_shape_t *s, int mode, const pkv_plan_cfg_t *c, void *d_ws, const void *q,
                const void *k, const void *v, const int32_t *bt, const int32_t *sl, float *part,
                void *o, float *lse, cudaStream_t st, const int32_t *rows = nullptr,
                int n_rows = -1, bool fuse = false)
 {
+    if (mode != kModeSingle)
+        PKV_TRY(check_slots(s, c, rows ? n_rows : -1));
     int slots = 0;
     PKV_TRY(device_slots(s->d, &slots));
     const int box_tok = s->page_size < 64 ? s->page_size : 64;
@@ -359,6 +372,7 @@ int pkv_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, const int32_t *d_seq
         return PKV_OK;  // an empty batch: nothing to do
     if (c->path != PKV_PATH_WORKQUEUE)
         return PKV_OK;
+    PKV_TRY(check_slots(s, c));
     PKV_TRY(check_ptr(d_seq_lens, "seq_lens"));
     PKV_TRY(check_ptr(d_ws, "workspace"));
     const PlanParams p = plan_params(s, c, d_seq_lens, d_ws);
@@ -379,6 +393,7 @@ int pkv_append_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, c
         return PKV_OK;  // an empty batch: nothing to do
     if (c->path != PKV_PATH_WORKQUEUE)
         return fail(PKV_EINVAL, "pkv_append_plan builds the WORKQUEUE plan");
+    PKV_TRY(check_slots(s, c));
     PKV_TRY(check_ptr(d_ws, "workspace"));
     PKV_TRY(check_ptr(k_new, "k_new"));
     PKV_TRY(check_ptr(v_new, "v_new"));
@@ -466,6 +481,7 @@ int run_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const i
               const float *part, void *o, float *lse, void *stream, const int32_t *rows,
               int n_rows)
 {
+    PKV_TRY(check_slots(s, c, rows ? n_rows : -1));
     const int64_t slots = partial_slots(s, c, rows ? n_rows : -1);
     MergeParams p = {};
     p.rows = rows;

@@ -142,6 +142,22 @@ def test_unknown_plan_mode_is_rejected(L):
                 L.pkv_plan_workspace_size(ctypes.byref(s), ctypes.byref(same)) > 0)
 
 
+def test_state_slots_beyond_int32_are_refused(L):
+    """State slots are int32 in the task records and the kernels: a split
+    configuration whose partial-state buffer would hold more than 2^31 - 1 slots
+    is refused before any launch (it could only wrap to a negative index)."""
+    s = shape()
+    wq = cfg(max_tasks=1 << 30)                      # 2^30 tasks x G=4 slots
+    rect = cfg(path=_lib.PKV_PATH_BUCKETED_SPLIT, C=16, bucket=0x7fffffff)  # 2 x 2^27 x 8 slots
+    for c in (wq, rect):
+        assert L.pkv_decode(ctypes.byref(s), ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                            FAKE, None) == _lib.PKV_EUNSUPPORTED
+        assert L.pkv_merge(ctypes.byref(s), ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE,
+                           None) == _lib.PKV_EUNSUPPORTED
+        assert "int32" in _lib.last_error()
+    assert L.pkv_plan(ctypes.byref(s), ctypes.byref(wq), FAKE, FAKE, None) == _lib.PKV_EUNSUPPORTED
+
+
 def test_plan_is_a_noop_off_the_workqueue(L):
     s = shape()
     for p in (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_PATH_SINGLE_PASS):
