@@ -354,6 +354,22 @@ def test_launch_counts_reproduce_the_pages_bimodal_figures():
     assert wq.attn_launches == gold["compact_workqueue_launches_per_step"]
 
 
+def test_merge_state_traffic_reproduces_the_pages_bimodal_figure():
+    """The same Results bullet prints a merge-state traffic reduction of about
+    37% for the compact workqueue; under the reading in the golden file (state
+    bytes written by the split kernel plus read by the merge, the rectangular
+    grid as the baseline) the counter model must land within that figure's
+    rounding on the B=8 bimodal trace."""
+    gold = json.load(open(os.path.join(GOLDEN, "launch_counts.json")))
+    tr = T.make_trace(3)
+    C = 1024
+    S_b = -(-int(tr.n_max) // C)
+    wq = oracle.counters(oracle.PATH_WORKQUEUE, tr.seq_lens, tr.Hq, tr.Hkv, tr.d, C)
+    rect = oracle.counters(oracle.PATH_BUCKETED, tr.seq_lens, tr.Hq, tr.Hkv, tr.d, C, S_b)
+    reduction = 1.0 - wq.merge_state_bytes / rect.merge_state_bytes
+    assert abs(reduction - gold["merge_state_traffic_reduction"]) <= 0.005, reduction
+
+
 def test_counters_closed_forms():
     tr = T.make_trace(2)
     c = oracle.counters(oracle.PATH_BUCKETED, tr.seq_lens, tr.Hq, tr.Hkv, tr.d, 1024, 32)

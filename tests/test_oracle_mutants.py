@@ -43,6 +43,10 @@ MUTANTS = [
     ("exact-bucket-count", "out->attn_launches = 2 * distinct;", "out->attn_launches = 2 * B;"),
     ("rect-empty-flag", "empty[T] = ((int64_t)j * C >= seq_lens[i]) ? 1 : 0;",
      "empty[T] = ((int64_t)j * C > seq_lens[i]) ? 1 : 0;"),
+    ("rect-writes-only-nonempty", "out->states_written = (int64_t)B * S_b * Hq;",
+     "out->states_written = sum_n * Hq;"),
+    ("state-bytes-drop-ml", "int64_t state_bytes = (int64_t)(d + 2) * 4;",
+     "int64_t state_bytes = (int64_t)d * 4;"),
 ]
 
 
