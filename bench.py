@@ -1,26 +1,37 @@
 #!/usr/bin/env python3
 """Benchmark: decode-attention KV-read GB/s and microseconds per decode step.
 
-Default workload (N=1): B=1 long-context bucketed trace -- Hq=32, Hkv=8,
-d=128, N=32768 tokens, page_size 16, block table a random permutation of a
-2048-page pool, S=32 splits of 1024 tokens, keys scaled 0.5 -- on the
-length-bucketed split path (decode + merge per step).  `--config 1..5` selects
-the other workloads.
+Default workload (N=1): B=64 uniform lengths U[128, 65536], Hq=64, Hkv=8
+(G=8), d=128, page_size 16, a shuffled pool sized to the total length, the
+compact workqueue with C=1024, and every step appending one token per row
+(the append allocates pages from a device free list and builds the plan in
+one launch, then decode and merge) -- the largest workload that fits one
+GPU.  `--config 1..4` selects the smaller workloads (1: B=1 N=1024; 2: B=1
+N=32768 bucketed split; 3: B=8 bimodal; 4: B=8 Zipf).
 
 One JSON line on rank 0:
   value        K+V bytes of the step's valid tokens / device time per step
                (CUDA events around K back-to-back steps replayed from CUDA
-               graphs; inputs resident in HBM; KV pools rotated so the data a
-               step reads is not in L2)
-  roofline     the decode kernel alone: algorithmic K+V bytes per launch /
-               its average CUDA-event duration, against the measured HBM peak
-  e2e          the same metric through the public API (HostDecodeLoop, one
-               captured graph per step) with the step's inputs and outputs in
-               pinned host memory, synchronized wall clock per step
+               graphs of at least 8 chained steps; inputs resident in HBM;
+               inputs larger than L2, or KV pools rotated so the data a step
+               reads is not in L2)
+  roofline     the decode kernel: algorithmic K+V bytes per launch / its
+               duration per launch in a CUDA graph of back-to-back decode
+               launches chained by programmatic dependent launch, as inside
+               the step; the per-launch event-bracketed times (launched alone)
+               are reported apart under `isolated`
+  e2e          the same metric through the C ABI's host-buffer step
+               (pkv_decode_step_host, or pkv_append_decode_step_host when the
+               workload appends): the step's inputs copied from pinned host
+               memory, the step, its outputs copied back, synchronized; wall
+               clock per step.  `e2e.graph_loop` times the Python
+               HostDecodeLoop (one captured graph per step) beside it
   cpu_baseline the float64 oracle on the host cores on a bounded sample
 `--merge fused` merges on the decode kernel's tail; on the workqueue the decode
-builds its own plan (no plan launch) unless `--plan separate`.  `--impl reference`
-times the oracle alone (the reference arm).
+builds its own plan (no plan launch) unless `--plan separate` or the workload
+appends.  `--len-scale f` scales the B=8 / B=64 workloads' lengths by f (small
+cases for profiler captures).  `--impl reference` times the oracle alone (the
+reference arm).
 Multi-GPU (torchrun): every rank runs an independent replica (no collective
 on the data path); value sums the ranks' bytes over the slowest rank's time.
 """
@@ -47,6 +58,7 @@ import numpy as np  # noqa: E402
 METRIC = "decode-attention KV-read GB/s (% of GB300 HBM peak); µs per decode step"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal (8 stacks at 3996 MHz), context for the copy peak
 
 WORKLOADS = {
     1: "B=1 GQA decode Hq=8 Hkv=2 d=128 N=1024 P=16 (64 pages of a 128-page pool) S=4 (C=256)",
@@ -64,7 +76,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--path", default="policy", choices=["policy", "bucketed", "workqueue", "single"])
     ap.add_argument("--no-graph", action="store_true", help="launch steps eagerly")
     ap.add_argument("--no-e2e", action="store_true")
@@ -74,7 +86,14 @@ def parse():
                     help="split paths: merge on the decode's tail, or in a second kernel")
     ap.add_argument("--plan", default="in-decode", choices=["in-decode", "separate"],
                     help="workqueue without appends: the decode builds its own plan, or a plan kernel")
+    ap.add_argument("--len-scale", type=float, default=1.0,
+                    help="scale the lengths of the B=8 bimodal and B=64 uniform workloads")
     return ap.parse_args()
+
+
+def workload_name(cfg_id: int, len_scale: float = 1.0) -> str:
+    name = WORKLOADS[cfg_id]
+    return name if len_scale == 1.0 else f"{name}, lengths x{len_scale:g}"
 
 
 def default_steps(cfg_id):
@@ -260,7 +279,7 @@ def run_reference(args, rank, ws, pg):
     import pkv_traces as T
     if rank != 0:
         return
-    tr = T.make_trace(args.config)
+    tr = T.make_trace(args.config, len_scale=args.len_scale)
     steps = args.steps if args.steps is not None else default_steps(args.config)
     warm = args.warmup if args.warmup is not None else 3
     # the sample per step: row 0 prefix, sized so that all steps fit in ~60 s
@@ -287,7 +306,8 @@ def run_reference(args, rank, ws, pg):
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": ws,
         "steps": steps, "warmup": warm, "ms_per_step": el / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOADS[args.config], "seed": tr.seed},
+        "data": "synthetic", "config": {"workload": workload_name(args.config, args.len_scale),
+                                       "seed": tr.seed},
         "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": oracle.max_threads(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -322,7 +342,7 @@ def run_pkv(args, rank, local, ws, pg):
     torch.cuda.set_stream(stream)
     L = _lib.load()
     cfg_id = args.config
-    tr = T.make_trace(cfg_id)
+    tr = T.make_trace(cfg_id, len_scale=args.len_scale)
     steps = args.steps if args.steps is not None else default_steps(cfg_id)
     warm = max(3, args.warmup if args.warmup is not None else 5)
     appends = tr.steps > 1
@@ -490,61 +510,87 @@ def run_pkv(args, rank, local, ws, pg):
     if st != 0:
         raise RuntimeError(f"device error in the timed region: {msg}")
 
-    # ---- the decode kernel alone (roofline): events around each launch
+    # ---- the decode kernel (roofline)
     if appends:
         reset_lengths()
-    kern_steps = min(steps, 2000)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(kern_steps)]
     if path != 2:
         L.pkv_plan(sref, cref, P(sl), P(wsb), sp)
-    for s in range(kern_steps):
+
+    def kernel(s):
         kk, vv = pools[s % R]
-        evs[s][0].record(stream)
         if path == 2:
             rc = L.pkv_single_pass(sref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(o), P(lse), sp)
         else:
             rc = (L.pkv_decode_merge(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(part),
                                      P(o), P(lse), sp) if fused else
                   L.pkv_decode(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(part), sp))
-        evs[s][1].record(stream)
         _lib.check(rc, "decode")
-    torch.cuda.synchronize()
-    launch_ms = sorted(a.elapsed_time(b) for a, b in evs)
-    kms = statistics.mean(launch_ms)
-    pct = lambda f: launch_ms[min(len(launch_ms) - 1, int(f * len(launch_ms)))] * 1e3
-    # the same launches back to back with no event between them, so that each
-    # overlaps the previous one's tail by programmatic dependent launch as in
-    # the step loop: the kernel's per-launch time once its launch and ramp-up
-    # are hidden
+
+    # (1) the basis of the roofline: the kernel as it runs inside the step --
+    # G launches back to back in one CUDA graph (pools in turn), each chained
+    # to the one before by programmatic dependent launch, replayed; events only
+    # around the replays, so the per-launch time is the kernel's share of a
+    # step loop with the other launches of the step taken out
+    kern_launches = G * max(1, min(steps, 2000) // G)
+    kgraph = None
+    if graphs:
+        try:
+            kgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(kgraph, stream=stream):
+                for s in range(G):
+                    kernel(s)
+            kgraph.replay()
+            torch.cuda.synchronize()
+        except Exception as e:
+            print(f"# decode graph capture failed ({e}); chaining eager launches", file=sys.stderr)
+            kgraph = None
     c0 = torch.cuda.Event(enable_timing=True)
     c1 = torch.cuda.Event(enable_timing=True)
     c0.record(stream)
-    for s in range(kern_steps):
-        kk, vv = pools[s % R]
-        if path == 2:
-            rc = L.pkv_single_pass(sref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(o), P(lse), sp)
-        else:
-            rc = (L.pkv_decode_merge(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(part),
-                                     P(o), P(lse), sp) if fused else
-                  L.pkv_decode(sref, cref, P(wsb), P(q), P(kk), P(vv), P(bt), P(sl), P(part), sp))
-        _lib.check(rc, "decode")
+    if kgraph is not None:
+        for _ in range(kern_launches // G):
+            kgraph.replay()
+    else:
+        for s in range(kern_launches):
+            kernel(s)
     c1.record(stream)
     torch.cuda.synchronize()
-    chained_ms = c0.elapsed_time(c1) / kern_steps
+    chained_ms = c0.elapsed_time(c1) / kern_launches
+    # (2) each launch alone, with events around it: adds the launch, ramp-up
+    # and drain that a chain hides (reported apart, not the roofline basis)
+    iso_launches = min(steps, 2000)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iso_launches)]
+    for s in range(iso_launches):
+        evs[s][0].record(stream)
+        kernel(s)
+        evs[s][1].record(stream)
+    torch.cuda.synchronize()
+    launch_ms = sorted(a.elapsed_time(b) for a, b in evs)
+    iso_ms = statistics.mean(launch_ms)
+    pct = lambda f: launch_ms[min(len(launch_ms) - 1, int(f * len(launch_ms)))] * 1e3
+    st, msg = api.pkv_get_error(wsb)
+    if st != 0:
+        raise RuntimeError(f"device error while timing the decode kernel: {msg}")
     kv_launch = tr.kv_bytes()
     peak, peak_src = peaks()
-    achieved = kv_launch / (kms * 1e-3) / 1e9
+    achieved = kv_launch / (chained_ms * 1e-3) / 1e9
+    achieved_iso = kv_launch / (iso_ms * 1e-3) / 1e9
 
-    # ---- end to end through the public API with pinned host buffers
+    # ---- end to end through the C ABI with pinned host buffers
     e2e = None
     if not args.no_e2e:
         if appends:
             reset_lengths()
-        e2e = run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps if not appends else steps,
-                      appends, kn, vn, wsb, cfg.merge, cfg.plan)
+        e2e = run_e2e_cabi(L, torch, tr, q_h, pools, dev, sref, cref, cfg, wsb, part if npart else None,
+                           steps, appends, path)
+        # the Python serving loop (one captured graph per step), beside it
+        if appends:
+            reset_lengths()
+        e2e["graph_loop"] = run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn,
+                                    wsb, cfg.merge, cfg.plan)
 
-    gbs = kv_step / (ms * 1e-3) / 1e9
+    traffic = profiled_traffic(cfg_id) if args.len_scale == 1.0 else None
     total = whole_job_gbs(kv_step, ms_max, ws)
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -563,7 +609,7 @@ def run_pkv(args, rank, local, ws, pg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
         "config": {
-            "workload": WORKLOADS[cfg_id], "path": ["bucketed-split", "workqueue", "single-pass"][path],
+            "workload": workload_name(cfg_id, args.len_scale), "path": ["bucketed-split", "workqueue", "single-pass"][path],
             "merge": ("fused" if fused else "separate") if path != 2 else None,
             "plan": ("in-decode" if self_plan else "append+plan kernel" if appends else "plan kernel")
                     if path == 1 else None,
@@ -576,15 +622,18 @@ def run_pkv(args, rank, local, ws, pg):
         "roofline": {"bound": "hbm",
                      "kernel": ("decode_merge" if fused else "decode") if path != 2 else "single_pass",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_src, "traffic": profiled_traffic(cfg_id),
-                     "us_per_launch": kms * 1e3, "bytes_per_launch": kv_launch,
-                     "us_per_launch_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
-                     "chained": {"us_per_launch": chained_ms * 1e3,
-                                 "achieved": kv_launch / (chained_ms * 1e-3) / 1e9,
-                                 "frac": kv_launch / (chained_ms * 1e-3) / 1e9 / peak,
-                                 "how": "the same launches back to back, no event between them "
-                                        "(programmatic dependent launch overlaps each with the "
-                                        "previous one's tail)"}},
+                     "peak_source": peak_src, "traffic": traffic,
+                     "bytes_per_launch": kv_launch, "us_per_launch": chained_ms * 1e3,
+                     "timing": f"CUDA events around replays of a CUDA graph of {G} back-to-back "
+                               f"launches chained by programmatic dependent launch (as inside the "
+                               f"step); {kern_launches} launches",
+                     "share_of_step": chained_ms / ms,
+                     "frac_of_nominal_hbm": achieved / NOMINAL_HBM_GBS,
+                     "isolated": {"us_per_launch": iso_ms * 1e3,
+                                  "us_per_launch_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
+                                  "achieved": achieved_iso, "frac": achieved_iso / peak,
+                                  "how": f"{iso_launches} launches, each alone between two "
+                                         "events (launch, ramp-up and drain included)"}},
         "gpu_launches": launches_per_step * steps,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -605,6 +654,84 @@ def _gpu_id(torch, dev):
 def _ctypes_refs(shape, cfg):
     import ctypes
     return ctypes.byref(shape), ctypes.byref(cfg)
+
+
+def run_e2e_cabi(L, torch, tr, q_h, pools, dev, sref, cref, cfg, wsb, part, steps, appends, path):
+    """The C ABI's host-buffer step, once per step on the wall clock: every call
+    copies the step's inputs from pinned host memory (q and the block table and
+    lengths; or, when the workload appends, q and the new K/V token, the table
+    and lengths being device state the step advances), runs the step, copies o
+    and lse into pinned host memory and synchronizes the stream."""
+    import pkv_traces as T
+    from paged_kv_gqa_09_gb300 import _lib
+    R = len(pools)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    P = lambda t: t.data_ptr() if t is not None else None
+    h_q = torch.from_numpy(q_h).pin_memory()
+    d_q = torch.empty(h_q.shape, dtype=torch.float16, device=dev)
+    h_o = torch.empty(h_q.shape, dtype=torch.float16).pin_memory()
+    d_o = torch.empty_like(d_q)
+    h_lse = torch.empty(h_q.shape[:2], dtype=torch.float32).pin_memory()
+    d_lse = torch.empty(h_q.shape[:2], dtype=torch.float32, device=dev)
+    qb, ob, lb = h_q.numel() * 2, h_o.numel() * 2, h_lse.numel() * 4
+    if appends:
+        kn_h, vn_h = T.gen_append_tokens(tr, 0)
+        h_kn = torch.from_numpy(kn_h).pin_memory()
+        h_vn = torch.from_numpy(vn_h).pin_memory()
+        d_kn, d_vn = torch.empty_like(h_kn, device=dev), torch.empty_like(h_vn, device=dev)
+        # as in the device loop: on the workqueue the rows' pages come from a
+        # device free list as they grow
+        bt0, free_np = T.allocation_split(tr) if path == 1 else (tr.block_table, None)
+        d_bt = torch.from_numpy(np.ascontiguousarray(bt0)).to(dev)
+        d_sl = torch.from_numpy(tr.seq_lens).to(dev)
+        free = torch.from_numpy(free_np).to(dev) if free_np is not None else None
+        cnt = torch.tensor([free_np.size], dtype=torch.int32, device=dev) if free is not None else None
+        steps = min(steps, tr.steps - 4)  # the block table holds room for tr.steps tokens per row
+        h2d = qb + 2 * h_kn.numel() * 2
+    else:
+        h_bt = torch.from_numpy(np.ascontiguousarray(tr.block_table)).pin_memory()
+        h_sl = torch.from_numpy(tr.seq_lens).pin_memory()
+        d_bt = torch.empty(h_bt.shape, dtype=torch.int32, device=dev)
+        d_sl = torch.empty(h_sl.shape, dtype=torch.int32, device=dev)
+        steps = min(steps, 4000)
+        h2d = qb + h_bt.numel() * 4 + h_sl.numel() * 4
+    per_tok = tr.Hkv * tr.d * 4
+    sl0 = int(tr.seq_lens.astype(np.int64).sum())
+    appended = [0]
+
+    def one(s):
+        kk, vv = pools[s % R]
+        if appends:
+            rc = L.pkv_append_decode_step_host(
+                sref, cref, P(wsb), P(part), P(h_q), P(d_q), P(h_kn), P(h_vn), P(d_kn), P(d_vn),
+                P(d_bt), P(d_sl), P(free), P(cnt), P(kk), P(vv), P(d_o), P(h_o), P(d_lse), P(h_lse),
+                sp)
+            _lib.check(rc, "pkv_append_decode_step_host")
+            appended[0] += 1
+        else:
+            rc = L.pkv_decode_step_host(sref, cref, P(wsb), P(part), P(h_q), P(d_q), P(h_bt),
+                                        P(d_bt), P(h_sl), P(d_sl), P(kk), P(vv), P(d_o), P(h_o),
+                                        P(d_lse), P(h_lse), sp)
+            _lib.check(rc, "pkv_decode_step_host")
+        return (sl0 + tr.B * appended[0]) * per_tok
+
+    for s in range(3):
+        one(s)
+    kv = 0
+    t0 = time.perf_counter()
+    for s in range(steps):
+        kv += one(s)
+    el = time.perf_counter() - t0
+    from paged_kv_gqa_09_gb300 import api
+    st, msg = api.pkv_get_error(wsb)
+    if st != 0:
+        raise RuntimeError(f"device error in the end-to-end steps: {msg}")
+    name = "pkv_append_decode_step_host" if appends else "pkv_decode_step_host"
+    return {"value": kv / el / 1e9, "unit": UNIT, "us_per_step": el / steps * 1e6, "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ob + lb,
+            "timing": f"synchronized wall clock per step: one {name} call (C ABI) per step -- "
+                      "pinned host inputs copied in, the step's kernels, o/lse copied back, "
+                      "stream synchronized"}
 
 
 def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, wsb, merge, plan):

@@ -231,7 +231,35 @@ int pkv_decode_step_host(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, vo
                          const void *d_k_cache, const void *d_v_cache,
                          void *d_o, void *h_o, float *d_lse, float *h_lse, void *stream);
 
-/* pkv_append_plan -- the step's KV write fused into the workqueue plan: one
+/* pkv_append_decode_step_host -- one step of a serving loop that grows every
+ * row by one token, with the step's inputs and outputs in host memory and the
+ * KV cache, block table and lengths resident on the device (they are state the
+ * step advances).  (Not a step of the pages' method by itself: the serving
+ * loop around it, whose wall clock the pages' evaluation protocol,
+ * Methodology 3, counts with the host's share.)  In order, on `stream`:
+ *   1. copies h_q [B][Hq][d] into d_q and the new token's h_k_new, h_v_new
+ *      [B][Hkv][d] (fp16) into d_k_new, d_v_new -- one cudaMemcpyAsync each;
+ *   2. WORKQUEUE: pkv_append_plan (appends, allocates pages from the device
+ *      free list when d_free_pages != NULL, plans), then pkv_decode + pkv_merge
+ *      on that plan (pkv_decode_merge with PKV_MERGE_FUSED; cfg->plan is not
+ *      consulted); other paths: pkv_append, then pkv_decode_step;
+ *   3. copies d_o into h_o (and d_lse into h_lse when both are non-NULL);
+ *   4. synchronizes `stream`.
+ * After the call every row has one more token and o / lse are those of the
+ * advanced lengths.  Host buffers should be page-locked for the copies to be
+ * asynchronous.  d_free_pages / d_free_count go together and only with the
+ * WORKQUEUE path.  All arguments are checked before anything is enqueued;
+ * device-side results (a row without room, an exhausted free list, a bad page
+ * id) land in the error word as for those calls (read with pkv_get_error). */
+int pkv_append_decode_step_host(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
+                                float *d_partials, const void *h_q, void *d_q,
+                                const void *h_k_new, const void *h_v_new, void *d_k_new,
+                                void *d_v_new, int32_t *d_block_table, int32_t *d_seq_lens,
+                                const int32_t *d_free_pages, int32_t *d_free_count,
+                                void *d_k_cache, void *d_v_cache, void *d_o, void *h_o,
+                                float *d_lse, float *h_lse, void *stream);
+
+/* pkv_append_plan --the step's KV write fused into the workqueue plan: one
  * kernel launch that appends one token per row exactly as pkv_append does and
  * then builds pkv_plan's task list from the advanced lengths.  With
  * d_free_pages != NULL a token that starts a new page (N % page_size == 0)
@@ -286,8 +314,14 @@ int pkv_decode_step_rows(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, vo
  * process exits.  The call allocates nothing.
  * - A step whose plan workspace (rounded up to 256 bytes) plus partial states
  *   exceed PKV_NOALLOC_SCRATCH_BYTES is rejected with PKV_ECAPACITY.
- * - The first call on each device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
+ * - Set-up on first use: the first call on each device looks up the array's
+ *   device address (with that device current).  Under CUDA's default lazy
+ *   module loading that first call -- and the first call of each path, merge
+ *   and plan mode, whose kernels then load -- also brings the library's code
+ *   and the array onto the device, which the CUDA driver backs with device
+ *   memory.  So make one call per configuration you will use outside any
+ *   context where allocation is forbidden, and before any stream capture (or
+ *   run with CUDA_MODULE_LOADING=EAGER); later calls allocate nothing.
  * - Every call shares the one array and it keeps the last call's contents:
  *   the call clears the workspace header (error word, task count, counters),
  *   but calls that overlap on the GPU (different streams, or other host
@@ -410,7 +444,11 @@ int pkv_get_error(void *d_ws, void *stream);
  * launches run with CTA 0 leaving its first pipeline stage unfilled, so the
  * consumer warps' wait on it runs out (after about 1 s); the kernel records
  * PKV_ETIMEOUT, drains its own copies and returns.  Nothing faults, traps or
- * hangs; the outputs of such a launch are meaningless.  0 switches it off. */
+ * hangs; the outputs of such a launch are meaningless.  0 switches it off.
+ * The hook is off unless the process runs with the environment variable
+ * PKV_TEST_HOOKS=1 (read at each call); otherwise it changes nothing and
+ * returns PKV_EUNSUPPORTED.  It stays in the one library so that the tests
+ * exercise the very binary a serving process loads. */
 int pkv_test_starve_next_decodes(int32_t n);
 
 /* Description of the last failure on the calling thread ("" if none). */

@@ -43,7 +43,7 @@ EXPORTS = [
     "pkv_plan_workspace_size", "pkv_partials_size", "pkv_plan", "pkv_decode", "pkv_merge",
     "pkv_decode_merge",
     "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_rows", "pkv_decode_step_noalloc",
-    "pkv_decode_step_host",
+    "pkv_decode_step_host", "pkv_append_decode_step_host",
     "pkv_append", "pkv_append_plan", "pkv_policy_default", "pkv_policy",
     "pkv_cost_model_default", "pkv_policy_learned",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error",
@@ -139,6 +139,7 @@ def load() -> ctypes.CDLL:
             "pkv_decode_step": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_decode_step_noalloc": (ctypes.c_int, [S, C, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_decode_step_host": (ctypes.c_int, [S, C] + [vp] * 15),
+            "pkv_append_decode_step_host": (ctypes.c_int, [S, C] + [vp] * 19),
             "pkv_decode_step_rows": (ctypes.c_int, [S, C, vp, vp, i32] + [vp] * 9),
             "pkv_append": (ctypes.c_int, [S, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_append_plan": (ctypes.c_int, [S, C] + [vp] * 10),

@@ -27,7 +27,8 @@ __all__ = [
     "pkv_decode_merge", "PKV_MERGE_SEPARATE", "PKV_MERGE_FUSED", "PKV_PLAN_SEPARATE",
     "PKV_PLAN_IN_DECODE", "PKV_SELF_PLAN_MAX_B", "pkv_single_pass",
     "pkv_decode_step", "pkv_decode_step_noalloc",
-    "pkv_decode_step_host", "pkv_decode_step_rows", "exact_length_buckets_step", "pkv_append",
+    "pkv_decode_step_host", "pkv_append_decode_step_host", "pkv_decode_step_rows",
+    "exact_length_buckets_step", "pkv_append",
     "pkv_append_plan", "pkv_policy", "pkv_policy_default",
     "pkv_cost_model_default", "pkv_policy_learned",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error", "pkv_version",
@@ -271,6 +272,29 @@ def pkv_decode_step_host(shape, cfg, ws, partials, h_q, q, h_block_table, block_
         _stream(stream)), "pkv_decode_step_host")
 
 
+def pkv_append_decode_step_host(shape, cfg, ws, partials, h_q, q, h_k_new, h_v_new, k_new, v_new,
+                                block_table, seq_lens, k_cache, v_cache, o, h_o, lse=None,
+                                h_lse=None, free_pages=None, free_count=None, stream=None) -> None:
+    """One synchronized serving-loop step with host q / new token in and o / lse
+    out: append (allocating pages from the free list when given), decode, merge
+    (see include/pkv.h)."""
+    L = _lib.load()
+    part = _dev(partials, "partials", torch.float32,
+                nullable=cfg.path == PKV_PATH_SINGLE_PASS or shape.B == 0)
+    check(L.pkv_append_decode_step_host(
+        ctypes.byref(shape), ctypes.byref(cfg), _ws(ws), part, _host(h_q, "h_q", torch.float16),
+        _dev(q, "q", torch.float16), _host(h_k_new, "h_k_new", torch.float16),
+        _host(h_v_new, "h_v_new", torch.float16), _dev(k_new, "k_new", torch.float16),
+        _dev(v_new, "v_new", torch.float16), _dev(block_table, "block_table", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(free_pages, "free_pages", torch.int32, nullable=True),
+        _dev(free_count, "free_count", torch.int32, nullable=True),
+        _dev(k_cache, "k_cache", torch.float16), _dev(v_cache, "v_cache", torch.float16),
+        _dev(o, "o", torch.float16), _host(h_o, "h_o", torch.float16),
+        _dev(lse, "lse", torch.float32, nullable=True), _host(h_lse, "h_lse", torch.float32, True),
+        _stream(stream)), "pkv_append_decode_step_host")
+
+
 def pkv_append(shape, ws, k_new, v_new, block_table, seq_lens, k_cache, v_cache,
                stream=None) -> None:
     L = _lib.load()
@@ -358,7 +382,9 @@ def pkv_get_error(ws: torch.Tensor, stream=None) -> tuple[int, str]:
 
 class PagedDecoder:
     """Owns the workspace and partial-state buffers for one (shape, path) and
-    runs whole decode steps: pkv_policy (host) then pkv_decode_step.
+    runs whole decode steps: pkv_policy (host) then pkv_decode_step.  With
+    `learned` (or a `cost_model`) the route comes from pkv_policy_learned, the
+    cost model the pages name as future work, instead of the thresholds.
 
     Buffers come from the torch caching allocator on the current device and are
     reused across steps; they are resized when a larger configuration arrives.
@@ -371,18 +397,32 @@ class PagedDecoder:
     """
 
     def __init__(self, policy: Optional[PolicyCfg] = None, max_split_tasks: int = 0,
-                 merge: int = PKV_MERGE_SEPARATE, plan: int = PKV_PLAN_IN_DECODE):
+                 merge: int = PKV_MERGE_SEPARATE, plan: int = PKV_PLAN_IN_DECODE,
+                 learned: bool = False, cost_model: Optional[_lib.CostModel] = None):
         self.policy = policy
         self.max_split_tasks = max_split_tasks
         self.merge = merge
         self.plan = plan
+        self.learned = learned or cost_model is not None
+        self.cost_model = cost_model
         self._ws: dict = {}
         self._part: dict = {}
         self._key: dict = {}
 
+    def route(self, B: int, n_max: int, n_sum: Optional[int] = None) -> tuple[int, int]:
+        """(path, split_tokens) for a batch: the calibrated thresholds, or with
+        `learned` the cost model's fastest route, which also needs the batch's
+        total tokens n_sum."""
+        if not self.learned:
+            return pkv_policy(B, n_max, self.policy)
+        if n_sum is None:
+            raise ValueError("the learned cost model needs n_sum, the batch's total tokens")
+        return pkv_policy_learned(B, n_max, int(n_sum), self.cost_model)
+
     def plan_cfg(self, B: int, n_max: int, path: Optional[int] = None,
-                 split_tokens: Optional[int] = None) -> PlanCfg:
-        p, c = pkv_policy(B, n_max, self.policy)
+                 split_tokens: Optional[int] = None, n_sum: Optional[int] = None) -> PlanCfg:
+        p, c = self.route(B, n_max, n_sum) if (path is None or split_tokens is None) else \
+            (path, split_tokens)
         if path is not None:
             p = path
         if split_tokens is not None:
@@ -414,10 +454,12 @@ class PagedDecoder:
     def step(self, q, k_cache, v_cache, block_table, seq_lens, n_max: int,
              path: Optional[int] = None, split_tokens: Optional[int] = None,
              o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-             want_lse: bool = True, scale: Optional[float] = None, stream=None):
-        """One decode step; n_max is the longest row (host scalar the caller knows)."""
+             want_lse: bool = True, scale: Optional[float] = None, stream=None,
+             n_sum: Optional[int] = None):
+        """One decode step; n_max is the longest row and n_sum the total of the
+        lengths (host scalars the caller knows; n_sum only for `learned`)."""
         shape = make_shape(q, k_cache, block_table, scale)
-        cfg = self.plan_cfg(shape.B, int(n_max), path, split_tokens)
+        cfg = self.plan_cfg(shape.B, int(n_max), path, split_tokens, n_sum)
         ws, part = self.buffers(shape, cfg, q.device)
         if o is None:
             o = torch.empty_like(q)

@@ -10,6 +10,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -642,6 +643,80 @@ int pkv_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_
     return PKV_OK;
 }
 
+int pkv_append_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws,
+                                float *part, const void *h_q, void *d_q, const void *h_k_new,
+                                const void *h_v_new, void *d_k_new, void *d_v_new, int32_t *d_bt,
+                                int32_t *d_sl, const int32_t *free_pages, int32_t *free_count,
+                                void *k, void *v, void *d_o, void *h_o, float *d_lse,
+                                float *h_lse, void *stream)
+{
+    // every argument is checked here, so that a call that fails enqueues nothing
+    PKV_TRY(check_shape(s));
+    PKV_TRY(check_cfg(s, c));
+    if (s->B == 0)
+        return PKV_OK;  // an empty batch: nothing to do
+    if (c->path != PKV_PATH_SINGLE_PASS)
+        PKV_TRY(check_slots(s, c));
+    PKV_TRY(check_ptr(d_ws, "workspace"));
+    PKV_TRY(check_ptr(d_q, "q"));
+    PKV_TRY(check_ptr(d_k_new, "k_new"));
+    PKV_TRY(check_ptr(d_v_new, "v_new"));
+    PKV_TRY(check_ptr(k, "k_cache"));
+    PKV_TRY(check_ptr(v, "v_cache"));
+    PKV_TRY(check_ptr(d_bt, "block_table"));
+    PKV_TRY(check_ptr(d_sl, "seq_lens"));
+    PKV_TRY(check_ptr(d_o, "o"));
+    PKV_TRY(check_ptr(d_lse, "lse", true));
+    if (c->path != PKV_PATH_SINGLE_PASS)
+        PKV_TRY(check_ptr(part, "partials"));
+    if ((free_pages == nullptr) != (free_count == nullptr))
+        return fail(PKV_EINVAL, "free_pages and free_count go together");
+    if (free_pages) {
+        if (c->path != PKV_PATH_WORKQUEUE)
+            return fail(PKV_EINVAL, "device page allocation comes with the WORKQUEUE path");
+        PKV_TRY(check_ptr(free_pages, "free_pages"));
+        if (reinterpret_cast<uintptr_t>(free_count) & 3u)
+            return fail(PKV_EINVAL, "free_count is not 4-byte aligned");
+    }
+    if (!h_q || !h_k_new || !h_v_new || !h_o)
+        return fail(PKV_EINVAL, "host q, k_new, v_new and o are required");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t qbytes = (size_t)s->B * s->Hq * s->d * 2;
+    const size_t nbytes = (size_t)s->B * s->Hkv * s->d * 2;
+    cudaError_t e = cudaMemcpyAsync(d_q, h_q, qbytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(d_k_new, h_k_new, nbytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(d_v_new, h_v_new, nbytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "host-to-device copy");
+    if (c->path == PKV_PATH_WORKQUEUE) {
+        // the append launch builds the plan from the advanced lengths
+        PKV_TRY(pkv_append_plan(s, c, d_ws, d_k_new, d_v_new, d_bt, d_sl, free_pages, free_count,
+                                k, v, stream));
+        if (c->merge == PKV_MERGE_FUSED) {
+            PKV_TRY(pkv_decode_merge(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, d_o, d_lse, stream));
+        } else {
+            pkv_plan_cfg_t planned = *c;
+            planned.plan = PKV_PLAN_SEPARATE;
+            PKV_TRY(pkv_decode(s, &planned, d_ws, d_q, k, v, d_bt, d_sl, part, stream));
+            PKV_TRY(pkv_merge(s, &planned, d_ws, d_sl, part, d_o, d_lse, stream));
+        }
+    } else {
+        PKV_TRY(pkv_append(s, d_ws, d_k_new, d_v_new, d_bt, d_sl, k, v, stream));
+        PKV_TRY(pkv_decode_step(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, d_o, d_lse, stream));
+    }
+    e = cudaMemcpyAsync(h_o, d_o, qbytes, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && h_lse && d_lse)
+        e = cudaMemcpyAsync(h_lse, d_lse, (size_t)s->B * s->Hq * 4, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device-to-host copy");
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    return PKV_OK;
+}
+
 int pkv_append(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *v_new,
                const int32_t *bt, int32_t *sl, void *k_cache, void *v_cache, void *stream)
 {
@@ -914,6 +989,11 @@ int pkv_get_error(void *d_ws, void *stream)
 
 int pkv_test_starve_next_decodes(int32_t n)
 {
+    // off unless the process opted in: a production caller cannot make its
+    // decodes time out by accident
+    const char *opt_in = std::getenv("PKV_TEST_HOOKS");
+    if (!opt_in || std::strcmp(opt_in, "1") != 0)
+        return fail(PKV_EUNSUPPORTED, "test hooks are off (set PKV_TEST_HOOKS=1 in the environment)");
     if (n < 0)
         return fail(PKV_EINVAL, "negative count");
     g_starve = n;

@@ -13,7 +13,9 @@
 // must not pass the array's name to a kernel: on the host that name is only a
 // stand-in, not a device address.  Its address is looked up once per device,
 // with that device current, by cudaGetSymbolAddress on the first call made on
-// that device.
+// that device.  With lazy module loading (CUDA's default) that lookup, and the
+// first launch of each kernel, load code and the array onto the device: that
+// first call is set-up, to be made where allocating is still allowed.
 #include "pkv.h"
 #include "pkv_kernels.h"
 

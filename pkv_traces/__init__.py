@@ -127,9 +127,18 @@ def _pages(n: int, P: int) -> int:
 
 # ----------------------------------------------------------------- configs
 
-def make_trace(cfg_id: int, seed: int = HELDOUT_SEED, B: Optional[int] = None) -> Trace:
-    """Build the (lengths, block table) part of workload ``cfg_id`` (1..5)."""
+def make_trace(cfg_id: int, seed: int = HELDOUT_SEED, B: Optional[int] = None,
+               len_scale: float = 1.0) -> Trace:
+    """Build the (lengths, block table) part of workload ``cfg_id`` (1..5).
+
+    len_scale (workloads 3 and 5 only) multiplies every drawn length (rounded,
+    at least 1) before the pages are laid out: the same batch structure with a
+    smaller pool, for profiler captures that must stay small."""
     rng = np.random.default_rng([seed, cfg_id])
+    if len_scale != 1.0 and cfg_id not in (3, 5):
+        raise ValueError("len_scale applies to workloads 3 and 5")
+    scaled = lambda a: np.maximum(1, np.rint(a * len_scale)).astype(np.int32) \
+        if len_scale != 1.0 else a
     P = 16
     if cfg_id == 1:
         N = 1024
@@ -148,7 +157,7 @@ def make_trace(cfg_id: int, seed: int = HELDOUT_SEED, B: Optional[int] = None) -
     if cfg_id == 3:
         short = rng.integers(512, 2048, size=4, endpoint=True)
         long_ = rng.integers(24576, 32768, size=4, endpoint=True)
-        lens = np.concatenate([short, long_])[rng.permutation(8)].astype(np.int32)
+        lens = scaled(np.concatenate([short, long_])[rng.permutation(8)].astype(np.int32))
         bt, pool = _scatter_pages(rng, [_pages(int(n), P) for n in lens])
         return Trace("bimodal", 3, seed, 8, 32, 8, 128, P, 1024, pool, lens, bt,
                      path_hint="workqueue")
@@ -159,7 +168,7 @@ def make_trace(cfg_id: int, seed: int = HELDOUT_SEED, B: Optional[int] = None) -
         return Trace(f"zipf-B{b}", 4, seed, b, 32, 8, 128, P, 1024, pool, lens, bt,
                      path_hint="policy")
     if cfg_id == 5:
-        lens = rng.integers(128, 65536, size=64, endpoint=True).astype(np.int32)
+        lens = scaled(rng.integers(128, 65536, size=64, endpoint=True).astype(np.int32))
         bt, pool = _scatter_pages(rng, [_pages(int(n) + 256, P) for n in lens])
         return Trace("uniform-B64", 5, seed, 64, 64, 8, 128, P, 1024, pool, lens, bt,
                      steps=256, path_hint="workqueue")

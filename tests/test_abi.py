@@ -103,6 +103,7 @@ def test_empty_batch_is_a_no_op(L):
                                              None) == 0
             assert L.pkv_decode_step_host(*args, None, None, None, None, None, None, None, None,
                                           None, None, None, None, None, None, None) == 0
+            assert L.pkv_append_decode_step_host(*args, *([None] * 19)) == 0
             if path != _lib.PKV_PATH_SINGLE_PASS:
                 assert L.pkv_plan(*args, None, None, None) == 0
                 assert L.pkv_decode(*args, None, None, None, None, None, None, None, None) == 0
@@ -259,3 +260,44 @@ def test_learned_policy_prefers_workqueue_for_ragged_and_split_for_b1(L):
     assert p1 in (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_PATH_WORKQUEUE)
     p2, _ = api.pkv_policy_learned(16, 32768, 16 * 900)       # one long row, the rest short
     assert p2 == _lib.PKV_PATH_WORKQUEUE
+
+
+def test_host_append_step_checks_arguments_first(L):
+    """pkv_append_decode_step_host refuses bad arguments before it copies or
+    launches anything (so with no GPU it never reaches the device)."""
+    s = shape()
+    wq = cfg()
+    args = [FAKE] * 19
+    # host q missing
+    a = list(args)
+    a[2] = None
+    assert L.pkv_append_decode_step_host(ctypes.byref(s), ctypes.byref(wq), *a) == _lib.PKV_EINVAL
+    # a free list without its count
+    a = list(args)
+    a[11] = None
+    assert L.pkv_append_decode_step_host(ctypes.byref(s), ctypes.byref(wq), *a) == _lib.PKV_EINVAL
+    # a free list off the workqueue
+    rect = cfg(path=_lib.PKV_PATH_BUCKETED_SPLIT)
+    assert L.pkv_append_decode_step_host(ctypes.byref(s), ctypes.byref(rect), *args) == _lib.PKV_EINVAL
+    assert "WORKQUEUE" in _lib.last_error()
+    # an unaligned device pointer
+    a = list(args)
+    a[3] = FAKE + 8  # d_q
+    assert L.pkv_append_decode_step_host(ctypes.byref(s), ctypes.byref(wq), *a) == _lib.PKV_EINVAL
+
+
+def test_learned_route_of_the_decoder_needs_the_total_tokens(L):
+    dec = api.PagedDecoder(learned=True)
+    with pytest.raises(ValueError):
+        dec.route(8, 32768)
+    assert dec.route(8, 32768, 8 * 900) == api.pkv_policy_learned(8, 32768, 8 * 900)
+    assert api.PagedDecoder().route(8, 32768) == api.pkv_policy(8, 32768)
+
+
+def test_the_test_hook_needs_the_opt_in(L, monkeypatch):
+    """pkv_test_starve_next_decodes is inert unless PKV_TEST_HOOKS=1."""
+    monkeypatch.setenv("PKV_TEST_HOOKS", "0")
+    assert L.pkv_test_starve_next_decodes(1) == _lib.PKV_EUNSUPPORTED
+    assert "PKV_TEST_HOOKS" in _lib.last_error()
+    monkeypatch.setenv("PKV_TEST_HOOKS", "1")
+    assert L.pkv_test_starve_next_decodes(0) == 0

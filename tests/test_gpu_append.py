@@ -167,3 +167,95 @@ def test_host_loop_append_graph_matches_mirror(path, alloc):
             oref, lref = oracle.attention(q, k_h, v_h, bt_h, lens_h.astype(np.int32), tr.scale)
             close(o, oref, f"o at step {step}")
             close_lse(lse, lref)
+
+
+@pytest.mark.parametrize("path,merge,alloc", [
+    (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_SEPARATE, True),
+    (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_FUSED, True),
+    (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_SEPARATE, False),
+    (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_MERGE_SEPARATE, False),
+    (_lib.PKV_PATH_SINGLE_PASS, _lib.PKV_MERGE_SEPARATE, False)])
+def test_append_decode_step_host_matches_mirror(path, merge, alloc):
+    """pkv_append_decode_step_host, one synchronized C call per step: q and
+    the new token come from pinned host memory, o / lse land in pinned host
+    memory, the block table and lengths advance on the device.  Checked
+    against the host mirror of the append rule and the oracle."""
+    steps = 20
+    tr, k, v, free = setup([15, 16, 40, 0, 33, 64, 1], steps, spare_pages=30)
+    k_h, v_h = k.copy(), v.copy()
+    bt_h, lens_h, count = tr.block_table.copy(), tr.seq_lens.astype(np.int64).copy(), len(free)
+    if not alloc:
+        for i in range(tr.B):
+            for col in range(tr.bt_stride):
+                if bt_h[i, col] < 0:
+                    bt_h[i, col] = free[count - 1]
+                    count -= 1
+    kd, vd = dev(k), dev(v)
+    btd, sld = dev(bt_h.astype(np.int32)), dev(lens_h.astype(np.int32))
+    freed = dev(np.array(free, np.int32)) if alloc else None
+    cnt = torch.tensor([count], dtype=torch.int32, device="cuda") if alloc else None
+    shape = shape_of(tr)
+    n_max = int(lens_h.max()) + steps + 1
+    cfg = api.make_cfg(path, C, n_max if path == _lib.PKV_PATH_BUCKETED_SPLIT else 0, 0, merge,
+                       _lib.PKV_PLAN_IN_DECODE)  # the append launch plans; the field is ignored
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    npart = api.pkv_partials_size(shape, cfg)
+    part = torch.empty(max(npart // 4, 4), dtype=torch.float32, device="cuda") if npart else None
+    h_q = torch.empty((tr.B, HQ, D), dtype=torch.float16).pin_memory()
+    h_kn = torch.empty((tr.B, HKV, D), dtype=torch.float16).pin_memory()
+    h_vn = torch.empty_like(h_kn).pin_memory()
+    h_o = torch.full((tr.B, HQ, D), float("nan"), dtype=torch.float16).pin_memory()
+    h_lse = torch.full((tr.B, HQ), float("nan"), dtype=torch.float32).pin_memory()
+    d_q = torch.empty((tr.B, HQ, D), dtype=torch.float16, device="cuda")
+    d_kn = torch.empty((tr.B, HKV, D), dtype=torch.float16, device="cuda")
+    d_vn = torch.empty_like(d_kn)
+    d_o = torch.empty_like(d_q)
+    d_lse = torch.empty((tr.B, HQ), dtype=torch.float32, device="cuda")
+    for step in range(steps):
+        kn, vn = T.gen_append_tokens(tr, step)
+        q = T.gen_step_q(tr, step)
+        h_q.copy_(torch.from_numpy(q))
+        h_kn.copy_(torch.from_numpy(kn))
+        h_vn.copy_(torch.from_numpy(vn))
+        if alloc:
+            count = mirror_append(tr, k_h, v_h, bt_h, lens_h, free, count, kn, vn)
+        else:
+            for i in range(tr.B):
+                pg, sl = bt_h[i, lens_h[i] // P], lens_h[i] % P
+                k_h[pg, sl], v_h[pg, sl] = kn[i], vn[i]
+                lens_h[i] += 1
+        api.pkv_append_decode_step_host(shape, cfg, ws, part, h_q, d_q, h_kn, h_vn, d_kn, d_vn,
+                                        btd, sld, kd, vd, d_o, h_o, d_lse, h_lse, freed, cnt)
+        if step in (0, 1, 9, steps - 1):  # the call has synchronized: h_o is final
+            check_error_free(ws)
+            assert np.array_equal(sld.cpu().numpy(), lens_h)
+            assert np.array_equal(btd.cpu().numpy(), bt_h)
+            if alloc:
+                assert int(cnt.item()) == count
+            oref, lref = oracle.attention(q, k_h, v_h, bt_h, lens_h.astype(np.int32), tr.scale)
+            close(h_o, oref, f"o at step {step}")
+            close_lse(h_lse, lref)
+
+
+def test_append_decode_step_host_checks_before_enqueueing():
+    """A free list on a path without device allocation is refused before any
+    copy or launch: the lengths stay as they were."""
+    tr, k, v, free = setup([15, 16], steps=4, spare_pages=4)
+    kd, vd, btd, sld = dev(k), dev(v), dev(tr.block_table), dev(tr.seq_lens)
+    freed = dev(np.array(free, np.int32))
+    cnt = torch.tensor([len(free)], dtype=torch.int32, device="cuda")
+    shape = shape_of(tr)
+    cfg = api.make_cfg(_lib.PKV_PATH_BUCKETED_SPLIT, C, 64)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    part = torch.empty(api.pkv_partials_size(shape, cfg) // 4, dtype=torch.float32, device="cuda")
+    h_q = torch.zeros((tr.B, HQ, D), dtype=torch.float16).pin_memory()
+    h_kn = torch.zeros((tr.B, HKV, D), dtype=torch.float16).pin_memory()
+    d_q = torch.empty((tr.B, HQ, D), dtype=torch.float16, device="cuda")
+    d_kn = torch.empty((tr.B, HKV, D), dtype=torch.float16, device="cuda")
+    with pytest.raises(_lib.PkvError) as ei:
+        api.pkv_append_decode_step_host(shape, cfg, ws, part, h_q, d_q, h_kn, h_kn, d_kn, d_kn,
+                                        btd, sld, kd, vd, d_q.clone(), h_q.clone(), None, None,
+                                        freed, cnt)
+    assert ei.value.status == _lib.PKV_EINVAL
+    torch.cuda.synchronize()
+    assert sld.cpu().numpy().tolist() == [15, 16]

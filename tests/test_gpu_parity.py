@@ -194,6 +194,36 @@ def test_zipf_policy_route_matches_oracle(B):
         close(o2, oref)
 
 
+@pytest.mark.parametrize("cfg_id,B", [(3, 8), (4, 4), (4, 8)])
+def test_learned_cost_model_route_matches_oracle(cfg_id, B):
+    """PagedDecoder(learned=True) routes each batch by pkv_policy_learned (the
+    learned cost model of the pages' future work) on (B, N_max, N_sum) and runs
+    that route's step: the launches are the route's, the outputs match the
+    oracle."""
+    tr = T.make_trace(4, B=B) if cfg_id == 4 else T.make_trace(cfg_id)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    d = upload(tr, q, k, v)
+    n_sum = int(tr.seq_lens.astype(np.int64).sum())
+    path, C = api.pkv_policy_learned(tr.B, tr.n_max, n_sum)
+    dec = api.PagedDecoder(learned=True)
+    cfg = dec.plan_cfg(tr.B, tr.n_max, n_sum=n_sum)
+    assert (cfg.path, cfg.split_tokens if path != SINGLE else C) == (path, C)
+    api.pkv_reset_counters()
+    o, lse = dec.step(d["q"], d["k"], d["v"], d["bt"], d["sl"], tr.n_max, n_sum=n_sum)
+    torch.cuda.synchronize()
+    c = api.pkv_get_counters()
+    if path == SINGLE:
+        assert (c["single_pass_launches"], c["decode_launches"], c["merge_launches"]) == (1, 0, 0)
+    else:
+        assert (c["decode_launches"], c["merge_launches"]) == (1, 1)
+        assert c["plan_launches"] == 0  # bucketed, or the workqueue planning in its decode
+    check_error_free(dec.workspace(d["q"].device))
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o, oref)
+    close_lse(lse, lref)
+
+
 # ------------------------------------------------------------------ edge cases
 
 P_C = [(8, 64), (16, 16), (16, 48), (16, 256), (32, 64), (64, 128), (128, 256), (256, 512)]
