@@ -4,8 +4,8 @@
 Default workload (N=1): B=64 uniform lengths U[128, 65536], Hq=64, Hkv=8
 (G=8), d=128, page_size 16, a shuffled pool sized to the total length, the
 compact workqueue with C=1024, and every step appending one token per row
-(the append allocates pages from a device free list and builds the plan in
-one launch, then decode and merge) -- the largest workload that fits one
+(an append launch that allocates pages from a device free list, then the
+decode, which builds the workqueue's plan itself, and the merge) -- the largest workload that fits one
 GPU.  `--config 1..4` selects the smaller workloads (1: B=1 N=1024; 2: B=1
 N=32768 bucketed split; 3: B=8 bimodal; 4: B=8 Zipf).
 
@@ -28,8 +28,8 @@ One JSON line on rank 0:
                HostDecodeLoop (one captured graph per step) beside it
   cpu_baseline the float64 oracle on the host cores on a bounded sample
 `--merge fused` merges on the decode kernel's tail; on the workqueue the decode
-builds its own plan (no plan launch) unless `--plan separate` or the workload
-appends.  `--len-scale f` scales the B=8 / B=64 workloads' lengths by f (small
+builds its own plan (no plan launch; an appending step's append launch then
+only appends and allocates) unless `--plan separate`.  `--len-scale f` scales the B=8 / B=64 workloads' lengths by f (small
 cases for profiler captures).  `--impl reference` times the oracle alone (the
 reference arm).
 Multi-GPU (torchrun): every rank runs an independent replica (no collective
@@ -234,7 +234,7 @@ def profiled_traffic(cfg_id: int):
     return int(m_tr.group(1))
 
 
-def cpu_baseline_run(tr, q, k, v, seconds: float):
+def cpu_baseline_run(tr, q, k, v, seconds: float, sample_of: str = "the workload"):
     """The oracle, as it stands, on this host's cores: repeated whole decode
     steps of the workload (or, for large workloads, a row-prefix sample) for
     about `seconds` on all cores, then a quarter of that on one thread; returns
@@ -250,7 +250,7 @@ def cpu_baseline_run(tr, q, k, v, seconds: float):
     total_tok = int(lens.sum())
     if per_tok * total_tok <= seconds / 2:
         sample_lens, sample_q, sample_bt = lens, q, tr.block_table
-        desc = "whole decode steps of the workload"
+        desc = f"whole decode steps of {sample_of}"
     else:
         n = max(16, min(int(lens[0]), int(seconds / 4 / per_tok)))
         sample_lens = np.array([n], np.int32)
@@ -383,8 +383,8 @@ def run_pkv(args, rank, local, ws, pg):
     n_max_run = tr.n_max + (tr.steps if appends else 0)
     bucket = n_max_run if path == 0 else 0
     fused = args.merge == "fused" and path != 2
-    # the appending workqueue builds its plan in the append launch already
-    self_plan = (args.plan == "in-decode" and path == 1 and not appends and not fused
+    # with appends the append launch then allocates pages only and the decode plans
+    self_plan = (args.plan == "in-decode" and path == 1 and not fused
                  and tr.B <= api.PKV_SELF_PLAN_MAX_B)
     plan_mode = api.PKV_PLAN_IN_DECODE if self_plan else api.PKV_PLAN_SEPARATE
     cfg = api.make_cfg(path, C, bucket, 0, api.PKV_MERGE_FUSED if fused else api.PKV_MERGE_SEPARATE,
@@ -596,9 +596,11 @@ def run_pkv(args, rank, local, ws, pg):
     if rank == 0 and not args.no_cpu:
         if k_h is None:
             tr_s, qb, k_s, v_s = _row0_sample(tr)
+            of = f"row 0 of the workload ({int(tr.seq_lens[0])} tokens, all {tr.Hq} query heads)"
         else:
             tr_s, qb, k_s, v_s = tr, q_h, k_h, v_h
-        val, cores, desc, one = cpu_baseline_run(tr_s, qb, k_s, v_s, args.cpu_seconds)
+            of = "the workload"
+        val, cores, desc, one = cpu_baseline_run(tr_s, qb, k_s, v_s, args.cpu_seconds, of)
         cpu = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
                "single_thread_value": one}
     if rank != 0:
@@ -613,6 +615,7 @@ def run_pkv(args, rank, local, ws, pg):
             "merge": ("fused" if fused else "separate") if path != 2 else None,
             "plan": ("in-decode" if self_plan else "append+plan kernel" if appends else "plan kernel")
                     if path == 1 else None,
+            "launches_per_step": launches_per_step,
             "split_tokens": C, "kv_bytes_per_step": kv_step, "seed": tr.seed,
             "l2": (f"{R} KV pools rotated ({R * pool_bytes / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB)"
                    if R > 1 else f"inputs ({pool_bytes / 2**30:.1f} GiB) larger than L2"),
@@ -760,7 +763,7 @@ def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, ws
             fc = torch.tensor([free_np.size], dtype=torch.int32, device=dev) if fp is not None else None
             lp = api.HostDecodeLoop(kk, vv, tr.B, tr.Hq, tr.bt_stride, n_max, path=path,
                                     split_tokens=C, merge=merge, append=True, free_pages=fp,
-                                    free_count=fc)
+                                    free_count=fc, plan=plan)
             lp.set_state(torch.from_numpy(np.ascontiguousarray(bt0)), torch.from_numpy(tr.seq_lens))
             lp.h_kn.copy_(kn.cpu())
             lp.h_vn.copy_(vn.cpu())

@@ -240,9 +240,9 @@ int pkv_decode_step_host(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, vo
  *   1. copies h_q [B][Hq][d] into d_q and the new token's h_k_new, h_v_new
  *      [B][Hkv][d] (fp16) into d_k_new, d_v_new -- one cudaMemcpyAsync each;
  *   2. WORKQUEUE: pkv_append_plan (appends, allocates pages from the device
- *      free list when d_free_pages != NULL, plans), then pkv_decode + pkv_merge
- *      on that plan (pkv_decode_merge with PKV_MERGE_FUSED; cfg->plan is not
- *      consulted); other paths: pkv_append, then pkv_decode_step;
+ *      free list when d_free_pages != NULL, and plans unless the decode will),
+ *      then pkv_decode + pkv_merge (pkv_decode_merge with PKV_MERGE_FUSED),
+ *      all with `cfg`; other paths: pkv_append, then pkv_decode_step;
  *   3. copies d_o into h_o (and d_lse into h_lse when both are non-NULL);
  *   4. synchronizes `stream`.
  * After the call every row has one more token and o / lse are those of the
@@ -268,9 +268,13 @@ int pkv_append_decode_step_host(const pkv_shape_t *shape, const pkv_plan_cfg_t *
  * from the top, block_table[i][N / page_size] is set to it and *d_free_count
  * drops by the pages taken.  A row with no free page left, no room in its
  * block table or a bad page id keeps its length and the error word records it.
- * cfg->path must be WORKQUEUE.  (Not a step of the pages' method: the per-step
- * KV write and page allocation of a serving loop, folded into the launch the
- * workqueue path makes anyway.) */
+ * cfg->path must be WORKQUEUE.  With cfg->plan == PKV_PLAN_IN_DECODE, the
+ * separate merge and B <= PKV_SELF_PLAN_MAX_B the decode that follows builds
+ * the plan itself (see pkv_decode): the launch then only appends and
+ * allocates -- same rule, same results, one CTA per row -- writes no plan,
+ * and counts as an append launch in pkv_get_counters.  (Not a step of the
+ * pages' method: the per-step KV write and page allocation of a serving loop,
+ * folded into the launch the workqueue path makes anyway.) */
 int pkv_append_plan(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
                     const void *d_k_new, const void *d_v_new, int32_t *d_block_table,
                     int32_t *d_seq_lens, const int32_t *d_free_pages, int32_t *d_free_count,

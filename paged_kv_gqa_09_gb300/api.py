@@ -487,11 +487,11 @@ class HostDecodeLoop:
     (pinned staging `h_kn`, `h_vn` [B, Hkv, d]) into its page and advances the
     lengths, then decodes: the block table and lengths are device-resident
     state, loaded once by `set_state()` and advanced by the step's kernels.  On
-    the workqueue the append is fused into the plan launch, and with
-    `free_pages` / `free_count` (device int32) a token that starts a page takes
-    one from that free list.  `n_max` must then cover the lengths the loop will
-    reach.  `merge` and `plan` choose the step's launches as in PagedDecoder
-    (with `append` the workqueue's plan comes from the append launch).
+    the workqueue the append is pkv_append_plan (which also plans unless the
+    decode does), and with `free_pages` / `free_count` (device int32) a token
+    that starts a page takes one from that free list.  `n_max` must then cover
+    the lengths the loop will reach.  `merge` and `plan` choose the step's
+    launches as in PagedDecoder.
     """
 
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, B: int, Hq: int, bt_stride: int,
@@ -538,8 +538,6 @@ class HostDecodeLoop:
             p = path
         if split_tokens is not None:
             c = split_tokens
-        if append:
-            plan = PKV_PLAN_SEPARATE  # the fused append launch builds the workqueue's plan
         self.cfg = make_cfg(p, c, n_max if p == PKV_PATH_BUCKETED_SPLIT else 0,
                             max_tasks if p == PKV_PATH_WORKQUEUE else 0, merge, plan)
         self.ws = torch.zeros(pkv_plan_workspace_size(self.shape, self.cfg), dtype=torch.uint8, device=dev)

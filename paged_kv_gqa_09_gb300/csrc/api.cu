@@ -108,6 +108,35 @@ bool self_plans(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
     return c->path == PKV_PATH_WORKQUEUE && c->plan == PKV_PLAN_IN_DECODE && s->B <= kSelfPlanMaxB;
 }
 
+WsHeader *ws_hdr(void *ws) { return reinterpret_cast<WsHeader *>(ws); }
+
+// pkv_append_plan leaves the plan to the decode that follows it: that decode
+// plans for itself (the fused merge's decode reads a plan built before it).
+bool append_defers_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
+{
+    return self_plans(s, c) && c->merge == PKV_MERGE_SEPARATE;
+}
+
+AppendParams append_params(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *v_new,
+                           int32_t *bt, int32_t *sl, void *k_cache, void *v_cache)
+{
+    AppendParams p = {};
+    p.k_new = static_cast<const __half *>(k_new);
+    p.v_new = static_cast<const __half *>(v_new);
+    p.bt = bt;
+    p.seq_lens = sl;
+    p.k_cache = static_cast<__half *>(k_cache);
+    p.v_cache = static_cast<__half *>(v_cache);
+    p.ws = ws_hdr(d_ws);
+    p.B = s->B;
+    p.Hkv = s->Hkv;
+    p.d = s->d;
+    p.log2P = ilog2(s->page_size);
+    p.num_pages = s->num_pages;
+    p.bt_stride = s->bt_stride;
+    return p;
+}
+
 int len_cap(const pkv_shape_t *s) { return s->bt_stride * s->page_size; }
 
 int s_b(const pkv_shape_t *s, const pkv_plan_cfg_t *c)
@@ -220,8 +249,6 @@ int encode_kv_map(CUtensorMap *m, const void *base, const pkv_shape_t *s, int bo
         return fail(PKV_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return PKV_OK;
 }
-
-WsHeader *ws_hdr(void *ws) { return reinterpret_cast<WsHeader *>(ws); }
 
 // State slots are int32 in the task records and the kernels: a split path
 // whose partial-state buffer would hold more is refused before any launch.
@@ -408,6 +435,17 @@ int pkv_append_plan(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, c
         PKV_TRY(check_ptr(free_pages, "free_pages"));
         if (reinterpret_cast<uintptr_t>(free_count) & 3u)
             return fail(PKV_EINVAL, "free_count is not 4-byte aligned");
+    }
+    if (append_defers_plan(s, c)) {
+        // append (and allocate) only: the decode that follows builds the plan
+        AppendParams a = append_params(s, d_ws, k_new, v_new, bt, sl, k_cache, v_cache);
+        a.free_pages = free_pages;
+        a.free_count = free_count;
+        cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream), true);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "append launch");
+        g_cnt.append++;
+        return PKV_OK;
     }
     PlanParams p = plan_params(s, c, sl, d_ws);
     p.k_new = static_cast<const __half *>(k_new);
@@ -691,16 +729,15 @@ int pkv_append_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, v
     if (e != cudaSuccess)
         return cuda_fail(e, "host-to-device copy");
     if (c->path == PKV_PATH_WORKQUEUE) {
-        // the append launch builds the plan from the advanced lengths
+        // the append launch allocates pages and, unless the decode plans, plans
         PKV_TRY(pkv_append_plan(s, c, d_ws, d_k_new, d_v_new, d_bt, d_sl, free_pages, free_count,
                                 k, v, stream));
+        // the decode then plans for itself, or reads the plan the append built
         if (c->merge == PKV_MERGE_FUSED) {
             PKV_TRY(pkv_decode_merge(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, d_o, d_lse, stream));
         } else {
-            pkv_plan_cfg_t planned = *c;
-            planned.plan = PKV_PLAN_SEPARATE;
-            PKV_TRY(pkv_decode(s, &planned, d_ws, d_q, k, v, d_bt, d_sl, part, stream));
-            PKV_TRY(pkv_merge(s, &planned, d_ws, d_sl, part, d_o, d_lse, stream));
+            PKV_TRY(pkv_decode(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, stream));
+            PKV_TRY(pkv_merge(s, c, d_ws, d_sl, part, d_o, d_lse, stream));
         }
     } else {
         PKV_TRY(pkv_append(s, d_ws, d_k_new, d_v_new, d_bt, d_sl, k, v, stream));
@@ -730,20 +767,9 @@ int pkv_append(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *
     PKV_TRY(check_ptr(sl, "seq_lens"));
     PKV_TRY(check_ptr(k_cache, "k_cache"));
     PKV_TRY(check_ptr(v_cache, "v_cache"));
-    AppendParams p = {};
-    p.k_new = static_cast<const __half *>(k_new);
-    p.v_new = static_cast<const __half *>(v_new);
-    p.bt = bt;
-    p.seq_lens = sl;
-    p.k_cache = static_cast<__half *>(k_cache);
-    p.v_cache = static_cast<__half *>(v_cache);
-    p.ws = ws_hdr(d_ws);
-    p.B = s->B;
-    p.Hkv = s->Hkv;
-    p.d = s->d;
-    p.log2P = ilog2(s->page_size);
-    p.num_pages = s->num_pages;
-    p.bt_stride = s->bt_stride;
+    // no free list: the kernel writes no block-table entry
+    AppendParams p = append_params(s, d_ws, k_new, v_new, const_cast<int32_t *>(bt), sl, k_cache,
+                                   v_cache);
     cudaError_t e = launch_append(p, static_cast<cudaStream_t>(stream), true);
     if (e != cudaSuccess)
         return cuda_fail(e, "append launch");

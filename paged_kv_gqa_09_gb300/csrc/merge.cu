@@ -176,40 +176,158 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
         p.lse[wg] = M + logf(Lt);
 }
 
-// Append: one CTA per row, one thread per 16 bytes of the row's new K and V.
-__global__ void __launch_bounds__(256) append_kernel(const AppendParams p)
+// Append: one CTA per row, its threads copying the row's new K and V 16 bytes
+// at a time into page block_table[i][N / P], slot N % P, then N -> N + 1.
+constexpr int kAppendThreads = 128;
+
+// A row's new token starts a page that the free list must supply.
+__device__ __forceinline__ bool append_needs_page(const AppendParams &p, int N, int64_t cap)
 {
+    return N >= 0 && (int64_t)N < cap && (N & ((1 << p.log2P) - 1)) == 0;
+}
+
+// Where row i's token goes: its page, or -1 when the row cannot append (no
+// room in its table, no free page left, a bad page id).  With `commit` (the
+// row's own CTA) an allocated page is entered in the block table and a
+// failure is reported; without, nothing is written.
+__device__ int append_page(const AppendParams &p, int i, int N, int avail, int rank, bool commit)
+{
+    const int64_t cap = (int64_t)p.bt_stride << p.log2P;
+    if (N < 0 || (int64_t)N >= cap) {
+        if (commit)
+            report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, (int32_t)cap);
+        return -1;
+    }
+    int page;
+    const int64_t entry = (int64_t)i * p.bt_stride + (N >> p.log2P);
+    if (p.free_pages && append_needs_page(p, N, cap)) {
+        const int slot = avail - 1 - rank;
+        if (slot < 0) {
+            if (commit)
+                report_error(p.ws, kErrNoPage, i, N, avail);
+            return -1;
+        }
+        page = p.free_pages[slot];
+        if (commit)
+            p.bt[entry] = page;
+    } else {
+        page = p.bt[entry];
+    }
+    if (page < 0 || page >= p.num_pages) {
+        if (commit)
+            report_error(p.ws, kErrBadPage, i, N >> p.log2P, page);
+        return -1;
+    }
+    return page;
+}
+
+// Sum of one int per thread over the CTA (every thread gets it).
+__device__ __forceinline__ int append_block_sum(int x, int *s_warp)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0)
+        s_warp[threadIdx.x >> 5] = x;
+    __syncthreads();
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < kAppendThreads / 32; ++w)
+        t += s_warp[w];
+    return t;
+}
+
+// Without a free list every row's CTA advances its own length.  With one, a
+// row whose token starts a page takes free_pages[avail - 1 - rank], rank = the
+// rows before it that need one (the order the fused append-and-plan launch
+// serves them in); each CTA counts those rows from the lengths itself, so no
+// length may change before every CTA has read them: the last CTA to finish
+// (a counter in the workspace header, which it zeroes again) advances the
+// lengths of every row that appended and lowers the free count.
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p)
+{
+    __shared__ int s_warp[kAppendThreads / 32];
+    __shared__ int s_last;
     pdl_wait();
     pdl_trigger();
     const int i = blockIdx.x;
     if (i >= p.B)
         return;
+    const int64_t cap = (int64_t)p.bt_stride << p.log2P;
     const int N = p.seq_lens[i];
-    const int P = 1 << p.log2P;
-    const int chunks = p.Hkv * p.d / 8;  // 16-byte chunks per token
-    bool ok = N >= 0 && (int64_t)N < (int64_t)p.bt_stride * P;
-    int page = 0;
-    if (ok) {
-        page = p.bt[(int64_t)i * p.bt_stride + (N >> p.log2P)];
-        if (page < 0 || page >= p.num_pages) {
-            if (threadIdx.x == 0)
-                report_error(p.ws, kErrBadPage, i, N >> p.log2P, page);
-            ok = false;
-        }
-    } else if (threadIdx.x == 0) {
-        report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.bt_stride * P);
+    int avail = 0, rank = 0;
+    if (p.free_pages) {
+        avail = *p.free_count;
+        int before = 0;
+        for (int r = threadIdx.x; r < i; r += kAppendThreads)
+            before += append_needs_page(p, p.seq_lens[r], cap) ? 1 : 0;
+        rank = append_block_sum(before, s_warp);
     }
-    if (ok) {
-        const size_t dst = ((size_t)page * P + (N & (P - 1))) * (size_t)chunks;
+    __shared__ int s_page;
+    if (threadIdx.x == 0)
+        s_page = append_page(p, i, N, avail, rank, true);
+    __syncthreads();
+    const int page = s_page;
+    if (page >= 0) {
+        const int chunks = p.Hkv * p.d / 8;  // 16-byte chunks per token
+        const size_t dst = ((size_t)page << p.log2P | (size_t)(N & ((1 << p.log2P) - 1))) * chunks;
         const size_t src = (size_t)i * chunks;
-        for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+        for (int c = threadIdx.x; c < chunks; c += kAppendThreads) {
             reinterpret_cast<int4 *>(p.k_cache)[dst + c] = reinterpret_cast<const int4 *>(p.k_new)[src + c];
             reinterpret_cast<int4 *>(p.v_cache)[dst + c] = reinterpret_cast<const int4 *>(p.v_new)[src + c];
         }
     }
-    __syncthreads();  // every thread has read N before it changes
-    if (ok && threadIdx.x == 0)
-        p.seq_lens[i] = N + 1;
+    if (!p.free_pages) {
+        __syncthreads();  // every thread has read N before it changes
+        if (page >= 0 && threadIdx.x == 0)
+            p.seq_lens[i] = N + 1;
+        return;
+    }
+    __syncthreads();  // this CTA's reads of the lengths are done
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(&p.ws->append_done, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    // every other CTA has read what it needed: settle each row as its CTA did
+    // (same inputs, none of them written by this launch) and advance it
+    int carry = 0;
+    for (int base = 0; base < p.B; base += kAppendThreads) {
+        const int r = base + threadIdx.x;
+        const int Nr = r < p.B ? p.seq_lens[r] : -1;
+        const int need = r < p.B && append_needs_page(p, Nr, cap) ? 1 : 0;
+        // exclusive prefix of `need` over this chunk's rows
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        int incl = need;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        __syncthreads();
+        if (lane == 31)
+            s_warp[warp] = incl;
+        __syncthreads();
+        int before_warp = 0, chunk_total = 0;
+#pragma unroll
+        for (int w = 0; w < kAppendThreads / 32; ++w) {
+            before_warp += w < warp ? s_warp[w] : 0;
+            chunk_total += s_warp[w];
+        }
+        const int rank_r = carry + before_warp + incl - need;
+        if (r < p.B && append_page(p, r, Nr, avail, rank_r, false) >= 0)
+            p.seq_lens[r] = Nr + 1;
+        carry += chunk_total;
+    }
+    if (threadIdx.x == 0) {
+        *p.free_count = avail - (carry < avail ? carry : avail);
+        p.ws->append_done = 0;
+    }
 }
 
 cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttribute *attr, bool pdl)
@@ -240,7 +358,7 @@ cudaError_t launch_merge(int d, const MergeParams &p, cudaStream_t s, bool pdl)
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s, bool pdl)
 {
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = make_cfg(dim3(p.B > 0 ? p.B : 1), dim3(128), s, attr, pdl);
+    cudaLaunchConfig_t cfg = make_cfg(dim3(p.B > 0 ? p.B : 1), dim3(kAppendThreads), s, attr, pdl);
     return cudaLaunchKernelEx(&cfg, append_kernel, p);
 }
 

@@ -40,7 +40,10 @@ struct WsHeader {
     // last arrival advances (the count is back at zero after every launch)
     int32_t bar_count;
     int32_t bar_gen;
-    int32_t pad[5];
+    // CTAs of an allocating append that have read the lengths; the last one
+    // zeroes it after advancing them
+    int32_t append_done;
+    int32_t pad[4];
 };
 static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
 

@@ -97,10 +97,13 @@ struct MergeParams {
 
 struct AppendParams {
     const __half *k_new, *v_new;
-    const int32_t *bt;
+    int32_t *bt;  // written only when a page is allocated
     int32_t *seq_lens;
     __half *k_cache, *v_cache;
     WsHeader *ws;
+    // with free_pages, a token that starts a page takes one from the free list
+    const int32_t *free_pages;  // free page ids, top of the stack at the end
+    int32_t *free_count;        // entries of free_pages in use
     int B, Hkv, d, log2P, num_pages, bt_stride;
 };
 

@@ -50,10 +50,15 @@ def mirror_append(tr, k_h, v_h, bt_h, lens_h, free_h, count, kn, vn):
     return count
 
 
-@pytest.mark.parametrize("merge", [_lib.PKV_MERGE_SEPARATE, _lib.PKV_MERGE_FUSED])
-def test_fused_append_allocates_pages_and_matches_oracle(merge):
+@pytest.mark.parametrize("merge,plan", [(_lib.PKV_MERGE_SEPARATE, _lib.PKV_PLAN_SEPARATE),
+                                        (_lib.PKV_MERGE_FUSED, _lib.PKV_PLAN_SEPARATE),
+                                        (_lib.PKV_MERGE_SEPARATE, _lib.PKV_PLAN_IN_DECODE),
+                                        (_lib.PKV_MERGE_FUSED, _lib.PKV_PLAN_IN_DECODE)])
+def test_fused_append_allocates_pages_and_matches_oracle(merge, plan):
     """With merge == FUSED the loop runs two launches per step: append + plan,
-    then the decode with the merge on its tail (pkv_decode_merge)."""
+    then the decode with the merge on its tail (pkv_decode_merge).  With the
+    separate merge and plan == IN_DECODE the append launch only appends and
+    allocates, and the decode builds the plan."""
     steps = 40
     tr, k, v, free = setup([15, 16, 40, 0, 33, 64, 1], steps, spare_pages=30)
     k_h, v_h = k.copy(), v.copy()
@@ -62,7 +67,8 @@ def test_fused_append_allocates_pages_and_matches_oracle(merge):
     freed = dev(np.array(free, np.int32))
     cnt = torch.tensor([len(free)], dtype=torch.int32, device="cuda")
     shape = shape_of(tr)
-    cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, C)
+    cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, C, 0, 0, merge, plan)
+    deferred = merge == _lib.PKV_MERGE_SEPARATE and plan == _lib.PKV_PLAN_IN_DECODE
     ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
     part = torch.empty(api.pkv_partials_size(shape, cfg) // 4, dtype=torch.float32, device="cuda")
     o = torch.empty((tr.B, HQ, D), dtype=torch.float16, device="cuda")
@@ -88,20 +94,24 @@ def test_fused_append_allocates_pages_and_matches_oracle(merge):
             close(o, oref, f"o at step {step}")
             close_lse(lse, lref)
     c = api.pkv_get_counters()
-    assert c["plan_launches"] == steps and c["append_launches"] == 0      # one launch per step
+    if deferred:
+        assert c["plan_launches"] == 0 and c["append_launches"] == steps  # the decode plans
+    else:
+        assert c["plan_launches"] == steps and c["append_launches"] == 0  # append + plan in one
     assert c["decode_launches"] == steps
     assert c["merge_launches"] == (0 if merge == _lib.PKV_MERGE_FUSED else steps)
     used = bt_h[bt_h >= 0]
     assert len(np.unique(used)) == used.size                               # no page handed out twice
 
 
-def test_fused_append_reports_an_empty_free_list():
+@pytest.mark.parametrize("plan", [_lib.PKV_PLAN_SEPARATE, _lib.PKV_PLAN_IN_DECODE])
+def test_fused_append_reports_an_empty_free_list(plan):
     tr, k, v, free = setup([16, 32, 5], steps=4, spare_pages=1)
     kd, vd, btd, sld = dev(k), dev(v), dev(tr.block_table), dev(tr.seq_lens)
     freed = dev(np.array(free, np.int32))
     cnt = torch.tensor([len(free)], dtype=torch.int32, device="cuda")
     shape = shape_of(tr)
-    cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, C)
+    cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, C, plan=plan)
     ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
     kn, vn = T.gen_append_tokens(tr, 0)
     api.pkv_append_plan(shape, cfg, ws, dev(kn), dev(vn), btd, sld, kd, vd, freed, cnt)
@@ -111,6 +121,52 @@ def test_fused_append_reports_an_empty_free_list():
     assert sld.cpu().numpy().tolist() == [17, 32, 6]
     assert int(cnt.item()) == 0
     assert btd.cpu().numpy()[0, 1] == free[len(free) - 1]
+
+
+def test_row_parallel_append_matches_the_plan_kernels_append():
+    """The append launch that leaves the plan to the decode (one CTA per row,
+    each counting the rows before it that need a page) against the plan
+    kernel's fused append (one CTA, a block scan), on two copies of the same
+    state: 300 rows, most of them starting a page, and a free list of 160
+    pages that runs out at the first step (rows left without a page keep
+    asking).  Every step must leave the same block table, lengths, free count,
+    error status and cache contents."""
+    rng = np.random.default_rng([T.HELDOUT_SEED, 702])
+    lens0 = (rng.integers(0, 40, 300) * P + rng.integers(0, 3, 300) * (rng.random(300) < 0.3)).tolist()
+    tr = T.custom_trace(lens0, HQ, HKV, D, P, C, extra_pages=160, extra_cols=2, tag=703)
+    k, v = T.gen_kv(tr)
+    used = set(tr.block_table[tr.block_table >= 0].tolist())
+    free = np.array([x for x in rng.permutation(tr.num_pages) if int(x) not in used], np.int32)
+    assert free.size == 160
+    shape = shape_of(tr)
+    states = []
+    for plan in (_lib.PKV_PLAN_SEPARATE, _lib.PKV_PLAN_IN_DECODE):
+        cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, C, plan=plan)
+        ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+        states.append(dict(cfg=cfg, ws=ws, k=dev(k), v=dev(v), bt=dev(tr.block_table),
+                           sl=dev(tr.seq_lens), free=dev(free),
+                           cnt=torch.tensor([free.size], dtype=torch.int32, device="cuda")))
+    statuses = []
+    for step in range(4):
+        kn, vn = T.gen_append_tokens(tr, step)
+        seen = []
+        for s_ in states:
+            api.pkv_append_plan(shape, s_["cfg"], s_["ws"], dev(kn), dev(vn), s_["bt"], s_["sl"],
+                                s_["k"], s_["v"], s_["free"], s_["cnt"])
+            st, _ = api.pkv_get_error(s_["ws"])
+            seen.append((st, s_["bt"].cpu().numpy(), s_["sl"].cpu().numpy(), int(s_["cnt"].item())))
+        a, b = seen
+        assert a[0] == b[0], f"step {step}: status {a[0]} vs {b[0]}"
+        assert np.array_equal(a[1], b[1]), f"step {step}: block tables differ"
+        assert np.array_equal(a[2], b[2]), f"step {step}: lengths differ"
+        assert a[3] == b[3], f"step {step}: free counts differ"
+        assert torch.equal(states[0]["k"], states[1]["k"]) and torch.equal(states[0]["v"], states[1]["v"])
+        statuses.append(a[0])
+    assert int(states[0]["cnt"].item()) == 0
+    assert statuses == [_lib.PKV_EDEVICE] * 4  # the exhausted list is reported every step
+    # rows that got a page advanced; the others kept their length
+    grew = states[1]["sl"].cpu().numpy() - np.asarray(lens0)
+    assert grew.max() == 4 and grew.min() < 4
 
 
 @pytest.mark.parametrize("path,alloc", [(_lib.PKV_PATH_WORKQUEUE, True),

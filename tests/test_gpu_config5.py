@@ -42,8 +42,11 @@ def row_oracle(tr, q_step, kc, vc, bt, seq_lens, rows):
     return o, lse
 
 
-@pytest.mark.parametrize("per_graph", [1, 8])
-def test_uniform_b64_decode_loop_matches_oracle(per_graph):
+@pytest.mark.parametrize("per_graph,plan", [(1, _lib.PKV_PLAN_SEPARATE), (8, _lib.PKV_PLAN_SEPARATE),
+                                           (8, _lib.PKV_PLAN_IN_DECODE)])
+def test_uniform_b64_decode_loop_matches_oracle(per_graph, plan):
+    """plan = IN_DECODE is the benchmark's step: the append launch only appends
+    and allocates (one CTA per row) and the decode builds the plan itself."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     tr = T.make_trace(5)
@@ -55,7 +58,7 @@ def test_uniform_b64_decode_loop_matches_oracle(per_graph):
     free = dev(free_np)
     cnt = torch.tensor([free_np.size], dtype=torch.int32, device="cuda")
     shape = shape_of(tr)
-    cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, tr.split_tokens)
+    cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, tr.split_tokens, plan=plan)
     ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
     part = torch.empty(api.pkv_partials_size(shape, cfg) // 4, dtype=torch.float32, device="cuda")
     S = per_graph
