@@ -13,8 +13,10 @@
 //   g = (k - Hkv*offsets[i]) / n_i, j = ... % n_i -- the lexicographic
 //   (row, kv-head, split) order.  The host never reads T back.
 // A second copy of the same records, in balance order (every full-length
-// split first, then each row's shorter last split), is what the decode
-// kernel's CTAs stride over: the launch then ends on short tasks.
+// split first, by row, split and kv head, then each row's shorter last
+// split), is what the decode kernel's CTAs claim from: the launch ends on
+// short tasks, and the kv heads of one split, claimed together, read the same
+// pages at about the same time.
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
 
@@ -245,13 +247,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
                 const int g = kk / ni, j = kk - g * ni;
                 const int4 rec = make_int4(base + lo, g, j, (oi + j) * p.Hq + g * p.G);
                 p.tasks[k] = rec;
-                // balance order: shorter splits before this task = Hkv * (rows
-                // before with one) + g * (this row has one)
+                // balance order: a shorter split goes after every full one, by
+                // row then kv head; a full split j of row i sits at
+                // Hkv * (full splits before row i + j) + g
                 const int sb = s_sb[lo];
                 const int has_short = s_sb[lo + 1] - sb;
                 const bool is_short = has_short && j == ni - 1;
                 const int64_t pos = is_short ? n_full + (int64_t)sb * p.Hkv + g
-                                             : k - ((int64_t)sb * p.Hkv + (int64_t)g * has_short);
+                                             : ((int64_t)(oi - sb) + j) * p.Hkv + g;
                 p.tasks_ordered[pos] = rec;
             }
         }

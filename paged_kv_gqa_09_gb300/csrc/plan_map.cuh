@@ -8,8 +8,11 @@
 // exclusive prefix sums of f and r over the rows.  The task list in
 // lexicographic (row, kv head, split) order is the contract; the decode's CTAs
 // consume the same records in balance order:
-//   positions [0, Hkv*F_B)         every full split, lexicographic
-//                                  (row i owns Hkv*f_i of them, kv head major);
+//   positions [0, Hkv*F_B)         every full split by (row, split, kv head):
+//                                  row i owns Hkv*f_i of them, and the Hkv
+//                                  heads of one split sit side by side, so
+//                                  CTAs that claim them together read the
+//                                  same pages at about the same time;
 //   positions [Hkv*F_B, Hkv*(F_B+R_B))  each shorter last split, by row, then
 //                                  kv head.
 // Both lists are the plan kernel's output; the self-planning decode rebuilds
@@ -48,10 +51,9 @@ __host__ __device__ inline int4 plan_task_at(int t, const int *F, const int *R, 
     int i, g, j;
     if (t < n_full) {
         i = plan_last_row_at_or_below(F, B, Hkv, t);
-        const int f = F[i + 1] - F[i];
         const int kk = t - Hkv * F[i];
-        g = kk / f;
-        j = kk - g * f;
+        j = kk / Hkv;
+        g = kk - j * Hkv;
     } else {
         const int u = t - n_full;
         const int q = u / Hkv;

@@ -66,12 +66,17 @@ def test_plan_matches_oracle_bit_exact(lens, C):
     assert h[0] == 0 and h[6] == 0
     check_error_free(ws)
     # the decode walks a balance-ordered copy: the same records, every
-    # full-length split first, then the rows' shorter last splits, each group
-    # in canonical order
+    # full-length split first by (row, split, kv head), then the rows' shorter
+    # last splits in canonical order
     lens = np.asarray(lens)
     n = -(-lens // C)
-    short = [(lens[r[0]] % C != 0) and r[2] == n[r[0]] - 1 for r in want]
-    expect = np.concatenate([want[[not x for x in short]], want[short]]) if count else want
+    short = np.array([(lens[r[0]] % C != 0) and r[2] == n[r[0]] - 1 for r in want], dtype=bool)
+    if count:
+        full = want[~short]
+        full = full[np.lexsort((full[:, 1], full[:, 2], full[:, 0]))]
+        expect = np.concatenate([full, want[short]])
+    else:
+        expect = want
     assert np.array_equal(ordered, expect)
 
 

@@ -36,12 +36,17 @@ def _lib_loaded():
 
 
 def expected_order(want, lens, C):
-    """The balance order: every full-length split, then each row's shorter
-    last split, both in canonical order."""
+    """The balance order: every full-length split by (row, split, kv head) --
+    the kv heads of one split side by side -- then each row's shorter last
+    split in canonical order."""
     lens = np.asarray(lens)
     n = -(-lens // C)
     short = np.array([(lens[r[0]] % C != 0) and r[2] == n[r[0]] - 1 for r in want], dtype=bool)
-    return np.concatenate([want[~short], want[short]]) if len(want) else want
+    if not len(want):
+        return want
+    full = want[~short]
+    full = full[np.lexsort((full[:, 1], full[:, 2], full[:, 0]))]
+    return np.concatenate([full, want[short]])
 
 
 def check_plan(ws, tr, C):

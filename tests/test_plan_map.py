@@ -3,6 +3,7 @@
 "PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM Serving on
 Commodity GPUs", technical summary, Methodology 1, "Compact workqueue": the
 decode's CTAs take the plan's tasks in balance order (every full-length split,
+by row, then split, then kv head -- the kv heads of one split side by side --
 then each row's shorter last split).  When the decode builds the plan itself it
 maps a position t to its task from two per-row prefix sums (plan_map.cuh, a
 host-and-device function).  Here that map, compiled for the host, is compared
@@ -44,7 +45,10 @@ def check(L, lens, C, Hkv, G):
     T = canon.shape[0]
     n = -(-lens.astype(np.int64) // C)
     short = np.array([(lens[r[0]] % C != 0) and r[2] == n[r[0]] - 1 for r in canon], dtype=bool)
-    order = np.concatenate([np.flatnonzero(~short), np.flatnonzero(short)]).astype(np.int64)
+    full = np.flatnonzero(~short)
+    # full splits by (row, split, kv head); the shorter ones in canonical order
+    full = full[np.lexsort((canon[full, 1], canon[full, 2], canon[full, 0]))]
+    order = np.concatenate([full, np.flatnonzero(short)]).astype(np.int64)
     F = np.concatenate([[0], np.cumsum(lens // C)]).astype(np.int32)
     R = np.concatenate([[0], np.cumsum(lens % C != 0)]).astype(np.int32)
     rec = np.zeros((max(T, 1), 4), np.int32)
