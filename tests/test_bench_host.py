@@ -22,7 +22,7 @@ def test_committed_traffic_summaries_are_readable():
     import os
     h = bench.decode_source_hash()
     assert re.fullmatch(r"[0-9a-f]{16}", h)
-    for cfg in (2, 3):
+    for cfg in (2, 3, 5):
         txt = open(os.path.join(bench.ROOT, "profiles", f"decode_config{cfg}_traffic.md")).read()
         sha = re.search(r"kernel_source_sha:\s*([0-9a-f]{16})", txt)
         tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)

@@ -368,6 +368,75 @@ def test_launch_counts_match_model(path, expect):
 
 # ------------------------------------------------------------------ device-side checks
 
+@pytest.mark.parametrize("path", [BUCKETED, WORKQUEUE])
+def test_state_traffic_is_what_the_kernels_write_and_read(path):
+    """The merge-state counts of the step model (behind the pages' merge-state
+    traffic comparison, Results, 'Scheduling overhead') against the kernels
+    themselves.  Written: every slot the split decode changes in a buffer
+    filled with a marker.  Read: with every slot outside the counted set
+    replaced by a state that would ruin any merge using it (l = 1, m = 0,
+    acc = NaN) the merge is bit-identical; replacing the counted slots of
+    split j ruins exactly the rows that have a split j."""
+    lens = [100, 3000, 40, 0, 1024, 2049]
+    Hq, Hkv, d, C = 8, 2, 64, 256
+    tr, q, k, v = case(lens, Hq, Hkv, d, 16, C)
+    dd = upload(tr, q, k, v)
+    shape = shape_of(tr)
+    S_b = -(-max(lens) // C)
+    cfg = api.make_cfg(path, C, max(lens) if path == BUCKETED else 0)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    npart = api.pkv_partials_size(shape, cfg) // 4
+    slots = npart // (d + 2)
+    part = torch.full((npart,), 1234.5, dtype=torch.float32, device="cuda")
+    if path == WORKQUEUE:
+        api.pkv_plan(shape, cfg, dd["sl"], ws)
+    api.pkv_decode(shape, cfg, ws, dd["q"], dd["k"], dd["v"], dd["bt"], dd["sl"], part)
+    torch.cuda.synchronize()
+    check_error_free(ws)
+    acc = part[:slots * d].view(slots, d)
+    m, l = part[slots * d:slots * (d + 1)], part[slots * (d + 1):]
+    written = int(((l != 1234.5) | (m != 1234.5)).sum())
+    model = api.pkv_step_model(path, shape, C, max(lens), lens)
+    assert written == model["states_written"] == oracle.counters(
+        path, lens, Hq, Hkv, d, C, S_b).states_written
+    n = [-(-x // C) for x in lens]
+    off = np.concatenate([[0], np.cumsum(n)])
+    split_slots = {}  # split j -> the counted slots of every row's split j
+    for i, ni in enumerate(n):
+        for j in range(ni):
+            base = (i * S_b + j) * Hq if path == BUCKETED else (off[i] + j) * Hq
+            split_slots.setdefault(j, []).extend(range(base, base + Hq))
+    counted = sorted(s_ for v_ in split_slots.values() for s_ in v_)
+    assert len(counted) == model["states_read"] == oracle.counters(
+        path, lens, Hq, Hkv, d, C, S_b).states_read
+    o0 = torch.empty((tr.B, Hq, d), dtype=torch.float16, device="cuda")
+    api.pkv_merge(shape, cfg, ws, dd["sl"], part, o0)
+    clean = part.clone()
+
+    def ruin(idx):
+        t = clean.clone()
+        ix = torch.tensor(idx, dtype=torch.long, device="cuda")
+        t[slots * d:slots * (d + 1)][ix] = 0.0
+        t[slots * (d + 1):][ix] = 1.0
+        t[:slots * d].view(slots, d)[ix] = float("nan")
+        o = torch.empty_like(o0)
+        api.pkv_merge(shape, cfg, ws, dd["sl"], t, o)
+        torch.cuda.synchronize()
+        return o.float().cpu().numpy()
+
+    others = sorted(set(range(slots)) - set(counted))
+    if others:
+        assert np.array_equal(ruin(others), o0.float().cpu().numpy(), equal_nan=True)
+    base_o = o0.float().cpu().numpy()
+    for j, idx in split_slots.items():
+        got = ruin(idx)
+        for i, ni in enumerate(n):
+            if ni > j:
+                assert np.isnan(got[i]).all(), (j, i)
+            else:
+                assert np.array_equal(got[i], base_o[i]), (j, i)
+
+
 def test_bad_page_id_is_reported_not_faulted():
     tr, q, k, v = case([100, 50], Hq=8, Hkv=2, C=64)
     tr.block_table[1, 2] = tr.num_pages + 7     # out of range

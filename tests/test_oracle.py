@@ -354,20 +354,38 @@ def test_launch_counts_reproduce_the_pages_bimodal_figures():
     assert wq.attn_launches == gold["compact_workqueue_launches_per_step"]
 
 
-def test_merge_state_traffic_reproduces_the_pages_bimodal_figure():
-    """The same Results bullet prints a merge-state traffic reduction of about
-    37% for the compact workqueue; under the reading in the golden file (state
-    bytes written by the split kernel plus read by the merge, the rectangular
-    grid as the baseline) the counter model must land within that figure's
-    rounding on the B=8 bimodal trace."""
-    gold = json.load(open(os.path.join(GOLDEN, "launch_counts.json")))
-    tr = T.make_trace(3)
-    C = 1024
-    S_b = -(-int(tr.n_max) // C)
-    wq = oracle.counters(oracle.PATH_WORKQUEUE, tr.seq_lens, tr.Hq, tr.Hkv, tr.d, C)
-    rect = oracle.counters(oracle.PATH_BUCKETED, tr.seq_lens, tr.Hq, tr.Hkv, tr.d, C, S_b)
-    reduction = 1.0 - wq.merge_state_bytes / rect.merge_state_bytes
-    assert abs(reduction - gold["merge_state_traffic_reduction"]) <= 0.005, reduction
+def _state_traffic_enumerated(lens, Hq, Hkv, C, S_b):
+    """States written by the split step and read by the merge, enumerated from
+    the plans' records rather than from the counter model's sums: the
+    rectangular grid writes one state per query head of every cell (an empty
+    cell gets the neutral state) and the merge reads the cells a row's length
+    reaches; the compact queue lists only those cells."""
+    G = Hq // Hkv
+    rect, empty = oracle.plan_rect(lens, Hq, Hkv, C, S_b)
+    comp, _ = oracle.plan_compact(lens, Hq, Hkv, C)
+    return {"rect": (len(rect) * G, int((empty == 0).sum()) * G),
+            "compact": (len(comp) * G, len(comp) * G)}
+
+
+@pytest.mark.parametrize("seed", [T.HELDOUT_SEED, T.CALIBRATION_SEED, 1, 2])
+def test_merge_state_counts_match_the_enumerated_plans(seed):
+    """The counter model behind the pages' merge-state traffic comparison
+    (Results, 'Scheduling overhead') against the plans' records, on the B=8
+    bimodal batch of several draws and on edge cases (empty rows, a length at
+    a split boundary, one split)."""
+    cases = [(T.make_trace(3, seed=seed).seq_lens, 32, 8, 1024)]
+    if seed == T.HELDOUT_SEED:
+        cases += [([100, 3000, 40, 0, 1024, 2049], 8, 2, 256), ([0, 0, 5], 8, 8, 16),
+                  ([256], 4, 1, 256)]
+    for lens, Hq, Hkv, C in cases:
+        S_b = max(1, -(-int(np.max(lens)) // C))
+        got = _state_traffic_enumerated(lens, Hq, Hkv, C, S_b)
+        r = oracle.counters(oracle.PATH_BUCKETED, lens, Hq, Hkv, 128, C, S_b)
+        w = oracle.counters(oracle.PATH_WORKQUEUE, lens, Hq, Hkv, 128, C)
+        assert (r.states_written, r.states_read) == got["rect"]
+        assert (w.states_written, w.states_read) == got["compact"]
+        for c in (r, w):
+            assert c.merge_state_bytes == (c.states_written + c.states_read) * (128 + 2) * 4
 
 
 def test_counters_closed_forms():
