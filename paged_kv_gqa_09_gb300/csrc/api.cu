@@ -783,7 +783,9 @@ int pkv_append(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *
 // 224 traces (bucketed, bimodal, uniform, Zipf; B 1..64; N_max 256..32768;
 // Hq=32, Hkv=8, d=128, P=16) drawn with the calibration seed 20260622, timed as
 // synchronized wall-clock per step (the workqueue with its plan built inside the
-// decode); held-out seed 20260623 mean regret 1.046 (worst 1.21x).
+// decode; refitted after its full splits came to be claimed kv heads side by
+// side, with the same result); held-out seed 20260623 mean regret 1.046 (worst
+// 1.21x).
 void pkv_policy_default(pkv_policy_cfg_t *c)
 {
     if (!c)
@@ -825,19 +827,19 @@ int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t
 
 // Routes and weights fitted by paged_kv_gqa_09_gb300/calibrate.py (least
 // squares of log step time, calibration seed 20260622, 224 GB300 traces, the
-// workqueue with its plan built inside the decode); held-out seed 20260623 mean
-// regret 1.026 (worst 1.21x).
+// workqueue with its plan built inside the decode and its full splits claimed
+// kv heads side by side); held-out seed 20260623 mean regret 1.026 (worst 1.20x).
 static const pkv_cost_route_t kGb300Routes[] = {
-    {0, 128, {6.30381386f, 0.146490208f, 0.0766507722f, -0.817804401f, 0.00221713447f, 0.00773811571f, 0.005210673f, 0.344296909f, -0.0570552701f, 0.032716484f}},
-    {0, 256, {6.80283592f, 0.0684275072f, 0.0648224914f, -0.839746221f, 0.00700632318f, 0.00431572125f, 0.00229686144f, 0.258659391f, -0.0598971814f, 0.0350487925f}},
-    {0, 512, {6.81804098f, -0.0406811549f, 0.0664215198f, -0.803152733f, 0.0137774587f, 0.00563256323f, 0.000659806355f, 0.207581675f, -0.04293712f, 0.0338510971f}},
-    {0, 1024, {6.40653584f, -0.166238885f, 0.116008665f, -0.731888572f, 0.0191883576f, 0.00827006613f, -0.00325081398f, 0.0964632869f, -0.0286775284f, 0.0319785319f}},
-    {0, 2048, {5.2492311f, -0.202409639f, 0.333875118f, -0.719615545f, 0.0174190081f, 0.0127817358f, -0.0118381823f, 0.0226557524f, -0.011753664f, 0.0312219853f}},
-    {1, 256, {7.32420448f, 0.112937442f, 0.023359348f, -0.869745583f, -0.00706408591f, 7.99227637e-05f, 0.00136712949f, 0.0523260483f, -0.0168115665f, 0.0396993464f}},
-    {1, 512, {7.12917364f, 0.136180101f, 0.153859026f, -0.935766956f, -0.00738813911f, -0.00292030006f, -0.00495750755f, 0.0771535752f, -0.0287264073f, 0.0420219287f}},
-    {1, 1024, {6.05268677f, 0.154866756f, 0.430157638f, -0.992877683f, -0.00919112845f, -0.00266958781f, -0.0163468768f, 0.0599483139f, -0.0263472104f, 0.0435006428f}},
-    {1, 2048, {4.38967457f, 0.207614697f, 0.802688683f, -1.0557703f, -0.0152409556f, -0.00017741742f, -0.029851963f, 0.0251214756f, -0.0119293571f, 0.0444260996f}},
-    {2, 1024, {5.96752215f, -0.106514951f, -0.280153379f, -0.420131456f, -0.00988210887f, 0.0331434419f, 0.0320161238f, -0.345054899f, 0.147479276f, 0.0150444364f}},
+    {0, 128, {6.37893382f, 0.170615139f, 0.10530812f, -0.858705666f, 0.000193721028f, 0.00764236856f, 0.00430371841f, 0.339969458f, -0.0583645925f, 0.0342088869f}},
+    {0, 256, {6.91803431f, 0.086364198f, 0.0838334308f, -0.877535704f, 0.0055556387f, 0.00455079629f, 0.00182357596f, 0.261572754f, -0.0602490915f, 0.036329164f}},
+    {0, 512, {6.95596685f, -0.0414725812f, 0.0685039831f, -0.824151421f, 0.0133199074f, 0.00596759028f, 0.000691617587f, 0.189865697f, -0.0382477556f, 0.0346018921f}},
+    {0, 1024, {6.39920834f, -0.146957372f, 0.140989561f, -0.757397335f, 0.0178196747f, 0.00809220292f, -0.00402061834f, 0.10288432f, -0.0276012258f, 0.0328447786f}},
+    {0, 2048, {5.29898522f, -0.168081875f, 0.348305975f, -0.748684542f, 0.0155538531f, 0.01174969f, -0.0120188905f, 0.0451341569f, -0.0128900628f, 0.0321279087f}},
+    {1, 256, {7.38087955f, 0.155318192f, 0.066164181f, -0.923406785f, -0.00986350743f, 0.000321624704f, 0.000410297829f, 0.0641619519f, -0.0144386881f, 0.0411520044f}},
+    {1, 512, {7.14670578f, 0.15409992f, 0.166507884f, -0.950205657f, -0.00890024271f, -0.00217965337f, -0.00531239341f, 0.0749956238f, -0.0325700657f, 0.0424897811f}},
+    {1, 1024, {6.09056068f, 0.148111501f, 0.419567256f, -0.9843811f, -0.00952862822f, -0.00167480935f, -0.0162033182f, 0.0394223106f, -0.0281193987f, 0.0434735812f}},
+    {1, 2048, {4.44974918f, 0.188729173f, 0.78447106f, -1.04063316f, -0.0151122813f, 0.00165503706f, -0.0294351031f, -0.0110330845f, -0.00936690114f, 0.0441417604f}},
+    {2, 1024, {6.03505548f, -0.10174207f, -0.27518526f, -0.430179728f, -0.0103144304f, 0.0329394824f, 0.0316009504f, -0.351783337f, 0.147098237f, 0.0155151357f}},
 };
 
 void pkv_cost_model_default(pkv_cost_model_t *m)

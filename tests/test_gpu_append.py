@@ -123,7 +123,8 @@ def test_fused_append_reports_an_empty_free_list(plan):
     assert btd.cpu().numpy()[0, 1] == free[len(free) - 1]
 
 
-def test_row_parallel_append_matches_the_plan_kernels_append():
+@pytest.mark.parametrize("page,dd,hkv", [(P, D, HKV), (8, 64, 8), (64, 128, 1), (256, 64, 4)])
+def test_row_parallel_append_matches_the_plan_kernels_append(page, dd, hkv):
     """The append launch that leaves the plan to the decode (one CTA per row,
     each counting the rows before it that need a page) against the plan
     kernel's fused append (one CTA, a block scan), on two copies of the same
@@ -131,9 +132,12 @@ def test_row_parallel_append_matches_the_plan_kernels_append():
     pages that runs out at the first step (rows left without a page keep
     asking).  Every step must leave the same block table, lengths, free count,
     error status and cache contents."""
-    rng = np.random.default_rng([T.HELDOUT_SEED, 702])
-    lens0 = (rng.integers(0, 40, 300) * P + rng.integers(0, 3, 300) * (rng.random(300) < 0.3)).tolist()
-    tr = T.custom_trace(lens0, HQ, HKV, D, P, C, extra_pages=160, extra_cols=2, tag=703)
+    rng = np.random.default_rng([T.HELDOUT_SEED, 702, page])
+    nmax = 40 if page <= 16 else 6
+    lens0 = (rng.integers(0, nmax, 300) * page
+             + rng.integers(0, 3, 300) * (rng.random(300) < 0.3)).tolist()
+    tr = T.custom_trace(lens0, hkv * 2, hkv, dd, page, max(C, page), extra_pages=160, extra_cols=2,
+                        tag=703)
     k, v = T.gen_kv(tr)
     used = set(tr.block_table[tr.block_table >= 0].tolist())
     free = np.array([x for x in rng.permutation(tr.num_pages) if int(x) not in used], np.int32)
@@ -141,7 +145,7 @@ def test_row_parallel_append_matches_the_plan_kernels_append():
     shape = shape_of(tr)
     states = []
     for plan in (_lib.PKV_PLAN_SEPARATE, _lib.PKV_PLAN_IN_DECODE):
-        cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, C, plan=plan)
+        cfg = api.make_cfg(_lib.PKV_PATH_WORKQUEUE, max(C, page), plan=plan)
         ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
         states.append(dict(cfg=cfg, ws=ws, k=dev(k), v=dev(v), bt=dev(tr.block_table),
                            sl=dev(tr.seq_lens), free=dev(free),
