@@ -220,8 +220,11 @@ int pkv_decode_step(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d
  * device: copies h_q into d_q (and, when non-NULL, h_block_table into
  * d_block_table and h_seq_lens into d_seq_lens) on `stream`, runs
  * pkv_decode_step, copies d_o into h_o (and d_lse into h_lse when both are
- * non-NULL), then synchronizes `stream`.  One cudaMemcpyAsync per buffer; host
- * buffers should be page-locked for the copies to run asynchronously.  All
+ * non-NULL), then synchronizes `stream`.  One cudaMemcpyAsync per buffer --
+ * except that a page-locked (pinned or registered), 16-byte aligned h_o
+ * (h_lse) is written straight by the step's last kernel, and d_o (d_lse) is
+ * then not written.  Host input buffers should be page-locked for their copies
+ * to run asynchronously.  All
  * arguments are checked before anything is enqueued.  Same path semantics,
  * layouts and errors as pkv_decode_step. */
 int pkv_decode_step_host(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
@@ -238,16 +241,22 @@ int pkv_decode_step_host(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, vo
  * loop around it, whose wall clock the pages' evaluation protocol,
  * Methodology 3, counts with the host's share.)  In order, on `stream`:
  *   1. copies h_q [B][Hq][d] into d_q and the new token's h_k_new, h_v_new
- *      [B][Hkv][d] (fp16) into d_k_new, d_v_new -- one cudaMemcpyAsync each;
+ *      [B][Hkv][d] (fp16) into d_k_new, d_v_new -- one cudaMemcpyAsync each,
+ *      except that when h_k_new and h_v_new are both page-locked (pinned or
+ *      registered) and 16-byte aligned the append reads them in place and
+ *      d_k_new, d_v_new are not written;
  *   2. WORKQUEUE: pkv_append_plan (appends, allocates pages from the device
  *      free list when d_free_pages != NULL, and plans unless the decode will),
  *      then pkv_decode + pkv_merge (pkv_decode_merge with PKV_MERGE_FUSED),
  *      all with `cfg`; other paths: pkv_append, then pkv_decode_step;
- *   3. copies d_o into h_o (and d_lse into h_lse when both are non-NULL);
+ *   3. copies d_o into h_o (and d_lse into h_lse when both are non-NULL) --
+ *      except that a page-locked, 16-byte aligned h_o (h_lse) is written
+ *      straight by the step's last kernel and d_o (d_lse) is then not written;
  *   4. synchronizes `stream`.
  * After the call every row has one more token and o / lse are those of the
- * advanced lengths.  Host buffers should be page-locked for the copies to be
- * asynchronous.  d_free_pages / d_free_count go together and only with the
+ * advanced lengths.  Page-locked host buffers save the copies above; pageable
+ * ones work too (their copies are then synchronous with the host).  The device
+ * buffers d_q, d_k_new, d_v_new and d_o are always required.  d_free_pages / d_free_count go together and only with the
  * WORKQUEUE path.  All arguments are checked before anything is enqueued;
  * device-side results (a row without room, an exhausted free list, a bad page
  * id) land in the error word as for those calls (read with pkv_get_error). */

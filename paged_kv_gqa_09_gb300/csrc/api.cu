@@ -639,6 +639,25 @@ int pkv_decode_step(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, c
     return pkv_merge(s, c, d_ws, sl, part, o, lse, stream);
 }
 
+namespace {
+
+// The current device's address of a page-locked host buffer that kernels may
+// read or write in place over the host link, or nullptr when `h` is pageable,
+// not 16-byte aligned or not mapped for the device.
+void *mapped_host(const void *h)
+{
+    if (!h || !aligned16(h))
+        return nullptr;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer: not an error of this call
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+}  // namespace
+
 int pkv_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, float *part,
                          const void *h_q, void *d_q, const int32_t *h_bt, int32_t *d_bt,
                          const int32_t *h_sl, int32_t *d_sl, const void *k, const void *v, void *d_o,
@@ -669,9 +688,19 @@ int pkv_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_
         e = cudaMemcpyAsync(d_sl, h_sl, (size_t)s->B * 4, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "host-to-device copy");
-    PKV_TRY(pkv_decode_step(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, d_o, d_lse, stream));
-    e = cudaMemcpyAsync(h_o, d_o, qbytes, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && h_lse && d_lse)
+    // o / lse are written once: page-locked host buffers take them in place
+    void *o_out = mapped_host(h_o);
+    float *lse_out = static_cast<float *>(h_lse ? mapped_host(h_lse) : nullptr);
+    const bool copy_o = o_out == nullptr, copy_lse = h_lse && d_lse && lse_out == nullptr;
+    if (copy_o)
+        o_out = d_o;
+    if (!lse_out)
+        lse_out = d_lse;
+    PKV_TRY(pkv_decode_step(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, o_out, lse_out, stream));
+    e = cudaSuccess;
+    if (copy_o)
+        e = cudaMemcpyAsync(h_o, d_o, qbytes, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && copy_lse)
         e = cudaMemcpyAsync(h_lse, d_lse, (size_t)s->B * s->Hq * 4, cudaMemcpyDeviceToHost, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "device-to-host copy");
@@ -721,30 +750,50 @@ int pkv_append_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, v
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t qbytes = (size_t)s->B * s->Hq * s->d * 2;
     const size_t nbytes = (size_t)s->B * s->Hkv * s->d * 2;
+    // q is re-read by every split of every kv head: always copied.  The new
+    // token is read once and o / lse written once: page-locked buffers are used
+    // in place, pageable ones go through the device buffers.
+    const void *kn = mapped_host(h_k_new), *vn = mapped_host(h_v_new);
+    if (!kn || !vn)
+        kn = vn = nullptr;
+    void *o_out = mapped_host(h_o);
+    float *lse_out = static_cast<float *>(h_lse ? mapped_host(h_lse) : nullptr);
+    const bool copy_o = o_out == nullptr, copy_lse = h_lse && d_lse && lse_out == nullptr;
+    if (copy_o)
+        o_out = d_o;
+    if (!lse_out)
+        lse_out = d_lse;
     cudaError_t e = cudaMemcpyAsync(d_q, h_q, qbytes, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !kn)
         e = cudaMemcpyAsync(d_k_new, h_k_new, nbytes, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !vn)
         e = cudaMemcpyAsync(d_v_new, h_v_new, nbytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "host-to-device copy");
+    if (!kn) {
+        kn = d_k_new;
+        vn = d_v_new;
+    }
     if (c->path == PKV_PATH_WORKQUEUE) {
         // the append launch allocates pages and, unless the decode plans, plans
-        PKV_TRY(pkv_append_plan(s, c, d_ws, d_k_new, d_v_new, d_bt, d_sl, free_pages, free_count,
-                                k, v, stream));
+        PKV_TRY(pkv_append_plan(s, c, d_ws, kn, vn, d_bt, d_sl, free_pages, free_count, k, v,
+                                stream));
         // the decode then plans for itself, or reads the plan the append built
         if (c->merge == PKV_MERGE_FUSED) {
-            PKV_TRY(pkv_decode_merge(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, d_o, d_lse, stream));
+            PKV_TRY(pkv_decode_merge(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, o_out, lse_out,
+                                     stream));
         } else {
             PKV_TRY(pkv_decode(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, stream));
-            PKV_TRY(pkv_merge(s, c, d_ws, d_sl, part, d_o, d_lse, stream));
+            PKV_TRY(pkv_merge(s, c, d_ws, d_sl, part, o_out, lse_out, stream));
         }
     } else {
-        PKV_TRY(pkv_append(s, d_ws, d_k_new, d_v_new, d_bt, d_sl, k, v, stream));
-        PKV_TRY(pkv_decode_step(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, d_o, d_lse, stream));
+        PKV_TRY(pkv_append(s, d_ws, kn, vn, d_bt, d_sl, k, v, stream));
+        PKV_TRY(pkv_decode_step(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, o_out, lse_out, stream));
     }
-    e = cudaMemcpyAsync(h_o, d_o, qbytes, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && h_lse && d_lse)
+    e = cudaSuccess;
+    if (copy_o)
+        e = cudaMemcpyAsync(h_o, d_o, qbytes, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && copy_lse)
         e = cudaMemcpyAsync(h_lse, d_lse, (size_t)s->B * s->Hq * 4, cudaMemcpyDeviceToHost, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "device-to-host copy");

@@ -229,17 +229,22 @@ def test_host_loop_append_graph_matches_mirror(path, alloc):
             close_lse(lse, lref)
 
 
-@pytest.mark.parametrize("path,merge,alloc", [
-    (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_SEPARATE, True),
-    (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_FUSED, True),
-    (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_SEPARATE, False),
-    (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_MERGE_SEPARATE, False),
-    (_lib.PKV_PATH_SINGLE_PASS, _lib.PKV_MERGE_SEPARATE, False)])
-def test_append_decode_step_host_matches_mirror(path, merge, alloc):
+@pytest.mark.parametrize("path,merge,alloc,pinned", [
+    (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_SEPARATE, True, True),
+    (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_SEPARATE, True, False),
+    (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_FUSED, True, True),
+    (_lib.PKV_PATH_WORKQUEUE, _lib.PKV_MERGE_SEPARATE, False, True),
+    (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_MERGE_SEPARATE, False, True),
+    (_lib.PKV_PATH_BUCKETED_SPLIT, _lib.PKV_MERGE_SEPARATE, False, False),
+    (_lib.PKV_PATH_SINGLE_PASS, _lib.PKV_MERGE_SEPARATE, False, True)])
+def test_append_decode_step_host_matches_mirror(path, merge, alloc, pinned):
     """pkv_append_decode_step_host, one synchronized C call per step: q and
-    the new token come from pinned host memory, o / lse land in pinned host
-    memory, the block table and lengths advance on the device.  Checked
-    against the host mirror of the append rule and the oracle."""
+    the new token come from host memory, o / lse land in host memory, the
+    block table and lengths advance on the device.  With page-locked host
+    buffers the new token is read and o / lse written in place (the device
+    staging for them stays untouched); with pageable ones every buffer goes
+    through its device copy.  Checked against the host mirror of the append
+    rule and the oracle."""
     steps = 20
     tr, k, v, free = setup([15, 16, 40, 0, 33, 64, 1], steps, spare_pages=30)
     k_h, v_h = k.copy(), v.copy()
@@ -261,16 +266,17 @@ def test_append_decode_step_host_matches_mirror(path, merge, alloc):
     ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
     npart = api.pkv_partials_size(shape, cfg)
     part = torch.empty(max(npart // 4, 4), dtype=torch.float32, device="cuda") if npart else None
-    h_q = torch.empty((tr.B, HQ, D), dtype=torch.float16).pin_memory()
-    h_kn = torch.empty((tr.B, HKV, D), dtype=torch.float16).pin_memory()
-    h_vn = torch.empty_like(h_kn).pin_memory()
-    h_o = torch.full((tr.B, HQ, D), float("nan"), dtype=torch.float16).pin_memory()
-    h_lse = torch.full((tr.B, HQ), float("nan"), dtype=torch.float32).pin_memory()
+    host = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    h_q = host(torch.empty((tr.B, HQ, D), dtype=torch.float16))
+    h_kn = host(torch.empty((tr.B, HKV, D), dtype=torch.float16))
+    h_vn = host(torch.empty((tr.B, HKV, D), dtype=torch.float16))
+    h_o = host(torch.full((tr.B, HQ, D), float("nan"), dtype=torch.float16))
+    h_lse = host(torch.full((tr.B, HQ), float("nan"), dtype=torch.float32))
     d_q = torch.empty((tr.B, HQ, D), dtype=torch.float16, device="cuda")
-    d_kn = torch.empty((tr.B, HKV, D), dtype=torch.float16, device="cuda")
-    d_vn = torch.empty_like(d_kn)
-    d_o = torch.empty_like(d_q)
-    d_lse = torch.empty((tr.B, HQ), dtype=torch.float32, device="cuda")
+    d_kn = torch.full((tr.B, HKV, D), float("nan"), dtype=torch.float16, device="cuda")
+    d_vn = torch.full_like(d_kn, float("nan"))
+    d_o = torch.full_like(d_q, float("nan"))
+    d_lse = torch.full((tr.B, HQ), float("nan"), dtype=torch.float32, device="cuda")
     for step in range(steps):
         kn, vn = T.gen_append_tokens(tr, step)
         q = T.gen_step_q(tr, step)
@@ -295,6 +301,11 @@ def test_append_decode_step_host_matches_mirror(path, merge, alloc):
             oref, lref = oracle.attention(q, k_h, v_h, bt_h, lens_h.astype(np.int32), tr.scale)
             close(h_o, oref, f"o at step {step}")
             close_lse(h_lse, lref)
+            staged = [d_kn, d_vn, d_o, d_lse]
+            if pinned:  # used in place: the device staging was never written
+                assert all(torch.isnan(t.float()).all() for t in staged)
+            else:       # copied through it
+                assert torch.equal(d_o.cpu(), h_o) and torch.equal(d_kn.cpu(), h_kn)
 
 
 def test_append_decode_step_host_checks_before_enqueueing():

@@ -517,6 +517,39 @@ def test_host_buffer_step_matches_oracle(cfg_id, path):
     check_error_free(loop.ws)
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_step_outputs_in_place_or_copied(pinned):
+    """pkv_decode_step_host writes page-locked h_o / h_lse straight from the
+    step's last kernel (the device buffers stay untouched) and copies through
+    d_o / d_lse into pageable ones; both match the oracle."""
+    tr = T.make_trace(3)
+    q = T.gen_q(tr)
+    k, v = T.gen_kv(tr)
+    d = upload(tr, q, k, v)
+    shape = shape_of(tr)
+    cfg = api.make_cfg(WORKQUEUE, tr.split_tokens, 0, 0, 0, _lib.PKV_PLAN_IN_DECODE)
+    ws = torch.zeros(api.pkv_plan_workspace_size(shape, cfg), dtype=torch.uint8, device="cuda")
+    part = torch.empty(api.pkv_partials_size(shape, cfg) // 4, dtype=torch.float32, device="cuda")
+    host = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    hq = host(torch.from_numpy(q))
+    hbt = host(torch.from_numpy(tr.block_table))
+    hsl = host(torch.from_numpy(tr.seq_lens))
+    h_o = host(torch.full(q.shape, float("nan"), dtype=torch.float16))
+    h_lse = host(torch.full(q.shape[:2], float("nan"), dtype=torch.float32))
+    d_o = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
+    d_lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+    api.pkv_decode_step_host(shape, cfg, ws, part, hq, d["q"], hbt, d["bt"], hsl, d["sl"], d["k"],
+                             d["v"], d_o, h_o, d_lse, h_lse)
+    check_error_free(ws)
+    oref, lref = oracle_out(tr, q, k, v)
+    close(h_o, oref)
+    close_lse(h_lse, lref)
+    if pinned:
+        assert torch.isnan(d_o.float()).all() and torch.isnan(d_lse).all()
+    else:
+        assert torch.equal(d_o.cpu(), h_o) and torch.equal(d_lse.cpu(), h_lse)
+
+
 # ------------------------------------------------------------------ exact-length buckets
 
 def test_exact_length_buckets_match_oracle_and_launch_twice_per_length():
