@@ -3,7 +3,7 @@
 
 Default workload (N=1): B=64 uniform lengths U[128, 65536], Hq=64, Hkv=8
 (G=8), d=128, page_size 16, a shuffled pool sized to the total length, the
-compact workqueue with C=1024, and every step appending one token per row
+compact workqueue with C=4096, and every step appending one token per row
 (an append launch that allocates pages from a device free list, then the
 decode, which builds the workqueue's plan itself, and the merge) -- the largest workload that fits one
 GPU.  `--config 1..4` selects the smaller workloads (1: B=1 N=1024; 2: B=1
@@ -66,7 +66,7 @@ WORKLOADS = {
        "S=32 (C=1024), keys x0.5",
     3: "B=8 bimodal (4x U[512,2048], 4x U[24576,32768]) Hq=32 Hkv=8 d=128 P=16 C=1024 workqueue",
     4: "B=8 Zipf s=1.2 on [16,32768] Hq=32 Hkv=8 d=128 P=16, policy route",
-    5: "B=64 uniform U[128,65536] Hq=64 Hkv=8 d=128 P=16 C=1024 workqueue, +1 token/row/step",
+    5: "B=64 uniform U[128,65536] Hq=64 Hkv=8 d=128 P=16 C=4096 workqueue, +1 token/row/step",
 }
 
 
@@ -88,6 +88,8 @@ def parse():
                     help="workqueue without appends: the decode builds its own plan, or a plan kernel")
     ap.add_argument("--len-scale", type=float, default=1.0,
                     help="scale the lengths of the B=8 bimodal and B=64 uniform workloads")
+    ap.add_argument("--split-tokens", type=int, default=None,
+                    help="split size C on the split paths, instead of the workload's")
     return ap.parse_args()
 
 
@@ -380,6 +382,8 @@ def run_pkv(args, rank, local, ws, pg):
         path = forced
     if path != 2 and tr.path_hint != "policy":
         C = tr.split_tokens  # the workload fixes its split size (S splits)
+    if path != 2 and args.split_tokens:
+        C = args.split_tokens
     n_max_run = tr.n_max + (tr.steps if appends else 0)
     bucket = n_max_run if path == 0 else 0
     fused = args.merge == "fused" and path != 2

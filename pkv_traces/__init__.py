@@ -20,7 +20,9 @@ the five workloads this library is measured on:
      ~U[24576,32768] (row order shuffled); C=1024; pool = sum of pages, shuffled
   4  B=4 or 8, Hq=32 Hkv=8 d=128 P=16  truncated Zipf s=1.2 on [16,32768]
   5  B=64 Hq=64 Hkv=8 d=128 P=16  U[128,65536]; pool sum ceil((N+256)/P)
-     pages shuffled so 256 appended tokens per row fit; 256 decode steps
+     pages shuffled so 256 appended tokens per row fit; 256 decode steps; the
+     workload names no split size: C=4096 (the fastest measured on GB300,
+     where each split's fp32 partial state costs write traffic)
 
 Seeds: results use the held-out seed 20260623, policy thresholds the
 calibration seed 20260622 (technical summary, "Results", first paragraph).
@@ -170,7 +172,7 @@ def make_trace(cfg_id: int, seed: int = HELDOUT_SEED, B: Optional[int] = None,
     if cfg_id == 5:
         lens = scaled(rng.integers(128, 65536, size=64, endpoint=True).astype(np.int32))
         bt, pool = _scatter_pages(rng, [_pages(int(n) + 256, P) for n in lens])
-        return Trace("uniform-B64", 5, seed, 64, 64, 8, 128, P, 1024, pool, lens, bt,
+        return Trace("uniform-B64", 5, seed, 64, 64, 8, 128, P, 4096, pool, lens, bt,
                      steps=256, path_hint="workqueue")
     raise ValueError(f"unknown config {cfg_id}")
 
