@@ -8,7 +8,7 @@ import oracle
 import pkv_traces as T
 from paged_kv_gqa_09_gb300 import api, _lib
 
-# Spec tolerance for fp16 outputs against the float64 oracle, applied
+# Parity tolerance for fp16 outputs against the float64 oracle, applied
 # element-wise in allclose form: |x - y| <= ATOL + RTOL * |y|.
 ATOL, RTOL = 3e-3, 1e-2
 # lse (fp32): scores are exact fp16 products summed in fp32 and the exponent

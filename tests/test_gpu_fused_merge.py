@@ -4,7 +4,7 @@ the float64 oracle, and its bookkeeping.
 The fused step computes what pkv_decode + pkv_merge compute -- the exact
 log-sum-exp merge of "Sequence splitting" -- with the merge run on the decode's
 tail: the CTAs meet at a grid-wide barrier, then share out the (row, query
-head) merges.  Besides the outputs (spec tolerance
+head) merges.  Besides the outputs (the parity tolerance
 |x - y| <= 3e-3 + 1e-2 |y|), these tests check that the header's counters
 (task claims, barrier) are back at zero after every launch, also after a
 timeout, that rows without tokens and workqueue overflows give the merge

@@ -3,7 +3,7 @@
 Every case draws seeded inputs once on the host, runs the oracle on the CPU
 and the CUDA path on the GPU, and compares element by element: the task list
 and launch counts bit-exactly, neutral states bit-exactly, outputs within the
-spec tolerance |x - y| <= 3e-3 + 1e-2 |y|.
+stated tolerance |x - y| <= 3e-3 + 1e-2 |y|.
 """
 import numpy as np
 import pytest

@@ -93,8 +93,8 @@ def test_reference_arm_prints_one_contract_line(nproc):
     lines = _reference_lines(nproc)
     assert len(lines) == 1
     d = json.loads(lines[0])
-    metric = json.load(open(os.path.join(ROOT, "BASELINE.json")))["metric"]
-    assert d["impl"] == "reference" and d["metric"] == metric and d["unit"] == "GB/s"
+    import bench
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
     assert (d["n_gpus"], d["steps"], d["warmup"]) == (nproc, 2, 1)
     assert d["vs_baseline"] is None and d["data"] == "synthetic" and d["dtype"] == "f64"
