@@ -898,26 +898,30 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
                             p.lse[ob + h0 + 1] = (M1 + log2f(L1)) * kLn2;
                     }
                 } else {
+                    // the merge reads these states back soon: they are written to
+                    // stay in L2 ahead of the KV stream, whose write-back into
+                    // DRAM would interrupt the stream's reads
+                    const uint64_t keep = l2_evict_last_policy();
 #pragma unroll
                     for (int x = 0; x < KS; ++x) {
                         const int d0 = 16 * x + r0;
                         if (ok0) {
-                            p.part_acc[(size_t)(sb0 + h0) * D + d0] = O[x][0];
-                            p.part_acc[(size_t)(sb0 + h0) * D + d0 + 8] = O[x][2];
+                            st_global_hint(p.part_acc + (size_t)(sb0 + h0) * D + d0, O[x][0], keep);
+                            st_global_hint(p.part_acc + (size_t)(sb0 + h0) * D + d0 + 8, O[x][2], keep);
                         }
                         if (ok1) {
-                            p.part_acc[(size_t)(sb0 + h0 + 1) * D + d0] = O[x][1];
-                            p.part_acc[(size_t)(sb0 + h0 + 1) * D + d0 + 8] = O[x][3];
+                            st_global_hint(p.part_acc + (size_t)(sb0 + h0 + 1) * D + d0, O[x][1], keep);
+                            st_global_hint(p.part_acc + (size_t)(sb0 + h0 + 1) * D + d0 + 8, O[x][3], keep);
                         }
                     }
                     if (lane < 4) {
                         if (ok0) {
-                            p.part_m[sb0 + h0] = M0 * kLn2;
-                            p.part_l[sb0 + h0] = L0;
+                            st_global_hint(p.part_m + sb0 + h0, M0 * kLn2, keep);
+                            st_global_hint(p.part_l + sb0 + h0, L0, keep);
                         }
                         if (ok1) {
-                            p.part_m[sb0 + h0 + 1] = M1 * kLn2;
-                            p.part_l[sb0 + h0 + 1] = L1;
+                            st_global_hint(p.part_m + sb0 + h0 + 1, M1 * kLn2, keep);
+                            st_global_hint(p.part_l + sb0 + h0 + 1, L1, keep);
                         }
                     }
                 }

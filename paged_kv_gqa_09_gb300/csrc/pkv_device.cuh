@@ -176,6 +176,21 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy()
     return pol;
 }
 
+// L2 policy for data written now and read back soon (the split states the
+// merge reads): kept ahead of the evict-first KV stream.
+__device__ __forceinline__ uint64_t l2_evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Global store of one float with an L2 cache-eviction policy.
+__device__ __forceinline__ void st_global_hint(float *p, float v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
+}
+
 // 5-D tiled TMA load into shared memory, completing on `bar` (tx bytes).
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
                                             int c0, int c1, int c2, int c3, int c4,
