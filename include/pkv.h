@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define PKV_VERSION 1
+#define PKV_VERSION 2
 
 /* status codes */
 #define PKV_OK 0
@@ -356,14 +356,20 @@ int pkv_decode_step_noalloc(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg,
  * each split route has its own long-context cut-off:
  *   B <= bucketed_max_batch  and N_max >= bucketed_min_tokens  -> BUCKETED_SPLIT
  *   else B >= workqueue_min_batch and N_max >= workqueue_min_tokens -> WORKQUEUE
- *   else SINGLE_PASS. */
+ *   else SINGLE_PASS.
+ * The workqueue's split size grows with the batch, because every split writes
+ * a partial state: C starts at split_tokens and doubles while
+ * B * ceil(N_max / C) > workqueue_target_splits, up to
+ * workqueue_max_split_tokens (a target of 0 keeps C = split_tokens). */
 typedef struct {
     int32_t bucketed_min_tokens;   /* long-context cut-off of the bucketed route */
     int32_t bucketed_max_batch;    /* largest B routed to BUCKETED_SPLIT */
     int32_t workqueue_min_tokens;  /* long-context cut-off of the workqueue route */
     int32_t workqueue_min_batch;   /* smallest B routed to WORKQUEUE */
-    int32_t split_tokens;          /* C handed to WORKQUEUE */
+    int32_t split_tokens;          /* smallest C handed to WORKQUEUE */
     int32_t bucketed_split_tokens; /* C handed to BUCKETED_SPLIT */
+    int32_t workqueue_max_split_tokens; /* largest C handed to WORKQUEUE */
+    int32_t workqueue_target_splits;    /* (row, split) pairs the workqueue's C aims at */
 } pkv_policy_cfg_t;
 
 /* Fill `cfg` with the thresholds calibrated on GB300 (calibration seed

@@ -77,7 +77,9 @@ class PlanCfg(ctypes.Structure):
 class PolicyCfg(ctypes.Structure):
     _fields_ = [("bucketed_min_tokens", ctypes.c_int32), ("bucketed_max_batch", ctypes.c_int32),
                 ("workqueue_min_tokens", ctypes.c_int32), ("workqueue_min_batch", ctypes.c_int32),
-                ("split_tokens", ctypes.c_int32), ("bucketed_split_tokens", ctypes.c_int32)]
+                ("split_tokens", ctypes.c_int32), ("bucketed_split_tokens", ctypes.c_int32),
+                ("workqueue_max_split_tokens", ctypes.c_int32),
+                ("workqueue_target_splits", ctypes.c_int32)]
 
 
 COST_FEATURES = 10

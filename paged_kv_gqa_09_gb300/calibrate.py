@@ -8,14 +8,18 @@ choosing the route by batch size B and the longest context N_max) and Results
 
 Procedure:
 1. For every trace of a grid -- families bucketed / bimodal / uniform / Zipf,
-   B in {1..64}, N_max in {256..32768}, Hq=32, Hkv=8, d=128, page_size 16 --
+   B in {1..64}, N_max in {256..65536}, Hq=32, Hkv=8, d=128, page_size 16 --
    time every route (bucketed split and workqueue at several split sizes C,
    single pass) as synchronized wall-clock per decode step through the C ABI
    (host planning and launches included, as the pages measure; the workqueue
    with its plan built inside the decode, as PagedDecoder runs it).
 2. Search the policy parameters (two long-context cut-offs, two batch cut-offs,
-   one C per split route) minimising the mean ratio of the chosen route's time
-   to the best route's time over the calibration traces.
+   the bucketed split's C, and the workqueue's split rule: C doubles from a
+   smallest value until the batch holds at most a target number of (row, split)
+   pairs, up to a largest value) minimising the mean ratio of the chosen
+   route's time to the best route's time over the calibration traces.  The
+   workqueue's rule is fitted first, on the workqueue's own times, then the
+   cut-offs with it.
 3. Re-time the same grid drawn with the held-out seed and report the chosen
    policy's regret there.
 
@@ -37,13 +41,19 @@ import pkv_traces as T
 
 HQ, HKV, D, P = 32, 8, 128, 16
 BATCHES = [1, 2, 4, 8, 16, 32, 64]
-NMAX = [256, 512, 1024, 2048, 4096, 8192, 16384, 32768]
+NMAX = [256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536]
 FAMILIES = ["bucketed", "bimodal", "uniform", "zipf"]
 BUCKETED_C = [128, 256, 512, 1024, 2048]
-WORKQUEUE_C = [256, 512, 1024, 2048]
-TOKEN_CUTS = [0, 256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 1 << 30]
+WORKQUEUE_C = [256, 512, 1024, 2048, 4096]
+WQ_TARGETS = [0, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096]  # 0: C fixed at its smallest
+TOKEN_CUTS = [0, 256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 1 << 30]
 BATCH_CUTS_MAX = [0, 1, 2, 4, 8, 16, 32, 64]
 BATCH_CUTS_MIN = [1, 2, 4, 8, 16, 32, 64, 1 << 30]
+
+
+PARAM_NAMES = ["bucketed_min_tokens", "bucketed_max_batch", "workqueue_min_tokens",
+               "workqueue_min_batch", "split_tokens", "bucketed_split_tokens",
+               "workqueue_max_split_tokens", "workqueue_target_splits"]
 
 
 def lengths(family: str, B: int, n_max: int, rng: np.random.Generator) -> np.ndarray:
@@ -130,12 +140,23 @@ def measure(seed: int, reps: int = 7, warm: int = 2, log=print):
     return results
 
 
+def wq_split(B: int, n_max: int, c_min: int, c_max: int, target: int) -> int:
+    """The workqueue's split size: c_min doubled while the batch would hold more
+    than `target` (row, split) pairs (B * ceil(n_max / C), the longest row's
+    count for every row), up to c_max; target 0 keeps c_min.  The same rule is
+    written in C in pkv_policy (api.cu)."""
+    C = c_min
+    while target > 0 and C < c_max and B * -(-n_max // C) > target:
+        C *= 2
+    return C
+
+
 def choose(params, B, n_max):
-    bmin_tok, bmax_b, wmin_tok, wmin_b, c_wq, c_b = params
+    bmin_tok, bmax_b, wmin_tok, wmin_b, c_wq, c_b, c_wq_max, target = params
     if 1 <= B <= bmax_b and n_max >= bmin_tok:
         return f"bucketed:{c_b}"
     if B >= wmin_b and n_max >= wmin_tok:
-        return f"workqueue:{c_wq}"
+        return f"workqueue:{wq_split(B, n_max, c_wq, c_wq_max, target)}"
     return "single:0"
 
 
@@ -144,28 +165,46 @@ def regret(params, results):
     return float(np.mean(r)), float(np.max(r))
 
 
+def fit_wq_rule(results):
+    """(c_min, c_max, target) of the workqueue's split rule minimising the mean
+    ratio of the rule's workqueue time to the best workqueue time, over the
+    traces long enough for the workqueue to be a candidate (N_max >= 1024)."""
+    rows = [r for r in results if r["n_max"] >= 1024]
+    best_rule, best_score = None, math.inf
+    for c_min, c_max, target in itertools.product(WORKQUEUE_C, WORKQUEUE_C, WQ_TARGETS):
+        if c_max < c_min or (target == 0 and c_max != c_min):
+            continue
+        score = float(np.mean([
+            r["us"][f"workqueue:{wq_split(r['B'], r['n_max'], c_min, c_max, target)}"]
+            / min(r["us"][f"workqueue:{c}"] for c in WORKQUEUE_C) for r in rows]))
+        if score < best_score - 1e-12:
+            best_rule, best_score = (c_min, c_max, target), score
+    return best_rule
+
+
 def fit(results):
+    c_min, c_max, target = fit_wq_rule(results)
     names = [f"{n}:{c}" for n, c in routes()]
     tmat = np.array([[res["us"][k] for k in names] for res in results])
     best = tmat.min(axis=1)
     Bv = np.array([res["B"] for res in results])
     Nv = np.array([res["n_max"] for res in results])
     col = {k: i for i, k in enumerate(names)}
+    wq = np.array([res["us"][f"workqueue:{wq_split(res['B'], res['n_max'], c_min, c_max, target)}"]
+                   for res in results])
+    single = tmat[:, col["single:0"]]
     best_params, best_score = None, math.inf
     for bmin_tok, bmax_b, wmin_tok, wmin_b in itertools.product(TOKEN_CUTS, BATCH_CUTS_MAX,
                                                                 TOKEN_CUTS, BATCH_CUTS_MIN):
         is_b = (Bv >= 1) & (Bv <= bmax_b) & (Nv >= bmin_tok)
         is_w = ~is_b & (Bv >= wmin_b) & (Nv >= wmin_tok)
-        single = tmat[:, col["single:0"]]
-        for c_wq in WORKQUEUE_C:
-            wq = tmat[:, col[f"workqueue:{c_wq}"]]
-            for c_b in BUCKETED_C:
-                bk = tmat[:, col[f"bucketed:{c_b}"]]
-                chosen = np.where(is_b, bk, np.where(is_w, wq, single))
-                score = float(np.mean(chosen / best))
-                if score < best_score - 1e-12:
-                    best_score = score
-                    best_params = (bmin_tok, bmax_b, wmin_tok, wmin_b, c_wq, c_b)
+        for c_b in BUCKETED_C:
+            bk = tmat[:, col[f"bucketed:{c_b}"]]
+            chosen = np.where(is_b, bk, np.where(is_w, wq, single))
+            score = float(np.mean(chosen / best))
+            if score < best_score - 1e-12:
+                best_score = score
+                best_params = (bmin_tok, bmax_b, wmin_tok, wmin_b, c_min, c_b, c_max, target)
     return best_params, best_score
 
 
@@ -225,8 +264,7 @@ def render_markdown(out: dict) -> str:
     """The calibration summary: frozen parameters, regrets, and the held-out
     chosen/best ratio with the best route for two families."""
     p = out["params"]
-    pv = tuple(p[k] for k in ["bucketed_min_tokens", "bucketed_max_batch", "workqueue_min_tokens",
-                              "workqueue_min_batch", "split_tokens", "bucketed_split_tokens"])
+    pv = tuple(p[k] for k in PARAM_NAMES)
     held = out["heldout"]
     short = {"bucketed": "b", "workqueue": "wq", "single": "sp"}
     lines = ["# Policy calibration on GB300", "",
@@ -235,8 +273,8 @@ def render_markdown(out: dict) -> str:
              "    python -m paged_kv_gqa_09_gb300.calibrate --from-json policy_calibration.json "
              "--md policy_calibration.md", "",
              "Grid: families bucketed / bimodal / uniform / Zipf x B in {1,2,4,8,16,32,64} x N_max in",
-             "{256..32768}; Hq=32, Hkv=8, d=128, page_size 16. Routes: bucketed split C in {128..2048},",
-             "workqueue C in {256..2048} (its plan built inside the decode), single pass. Time = median",
+             "{256..65536}; Hq=32, Hkv=8, d=128, page_size 16. Routes: bucketed split C in {128..2048},",
+             "workqueue C in {256..4096} (its plan built inside the decode), single pass. Time = median",
              "synchronized wall-clock per decode step through the C ABI (launches and host planning",
              "included). Policy parameters searched to minimise",
              "the mean chosen/best time ratio on the calibration seed 20260622, then checked on held-out seed",
@@ -308,10 +346,10 @@ def main(argv=None):
     model = fit_cost_model(cal)
     if held is None:
         held = measure(T.HELDOUT_SEED, a.reps)
-    pages_default = (4096, 1, 4096, 8, 1024, 1024)  # the pages' routing, RTX 3060-era cut-offs
+    # the pages' routing with RTX 3060-era cut-offs, one fixed C per route
+    pages_default = (4096, 1, 4096, 8, 1024, 1024, 1024, 0)
     out = {
-        "params": dict(zip(["bucketed_min_tokens", "bucketed_max_batch", "workqueue_min_tokens",
-                            "workqueue_min_batch", "split_tokens", "bucketed_split_tokens"], params)),
+        "params": dict(zip(PARAM_NAMES, params)),
         "calibration_mean_regret": score,
         "heldout_mean_max_regret": regret(params, held),
         "pages_structure_default_heldout_regret": regret(pages_default, held),

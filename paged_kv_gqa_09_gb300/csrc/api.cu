@@ -845,6 +845,8 @@ void pkv_policy_default(pkv_policy_cfg_t *c)
     c->workqueue_min_batch = 1;
     c->split_tokens = 512;
     c->bucketed_split_tokens = 1024;
+    c->workqueue_max_split_tokens = 512;
+    c->workqueue_target_splits = 0;
 }
 
 int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t *out_path,
@@ -857,7 +859,7 @@ int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t
     pkv_policy_cfg_t d;
     pkv_policy_default(&d);
     const pkv_policy_cfg_t *c = cfg ? cfg : &d;
-    if (c->split_tokens <= 0 || c->bucketed_split_tokens <= 0)
+    if (c->split_tokens <= 0 || c->bucketed_split_tokens <= 0 || c->workqueue_target_splits < 0)
         return fail(PKV_EINVAL, "policy split sizes must be positive");
     pkv_path_t path = PKV_PATH_SINGLE_PASS;
     int32_t C = c->split_tokens;
@@ -866,6 +868,10 @@ int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t
         C = c->bucketed_split_tokens;
     } else if (B >= c->workqueue_min_batch && n_max >= c->workqueue_min_tokens) {
         path = PKV_PATH_WORKQUEUE;
+        // fewer, longer splits for larger batches: every split writes a state
+        while (c->workqueue_target_splits > 0 && C < c->workqueue_max_split_tokens &&
+               (int64_t)B * ((n_max + (int64_t)C - 1) / C) > c->workqueue_target_splits)
+            C *= 2;
     }
     *out_path = path;
     *out_split = C;

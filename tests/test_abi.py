@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(L):
     for name in declared:
         assert hasattr(L, name), name
     assert sorted(_lib.EXPORTS) == declared
-    assert L.pkv_version() == 1
+    assert L.pkv_version() == 2
 
 
 def shape(**kw):

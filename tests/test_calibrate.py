@@ -44,9 +44,10 @@ def planted_results(params, rng):
 
 
 @pytest.mark.parametrize("planted", [
-    (1024, 4, 2048, 1, 512, 512),       # the shape of the frozen GB300 defaults
-    (4096, 1, 8192, 8, 1024, 1024),     # the pages' own routing: B=1 split, B>=8 workqueue
-    (0, 0, 256, 2, 2048, 128),          # no bucketed route at all
+    (1024, 4, 2048, 1, 512, 512, 512, 0),        # one fixed workqueue C
+    (4096, 1, 8192, 8, 1024, 1024, 1024, 0),     # the pages' own routing: B=1 split, B>=8 workqueue
+    (0, 0, 256, 2, 2048, 128, 2048, 0),          # no bucketed route at all
+    (16384, 2, 1024, 1, 512, 1024, 4096, 256),   # the workqueue's C growing with the batch
 ])
 def test_fit_recovers_a_planted_policy(planted):
     rng = np.random.default_rng(11)
@@ -59,7 +60,7 @@ def test_fit_recovers_a_planted_policy(planted):
 
 
 def test_regret_is_the_mean_and_max_of_chosen_over_best():
-    params = (1024, 1, 1 << 30, 1 << 30, 512, 256)      # B=1 and N_max>=1024 -> bucketed:256, else single
+    params = (1024, 1, 1 << 30, 1 << 30, 512, 256, 512, 0)  # B=1, N_max>=1024 -> bucketed:256, else single
     res = [{"B": 1, "n_max": 2048, "us": {"bucketed:256": 12.0, "single:0": 6.0}},
            {"B": 8, "n_max": 2048, "us": {"bucketed:256": 3.0, "single:0": 9.0}},
            {"B": 8, "n_max": 64, "us": {"bucketed:256": 9.0, "single:0": 9.0}}]
@@ -72,11 +73,15 @@ def test_python_rule_is_the_c_rule(L):
     """calibrate.choose (what the search scores) and pkv_policy (what runs) route
     every (B, N_max) alike, including both sides of every cut-off."""
     rng = np.random.default_rng(5)
-    cfgs = [api.pkv_policy_default(), _lib.PolicyCfg(1000, 1, 2000, 8, 512, 256),
-            _lib.PolicyCfg(0, 64, 0, 1, 256, 2048), _lib.PolicyCfg(1 << 30, 0, 1 << 30, 1 << 30, 1024, 1024)]
+    cfgs = [api.pkv_policy_default(), _lib.PolicyCfg(1000, 1, 2000, 8, 512, 256, 512, 0),
+            _lib.PolicyCfg(0, 64, 0, 1, 256, 2048, 256, 0),
+            _lib.PolicyCfg(1 << 30, 0, 1 << 30, 1 << 30, 1024, 1024, 1024, 0),
+            _lib.PolicyCfg(16384, 2, 1024, 1, 512, 1024, 4096, 256),
+            _lib.PolicyCfg(0, 0, 0, 1, 256, 1024, 2048, 16)]
     for c in cfgs:
         params = (c.bucketed_min_tokens, c.bucketed_max_batch, c.workqueue_min_tokens,
-                  c.workqueue_min_batch, c.split_tokens, c.bucketed_split_tokens)
+                  c.workqueue_min_batch, c.split_tokens, c.bucketed_split_tokens,
+                  c.workqueue_max_split_tokens, c.workqueue_target_splits)
         bs = {0, 1, 2, 3, 4, 5, 8, 9, 64, 65, c.bucketed_max_batch, c.bucketed_max_batch + 1,
               c.workqueue_min_batch, c.workqueue_min_batch - 1}
         ns = {0, 1, 256, 32768, c.bucketed_min_tokens, c.bucketed_min_tokens - 1,
@@ -119,3 +124,14 @@ def test_length_families(family):
             assert (n >= 3 * n_max // 4).sum() >= B - B // 2
         else:
             assert n.min() >= min(16, n_max)
+
+
+def test_workqueue_split_rule():
+    """The workqueue's C doubles from its smallest value while the batch holds
+    more than the target number of (row, split) pairs, up to its largest."""
+    assert calibrate.wq_split(64, 65536, 512, 4096, 256) == 4096
+    assert calibrate.wq_split(8, 32768, 512, 4096, 256) == 1024    # 8 x 32 = 256 pairs
+    assert calibrate.wq_split(8, 32769, 512, 4096, 256) == 2048
+    assert calibrate.wq_split(1, 1000, 512, 4096, 256) == 512
+    assert calibrate.wq_split(64, 65536, 512, 4096, 0) == 512      # target 0: fixed C
+    assert calibrate.wq_split(64, 10 ** 7, 256, 1024, 16) == 1024  # capped
