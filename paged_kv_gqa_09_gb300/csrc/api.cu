@@ -829,24 +829,22 @@ int pkv_append(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *
 // ------------------------------------------------------------------ policy
 
 // Thresholds calibrated on a GB300 (152 SMs) by paged_kv_gqa_09_gb300/calibrate.py:
-// 224 traces (bucketed, bimodal, uniform, Zipf; B 1..64; N_max 256..32768;
+// 252 traces (bucketed, bimodal, uniform, Zipf; B 1..64; N_max 256..65536;
 // Hq=32, Hkv=8, d=128, P=16) drawn with the calibration seed 20260622, timed as
 // synchronized wall-clock per step (the workqueue with its plan built inside the
-// decode; refitted after its full splits came to be claimed kv heads side by
-// side, with the same result); held-out seed 20260623 mean regret 1.046 (worst
-// 1.21x).
+// decode); held-out seed 20260623 mean regret 1.031 (worst 1.29x).
 void pkv_policy_default(pkv_policy_cfg_t *c)
 {
     if (!c)
         return;
-    c->bucketed_min_tokens = 16384;
+    c->bucketed_min_tokens = 32768;
     c->bucketed_max_batch = 2;
     c->workqueue_min_tokens = 1024;
     c->workqueue_min_batch = 1;
-    c->split_tokens = 512;
-    c->bucketed_split_tokens = 1024;
-    c->workqueue_max_split_tokens = 512;
-    c->workqueue_target_splits = 0;
+    c->split_tokens = 256;
+    c->bucketed_split_tokens = 2048;
+    c->workqueue_max_split_tokens = 1024;
+    c->workqueue_target_splits = 32;
 }
 
 int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t *out_path,
@@ -881,20 +879,21 @@ int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t
 // ------------------------------------------------------------ learned model
 
 // Routes and weights fitted by paged_kv_gqa_09_gb300/calibrate.py (least
-// squares of log step time, calibration seed 20260622, 224 GB300 traces, the
+// squares of log step time, calibration seed 20260622, 252 GB300 traces, the
 // workqueue with its plan built inside the decode and its full splits claimed
-// kv heads side by side); held-out seed 20260623 mean regret 1.026 (worst 1.20x).
+// kv heads side by side); held-out seed 20260623 mean regret 1.028 (worst 1.27x).
 static const pkv_cost_route_t kGb300Routes[] = {
-    {0, 128, {6.37893382f, 0.170615139f, 0.10530812f, -0.858705666f, 0.000193721028f, 0.00764236856f, 0.00430371841f, 0.339969458f, -0.0583645925f, 0.0342088869f}},
-    {0, 256, {6.91803431f, 0.086364198f, 0.0838334308f, -0.877535704f, 0.0055556387f, 0.00455079629f, 0.00182357596f, 0.261572754f, -0.0602490915f, 0.036329164f}},
-    {0, 512, {6.95596685f, -0.0414725812f, 0.0685039831f, -0.824151421f, 0.0133199074f, 0.00596759028f, 0.000691617587f, 0.189865697f, -0.0382477556f, 0.0346018921f}},
-    {0, 1024, {6.39920834f, -0.146957372f, 0.140989561f, -0.757397335f, 0.0178196747f, 0.00809220292f, -0.00402061834f, 0.10288432f, -0.0276012258f, 0.0328447786f}},
-    {0, 2048, {5.29898522f, -0.168081875f, 0.348305975f, -0.748684542f, 0.0155538531f, 0.01174969f, -0.0120188905f, 0.0451341569f, -0.0128900628f, 0.0321279087f}},
-    {1, 256, {7.38087955f, 0.155318192f, 0.066164181f, -0.923406785f, -0.00986350743f, 0.000321624704f, 0.000410297829f, 0.0641619519f, -0.0144386881f, 0.0411520044f}},
-    {1, 512, {7.14670578f, 0.15409992f, 0.166507884f, -0.950205657f, -0.00890024271f, -0.00217965337f, -0.00531239341f, 0.0749956238f, -0.0325700657f, 0.0424897811f}},
-    {1, 1024, {6.09056068f, 0.148111501f, 0.419567256f, -0.9843811f, -0.00952862822f, -0.00167480935f, -0.0162033182f, 0.0394223106f, -0.0281193987f, 0.0434735812f}},
-    {1, 2048, {4.44974918f, 0.188729173f, 0.78447106f, -1.04063316f, -0.0151122813f, 0.00165503706f, -0.0294351031f, -0.0110330845f, -0.00936690114f, 0.0441417604f}},
-    {2, 1024, {6.03505548f, -0.10174207f, -0.27518526f, -0.430179728f, -0.0103144304f, 0.0329394824f, 0.0316009504f, -0.351783337f, 0.147098237f, 0.0155151357f}},
+    {0, 128, {6.43522312f, 0.155240338f, 0.0571267949f, -0.826889369f, -9.77361572e-05f, 0.00964326087f, 0.00721835884f, 0.289587404f, -0.0323441347f, 0.0324759047f}},
+    {0, 256, {6.90634468f, 0.11561489f, 0.073463712f, -0.876175914f, 0.00222917506f, 0.00446850577f, 0.00291227527f, 0.228681386f, -0.0486112449f, 0.0362076469f}},
+    {0, 512, {6.97477146f, 0.0467281537f, 0.0915738729f, -0.871211625f, 0.00683948306f, 0.0035246084f, 0.000610483019f, 0.202537233f, -0.0440913988f, 0.036392998f}},
+    {0, 1024, {6.64072924f, -0.0816791098f, 0.118714733f, -0.800035849f, 0.0142438209f, 0.0063186658f, -0.00191515287f, 0.137929795f, -0.032207293f, 0.0340349367f}},
+    {0, 2048, {5.68597151f, -0.165830935f, 0.279803845f, -0.765341357f, 0.0179909369f, 0.0104575887f, -0.00777931812f, 0.0742148421f, -0.00307055634f, 0.031764219f}},
+    {1, 256, {7.44703206f, 0.0913338033f, -0.0127198193f, -0.85044607f, -0.00677249923f, 0.00184801015f, 0.00303694876f, -0.0062896096f, -0.00326680161f, 0.0389004989f}},
+    {1, 512, {7.34024419f, 0.0797576955f, 0.0538422433f, -0.869031817f, -0.00540252892f, -0.000320753882f, -0.00106146329f, -0.0132930549f, -0.0136234939f, 0.0399044083f}},
+    {1, 1024, {6.63672175f, 0.132269447f, 0.29915563f, -0.969923251f, -0.00846007637f, -0.000978926262f, -0.01053147f, 0.0130306204f, -0.0200417429f, 0.0427458306f}},
+    {1, 2048, {5.30163159f, 0.157605606f, 0.610701627f, -1.03036989f, -0.0108301085f, 0.000341900614f, -0.0219543845f, 0.0201782586f, -0.0148247786f, 0.043745093f}},
+    {1, 4096, {3.57397556f, 0.181893212f, 0.938083449f, -1.05388292f, -0.0154596275f, 0.00527058079f, -0.032130546f, -0.0361358704f, 0.0165122995f, 0.0426512845f}},
+    {2, 1024, {5.438266f, -0.164636353f, -0.215992675f, -0.377090117f, -0.00801042101f, 0.0382226743f, 0.0292699102f, -0.40541281f, 0.171905311f, 0.0130644566f}},
 };
 
 void pkv_cost_model_default(pkv_cost_model_t *m)

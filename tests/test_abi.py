@@ -204,6 +204,15 @@ def test_policy_routes_by_batch_and_length(L):
         api.pkv_policy(-1, 5)
     with pytest.raises(_lib.PkvError):
         api.pkv_policy(1, 5, _lib.PolicyCfg(0, 1, 0, 8, 0, 256))
+    # the workqueue's split size doubling with the batch, up to its largest
+    grow = _lib.PolicyCfg(1000, 1, 2000, 8, 512, 256, 4096, 256)
+    assert api.pkv_policy(9, 2000, grow) == (P.PKV_PATH_WORKQUEUE, 512)      # 9 x 4 pairs
+    assert api.pkv_policy(64, 8192, grow) == (P.PKV_PATH_WORKQUEUE, 2048)    # 64 x 4 pairs
+    assert api.pkv_policy(64, 8193, grow) == (P.PKV_PATH_WORKQUEUE, 4096)
+    assert api.pkv_policy(64, 10 ** 7, grow) == (P.PKV_PATH_WORKQUEUE, 4096)  # capped
+    assert api.pkv_policy(1, 10 ** 6, grow)[1] == 256                         # bucketed C unchanged
+    with pytest.raises(_lib.PkvError):
+        api.pkv_policy(9, 2000, _lib.PolicyCfg(1000, 1, 2000, 8, 512, 256, 4096, -1))
 
 
 @pytest.mark.parametrize("cfg_id", [1, 2, 3, 4, 5])
@@ -228,7 +237,7 @@ def test_learned_policy_matches_the_fitted_feature_map(L):
     (Python) on the default GB300 model: same route on a grid of batches."""
     from paged_kv_gqa_09_gb300 import calibrate
     m = api.pkv_cost_model_default()
-    assert m.n_routes == 10
+    assert m.n_routes == len(calibrate.routes()) == 11
     routes = [(m.route[r].path, m.route[r].split_tokens, np.array(m.route[r].w[:], np.float64))
               for r in range(m.n_routes)]
     assert {p for p, _, _ in routes} == {0, 1, 2}
