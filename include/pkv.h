@@ -359,7 +359,8 @@ int pkv_decode_step_noalloc(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg,
  *   else SINGLE_PASS.
  * The workqueue's split size grows with the batch, because every split writes
  * a partial state: C starts at split_tokens and doubles while
- * B * ceil(N_max / C) > workqueue_target_splits, up to
+ * B * ceil(N_max / C) > workqueue_target_splits and the longest row would keep
+ * at least workqueue_min_long_splits splits (ceil(N_max / 2C) of them), up to
  * workqueue_max_split_tokens (a target of 0 keeps C = split_tokens). */
 typedef struct {
     int32_t bucketed_min_tokens;   /* long-context cut-off of the bucketed route */
@@ -370,6 +371,7 @@ typedef struct {
     int32_t bucketed_split_tokens; /* C handed to BUCKETED_SPLIT */
     int32_t workqueue_max_split_tokens; /* largest C handed to WORKQUEUE */
     int32_t workqueue_target_splits;    /* (row, split) pairs the workqueue's C aims at */
+    int32_t workqueue_min_long_splits;  /* splits the longest row keeps as C grows */
 } pkv_policy_cfg_t;
 
 /* Fill `cfg` with the thresholds calibrated on GB300 (calibration seed

@@ -79,7 +79,8 @@ class PolicyCfg(ctypes.Structure):
                 ("workqueue_min_tokens", ctypes.c_int32), ("workqueue_min_batch", ctypes.c_int32),
                 ("split_tokens", ctypes.c_int32), ("bucketed_split_tokens", ctypes.c_int32),
                 ("workqueue_max_split_tokens", ctypes.c_int32),
-                ("workqueue_target_splits", ctypes.c_int32)]
+                ("workqueue_target_splits", ctypes.c_int32),
+                ("workqueue_min_long_splits", ctypes.c_int32)]
 
 
 COST_FEATURES = 10

@@ -16,7 +16,8 @@ Procedure:
 2. Search the policy parameters (two long-context cut-offs, two batch cut-offs,
    the bucketed split's C, and the workqueue's split rule: C doubles from a
    smallest value until the batch holds at most a target number of (row, split)
-   pairs, up to a largest value) minimising the mean ratio of the chosen
+   pairs, up to a largest value, and only while the longest row keeps a least
+   number of splits) minimising the mean ratio of the chosen
    route's time to the best route's time over the calibration traces.  The
    workqueue's rule is fitted first, on the workqueue's own times, then the
    cut-offs with it.
@@ -46,6 +47,7 @@ FAMILIES = ["bucketed", "bimodal", "uniform", "zipf"]
 BUCKETED_C = [128, 256, 512, 1024, 2048]
 WORKQUEUE_C = [256, 512, 1024, 2048, 4096]
 WQ_TARGETS = [0, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096]  # 0: C fixed at its smallest
+WQ_LONG_SPLITS = [0, 2, 4, 8, 16, 32]
 TOKEN_CUTS = [0, 256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 1 << 30]
 BATCH_CUTS_MAX = [0, 1, 2, 4, 8, 16, 32, 64]
 BATCH_CUTS_MIN = [1, 2, 4, 8, 16, 32, 64, 1 << 30]
@@ -53,7 +55,7 @@ BATCH_CUTS_MIN = [1, 2, 4, 8, 16, 32, 64, 1 << 30]
 
 PARAM_NAMES = ["bucketed_min_tokens", "bucketed_max_batch", "workqueue_min_tokens",
                "workqueue_min_batch", "split_tokens", "bucketed_split_tokens",
-               "workqueue_max_split_tokens", "workqueue_target_splits"]
+               "workqueue_max_split_tokens", "workqueue_target_splits", "workqueue_min_long_splits"]
 
 
 def lengths(family: str, B: int, n_max: int, rng: np.random.Generator) -> np.ndarray:
@@ -140,23 +142,25 @@ def measure(seed: int, reps: int = 7, warm: int = 2, log=print):
     return results
 
 
-def wq_split(B: int, n_max: int, c_min: int, c_max: int, target: int) -> int:
+def wq_split(B: int, n_max: int, c_min: int, c_max: int, target: int, long_splits: int = 0) -> int:
     """The workqueue's split size: c_min doubled while the batch would hold more
     than `target` (row, split) pairs (B * ceil(n_max / C), the longest row's
-    count for every row), up to c_max; target 0 keeps c_min.  The same rule is
-    written in C in pkv_policy (api.cu)."""
+    count for every row) and the longest row would keep at least `long_splits`
+    splits, up to c_max; target 0 keeps c_min.  The same rule is written in C
+    in pkv_policy (api.cu)."""
     C = c_min
-    while target > 0 and C < c_max and B * -(-n_max // C) > target:
+    while (target > 0 and C < c_max and B * -(-n_max // C) > target
+           and -(-n_max // (2 * C)) >= long_splits):
         C *= 2
     return C
 
 
 def choose(params, B, n_max):
-    bmin_tok, bmax_b, wmin_tok, wmin_b, c_wq, c_b, c_wq_max, target = params
+    bmin_tok, bmax_b, wmin_tok, wmin_b, c_wq, c_b, c_wq_max, target, long_splits = params
     if 1 <= B <= bmax_b and n_max >= bmin_tok:
         return f"bucketed:{c_b}"
     if B >= wmin_b and n_max >= wmin_tok:
-        return f"workqueue:{wq_split(B, n_max, c_wq, c_wq_max, target)}"
+        return f"workqueue:{wq_split(B, n_max, c_wq, c_wq_max, target, long_splits)}"
     return "single:0"
 
 
@@ -166,31 +170,34 @@ def regret(params, results):
 
 
 def fit_wq_rule(results):
-    """(c_min, c_max, target) of the workqueue's split rule minimising the mean
-    ratio of the rule's workqueue time to the best workqueue time, over the
-    traces long enough for the workqueue to be a candidate (N_max >= 1024)."""
+    """(c_min, c_max, target, long_splits) of the workqueue's split rule
+    minimising the mean ratio of the rule's workqueue time to the best
+    workqueue time, over the traces long enough for the workqueue to be a
+    candidate (N_max >= 1024)."""
     rows = [r for r in results if r["n_max"] >= 1024]
+    best_wq = [min(r["us"][f"workqueue:{c}"] for c in WORKQUEUE_C) for r in rows]
     best_rule, best_score = None, math.inf
-    for c_min, c_max, target in itertools.product(WORKQUEUE_C, WORKQUEUE_C, WQ_TARGETS):
-        if c_max < c_min or (target == 0 and c_max != c_min):
+    for c_min, c_max, target, ls in itertools.product(WORKQUEUE_C, WORKQUEUE_C, WQ_TARGETS,
+                                                      WQ_LONG_SPLITS):
+        if c_max < c_min or (target == 0 and (c_max != c_min or ls != 0)):
             continue
         score = float(np.mean([
-            r["us"][f"workqueue:{wq_split(r['B'], r['n_max'], c_min, c_max, target)}"]
-            / min(r["us"][f"workqueue:{c}"] for c in WORKQUEUE_C) for r in rows]))
+            r["us"][f"workqueue:{wq_split(r['B'], r['n_max'], c_min, c_max, target, ls)}"] / b
+            for r, b in zip(rows, best_wq)]))
         if score < best_score - 1e-12:
-            best_rule, best_score = (c_min, c_max, target), score
+            best_rule, best_score = (c_min, c_max, target, ls), score
     return best_rule
 
 
 def fit(results):
-    c_min, c_max, target = fit_wq_rule(results)
+    c_min, c_max, target, ls = fit_wq_rule(results)
     names = [f"{n}:{c}" for n, c in routes()]
     tmat = np.array([[res["us"][k] for k in names] for res in results])
     best = tmat.min(axis=1)
     Bv = np.array([res["B"] for res in results])
     Nv = np.array([res["n_max"] for res in results])
     col = {k: i for i, k in enumerate(names)}
-    wq = np.array([res["us"][f"workqueue:{wq_split(res['B'], res['n_max'], c_min, c_max, target)}"]
+    wq = np.array([res["us"][f"workqueue:{wq_split(res['B'], res['n_max'], c_min, c_max, target, ls)}"]
                    for res in results])
     single = tmat[:, col["single:0"]]
     best_params, best_score = None, math.inf
@@ -204,7 +211,7 @@ def fit(results):
             score = float(np.mean(chosen / best))
             if score < best_score - 1e-12:
                 best_score = score
-                best_params = (bmin_tok, bmax_b, wmin_tok, wmin_b, c_min, c_b, c_max, target)
+                best_params = (bmin_tok, bmax_b, wmin_tok, wmin_b, c_min, c_b, c_max, target, ls)
     return best_params, best_score
 
 
@@ -347,7 +354,7 @@ def main(argv=None):
     if held is None:
         held = measure(T.HELDOUT_SEED, a.reps)
     # the pages' routing with RTX 3060-era cut-offs, one fixed C per route
-    pages_default = (4096, 1, 4096, 8, 1024, 1024, 1024, 0)
+    pages_default = (4096, 1, 4096, 8, 1024, 1024, 1024, 0, 0)
     out = {
         "params": dict(zip(PARAM_NAMES, params)),
         "calibration_mean_regret": score,

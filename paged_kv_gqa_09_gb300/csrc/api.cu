@@ -832,19 +832,20 @@ int pkv_append(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *
 // 252 traces (bucketed, bimodal, uniform, Zipf; B 1..64; N_max 256..65536;
 // Hq=32, Hkv=8, d=128, P=16) drawn with the calibration seed 20260622, timed as
 // synchronized wall-clock per step (the workqueue with its plan built inside the
-// decode); held-out seed 20260623 mean regret 1.031 (worst 1.29x).
+// decode); held-out seed 20260623 mean regret 1.028 (worst 1.22x).
 void pkv_policy_default(pkv_policy_cfg_t *c)
 {
     if (!c)
         return;
-    c->bucketed_min_tokens = 32768;
-    c->bucketed_max_batch = 2;
+    c->bucketed_min_tokens = 16384;
+    c->bucketed_max_batch = 1;
     c->workqueue_min_tokens = 1024;
     c->workqueue_min_batch = 1;
     c->split_tokens = 256;
-    c->bucketed_split_tokens = 2048;
-    c->workqueue_max_split_tokens = 1024;
+    c->bucketed_split_tokens = 1024;
+    c->workqueue_max_split_tokens = 4096;
     c->workqueue_target_splits = 32;
+    c->workqueue_min_long_splits = 16;
 }
 
 int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t *out_path,
@@ -857,7 +858,8 @@ int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t
     pkv_policy_cfg_t d;
     pkv_policy_default(&d);
     const pkv_policy_cfg_t *c = cfg ? cfg : &d;
-    if (c->split_tokens <= 0 || c->bucketed_split_tokens <= 0 || c->workqueue_target_splits < 0)
+    if (c->split_tokens <= 0 || c->bucketed_split_tokens <= 0 || c->workqueue_target_splits < 0 ||
+        c->workqueue_min_long_splits < 0)
         return fail(PKV_EINVAL, "policy split sizes must be positive");
     pkv_path_t path = PKV_PATH_SINGLE_PASS;
     int32_t C = c->split_tokens;
@@ -868,7 +870,8 @@ int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t
         path = PKV_PATH_WORKQUEUE;
         // fewer, longer splits for larger batches: every split writes a state
         while (c->workqueue_target_splits > 0 && C < c->workqueue_max_split_tokens &&
-               (int64_t)B * ((n_max + (int64_t)C - 1) / C) > c->workqueue_target_splits)
+               (int64_t)B * ((n_max + (int64_t)C - 1) / C) > c->workqueue_target_splits &&
+               (n_max + 2 * (int64_t)C - 1) / (2 * (int64_t)C) >= c->workqueue_min_long_splits)
             C *= 2;
     }
     *out_path = path;

@@ -213,6 +213,11 @@ def test_policy_routes_by_batch_and_length(L):
     assert api.pkv_policy(1, 10 ** 6, grow)[1] == 256                         # bucketed C unchanged
     with pytest.raises(_lib.PkvError):
         api.pkv_policy(9, 2000, _lib.PolicyCfg(1000, 1, 2000, 8, 512, 256, 4096, -1))
+    keep = _lib.PolicyCfg(1000, 1, 2000, 8, 256, 256, 4096, 32, 16)   # the longest row keeps 16
+    assert api.pkv_policy(8, 2903, keep) == (P.PKV_PATH_WORKQUEUE, 256)
+    assert api.pkv_policy(64, 65536, keep) == (P.PKV_PATH_WORKQUEUE, 4096)
+    with pytest.raises(_lib.PkvError):
+        api.pkv_policy(9, 2000, _lib.PolicyCfg(1000, 1, 2000, 8, 512, 256, 4096, 32, -1))
 
 
 @pytest.mark.parametrize("cfg_id", [1, 2, 3, 4, 5])

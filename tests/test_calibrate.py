@@ -44,10 +44,11 @@ def planted_results(params, rng):
 
 
 @pytest.mark.parametrize("planted", [
-    (1024, 4, 2048, 1, 512, 512, 512, 0),        # one fixed workqueue C
-    (4096, 1, 8192, 8, 1024, 1024, 1024, 0),     # the pages' own routing: B=1 split, B>=8 workqueue
-    (0, 0, 256, 2, 2048, 128, 2048, 0),          # no bucketed route at all
-    (16384, 2, 1024, 1, 512, 1024, 4096, 256),   # the workqueue's C growing with the batch
+    (1024, 4, 2048, 1, 512, 512, 512, 0, 0),        # one fixed workqueue C
+    (4096, 1, 8192, 8, 1024, 1024, 1024, 0, 0),     # the pages' own routing: B=1 split, B>=8 workqueue
+    (0, 0, 256, 2, 2048, 128, 2048, 0, 0),          # no bucketed route at all
+    (16384, 2, 1024, 1, 512, 1024, 4096, 256, 0),   # the workqueue's C growing with the batch
+    (16384, 1, 1024, 1, 256, 1024, 4096, 32, 16),   # ... while the longest row keeps 16 splits
 ])
 def test_fit_recovers_a_planted_policy(planted):
     rng = np.random.default_rng(11)
@@ -60,7 +61,7 @@ def test_fit_recovers_a_planted_policy(planted):
 
 
 def test_regret_is_the_mean_and_max_of_chosen_over_best():
-    params = (1024, 1, 1 << 30, 1 << 30, 512, 256, 512, 0)  # B=1, N_max>=1024 -> bucketed:256, else single
+    params = (1024, 1, 1 << 30, 1 << 30, 512, 256, 512, 0, 0)  # B=1, N_max>=1024 -> bucketed:256, else single
     res = [{"B": 1, "n_max": 2048, "us": {"bucketed:256": 12.0, "single:0": 6.0}},
            {"B": 8, "n_max": 2048, "us": {"bucketed:256": 3.0, "single:0": 9.0}},
            {"B": 8, "n_max": 64, "us": {"bucketed:256": 9.0, "single:0": 9.0}}]
@@ -77,11 +78,13 @@ def test_python_rule_is_the_c_rule(L):
             _lib.PolicyCfg(0, 64, 0, 1, 256, 2048, 256, 0),
             _lib.PolicyCfg(1 << 30, 0, 1 << 30, 1 << 30, 1024, 1024, 1024, 0),
             _lib.PolicyCfg(16384, 2, 1024, 1, 512, 1024, 4096, 256),
-            _lib.PolicyCfg(0, 0, 0, 1, 256, 1024, 2048, 16)]
+            _lib.PolicyCfg(0, 0, 0, 1, 256, 1024, 2048, 16),
+            _lib.PolicyCfg(16384, 1, 1024, 1, 256, 1024, 4096, 32, 16)]
     for c in cfgs:
         params = (c.bucketed_min_tokens, c.bucketed_max_batch, c.workqueue_min_tokens,
                   c.workqueue_min_batch, c.split_tokens, c.bucketed_split_tokens,
-                  c.workqueue_max_split_tokens, c.workqueue_target_splits)
+                  c.workqueue_max_split_tokens, c.workqueue_target_splits,
+                  c.workqueue_min_long_splits)
         bs = {0, 1, 2, 3, 4, 5, 8, 9, 64, 65, c.bucketed_max_batch, c.bucketed_max_batch + 1,
               c.workqueue_min_batch, c.workqueue_min_batch - 1}
         ns = {0, 1, 256, 32768, c.bucketed_min_tokens, c.bucketed_min_tokens - 1,
@@ -135,3 +138,7 @@ def test_workqueue_split_rule():
     assert calibrate.wq_split(1, 1000, 512, 4096, 256) == 512
     assert calibrate.wq_split(64, 65536, 512, 4096, 0) == 512      # target 0: fixed C
     assert calibrate.wq_split(64, 10 ** 7, 256, 1024, 16) == 1024  # capped
+    # the longest row keeps at least 16 splits: a ragged batch of short rows
+    assert calibrate.wq_split(8, 2903, 256, 4096, 32, 16) == 256
+    assert calibrate.wq_split(8, 8192, 256, 4096, 32, 16) == 512    # 8192 / 1024 would leave 8
+    assert calibrate.wq_split(64, 65536, 256, 4096, 32, 16) == 4096
