@@ -316,6 +316,23 @@ int pkv_decode_step_rows(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, vo
                          const int32_t *d_block_table, const int32_t *d_seq_lens,
                          float *d_partials, void *d_o, float *d_lse, void *stream);
 
+/* pkv_exact_length_groups -- the launch groups of the exact-length-bucket
+ * scheme (Results, "Scheduling overhead": the scheme the compact workqueue
+ * replaces launches one split + merge pair per distinct row length), computed
+ * on the host from the host lengths seq_lens[B]; no CUDA call.  Writes:
+ *   rows[0 .. B): the rows with tokens grouped by length -- lengths ascending,
+ *     rows ascending within a length -- then the rows of length 0;
+ *   group_start[0 .. n_groups]: group g is rows[group_start[g] ..
+ *     group_start[g + 1]), group_start[n_groups] = the rows with tokens;
+ *   group_len[0 .. n_groups): the length of group g;
+ *   *n_groups: the number of distinct non-zero lengths.
+ * Arrays hold B (rows, group_len) and B + 1 (group_start) entries.  Each group
+ * runs as pkv_decode_step_rows with bucket_len = its length; the rows of length
+ * 0, if any, as one more pkv_decode_step_rows (any bucket_len), which gives them
+ * o = 0 and lse = -inf.  A negative length is PKV_EINVAL. */
+int pkv_exact_length_groups(const int32_t *seq_lens, int32_t B, int32_t *rows,
+                            int32_t *group_start, int32_t *group_len, int32_t *n_groups);
+
 /* pkv_decode_step_noalloc -- pkv_decode_step for callers that cannot
  * allocate device memory.  No counterpart in the paper: it serves callers that
  * must not call cudaMalloc -- code running inside an allocator's callbacks,

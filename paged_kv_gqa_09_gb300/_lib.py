@@ -44,7 +44,7 @@ EXPORTS = [
     "pkv_decode_merge",
     "pkv_single_pass", "pkv_decode_step", "pkv_decode_step_rows", "pkv_decode_step_noalloc",
     "pkv_decode_step_host", "pkv_append_decode_step_host",
-    "pkv_append", "pkv_append_plan", "pkv_policy_default", "pkv_policy",
+    "pkv_append", "pkv_append_plan", "pkv_exact_length_groups", "pkv_policy_default", "pkv_policy",
     "pkv_cost_model_default", "pkv_policy_learned",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error",
     "pkv_test_starve_next_decodes", "pkv_last_error_string", "pkv_version",
@@ -146,6 +146,7 @@ def load() -> ctypes.CDLL:
             "pkv_decode_step_rows": (ctypes.c_int, [S, C, vp, vp, i32] + [vp] * 9),
             "pkv_append": (ctypes.c_int, [S, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_append_plan": (ctypes.c_int, [S, C] + [vp] * 10),
+            "pkv_exact_length_groups": (ctypes.c_int, [vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int32)]),
             "pkv_policy_default": (None, [PC]),
             "pkv_policy": (ctypes.c_int, [i32, i32, PC, ctypes.POINTER(ctypes.c_int32),
                                           ctypes.POINTER(ctypes.c_int32)]),

@@ -28,7 +28,7 @@ __all__ = [
     "PKV_PLAN_IN_DECODE", "PKV_SELF_PLAN_MAX_B", "pkv_single_pass",
     "pkv_decode_step", "pkv_decode_step_noalloc",
     "pkv_decode_step_host", "pkv_append_decode_step_host", "pkv_decode_step_rows",
-    "exact_length_buckets_step", "pkv_append",
+    "exact_length_buckets_step", "pkv_exact_length_groups", "pkv_append",
     "pkv_append_plan", "pkv_policy", "pkv_policy_default",
     "pkv_cost_model_default", "pkv_policy_learned",
     "pkv_get_counters", "pkv_reset_counters", "pkv_step_model", "pkv_get_error", "pkv_version",
@@ -203,35 +203,49 @@ def pkv_decode_step_rows(shape, cfg, ws, rows, q, k_cache, v_cache, block_table,
           "pkv_decode_step_rows")
 
 
+def pkv_exact_length_groups(seq_lens_host) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """(rows, group_start, group_len) of the exact-length-bucket scheme from the
+    host lengths (see include/pkv.h): group g is rows[group_start[g] :
+    group_start[g + 1]] of length group_len[g]; rows[group_start[-1]:] have no
+    tokens."""
+    sl = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+    B = sl.size
+    rows = np.zeros(max(B, 1), np.int32)
+    start = np.zeros(B + 1, np.int32)
+    glen = np.zeros(max(B, 1), np.int32)
+    ng = ctypes.c_int32()
+    check(_lib.load().pkv_exact_length_groups(sl.ctypes.data, B, rows.ctypes.data, start.ctypes.data,
+                                              glen.ctypes.data, ctypes.byref(ng)),
+          "pkv_exact_length_groups")
+    g = int(ng.value)
+    return rows[:B], start[:g + 1], glen[:g]
+
+
 def exact_length_buckets_step(q, k_cache, v_cache, block_table, seq_lens, seq_lens_host,
                               split_tokens: int, o, lse=None, ws=None, partials=None,
                               rows_cache: Optional[dict] = None, stream=None):
     """The exact-length-bucket scheme the compact workqueue replaces (Results,
     "Scheduling overhead"): one bucketed split + merge launch pair per distinct
-    non-zero row length, each over the rows of that length.  Rows of length 0
-    get o = 0, lse = -inf.  `seq_lens_host` is the host copy of the lengths
-    (the host groups the rows).  Returns the number of launch groups."""
+    non-zero row length, each over the rows of that length (the groups come from
+    pkv_exact_length_groups), and one more pair over the rows of length 0, if
+    any, which gives them o = 0, lse = -inf.  `seq_lens_host` is the host copy
+    of the lengths.  Returns the number of launch pairs."""
     shape = make_shape(q, k_cache, block_table)
-    lens = np.asarray(seq_lens_host)
-    groups = {}
-    for i, n in enumerate(lens.tolist()):
-        groups.setdefault(int(n), []).append(i)
+    rows, start, glen = pkv_exact_length_groups(seq_lens_host)
+    groups = [(int(glen[g]), rows[start[g]:start[g + 1]]) for g in range(glen.size)]
+    if start[-1] < rows.size:
+        groups.append((0, rows[start[-1]:]))  # no tokens: neutral states, o = 0
     dev = q.device
-    if 0 in groups:
-        z = torch.tensor(groups.pop(0), dtype=torch.long, device=dev)
-        o.index_fill_(0, z, 0)
-        if lse is not None:
-            lse.index_fill_(0, z, float("-inf"))
-    for n, rows in sorted(groups.items()):
-        cfg = make_cfg(PKV_PATH_BUCKETED_SPLIT, split_tokens, n)
-        key = (n, tuple(rows))
+    for n, rws in groups:
+        cfg = make_cfg(PKV_PATH_BUCKETED_SPLIT, split_tokens, n if n > 0 else split_tokens)
+        key = (n, tuple(rws.tolist()))
         if rows_cache is not None and key in rows_cache:
             rows_t = rows_cache[key]
         else:
-            rows_t = torch.tensor(rows, dtype=torch.int32, device=dev)
+            rows_t = torch.from_numpy(np.ascontiguousarray(rws)).to(dev)
             if rows_cache is not None:
                 rows_cache[key] = rows_t
-        sub = Shape(len(rows), shape.Hq, shape.Hkv, shape.d, shape.page_size, shape.num_pages,
+        sub = Shape(len(rws), shape.Hq, shape.Hkv, shape.d, shape.page_size, shape.num_pages,
                     shape.bt_stride, shape.scale)
         need_p = pkv_partials_size(sub, cfg) // 4
         part = partials if partials is not None and partials.numel() >= need_p else \

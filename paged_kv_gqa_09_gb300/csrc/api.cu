@@ -826,6 +826,46 @@ int pkv_append(const pkv_shape_t *s, void *d_ws, const void *k_new, const void *
     return PKV_OK;
 }
 
+// ------------------------------------------------------ exact-length groups
+
+int pkv_exact_length_groups(const int32_t *seq_lens, int32_t B, int32_t *rows,
+                            int32_t *group_start, int32_t *group_len, int32_t *n_groups)
+{
+    if (B < 0 || !n_groups)
+        return fail(PKV_EINVAL, "pkv_exact_length_groups: negative B or NULL n_groups");
+    if (B > 0 && (!seq_lens || !rows || !group_start || !group_len))
+        return fail(PKV_EINVAL, "pkv_exact_length_groups: NULL array");
+    // rows by (length, index): a counting pass would need the length range, so
+    // sort the row indices (B is a batch: small) by a stable insertion order
+    int32_t n = 0;
+    for (int32_t i = 0; i < B; ++i) {
+        if (seq_lens[i] < 0)
+            return fail(PKV_EINVAL, "pkv_exact_length_groups: row %d has a negative length", i);
+        if (seq_lens[i] == 0)
+            continue;
+        int32_t k = n++;
+        while (k > 0 && seq_lens[rows[k - 1]] > seq_lens[i]) {
+            rows[k] = rows[k - 1];
+            --k;
+        }
+        rows[k] = i;
+    }
+    int32_t g = 0;
+    for (int32_t k = 0; k < n; ++k) {
+        if (k == 0 || seq_lens[rows[k]] != seq_lens[rows[k - 1]]) {
+            group_start[g] = k;
+            group_len[g] = seq_lens[rows[k]];
+            ++g;
+        }
+    }
+    group_start[g] = n;
+    for (int32_t i = 0, k = n; i < B; ++i)  // the rows without tokens, after the groups
+        if (seq_lens[i] == 0)
+            rows[k++] = i;
+    *n_groups = g;
+    return PKV_OK;
+}
+
 // ------------------------------------------------------------------ policy
 
 // Thresholds calibrated on a GB300 (152 SMs) by paged_kv_gqa_09_gb300/calibrate.py:

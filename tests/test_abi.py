@@ -315,3 +315,27 @@ def test_the_test_hook_needs_the_opt_in(L, monkeypatch):
     assert "PKV_TEST_HOOKS" in _lib.last_error()
     monkeypatch.setenv("PKV_TEST_HOOKS", "1")
     assert L.pkv_test_starve_next_decodes(0) == 0
+
+
+@pytest.mark.parametrize("lens", [[5, 5, 7, 0, 7, 9], [0, 0], [], [3], [9, 8, 7, 8, 9, 0, 1]])
+def test_exact_length_groups(L, lens):
+    """The exact-length-bucket scheme's launch groups, built by the library on
+    the host: each distinct non-zero length once, ascending, with its rows in
+    order; the rows without tokens last."""
+    rows, start, glen = api.pkv_exact_length_groups(lens)
+    want = sorted({n for n in lens if n > 0})
+    assert glen.tolist() == want
+    for g, n in enumerate(want):
+        assert rows[start[g]:start[g + 1]].tolist() == [i for i, x in enumerate(lens) if x == n]
+    assert rows[start[-1]:].tolist() == [i for i, x in enumerate(lens) if x == 0]
+    assert len(rows) == len(lens)
+    # the step model's exact-bucket launch count is two per group
+    if lens:
+        s = shape(B=len(lens), bt_stride=1)
+        m = api.pkv_step_model(_lib.PATH_EXACT_BUCKETS, s, 16, 16, lens)
+        assert m["attn_launches"] == 2 * len(want)
+
+
+def test_exact_length_groups_rejects_bad_input(L):
+    with pytest.raises(_lib.PkvError):
+        api.pkv_exact_length_groups([3, -1])

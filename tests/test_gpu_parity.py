@@ -576,6 +576,28 @@ def test_exact_length_buckets_match_oracle_and_launch_twice_per_length():
     close_lse(lse, lref)
 
 
+def test_exact_length_buckets_with_empty_and_repeated_lengths():
+    """Rows sharing a length run in one group; rows without tokens run as one
+    more group that gives them o = 0, lse = -inf."""
+    lens = [300, 0, 64, 300, 1, 0, 64, 1000]
+    tr, q, k, v = case(lens, 8, 2, 128, 16, 64)
+    d = upload(tr, q, k, v)
+    o = torch.full((tr.B, tr.Hq, tr.d), float("nan"), dtype=torch.float16, device="cuda")
+    lse = torch.full((tr.B, tr.Hq), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    api.pkv_reset_counters()
+    groups = api.exact_length_buckets_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], tr.seq_lens,
+                                           64, o, lse, ws=ws)
+    torch.cuda.synchronize()
+    check_error_free(ws)
+    assert groups == 4 + 1  # lengths 1, 64, 300, 1000, then the empty rows
+    c = api.pkv_get_counters()
+    assert c["decode_launches"] + c["merge_launches"] == 2 * groups
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o, oref)
+    close_lse(lse, lref)
+
+
 def test_row_list_step_leaves_other_rows_untouched():
     tr, q, k, v = case([300, 50, 300, 0, 128], Hq=8, Hkv=2, C=64)
     d = upload(tr, q, k, v)
