@@ -123,8 +123,9 @@ def test_fused_append_reports_an_empty_free_list(plan):
     assert btd.cpu().numpy()[0, 1] == free[len(free) - 1]
 
 
-@pytest.mark.parametrize("page,dd,hkv", [(P, D, HKV), (8, 64, 8), (64, 128, 1), (256, 64, 4)])
-def test_row_parallel_append_matches_the_plan_kernels_append(page, dd, hkv):
+@pytest.mark.parametrize("page,dd,hkv,nrows", [(P, D, HKV, 300), (8, 64, 8, 300), (64, 128, 1, 300),
+                                               (256, 64, 4, 300), (P, D, HKV, 512)])
+def test_row_parallel_append_matches_the_plan_kernels_append(page, dd, hkv, nrows):
     """The append launch that leaves the plan to the decode (one CTA per row,
     each counting the rows before it that need a page) against the plan
     kernel's fused append (one CTA, a block scan), on two copies of the same
@@ -132,10 +133,10 @@ def test_row_parallel_append_matches_the_plan_kernels_append(page, dd, hkv):
     pages that runs out at the first step (rows left without a page keep
     asking).  Every step must leave the same block table, lengths, free count,
     error status and cache contents."""
-    rng = np.random.default_rng([T.HELDOUT_SEED, 702, page])
+    rng = np.random.default_rng([T.HELDOUT_SEED, 702, page, nrows])
     nmax = 40 if page <= 16 else 6
-    lens0 = (rng.integers(0, nmax, 300) * page
-             + rng.integers(0, 3, 300) * (rng.random(300) < 0.3)).tolist()
+    lens0 = (rng.integers(0, nmax, nrows) * page
+             + rng.integers(0, 3, nrows) * (rng.random(nrows) < 0.3)).tolist()
     tr = T.custom_trace(lens0, hkv * 2, hkv, dd, page, max(C, page), extra_pages=160, extra_cols=2,
                         tag=703)
     k, v = T.gen_kv(tr)
