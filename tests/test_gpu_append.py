@@ -129,7 +129,7 @@ def test_row_parallel_append_matches_the_plan_kernels_append(page, dd, hkv, nrow
     """The append launch that leaves the plan to the decode (one CTA per row,
     each counting the rows before it that need a page) against the plan
     kernel's fused append (one CTA, a block scan), on two copies of the same
-    state: 300 rows, most of them starting a page, and a free list of 160
+    state: 300 or 512 rows, most of them starting a page, and a free list of 160
     pages that runs out at the first step (rows left without a page keep
     asking).  Every step must leave the same block table, lengths, free count,
     error status and cache contents."""
