@@ -227,33 +227,36 @@ def exact_length_buckets_step(q, k_cache, v_cache, block_table, seq_lens, seq_le
     """The exact-length-bucket scheme the compact workqueue replaces (Results,
     "Scheduling overhead"): one bucketed split + merge launch pair per distinct
     non-zero row length, each over the rows of that length (the groups come from
-    pkv_exact_length_groups), and one more pair over the rows of length 0, if
-    any, which gives them o = 0, lse = -inf.  `seq_lens_host` is the host copy
-    of the lengths.  Returns the number of launch pairs."""
+    pkv_exact_length_groups, every step), and one more pair over the rows of
+    length 0, if any, which gives them o = 0, lse = -inf.  `seq_lens_host` is
+    the host copy of the lengths.  With `rows_cache` the device row lists and
+    launch arguments of a grouping seen before are reused.  Returns the number
+    of launch pairs."""
     shape = make_shape(q, k_cache, block_table)
     rows, start, glen = pkv_exact_length_groups(seq_lens_host)
-    groups = [(int(glen[g]), rows[start[g]:start[g + 1]]) for g in range(glen.size)]
-    if start[-1] < rows.size:
-        groups.append((0, rows[start[-1]:]))  # no tokens: neutral states, o = 0
-    dev = q.device
-    for n, rws in groups:
-        cfg = make_cfg(PKV_PATH_BUCKETED_SPLIT, split_tokens, n if n > 0 else split_tokens)
-        key = (n, tuple(rws.tolist()))
-        if rows_cache is not None and key in rows_cache:
-            rows_t = rows_cache[key]
-        else:
-            rows_t = torch.from_numpy(np.ascontiguousarray(rws)).to(dev)
-            if rows_cache is not None:
-                rows_cache[key] = rows_t
-        sub = Shape(len(rws), shape.Hq, shape.Hkv, shape.d, shape.page_size, shape.num_pages,
-                    shape.bt_stride, shape.scale)
-        need_p = pkv_partials_size(sub, cfg) // 4
+    key = (split_tokens, rows.tobytes(), start.tobytes(), shape.num_pages, shape.bt_stride)
+    launches = rows_cache.get(key) if rows_cache is not None else None
+    if launches is None:
+        dev = q.device
+        groups = [(int(glen[g]), rows[start[g]:start[g + 1]]) for g in range(glen.size)]
+        if start[-1] < rows.size:
+            groups.append((0, rows[start[-1]:]))  # no tokens: neutral states, o = 0
+        launches = []
+        for n, rws in groups:
+            cfg = make_cfg(PKV_PATH_BUCKETED_SPLIT, split_tokens, n if n > 0 else split_tokens)
+            sub = Shape(len(rws), shape.Hq, shape.Hkv, shape.d, shape.page_size, shape.num_pages,
+                        shape.bt_stride, shape.scale)
+            launches.append((cfg, torch.from_numpy(np.ascontiguousarray(rws)).to(dev),
+                             pkv_partials_size(sub, cfg) // 4))
+        if rows_cache is not None:
+            rows_cache[key] = launches
+    for cfg, rows_t, need_p in launches:
         part = partials if partials is not None and partials.numel() >= need_p else \
-            torch.empty(max(need_p, 4), dtype=torch.float32, device=dev)
-        w = ws if ws is not None else torch.zeros(64, dtype=torch.uint8, device=dev)
+            torch.empty(max(need_p, 4), dtype=torch.float32, device=q.device)
+        w = ws if ws is not None else torch.zeros(64, dtype=torch.uint8, device=q.device)
         pkv_decode_step_rows(shape, cfg, w, rows_t, q, k_cache, v_cache, block_table, seq_lens,
                              part, o, lse, stream)
-    return len(groups)
+    return len(launches)
 
 
 def _host(t: Optional[torch.Tensor], name: str, dtype: torch.dtype, nullable: bool = False) -> int:
