@@ -666,10 +666,10 @@ def _ctypes_refs(shape, cfg):
 def run_e2e_cabi(L, torch, tr, q_h, pools, dev, sref, cref, cfg, wsb, part, steps, appends, path):
     """The C ABI's host-buffer step, once per step on the wall clock: every call
     takes the step's inputs from pinned host memory (q and the block table and
-    lengths, copied; or, when the workload appends, q, copied, and the new K/V
-    token, read in place -- the table and lengths being device state the step
-    advances), runs the step, has its last kernel write o and lse into pinned
-    host memory and synchronizes the stream."""
+    lengths; or, when the workload appends, q and the new K/V token -- the table
+    and lengths being device state the step advances), which its kernels read in
+    place, runs the step, has its last kernel write o and lse into pinned host
+    memory and synchronizes the stream."""
     import pkv_traces as T
     from paged_kv_gqa_09_gb300 import _lib
     R = len(pools)
@@ -738,10 +738,9 @@ def run_e2e_cabi(L, torch, tr, q_h, pools, dev, sref, cref, cfg, wsb, part, step
     return {"value": kv / el / 1e9, "unit": UNIT, "us_per_step": el / steps * 1e6, "steps": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ob + lb,
             "timing": f"synchronized wall clock per step: one {name} call (C ABI) per step -- "
-                      + ("q copied in from pinned memory, the new token read in place"
-                         if appends else "q, block table and lengths copied in from pinned memory")
-                      + ", the step's kernels, o/lse written in place into pinned memory by the "
-                        "last kernel, stream synchronized"}
+                      + ("q and the new token" if appends else "q, block table and lengths")
+                      + " read in place from pinned memory by the step's kernels, o/lse written "
+                        "in place into pinned memory by the last kernel, stream synchronized"}
 
 
 def run_e2e(api, torch, tr, q_h, pools, dev, path, C, steps, appends, kn, vn, wsb, merge, plan):

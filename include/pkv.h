@@ -221,10 +221,11 @@ int pkv_decode_step(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d
  * d_block_table and h_seq_lens into d_seq_lens) on `stream`, runs
  * pkv_decode_step, copies d_o into h_o (and d_lse into h_lse when both are
  * non-NULL), then synchronizes `stream`.  One cudaMemcpyAsync per buffer --
- * except that a page-locked (pinned or registered), 16-byte aligned h_o
- * (h_lse) is written straight by the step's last kernel, and d_o (d_lse) is
- * then not written.  Host input buffers should be page-locked for their copies
- * to run asynchronously.  All
+ * except that a page-locked (pinned or registered), 16-byte aligned host
+ * buffer is used in place: h_q, h_block_table and h_seq_lens are then read by
+ * the step's kernels, h_o and h_lse written by its last kernel, and the
+ * matching device buffer is not written.  Pageable host buffers go through the
+ * device buffers (their copies are then synchronous with the host).  All
  * arguments are checked before anything is enqueued.  Same path semantics,
  * layouts and errors as pkv_decode_step. */
 int pkv_decode_step_host(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, void *d_ws,
@@ -242,9 +243,9 @@ int pkv_decode_step_host(const pkv_shape_t *shape, const pkv_plan_cfg_t *cfg, vo
  * Methodology 3, counts with the host's share.)  In order, on `stream`:
  *   1. copies h_q [B][Hq][d] into d_q and the new token's h_k_new, h_v_new
  *      [B][Hkv][d] (fp16) into d_k_new, d_v_new -- one cudaMemcpyAsync each,
- *      except that when h_k_new and h_v_new are both page-locked (pinned or
- *      registered) and 16-byte aligned the append reads them in place and
- *      d_k_new, d_v_new are not written;
+ *      except that a page-locked (pinned or registered), 16-byte aligned h_q
+ *      is read in place by the decode, and page-locked h_k_new and h_v_new by
+ *      the append, and then d_q (d_k_new, d_v_new) is not written;
  *   2. WORKQUEUE: pkv_append_plan (appends, allocates pages from the device
  *      free list when d_free_pages != NULL, and plans unless the decode will),
  *      then pkv_decode + pkv_merge (pkv_decode_merge with PKV_MERGE_FUSED),

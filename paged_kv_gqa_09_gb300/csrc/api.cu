@@ -681,13 +681,26 @@ int pkv_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_
         return fail(PKV_EINVAL, "host q and o are required");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t qbytes = (size_t)s->B * s->Hq * s->d * 2;
-    cudaError_t e = cudaMemcpyAsync(d_q, h_q, qbytes, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && h_bt)
+    // page-locked inputs are read in place by the step's kernels, pageable ones
+    // are copied into the device buffers first
+    const void *q_in = mapped_host(h_q);
+    const int32_t *bt_in = static_cast<const int32_t *>(h_bt ? mapped_host(h_bt) : nullptr);
+    const int32_t *sl_in = static_cast<const int32_t *>(h_sl ? mapped_host(h_sl) : nullptr);
+    cudaError_t e = cudaSuccess;
+    if (!q_in) {
+        e = cudaMemcpyAsync(d_q, h_q, qbytes, cudaMemcpyHostToDevice, st);
+        q_in = d_q;
+    }
+    if (e == cudaSuccess && h_bt && !bt_in)
         e = cudaMemcpyAsync(d_bt, h_bt, (size_t)s->B * s->bt_stride * 4, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && h_sl)
+    if (e == cudaSuccess && h_sl && !sl_in)
         e = cudaMemcpyAsync(d_sl, h_sl, (size_t)s->B * 4, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "host-to-device copy");
+    if (!bt_in)
+        bt_in = d_bt;
+    if (!sl_in)
+        sl_in = d_sl;
     // o / lse are written once: page-locked host buffers take them in place
     void *o_out = mapped_host(h_o);
     float *lse_out = static_cast<float *>(h_lse ? mapped_host(h_lse) : nullptr);
@@ -696,7 +709,7 @@ int pkv_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_
         o_out = d_o;
     if (!lse_out)
         lse_out = d_lse;
-    PKV_TRY(pkv_decode_step(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, o_out, lse_out, stream));
+    PKV_TRY(pkv_decode_step(s, c, d_ws, q_in, k, v, bt_in, sl_in, part, o_out, lse_out, stream));
     e = cudaSuccess;
     if (copy_o)
         e = cudaMemcpyAsync(h_o, d_o, qbytes, cudaMemcpyDeviceToHost, st);
@@ -750,9 +763,10 @@ int pkv_append_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, v
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t qbytes = (size_t)s->B * s->Hq * s->d * 2;
     const size_t nbytes = (size_t)s->B * s->Hkv * s->d * 2;
-    // q is re-read by every split of every kv head: always copied.  The new
-    // token is read once and o / lse written once: page-locked buffers are used
-    // in place, pageable ones go through the device buffers.
+    // page-locked host buffers are used in place by the step's kernels (q,
+    // which every split of every kv head re-reads, mostly from L2), pageable
+    // ones go through the device buffers
+    const void *q_in = mapped_host(h_q);
     const void *kn = mapped_host(h_k_new), *vn = mapped_host(h_v_new);
     if (!kn || !vn)
         kn = vn = nullptr;
@@ -763,7 +777,11 @@ int pkv_append_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, v
         o_out = d_o;
     if (!lse_out)
         lse_out = d_lse;
-    cudaError_t e = cudaMemcpyAsync(d_q, h_q, qbytes, cudaMemcpyHostToDevice, st);
+    cudaError_t e = cudaSuccess;
+    if (!q_in) {
+        e = cudaMemcpyAsync(d_q, h_q, qbytes, cudaMemcpyHostToDevice, st);
+        q_in = d_q;
+    }
     if (e == cudaSuccess && !kn)
         e = cudaMemcpyAsync(d_k_new, h_k_new, nbytes, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess && !vn)
@@ -780,15 +798,15 @@ int pkv_append_decode_step_host(const pkv_shape_t *s, const pkv_plan_cfg_t *c, v
                                 stream));
         // the decode then plans for itself, or reads the plan the append built
         if (c->merge == PKV_MERGE_FUSED) {
-            PKV_TRY(pkv_decode_merge(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, o_out, lse_out,
+            PKV_TRY(pkv_decode_merge(s, c, d_ws, q_in, k, v, d_bt, d_sl, part, o_out, lse_out,
                                      stream));
         } else {
-            PKV_TRY(pkv_decode(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, stream));
+            PKV_TRY(pkv_decode(s, c, d_ws, q_in, k, v, d_bt, d_sl, part, stream));
             PKV_TRY(pkv_merge(s, c, d_ws, d_sl, part, o_out, lse_out, stream));
         }
     } else {
         PKV_TRY(pkv_append(s, d_ws, kn, vn, d_bt, d_sl, k, v, stream));
-        PKV_TRY(pkv_decode_step(s, c, d_ws, d_q, k, v, d_bt, d_sl, part, o_out, lse_out, stream));
+        PKV_TRY(pkv_decode_step(s, c, d_ws, q_in, k, v, d_bt, d_sl, part, o_out, lse_out, stream));
     }
     e = cudaSuccess;
     if (copy_o)

@@ -242,9 +242,9 @@ def test_append_decode_step_host_matches_mirror(path, merge, alloc, pinned):
     """pkv_append_decode_step_host, one synchronized C call per step: q and
     the new token come from host memory, o / lse land in host memory, the
     block table and lengths advance on the device.  With page-locked host
-    buffers the new token is read and o / lse written in place (the device
-    staging for them stays untouched); with pageable ones every buffer goes
-    through its device copy.  Checked against the host mirror of the append
+    buffers q and the new token are read and o / lse written in place (the
+    device staging for them stays untouched); with pageable ones every buffer
+    goes through its device copy.  Checked against the host mirror of the append
     rule and the oracle."""
     steps = 20
     tr, k, v, free = setup([15, 16, 40, 0, 33, 64, 1], steps, spare_pages=30)
@@ -273,7 +273,7 @@ def test_append_decode_step_host_matches_mirror(path, merge, alloc, pinned):
     h_vn = host(torch.empty((tr.B, HKV, D), dtype=torch.float16))
     h_o = host(torch.full((tr.B, HQ, D), float("nan"), dtype=torch.float16))
     h_lse = host(torch.full((tr.B, HQ), float("nan"), dtype=torch.float32))
-    d_q = torch.empty((tr.B, HQ, D), dtype=torch.float16, device="cuda")
+    d_q = torch.full((tr.B, HQ, D), float("nan"), dtype=torch.float16, device="cuda")
     d_kn = torch.full((tr.B, HKV, D), float("nan"), dtype=torch.float16, device="cuda")
     d_vn = torch.full_like(d_kn, float("nan"))
     d_o = torch.full_like(d_q, float("nan"))
@@ -302,11 +302,12 @@ def test_append_decode_step_host_matches_mirror(path, merge, alloc, pinned):
             oref, lref = oracle.attention(q, k_h, v_h, bt_h, lens_h.astype(np.int32), tr.scale)
             close(h_o, oref, f"o at step {step}")
             close_lse(h_lse, lref)
-            staged = [d_kn, d_vn, d_o, d_lse]
+            staged = [d_q, d_kn, d_vn, d_o, d_lse]
             if pinned:  # used in place: the device staging was never written
                 assert all(torch.isnan(t.float()).all() for t in staged)
             else:       # copied through it
                 assert torch.equal(d_o.cpu(), h_o) and torch.equal(d_kn.cpu(), h_kn)
+                assert torch.equal(d_q.cpu(), h_q)
 
 
 def test_append_decode_step_host_checks_before_enqueueing():

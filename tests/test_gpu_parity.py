@@ -519,9 +519,10 @@ def test_host_buffer_step_matches_oracle(cfg_id, path):
 
 @pytest.mark.parametrize("pinned", [True, False])
 def test_host_buffer_step_outputs_in_place_or_copied(pinned):
-    """pkv_decode_step_host writes page-locked h_o / h_lse straight from the
-    step's last kernel (the device buffers stay untouched) and copies through
-    d_o / d_lse into pageable ones; both match the oracle."""
+    """pkv_decode_step_host reads page-locked q, block table and lengths in
+    place and writes page-locked h_o / h_lse straight from the step's last
+    kernel (the device buffers stay untouched); pageable buffers go through the
+    device ones.  Both match the oracle."""
     tr = T.make_trace(3)
     q = T.gen_q(tr)
     k, v = T.gen_kv(tr)
@@ -538,16 +539,21 @@ def test_host_buffer_step_outputs_in_place_or_copied(pinned):
     h_lse = host(torch.full(q.shape[:2], float("nan"), dtype=torch.float32))
     d_o = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
     d_lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
-    api.pkv_decode_step_host(shape, cfg, ws, part, hq, d["q"], hbt, d["bt"], hsl, d["sl"], d["k"],
+    d_q = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
+    d_bt = torch.full_like(d["bt"], -7)
+    d_sl = torch.full_like(d["sl"], -7)
+    api.pkv_decode_step_host(shape, cfg, ws, part, hq, d_q, hbt, d_bt, hsl, d_sl, d["k"],
                              d["v"], d_o, h_o, d_lse, h_lse)
     check_error_free(ws)
     oref, lref = oracle_out(tr, q, k, v)
     close(h_o, oref)
     close_lse(h_lse, lref)
-    if pinned:
+    if pinned:  # every host buffer used in place: the device ones were never written
         assert torch.isnan(d_o.float()).all() and torch.isnan(d_lse).all()
+        assert torch.isnan(d_q.float()).all() and (d_bt == -7).all() and (d_sl == -7).all()
     else:
         assert torch.equal(d_o.cpu(), h_o) and torch.equal(d_lse.cpu(), h_lse)
+        assert torch.equal(d_q.cpu(), hq) and torch.equal(d_bt.cpu(), hbt) and torch.equal(d_sl.cpu(), hsl)
 
 
 # ------------------------------------------------------------------ exact-length buckets
