@@ -16,8 +16,9 @@
 //             directly (the policy's no-split route).
 //
 // CTA layout (160 threads, two CTAs per SM, ~104 KB shared memory each):
-//   warp 4      producer: walks this CTA's tasks (static stride over the task
-//               index), reads block-table entries, and streams each 64-token
+//   warp 4      producer: walks this CTA's tasks (claimed one at a time in
+//               the workqueue's balance order, or a static stride over the
+//               task index), reads block-table entries, and streams each 64-token
 //               tile of K and V straight from the pages into a ring of
 //               shared-memory stages with TMA (cp.async.bulk.tensor, 128-byte
 //               swizzle, evict-first L2 policy).  No page is repacked.
@@ -92,16 +93,18 @@ __device__ __forceinline__ TaskInfo shfl_task(const TaskInfo &a, int src)
 
 // Prefix sums of a self-planning workqueue launch in shared memory: F[i] full
 // splits and R[i] shorter last splits in the rows before i (B + 1 entries
-// each); F == nullptr when the plan kernel wrote the task list.
+// each), and S the rows that end in a shorter split, in balance order;
+// F == nullptr when the plan kernel wrote the task list.
 struct SelfPlan {
     const int *F, *R;
+    const int16_t *S;
 };
 
 // Workqueue task k (balance order) as {row, kv head, split, first state slot}.
 __device__ __forceinline__ int4 queue_record(const DecodeParams &p, const SelfPlan &sp, int k)
 {
     if (sp.F)
-        return plan_task_at(k, sp.F, sp.R, p.B, p.Hkv, p.Hq, p.G, nullptr);
+        return plan_task_at(k, sp.F, sp.R, sp.S, p.B, p.Hkv, p.Hq, p.G, nullptr);
     return p.tasks[k];
 }
 
@@ -946,11 +949,14 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &p, uint32_t sba
 // states start at the exclusive prefix of n).  Rows go 32 at a time, one per
 // lane (all lengths loaded at once); a warp scan per round plus a carry gives
 // the prefixes F (full splits) and R (shorter last splits) of every row,
-// B + 1 entries each, in shared memory.  CTA 0 also writes what the merge and
-// the workspace's readers expect of the plan kernel: offsets, short_before,
-// the header's task count, state rows and overflow flag, and any bad length.
-// Returns the task count (0 after an overflow of the launch's capacity).
-__device__ __forceinline__ int self_plan_warp(const DecodeParams &p, int *F, int *R)
+// B + 1 entries each, in shared memory, and a ballot per length class counts
+// the shorter splits of each class; a second pass over the lengths then
+// places each row with a shorter split in S, longest class first and by row
+// within a class.  CTA 0 also writes what the merge and the workspace's
+// readers expect of the plan kernel: offsets, short_before, the header's task
+// count, state rows and overflow flag, and any bad length.  Returns the task
+// count (0 after an overflow of the launch's capacity).
+__device__ __forceinline__ int self_plan_warp(const DecodeParams &p, int *F, int *R, int16_t *S)
 {
     constexpr int kRounds = kSelfPlanMaxB / 32;
     const int lane = threadIdx.x & 31;
@@ -970,6 +976,10 @@ __device__ __forceinline__ int self_plan_warp(const DecodeParams &p, int *F, int
         len[u] = i < p.B ? p.seq_lens[i] : 0;
     }
     long long cf = 0, cr = 0;  // splits of the rows before this round
+    int in_class[kShortClasses];  // shorter splits per length class
+#pragma unroll
+    for (int c = 0; c < kShortClasses; ++c)
+        in_class[c] = 0;
 #pragma unroll
     for (int u = 0; u < kRounds; ++u) {
         if (u * 32 >= p.B)
@@ -981,7 +991,12 @@ __device__ __forceinline__ int self_plan_warp(const DecodeParams &p, int *F, int
                 report_error(p.ws, N < 0 ? kErrNegLen : kErrTooLong, i, N, p.len_cap);
             N = N < 0 ? 0 : p.len_cap;
         }
+        len[u] = N;
         const int f = N / p.C, r = (N % p.C) != 0 ? 1 : 0;
+        const int cls = r ? plan_short_class(N % p.C, p.C) : -1;
+#pragma unroll
+        for (int c = 0; c < kShortClasses; ++c)
+            in_class[c] += __popc(__ballot_sync(0xffffffffu, cls == c));
         long long xf = f, xr = r;  // inclusive warp scans
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -1003,6 +1018,29 @@ __device__ __forceinline__ int self_plan_warp(const DecodeParams &p, int *F, int
         }
         cf += __shfl_sync(0xffffffffu, xf, 31);
         cr += __shfl_sync(0xffffffffu, xr, 31);
+    }
+    // S: the longest class first; within a class, rows in order
+    int next[kShortClasses];
+    int acc = 0;
+#pragma unroll
+    for (int c = kShortClasses - 1; c >= 0; --c) {
+        next[c] = acc;
+        acc += in_class[c];
+    }
+    const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+        if (u * 32 >= p.B)
+            break;
+        const int N = len[u];  // clamped above; 0 past the last row
+        const int cls = (N % p.C) != 0 ? plan_short_class(N % p.C, p.C) : -1;
+#pragma unroll
+        for (int c = 0; c < kShortClasses; ++c) {
+            const unsigned m = __ballot_sync(0xffffffffu, cls == c);
+            if (cls == c)
+                S[next[c] + __popc(m & below)] = (int16_t)(u * 32 + lane);
+            next[c] += __popc(m);
+        }
     }
     const long long T = (cf + cr) * p.Hkv;
     const bool over = T > p.n_tasks;  // the capacity, at most INT32_MAX: F and R fit in int
@@ -1045,7 +1083,7 @@ __device__ __forceinline__ void self_plan_write_tasks(const DecodeParams &p, con
     constexpr int kWriters = 32 * kCW;
     for (int64_t t = (int64_t)blockIdx.x * kWriters + threadIdx.x; t < ntasks; t += (int64_t)gridDim.x * kWriters) {
         int64_t lex;
-        const int4 rec = plan_task_at((int)t, sp.F, sp.R, p.B, p.Hkv, p.Hq, p.G, &lex);
+        const int4 rec = plan_task_at((int)t, sp.F, sp.R, sp.S, p.B, p.Hkv, p.Hq, p.G, &lex);
         p.plan_ordered[t] = rec;
         p.plan_tasks[lex] = rec;
     }
@@ -1070,6 +1108,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the self-planning workqueue's prefix sums F, R (the other instances keep one word)
     constexpr bool kSelf = MODE == kModeQueue && !FUSE;
     __shared__ int s_plan[kSelf ? 2 * (kSelfPlanMaxB + 1) + 1 : 1];  // + the task count
+    __shared__ int16_t s_short_rows[kSelf ? kSelfPlanMaxB : 1];           // and S
 
     if (threadIdx.x == 0) {
         s_ctl[0] = s_ctl[1] = 0;
@@ -1091,14 +1130,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     // it has finished and its writes are visible
     pdl_wait();
     pdl_trigger();
-    SelfPlan sp{nullptr, nullptr};
+    SelfPlan sp{nullptr, nullptr, nullptr};
     int ntasks = p.n_tasks;
     if constexpr (kSelf) {
         if (p.self_plan) {
-            sp = SelfPlan{s_plan, s_plan + kSelfPlanMaxB + 1};
+            sp = SelfPlan{s_plan, s_plan + kSelfPlanMaxB + 1, s_short_rows};
             int *s_count = s_plan + 2 * (kSelfPlanMaxB + 1);
             if (warp == kCW) {
-                ntasks = self_plan_warp(p, s_plan, s_plan + kSelfPlanMaxB + 1);
+                ntasks = self_plan_warp(p, s_plan, s_plan + kSelfPlanMaxB + 1, s_short_rows);
                 if ((threadIdx.x & 31) == 0)
                     *s_count = ntasks;
                 plan_barrier_arrive();

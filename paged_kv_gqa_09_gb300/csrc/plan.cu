@@ -13,12 +13,14 @@
 //   g = (k - Hkv*offsets[i]) / n_i, j = ... % n_i -- the lexicographic
 //   (row, kv-head, split) order.  The host never reads T back.
 // A second copy of the same records, in balance order (every full-length
-// split first, by row, split and kv head, then each row's shorter last
-// split), is what the decode kernel's CTAs claim from: the launch ends on
-// short tasks, and the kv heads of one split, claimed together, read the same
-// pages at about the same time.
+// split first, by row, split and kv head, then the shorter last splits,
+// longest length class first, by row and kv head), is what the decode
+// kernel's CTAs claim from: the launch ends on its shortest tasks, and the kv
+// heads of one split, claimed together, read the same pages at about the
+// same time.
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
+#include "plan_map.cuh"
 
 namespace pkv {
 namespace {
@@ -58,6 +60,49 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int *t
     *total = warp_tot[32];
     __syncthreads();
     return ex;
+}
+
+// The same over one 64-bit word per thread: four 16-bit counters scanned at
+// once (each stays below 2^16 within one block of rows).
+__device__ __forceinline__ unsigned long long block_exclusive_scan64(unsigned long long x,
+                                                                     unsigned long long *warp_tot,
+                                                                     unsigned long long *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const unsigned long long t = warp_tot[lane];
+        unsigned long long sc = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, sc, o);
+            if (lane >= o)
+                sc += y;
+        }
+        warp_tot[lane] = sc - t;
+        if (lane == 31)
+            warp_tot[32] = sc;
+    }
+    __syncthreads();
+    const unsigned long long ex = warp_tot[warp] + incl - x;
+    *total = warp_tot[32];
+    __syncthreads();
+    return ex;
+}
+
+// Counter c of a packed word.
+__device__ __forceinline__ int packed_field(unsigned long long x, int c)
+{
+    return (int)((x >> (16 * c)) & 0xffffull);
 }
 
 // The fused append: for every row i with length N, write k_new[i], v_new[i]
@@ -145,9 +190,10 @@ __device__ void append_tokens(const PlanParams &p, int *warp_tot, long long *s_d
     __syncthreads();
 }
 
-// n_i = ceil(N_i / C) of row i and r_i = 1 when it ends in a shorter split,
-// the length clamped to [0, len_cap] (reported when it was outside).
-__device__ __forceinline__ void row_splits(const PlanParams &p, int i, bool report, int &n, int &r)
+// n_i = ceil(N_i / C) of row i, r_i = 1 when it ends in a shorter split and
+// that split's length class (-1 without one), the length clamped to
+// [0, len_cap] (reported when it was outside).
+__device__ __forceinline__ void row_splits(const PlanParams &p, int i, bool report, int &n, int &r, int &cls)
 {
     int N = p.k_new ? p.seq_lens_rw[i] : p.seq_lens[i];  // the same thread appended to it
     if (report && (N < 0 || N > p.len_cap))
@@ -155,15 +201,27 @@ __device__ __forceinline__ void row_splits(const PlanParams &p, int i, bool repo
     N = N < 0 ? 0 : (N > p.len_cap ? p.len_cap : N);
     n = (N + p.C - 1) / p.C;
     r = (N % p.C) != 0 ? 1 : 0;
+    cls = r ? plan_short_class(N % p.C, p.C) : -1;
 }
+
+// A row's class as two packed words of four one-hot 16-bit counters.
+__device__ __forceinline__ void class_words(int cls, unsigned long long &lo, unsigned long long &hi)
+{
+    lo = (cls >= 0 && cls < 4) ? 1ull << (16 * cls) : 0ull;
+    hi = cls >= 4 ? 1ull << (16 * (cls - 4)) : 0ull;
+}
+static_assert(kShortClasses == 8, "two packed words of four classes");
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
 {
     __shared__ int warp_tot[33];
+    __shared__ unsigned long long warp_tot64[33];
     __shared__ long long s_dst[kPlanThreads];
-    // offsets and short-split prefix of the current chunk's rows (+ the row after)
+    // offsets and short-split prefix of the current chunk's rows (+ the row
+    // after), and each row's place among the shorter splits in balance order
     __shared__ int s_off[kPlanThreads + 1];
     __shared__ int s_sb[kPlanThreads + 1];
+    __shared__ int s_srank[kPlanThreads];
     pdl_wait();
     pdl_trigger();
     const int tid = threadIdx.x;
@@ -171,47 +229,64 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
     if (p.k_new)
         append_tokens(p, warp_tot, s_dst);
     // the balance order puts every full-length split before the shorter last
-    // splits, so the totals are needed before the first task is written: one
-    // extra pass over the lengths when the rows span several chunks
+    // splits, and those by length class, so the totals are needed before the
+    // first task is written: one extra pass over the lengths when the rows
+    // span several chunks
     int total = 0, total_r = 0;
+    int in_class[kShortClasses] = {};
     const bool chunks = p.B > kPlanThreads;
     if (chunks) {
         for (int base = 0; base < p.B; base += kPlanThreads) {
-            int n = 0, r = 0, tot, tot_r;
+            int n = 0, r = 0, cls = -1, tot, tot_r;
             if (base + tid < p.B)
-                row_splits(p, base + tid, false, n, r);
+                row_splits(p, base + tid, false, n, r, cls);
+            unsigned long long lo, hi, tlo, thi;
+            class_words(cls, lo, hi);
             block_exclusive_scan(n, warp_tot, &tot);
             block_exclusive_scan(r, warp_tot, &tot_r);
+            block_exclusive_scan64(lo, warp_tot64, &tlo);
+            block_exclusive_scan64(hi, warp_tot64, &thi);
             total += tot;
             total_r += tot_r;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                in_class[c] += packed_field(tlo, c);
+                in_class[c + 4] += packed_field(thi, c);
+            }
         }
     }
     int carry = 0, carry_r = 0;
+    int class_next[kShortClasses];  // next place among the shorter splits, per class
     bool overflow = false;
     int64_t n_full = 0;
     for (int base = 0; base < p.B || base == 0; base += kPlanThreads) {
         const int i = base + tid;
-        int n = 0, r = 0;
+        int n = 0, r = 0, cls = -1;
         if (i < p.B)
-            row_splits(p, i, true, n, r);
+            row_splits(p, i, true, n, r, cls);
         int tot, tot_r;
+        unsigned long long lo, hi, tlo, thi;
+        class_words(cls, lo, hi);
         const int ex = block_exclusive_scan(n, warp_tot, &tot);
         const int ex_r = block_exclusive_scan(r, warp_tot, &tot_r);
+        const unsigned long long ex_lo = block_exclusive_scan64(lo, warp_tot64, &tlo);
+        const unsigned long long ex_hi = block_exclusive_scan64(hi, warp_tot64, &thi);
         const int rows = min(kPlanThreads, p.B - base);
-        if (i < p.B) {
-            p.offsets[i] = carry + ex;
-            p.short_before[i] = carry_r + ex_r;
-            s_off[tid] = carry + ex;
-            s_sb[tid] = carry_r + ex_r;
-        }
-        if (tid == 0) {
-            s_off[rows] = carry + tot;
-            s_sb[rows] = carry_r + tot_r;
-        }
         if (base == 0) {
             if (!chunks) {
                 total = tot;
                 total_r = tot_r;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    in_class[c] = packed_field(tlo, c);
+                    in_class[c + 4] = packed_field(thi, c);
+                }
+            }
+            int acc = 0;
+#pragma unroll
+            for (int c = kShortClasses - 1; c >= 0; --c) {
+                class_next[c] = acc;
+                acc += in_class[c];
             }
             const int64_t T = (int64_t)total * p.Hkv;
             overflow = T > p.max_tasks;
@@ -226,6 +301,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
                                  (int32_t)p.max_tasks, 0);
             }
         }
+        if (i < p.B) {
+            p.offsets[i] = carry + ex;
+            p.short_before[i] = carry_r + ex_r;
+            s_off[tid] = carry + ex;
+            s_sb[tid] = carry_r + ex_r;
+            if (cls >= 0)
+                s_srank[tid] = class_next[cls] + packed_field(cls < 4 ? ex_lo : ex_hi, cls & 3);
+        }
+        if (tid == 0) {
+            s_off[rows] = carry + tot;
+            s_sb[rows] = carry_r + tot_r;
+        }
         __syncthreads();
         if (!overflow) {
             // this chunk's tasks: k in [Hkv * carry, Hkv * (carry + tot)), lexicographic
@@ -233,33 +320,38 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
             for (int64_t k = (int64_t)carry * p.Hkv + tid; k < k1; k += kPlanThreads) {
                 // last chunk row lo with Hkv * offsets <= k (rows without splits share
                 // the next row's offset, so the search lands on the row holding k)
-                int lo = 0, hi = rows - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
+                int lo_r = 0, hi_r = rows - 1;
+                while (lo_r < hi_r) {
+                    const int mid = (lo_r + hi_r + 1) >> 1;
                     if ((int64_t)s_off[mid] * p.Hkv <= k)
-                        lo = mid;
+                        lo_r = mid;
                     else
-                        hi = mid - 1;
+                        hi_r = mid - 1;
                 }
-                const int oi = s_off[lo];
-                const int ni = s_off[lo + 1] - oi;
+                const int oi = s_off[lo_r];
+                const int ni = s_off[lo_r + 1] - oi;
                 const int kk = (int)(k - (int64_t)oi * p.Hkv);
                 const int g = kk / ni, j = kk - g * ni;
-                const int4 rec = make_int4(base + lo, g, j, (oi + j) * p.Hq + g * p.G);
+                const int4 rec = make_int4(base + lo_r, g, j, (oi + j) * p.Hq + g * p.G);
                 p.tasks[k] = rec;
-                // balance order: a shorter split goes after every full one, by
-                // row then kv head; a full split j of row i sits at
-                // Hkv * (full splits before row i + j) + g
-                const int sb = s_sb[lo];
-                const int has_short = s_sb[lo + 1] - sb;
+                // balance order: a shorter split goes after every full one, at
+                // its row's place among them, then by kv head; a full split j
+                // of row i sits at Hkv * (full splits before row i + j) + g
+                const int sb = s_sb[lo_r];
+                const int has_short = s_sb[lo_r + 1] - sb;
                 const bool is_short = has_short && j == ni - 1;
-                const int64_t pos = is_short ? n_full + (int64_t)sb * p.Hkv + g
+                const int64_t pos = is_short ? n_full + (int64_t)s_srank[lo_r] * p.Hkv + g
                                              : ((int64_t)(oi - sb) + j) * p.Hkv + g;
                 p.tasks_ordered[pos] = rec;
             }
         }
         carry += tot;
         carry_r += tot_r;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            class_next[c] += packed_field(tlo, c);
+            class_next[c + 4] += packed_field(thi, c);
+        }
         __syncthreads();  // the chunk's shared offsets are rewritten next
         if (base + kPlanThreads >= p.B)
             break;

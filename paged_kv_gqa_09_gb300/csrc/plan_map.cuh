@@ -13,10 +13,16 @@
 //                                  heads of one split sit side by side, so
 //                                  CTAs that claim them together read the
 //                                  same pages at about the same time;
-//   positions [Hkv*F_B, Hkv*(F_B+R_B))  each shorter last split, by row, then
-//                                  kv head.
+//   positions [Hkv*F_B, Hkv*(F_B+R_B))  each shorter last split, longest
+//                                  class first, then by row, then kv head.
+//                                  The class of a shorter split of
+//                                  N_i mod C tokens is
+//                                  floor(kShortClasses * (N_i mod C) / C):
+//                                  the launch ends on its shortest tasks, so
+//                                  the CTAs finish closer together.
 // Both lists are the plan kernel's output; the self-planning decode rebuilds
-// the mapping from F and R held in shared memory.
+// the mapping from F, R and the class-ordered list of rows with a shorter
+// split (S), held in shared memory.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -26,6 +32,16 @@ namespace pkv {
 
 // Rows that the self-planning decode keeps in shared memory.
 constexpr int kSelfPlanMaxB = 512;
+
+// Length classes of the shorter last splits (the balance order takes them
+// from the longest class down).
+constexpr int kShortClasses = 8;
+
+// Class of a shorter split of r tokens, 0 < r < C.
+__host__ __device__ inline int plan_short_class(int r, int C)
+{
+    return (int)(((int64_t)r * kShortClasses) / C);
+}
 
 // Largest i in [0, B) with key * pre[i] <= x (pre non-decreasing, pre[0] = 0 <= x).
 __host__ __device__ inline int plan_last_row_at_or_below(const int *pre, int B, int key, int x)
@@ -43,9 +59,10 @@ __host__ __device__ inline int plan_last_row_at_or_below(const int *pre, int B, 
 
 // The task at balance position t (0 <= t < Hkv*(F[B]+R[B])) as the record
 // {row, kv head, split, first state slot}, and its lexicographic index.
-// F and R hold B + 1 entries each.
-__host__ __device__ inline int4 plan_task_at(int t, const int *F, const int *R, int B, int Hkv, int Hq,
-                                             int G, int64_t *lex)
+// F and R hold B + 1 entries each; S holds the R[B] rows that end in a
+// shorter split, in balance order.
+__host__ __device__ inline int4 plan_task_at(int t, const int *F, const int *R, const int16_t *S, int B,
+                                             int Hkv, int Hq, int G, int64_t *lex)
 {
     const int n_full = Hkv * F[B];
     int i, g, j;
@@ -58,7 +75,7 @@ __host__ __device__ inline int4 plan_task_at(int t, const int *F, const int *R, 
         const int u = t - n_full;
         const int q = u / Hkv;
         g = u - q * Hkv;
-        i = plan_last_row_at_or_below(R, B, 1, q);
+        i = S[q];
         j = F[i + 1] - F[i];  // the shorter split comes after the row's full ones
     }
     const int off = F[i] + R[i];

@@ -4,12 +4,12 @@
 // directory.
 #include "plan_map.cuh"
 
-extern "C" int plan_map_all(int B, const int *F, const int *R, int Hkv, int Hq, int G, int T,
-                            int *rec, long long *lex)
+extern "C" int plan_map_all(int B, const int *F, const int *R, const int16_t *S, int Hkv, int Hq,
+                            int G, int T, int *rec, long long *lex)
 {
     for (int t = 0; t < T; ++t) {
         int64_t k = -1;
-        const int4 r = pkv::plan_task_at(t, F, R, B, Hkv, Hq, G, &k);
+        const int4 r = pkv::plan_task_at(t, F, R, S, B, Hkv, Hq, G, &k);
         rec[4 * t] = r.x;
         rec[4 * t + 1] = r.y;
         rec[4 * t + 2] = r.z;

@@ -11,6 +11,7 @@ import torch
 
 import oracle
 import pkv_traces as T
+from plan_order import balance_order
 from paged_kv_gqa_09_gb300 import _lib, api
 
 from gpu_util import (check_error_free, close, close_lse, dev, oracle_out, read_plan, run_path,
@@ -65,18 +66,10 @@ def test_plan_matches_oracle_bit_exact(lens, C):
     assert np.array_equal(tasks, want)
     assert h[0] == 0 and h[6] == 0
     check_error_free(ws)
-    # the decode walks a balance-ordered copy: the same records, every
-    # full-length split first by (row, split, kv head), then the rows' shorter
-    # last splits in canonical order
-    lens = np.asarray(lens)
-    n = -(-lens // C)
-    short = np.array([(lens[r[0]] % C != 0) and r[2] == n[r[0]] - 1 for r in want], dtype=bool)
-    if count:
-        full = want[~short]
-        full = full[np.lexsort((full[:, 1], full[:, 2], full[:, 0]))]
-        expect = np.concatenate([full, want[short]])
-    else:
-        expect = want
+    # the decode walks a balance-ordered copy of the same records
+    # (plan_order.py: full-length splits first, then the shorter last splits
+    # from the longest length class down)
+    expect = want[balance_order(want, lens, C)] if count else want
     assert np.array_equal(ordered, expect)
 
 

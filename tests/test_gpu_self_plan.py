@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import oracle
+from plan_order import balance_order
 import pkv_traces as T
 from paged_kv_gqa_09_gb300 import _lib, api
 
@@ -36,17 +37,8 @@ def _lib_loaded():
 
 
 def expected_order(want, lens, C):
-    """The balance order: every full-length split by (row, split, kv head) --
-    the kv heads of one split side by side -- then each row's shorter last
-    split in canonical order."""
-    lens = np.asarray(lens)
-    n = -(-lens // C)
-    short = np.array([(lens[r[0]] % C != 0) and r[2] == n[r[0]] - 1 for r in want], dtype=bool)
-    if not len(want):
-        return want
-    full = want[~short]
-    full = full[np.lexsort((full[:, 1], full[:, 2], full[:, 0]))]
-    return np.concatenate([full, want[short]])
+    """The balance order (plan_order.py) of the canonical list `want`."""
+    return want[balance_order(want, lens, C)] if len(want) else want
 
 
 def check_plan(ws, tr, C):

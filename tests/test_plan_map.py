@@ -4,11 +4,13 @@
 Commodity GPUs", technical summary, Methodology 1, "Compact workqueue": the
 decode's CTAs take the plan's tasks in balance order (every full-length split,
 by row, then split, then kv head -- the kv heads of one split side by side --
-then each row's shorter last split).  When the decode builds the plan itself it
-maps a position t to its task from two per-row prefix sums (plan_map.cuh, a
-host-and-device function).  Here that map, compiled for the host, is compared
-with the oracle's canonical task list reordered by the definition: the same
-record at every position, and each position's index in the canonical list.
+then the shorter last splits, longest length class first, by row and kv head;
+`plan_order.py` states it).  When the decode builds the plan itself it maps a
+position t to its task from two per-row prefix sums and the class-ordered list
+of rows with a shorter split (plan_map.cuh, a host-and-device function).  Here
+that map, compiled for the host, is compared with the oracle's canonical task
+list reordered by the definition: the same record at every position, and each
+position's index in the canonical list.
 """
 import ctypes
 import os
@@ -19,6 +21,7 @@ import numpy as np
 import pytest
 
 import oracle
+from plan_order import balance_order, short_rows
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "paged_kv_gqa_09_gb300", "csrc")
@@ -34,7 +37,7 @@ def pmap(tmp_path_factory):
                     os.path.join(ROOT, "tests", "plan_map_host.cu")], check=True)
     L = ctypes.CDLL(str(out))
     vp, ci = ctypes.c_void_p, ctypes.c_int
-    L.plan_map_all.argtypes = [ci, vp, vp, ci, ci, ci, ci, vp, vp]
+    L.plan_map_all.argtypes = [ci, vp, vp, vp, ci, ci, ci, ci, vp, vp]
     return L
 
 
@@ -43,17 +46,15 @@ def check(L, lens, C, Hkv, G):
     B, Hq = lens.size, Hkv * G
     canon, off = oracle.plan_compact(lens, Hq, Hkv, C)
     T = canon.shape[0]
-    n = -(-lens.astype(np.int64) // C)
-    short = np.array([(lens[r[0]] % C != 0) and r[2] == n[r[0]] - 1 for r in canon], dtype=bool)
-    full = np.flatnonzero(~short)
-    # full splits by (row, split, kv head); the shorter ones in canonical order
-    full = full[np.lexsort((canon[full, 1], canon[full, 2], canon[full, 0]))]
-    order = np.concatenate([full, np.flatnonzero(short)]).astype(np.int64)
+    order = balance_order(canon, lens, C)
     F = np.concatenate([[0], np.cumsum(lens // C)]).astype(np.int32)
     R = np.concatenate([[0], np.cumsum(lens % C != 0)]).astype(np.int32)
+    S = np.zeros(max(B, 1), np.int16)
+    S[:R[-1]] = short_rows(lens, C)
     rec = np.zeros((max(T, 1), 4), np.int32)
     lex = np.zeros(max(T, 1), np.int64)
-    L.plan_map_all(B, F.ctypes.data, R.ctypes.data, Hkv, Hq, G, T, rec.ctypes.data, lex.ctypes.data)
+    L.plan_map_all(B, F.ctypes.data, R.ctypes.data, S.ctypes.data, Hkv, Hq, G, T, rec.ctypes.data,
+                   lex.ctypes.data)
     assert np.array_equal(rec[:T], canon[order]), (lens.tolist(), C)
     assert np.array_equal(lex[:T], order)
     assert np.array_equal(F + R, off)  # the map's prefix sums are the plan's offsets
@@ -67,6 +68,7 @@ def check(L, lens, C, Hkv, G):
     ([1, 2, 3, 4, 5], 64),                 # only shorter splits
     ([0] * 30 + [70] + [0] * 30, 16),      # one row among empty ones
     ([777], 256),
+    ([10, 250, 130, 70, 255, 31, 32, 224], 256),  # every length class, out of order
 ])
 @pytest.mark.parametrize("Hkv,G", [(1, 1), (2, 4), (8, 8)])
 def test_map_matches_the_plan_on_edge_cases(pmap, lens, C, Hkv, G):
@@ -94,3 +96,16 @@ def test_map_at_the_largest_self_planned_batch(pmap):
     rng = np.random.default_rng(7)
     check(pmap, rng.integers(0, 3000, size=512), 256, 8, 8)
     check(pmap, [1] * 512, 16, 2, 4)
+
+
+def test_balance_order_definition_on_a_worked_case():
+    """The definition itself, on a batch small enough to order by hand:
+    C = 256, one kv head, rows of 300, 100, 250 and 512 tokens.  Full splits:
+    row 0 split 0, row 3 splits 0 and 1.  Shorter splits: row 0 44 tokens
+    (class 1), row 1 100 (class 3), row 2 250 (class 7)."""
+    lens = np.array([300, 100, 250, 512])
+    canon, _ = oracle.plan_compact(lens, 1, 1, 256)
+    got = canon[balance_order(canon, lens, 256)][:, :3].tolist()
+    # full splits: row 0 split 0, row 3 splits 0 and 1; then rows 2, 1, 0 by class
+    assert got == [[0, 0, 0], [3, 0, 0], [3, 0, 1], [2, 0, 0], [1, 0, 0], [0, 0, 1]]
+    assert short_rows(lens, 256).tolist() == [2, 1, 0]
