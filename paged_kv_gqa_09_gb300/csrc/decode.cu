@@ -615,20 +615,44 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
     }
 }
 
+// L2 prefetch of the first `span` tokens from token t0 of row i0, kv head g0:
+// lane l takes page s0 + l of the range (tiles hold whole pages when
+// P <= 64); block-table entries are read past L1 and only valid page ids
+// drive a prefetch.
+__device__ __forceinline__ void prefetch_task_tiles(const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                                    const DecodeParams &p, int i0, int g0, int t0, int span)
+{
+    const int lane = threadIdx.x & 31;
+    const int log2P = p.log2P, btl = p.box_log2;
+    const int n_pages = ((span - 1) >> log2P) + 1;
+    const int64_t row = (int64_t)i0 * p.bt_stride;
+    const int s0 = t0 >> log2P;
+    if (lane < n_pages && s0 + lane < p.bt_stride) {
+        const int pg = __ldcg(p.bt + row + s0 + lane);
+        if (pg >= 0 && pg < p.num_pages) {
+            // one box per page when P <= 64, else the page's boxes inside the span
+            for (int b = 0; (b << btl) < (1 << log2P) && (b << btl) < span; ++b) {
+                tma_prefetch_5d(tmK, 0, b << btl, 0, g0, pg);
+                tma_prefetch_5d(tmV, 0, b << btl, 0, g0, pg);
+            }
+        }
+    }
+}
+
 // Before the kernel may read its inputs (griddepcontrol.wait), warm L2 with
 // the first tiles of this CTA's first task: block-table entries are read
 // L2-only (they may still be changing, so they must not land in L1) and only
 // drive TMA prefetches, which cannot change any result.  The real loads after
-// the wait re-read everything.  Rectangular and single modes only: the
-// workqueue's task list is being written by the plan kernel right before.
+// the wait re-read everything.  Rectangular and single modes: the workqueue's
+// task list is being written by the plan kernel right before, and a
+// self-planning workqueue finds its first task itself
+// (prefetch_first_queue_tiles).
 template <int D, int MODE>
 __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap *tmK, const CUtensorMap *tmV,
                                                      const DecodeParams &p)
 {
     if (MODE == kModeQueue || (int)blockIdx.x >= p.n_tasks)
         return;
-    const int lane = threadIdx.x & 31;
-    const int log2P = p.log2P, btl = p.box_log2;
     int i0, g0, j0;
     if (MODE == kModeRect) {
         const int per_row = p.Hkv * p.S_b;
@@ -643,21 +667,56 @@ __device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap *tmK, con
     }
     if (i0 < 0 || i0 >= p.B)
         return;
-    const int t0 = MODE == kModeSingle ? 0 : j0 * p.C;
-    const int span = MODE == kModeSingle ? kPrefetchTiles * kTile : min(p.C, kPrefetchTiles * kTile);
-    const int n_pages = ((span - 1) >> log2P) + 1;
-    const int64_t row = (int64_t)i0 * p.bt_stride;
-    // lane l prefetches page s0 + l of the range (tiles hold whole pages when P <= 64)
-    const int s0 = t0 >> log2P;
-    if (lane < n_pages && s0 + lane < p.bt_stride) {
-        const int pg = __ldcg(p.bt + row + s0 + lane);
-        if (pg >= 0 && pg < p.num_pages) {
-            // one box per page when P <= 64, else the page's boxes inside the span
-            for (int b = 0; (b << btl) < (1 << log2P) && (b << btl) < span; ++b) {
-                tma_prefetch_5d(tmK, 0, b << btl, 0, g0, pg);
-                tma_prefetch_5d(tmV, 0, b << btl, 0, g0, pg);
-            }
+    prefetch_task_tiles(tmK, tmV, p, i0, g0, MODE == kModeSingle ? 0 : j0 * p.C,
+                        MODE == kModeSingle ? kPrefetchTiles * kTile : min(p.C, kPrefetchTiles * kTile));
+}
+
+// The self-planning workqueue's version, run by consumer warp 0 while the
+// producer waits for the previous kernel and then plans: the CTA's first task
+// is balance position blockIdx.x, and when that is a full split (the whole
+// first round on a batch of long rows) its row, kv head and split follow from
+// a scan of f_i = floor(N_i / C) over the lengths as they are now (read past
+// L1, since they may still be changing).  Shorter first tasks are not
+// prefetched.  Nothing is written; the producer's own plan decides.
+__device__ __forceinline__ void prefetch_first_queue_tiles(const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                                           const DecodeParams &p)
+{
+    constexpr int kRounds = kSelfPlanMaxB / 32;
+    if (p.B > kSelfPlanMaxB)
+        return;
+    const int lane = threadIdx.x & 31;
+    const long long b = blockIdx.x;
+    int len[kRounds];
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+        const int i = u * 32 + lane;
+        len[u] = u * 32 < p.B && i < p.B ? __ldcg(p.seq_lens + i) : 0;
+    }
+    long long carry = 0;  // full splits of the rows before this round
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+        if (u * 32 >= p.B)
+            break;
+        const int N = min(max(len[u], 0), p.len_cap);
+        const int f = N / p.C;
+        long long x = f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += y;
         }
+        const long long lo = (carry + x - f) * p.Hkv;
+        const unsigned m = __ballot_sync(0xffffffffu, b >= lo && b < (carry + x) * p.Hkv);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            const int kk = (int)(b - __shfl_sync(0xffffffffu, lo, src));
+            const int j0 = kk / p.Hkv;
+            prefetch_task_tiles(tmK, tmV, p, u * 32 + src, kk - j0 * p.Hkv, j0 * p.C,
+                                min(p.C, kPrefetchTiles * kTile));
+            return;
+        }
+        carry += __shfl_sync(0xffffffffu, x, 31);
     }
 }
 
@@ -1126,6 +1185,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == kCW)
         prefetch_first_tiles<D, MODE>(&tmK, &tmV, p);
     __syncthreads();
+    if constexpr (kSelf)
+        if (p.self_plan && warp == 0)
+            prefetch_first_queue_tiles(&tmK, &tmV, p);
     // everything above overlaps the previous kernel; nothing below runs before
     // it has finished and its writes are visible
     pdl_wait();
