@@ -1182,12 +1182,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
     }
-    if (warp == kCW)
-        prefetch_first_tiles<D, MODE>(&tmK, &tmV, p);
     __syncthreads();
-    if constexpr (kSelf)
-        if (p.self_plan && warp == 0)
-            prefetch_first_queue_tiles(&tmK, &tmV, p);
+    // consumer warp 0 warms L2 with the CTA's first tiles while the producer
+    // waits for the previous kernel (and plans)
+    if (warp == 0) {
+        if constexpr (kSelf) {
+            if (p.self_plan)
+                prefetch_first_queue_tiles(&tmK, &tmV, p);
+        } else {
+            prefetch_first_tiles<D, MODE>(&tmK, &tmV, p);
+        }
+    }
     // everything above overlaps the previous kernel; nothing below runs before
     // it has finished and its writes are visible
     pdl_wait();
