@@ -53,7 +53,11 @@ constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any barrier wait
 constexpr uint64_t kDrainNs = 20000000ull;   // bound when draining after a timeout
 constexpr float kLn2 = 0.6931471805599453f;
 
-constexpr int kPrefetchTiles = 4;  // tiles of the first task prefetched into L2 early
+// tiles of the first task prefetched into L2 early: the workqueue's first
+// tasks are full splits of at least a few tiles; deeper prefetch on the
+// rectangular grid's one-row launches only competed with the real loads
+constexpr int kPrefetchTiles = 4;
+constexpr int kQueuePrefetchTiles = 8;
 
 constexpr int kFirst = 1 << 16;  // stage flags (low 16 bits: valid tokens)
 constexpr int kLast = 1 << 17;
@@ -713,7 +717,7 @@ __device__ __forceinline__ void prefetch_first_queue_tiles(const CUtensorMap *tm
             const int kk = (int)(b - __shfl_sync(0xffffffffu, lo, src));
             const int j0 = kk / p.Hkv;
             prefetch_task_tiles(tmK, tmV, p, u * 32 + src, kk - j0 * p.Hkv, j0 * p.C,
-                                min(p.C, kPrefetchTiles * kTile));
+                                min(p.C, kQueuePrefetchTiles * kTile));
             return;
         }
         carry += __shfl_sync(0xffffffffu, x, 31);
