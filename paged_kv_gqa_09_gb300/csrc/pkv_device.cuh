@@ -79,8 +79,6 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-// Programmatic dependent launch: wait for the preceding grid (and its memory),
-// and allow the next grid in the stream to be scheduled early.
 // GPU-scope acquire load / release store of one int (grid-wide barrier words).
 __device__ __forceinline__ int ld_acquire_gpu(const int *p)
 {
@@ -93,6 +91,8 @@ __device__ __forceinline__ void st_release_gpu(int *p, int v)
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Programmatic dependent launch: wait for the preceding grid (and its memory),
+// and allow the next grid in the stream to be scheduled early.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
