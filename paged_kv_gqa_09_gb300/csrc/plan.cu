@@ -62,47 +62,81 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int *t
     return ex;
 }
 
-// The same over one 64-bit word per thread: four 16-bit counters scanned at
-// once (each stays below 2^16 within one block of rows).
-__device__ __forceinline__ unsigned long long block_exclusive_scan64(unsigned long long x,
-                                                                     unsigned long long *warp_tot,
-                                                                     unsigned long long *total)
+// A row's counts for the plan: its splits n_i, and its shorter split (if
+// any) as a one-hot 16-bit counter of its length class -- classes 0..3 in
+// `lo`, 4..7 in `hi` (each counter stays below 2^16 within one block of
+// rows), so that the sum of the eight counters is r_i.
+struct RowCounts {
+    int n;
+    unsigned long long lo, hi;
+};
+
+__device__ __forceinline__ RowCounts operator+(const RowCounts &x, const RowCounts &y)
+{
+    return RowCounts{x.n + y.n, x.lo + y.lo, x.hi + y.hi};
+}
+
+__device__ __forceinline__ RowCounts operator-(const RowCounts &x, const RowCounts &y)
+{
+    return RowCounts{x.n - y.n, x.lo - y.lo, x.hi - y.hi};
+}
+
+__device__ __forceinline__ RowCounts shfl_up_counts(const RowCounts &x, int o)
+{
+    return RowCounts{__shfl_up_sync(0xffffffffu, x.n, o), __shfl_up_sync(0xffffffffu, x.lo, o),
+                     __shfl_up_sync(0xffffffffu, x.hi, o)};
+}
+
+// Block-wide exclusive scan of every count of a row at once (one pass, one
+// set of barriers); sets *total to the block sums.
+__device__ __forceinline__ RowCounts block_exclusive_scan_counts(const RowCounts &x, RowCounts *warp_tot,
+                                                                 RowCounts *total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    unsigned long long incl = x;
+    RowCounts incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        const RowCounts y = shfl_up_counts(incl, o);
         if (lane >= o)
-            incl += y;
+            incl = incl + y;
     }
     if (lane == 31)
         warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const unsigned long long t = warp_tot[lane];
-        unsigned long long sc = t;
+        const RowCounts t = warp_tot[lane];
+        RowCounts sc = t;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = __shfl_up_sync(0xffffffffu, sc, o);
+            const RowCounts y = shfl_up_counts(sc, o);
             if (lane >= o)
-                sc += y;
+                sc = sc + y;
         }
         warp_tot[lane] = sc - t;
         if (lane == 31)
             warp_tot[32] = sc;
     }
     __syncthreads();
-    const unsigned long long ex = warp_tot[warp] + incl - x;
+    const RowCounts ex = warp_tot[warp] + incl - x;
     *total = warp_tot[32];
     __syncthreads();
     return ex;
 }
 
-// Counter c of a packed word.
-__device__ __forceinline__ int packed_field(unsigned long long x, int c)
+// Counter c (0..7) of a row's packed class counters, and the sum of all
+// eight (the shorter splits).
+__device__ __forceinline__ int class_count(const RowCounts &x, int c)
 {
-    return (int)((x >> (16 * c)) & 0xffffull);
+    return (int)(((c < 4 ? x.lo : x.hi) >> (16 * (c & 3))) & 0xffffull);
+}
+
+__device__ __forceinline__ int short_count(const RowCounts &x)
+{
+    int r = 0;
+#pragma unroll
+    for (int c = 0; c < kShortClasses; ++c)
+        r += class_count(x, c);
+    return r;
 }
 
 // The fused append: for every row i with length N, write k_new[i], v_new[i]
@@ -204,18 +238,22 @@ __device__ __forceinline__ void row_splits(const PlanParams &p, int i, bool repo
     cls = r ? plan_short_class(N % p.C, p.C) : -1;
 }
 
-// A row's class as two packed words of four one-hot 16-bit counters.
-__device__ __forceinline__ void class_words(int cls, unsigned long long &lo, unsigned long long &hi)
+// A row's counts from its splits and its shorter split's class (-1: none).
+__device__ __forceinline__ RowCounts row_counts(int n, int cls)
 {
-    lo = (cls >= 0 && cls < 4) ? 1ull << (16 * cls) : 0ull;
-    hi = cls >= 4 ? 1ull << (16 * (cls - 4)) : 0ull;
+    RowCounts x{n, 0ull, 0ull};
+    if (cls >= 0 && cls < 4)
+        x.lo = 1ull << (16 * cls);
+    else if (cls >= 4)
+        x.hi = 1ull << (16 * (cls - 4));
+    return x;
 }
 static_assert(kShortClasses == 8, "two packed words of four classes");
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
 {
     __shared__ int warp_tot[33];
-    __shared__ unsigned long long warp_tot64[33];
+    __shared__ RowCounts warp_counts[33];
     __shared__ long long s_dst[kPlanThreads];
     // offsets and short-split prefix of the current chunk's rows (+ the row
     // after), and each row's place among the shorter splits in balance order
@@ -237,22 +275,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
     const bool chunks = p.B > kPlanThreads;
     if (chunks) {
         for (int base = 0; base < p.B; base += kPlanThreads) {
-            int n = 0, r = 0, cls = -1, tot, tot_r;
+            int n = 0, r = 0, cls = -1;
             if (base + tid < p.B)
                 row_splits(p, base + tid, false, n, r, cls);
-            unsigned long long lo, hi, tlo, thi;
-            class_words(cls, lo, hi);
-            block_exclusive_scan(n, warp_tot, &tot);
-            block_exclusive_scan(r, warp_tot, &tot_r);
-            block_exclusive_scan64(lo, warp_tot64, &tlo);
-            block_exclusive_scan64(hi, warp_tot64, &thi);
-            total += tot;
-            total_r += tot_r;
+            RowCounts tot;
+            block_exclusive_scan_counts(row_counts(n, cls), warp_counts, &tot);
+            total += tot.n;
+            total_r += short_count(tot);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                in_class[c] += packed_field(tlo, c);
-                in_class[c + 4] += packed_field(thi, c);
-            }
+            for (int c = 0; c < kShortClasses; ++c)
+                in_class[c] += class_count(tot, c);
         }
     }
     int carry = 0, carry_r = 0;
@@ -264,23 +296,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
         int n = 0, r = 0, cls = -1;
         if (i < p.B)
             row_splits(p, i, true, n, r, cls);
-        int tot, tot_r;
-        unsigned long long lo, hi, tlo, thi;
-        class_words(cls, lo, hi);
-        const int ex = block_exclusive_scan(n, warp_tot, &tot);
-        const int ex_r = block_exclusive_scan(r, warp_tot, &tot_r);
-        const unsigned long long ex_lo = block_exclusive_scan64(lo, warp_tot64, &tlo);
-        const unsigned long long ex_hi = block_exclusive_scan64(hi, warp_tot64, &thi);
+        RowCounts tot;
+        const RowCounts ex = block_exclusive_scan_counts(row_counts(n, cls), warp_counts, &tot);
+        const int ex_r = short_count(ex), tot_r = short_count(tot);
         const int rows = min(kPlanThreads, p.B - base);
         if (base == 0) {
             if (!chunks) {
-                total = tot;
+                total = tot.n;
                 total_r = tot_r;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    in_class[c] = packed_field(tlo, c);
-                    in_class[c + 4] = packed_field(thi, c);
-                }
+                for (int c = 0; c < kShortClasses; ++c)
+                    in_class[c] = class_count(tot, c);
             }
             int acc = 0;
 #pragma unroll
@@ -302,56 +328,54 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p)
             }
         }
         if (i < p.B) {
-            p.offsets[i] = carry + ex;
+            p.offsets[i] = carry + ex.n;
             p.short_before[i] = carry_r + ex_r;
-            s_off[tid] = carry + ex;
+            s_off[tid] = carry + ex.n;
             s_sb[tid] = carry_r + ex_r;
             if (cls >= 0)
-                s_srank[tid] = class_next[cls] + packed_field(cls < 4 ? ex_lo : ex_hi, cls & 3);
+                s_srank[tid] = class_next[cls] + class_count(ex, cls);
         }
         if (tid == 0) {
-            s_off[rows] = carry + tot;
+            s_off[rows] = carry + tot.n;
             s_sb[rows] = carry_r + tot_r;
         }
         __syncthreads();
         if (!overflow) {
-            // this chunk's tasks: k in [Hkv * carry, Hkv * (carry + tot)), lexicographic
-            const int64_t k1 = (int64_t)(carry + tot) * p.Hkv;
+            // this chunk's tasks: k in [Hkv * carry, Hkv * (carry + tot.n)), lexicographic
+            const int64_t k1 = (int64_t)(carry + tot.n) * p.Hkv;
             for (int64_t k = (int64_t)carry * p.Hkv + tid; k < k1; k += kPlanThreads) {
                 // last chunk row lo with Hkv * offsets <= k (rows without splits share
                 // the next row's offset, so the search lands on the row holding k)
-                int lo_r = 0, hi_r = rows - 1;
-                while (lo_r < hi_r) {
-                    const int mid = (lo_r + hi_r + 1) >> 1;
+                int lo = 0, hi = rows - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
                     if ((int64_t)s_off[mid] * p.Hkv <= k)
-                        lo_r = mid;
+                        lo = mid;
                     else
-                        hi_r = mid - 1;
+                        hi = mid - 1;
                 }
-                const int oi = s_off[lo_r];
-                const int ni = s_off[lo_r + 1] - oi;
+                const int oi = s_off[lo];
+                const int ni = s_off[lo + 1] - oi;
                 const int kk = (int)(k - (int64_t)oi * p.Hkv);
                 const int g = kk / ni, j = kk - g * ni;
-                const int4 rec = make_int4(base + lo_r, g, j, (oi + j) * p.Hq + g * p.G);
+                const int4 rec = make_int4(base + lo, g, j, (oi + j) * p.Hq + g * p.G);
                 p.tasks[k] = rec;
                 // balance order: a shorter split goes after every full one, at
                 // its row's place among them, then by kv head; a full split j
                 // of row i sits at Hkv * (full splits before row i + j) + g
-                const int sb = s_sb[lo_r];
-                const int has_short = s_sb[lo_r + 1] - sb;
+                const int sb = s_sb[lo];
+                const int has_short = s_sb[lo + 1] - sb;
                 const bool is_short = has_short && j == ni - 1;
-                const int64_t pos = is_short ? n_full + (int64_t)s_srank[lo_r] * p.Hkv + g
+                const int64_t pos = is_short ? n_full + (int64_t)s_srank[lo] * p.Hkv + g
                                              : ((int64_t)(oi - sb) + j) * p.Hkv + g;
                 p.tasks_ordered[pos] = rec;
             }
         }
-        carry += tot;
+        carry += tot.n;
         carry_r += tot_r;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            class_next[c] += packed_field(tlo, c);
-            class_next[c + 4] += packed_field(thi, c);
-        }
+        for (int c = 0; c < kShortClasses; ++c)
+            class_next[c] += class_count(tot, c);
         __syncthreads();  // the chunk's shared offsets are rewritten next
         if (base + kPlanThreads >= p.B)
             break;
