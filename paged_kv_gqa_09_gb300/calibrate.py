@@ -8,8 +8,10 @@ choosing the route by batch size B and the longest context N_max) and Results
 
 Procedure:
 1. For every trace of a grid -- families bucketed / bimodal / uniform / Zipf,
-   B in {1..64}, N_max in {256..65536}, Hq=32, Hkv=8, d=128, page_size 16 --
-   time every route (bucketed split and workqueue at several split sizes C,
+   B in {1..64}, N_max in {256..65536}, Hq=32, Hkv=8, d=128, page_size 16,
+   plus the uniform and bimodal families at G=8 (Hq=64) for B in {8..64} and
+   N_max >= 4096, where a split's fp32 state holds twice the bytes and the
+   split size matters most -- time every route (bucketed split and workqueue at several split sizes C,
    single pass) as synchronized wall-clock per decode step through the C ABI
    (host planning and launches included, as the pages measure; the workqueue
    with its plan built inside the decode, as PagedDecoder runs it).
@@ -20,7 +22,12 @@ Procedure:
    number of splits) minimising the mean ratio of the chosen
    route's time to the best route's time over the calibration traces.  The
    workqueue's rule is fitted first, on the workqueue's own times, then the
-   cut-offs with it.
+   cut-offs with it.  Each route is also timed on the device (its step
+   captured ten times in a CUDA graph and replayed); parameter sets whose
+   calibration regret lies within 0.25% of the best -- closer than two full
+   runs agree -- are told apart by their device-time regret.  The learned cost
+   model's features do not include G, so
+   it is fitted on the G=4 traces.
 3. Re-time the same grid drawn with the held-out seed and report the chosen
    policy's regret there.
 
@@ -44,6 +51,17 @@ HQ, HKV, D, P = 32, 8, 128, 16
 BATCHES = [1, 2, 4, 8, 16, 32, 64]
 NMAX = [256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536]
 FAMILIES = ["bucketed", "bimodal", "uniform", "zipf"]
+# the G=8 part of the grid (Hq=64): large batches of long rows
+HQ_G8 = 64
+G8_FAMILIES = ["bimodal", "uniform"]
+G8_BATCHES = [8, 16, 32, 64]
+G8_NMAX = [4096, 8192, 16384, 32768, 65536]
+
+
+def grid():
+    """(family, B, N_max, Hq) of every calibration trace."""
+    out = [(f, B, n, HQ) for f, B, n in itertools.product(FAMILIES, BATCHES, NMAX)]
+    return out + [(f, B, n, HQ_G8) for f, B, n in itertools.product(G8_FAMILIES, G8_BATCHES, G8_NMAX)]
 BUCKETED_C = [128, 256, 512, 1024, 2048]
 WORKQUEUE_C = [256, 512, 1024, 2048, 4096]
 WQ_TARGETS = [0, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096]  # 0: C fixed at its smallest
@@ -52,6 +70,11 @@ TOKEN_CUTS = [0, 256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 1 << 30]
 BATCH_CUTS_MAX = [0, 1, 2, 4, 8, 16, 32, 64]
 BATCH_CUTS_MIN = [1, 2, 4, 8, 16, 32, 64, 1 << 30]
 
+
+GRAPH_STEPS, GRAPH_REPLAYS = 10, 3  # device time per route: steps per graph, replays
+# parameter sets whose calibration regret is within this factor of the best
+# are tied at the measurement's resolution (two full runs differ by ~0.1-0.2%)
+TIE = 1.0025
 
 PARAM_NAMES = ["bucketed_min_tokens", "bucketed_max_batch", "workqueue_min_tokens",
                "workqueue_min_batch", "split_tokens", "bucketed_split_tokens",
@@ -79,7 +102,7 @@ def routes():
     return out + [("single", 0)]
 
 
-def measure(seed: int, reps: int = 7, warm: int = 2, log=print):
+def measure(seed: int, reps: int = 25, warm: int = 2, log=print):
     import torch
 
     from paged_kv_gqa_09_gb300 import _lib, api
@@ -92,7 +115,7 @@ def measure(seed: int, reps: int = 7, warm: int = 2, log=print):
     rng = np.random.default_rng([seed, 77])
     results = []
     stream = torch.cuda.current_stream().cuda_stream
-    for fam, B, n_max in itertools.product(FAMILIES, BATCHES, NMAX):
+    for fam, B, n_max, hq in grid():
         lens = lengths(fam, B, n_max, rng)
         npg = (lens + P - 1) // P
         stride = int(npg.max())
@@ -102,13 +125,13 @@ def measure(seed: int, reps: int = 7, warm: int = 2, log=print):
         for i in range(B):
             bt[i, : npg[i]] = pages[pos: pos + npg[i]]
             pos += npg[i]
-        q = torch.randn((B, HQ, D), dtype=torch.float16, device=dev)
+        q = torch.randn((B, hq, D), dtype=torch.float16, device=dev)
         btd = torch.from_numpy(bt).to(dev)
         sld = torch.from_numpy(lens).to(dev)
         o = torch.empty_like(q)
-        lse = torch.empty((B, HQ), dtype=torch.float32, device=dev)
-        shape = _lib.Shape(B, HQ, HKV, D, P, max_pages, stride, 1.0 / math.sqrt(D))
-        times = {}
+        lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
+        shape = _lib.Shape(B, hq, HKV, D, P, max_pages, stride, 1.0 / math.sqrt(D))
+        times, dev_times = {}, {}
         for name, C in routes():
             path = {"bucketed": 0, "workqueue": 1, "single": 2}[name]
             # the workqueue as PagedDecoder runs it: its plan built by the decode
@@ -131,14 +154,34 @@ def measure(seed: int, reps: int = 7, warm: int = 2, log=print):
                     raise RuntimeError(_lib.last_error())
                 if r >= warm:
                     ts.append(t1 - t0)
+            # device time: the same call captured GRAPH_STEPS times in a CUDA
+            # graph on a side stream and replayed, host launches out of the picture
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            args_side = args[:-1] + (side.cuda_stream,)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(GRAPH_STEPS):
+                    L.pkv_decode_step(*args_side)
+            graph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(GRAPH_REPLAYS):
+                graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            del graph
             st, msg = api.pkv_get_error(ws)
             if st != 0:
                 raise RuntimeError(msg)
             times[f"{name}:{C}"] = float(np.median(ts)) * 1e6
-        results.append({"family": fam, "B": B, "n_max": n_max,
-                        "kv_bytes": int(lens.astype(np.int64).sum()) * HKV * D * 4, "us": times})
+            dev_times[f"{name}:{C}"] = e0.elapsed_time(e1) * 1e3 / (GRAPH_REPLAYS * GRAPH_STEPS)
+        results.append({"family": fam, "B": B, "n_max": n_max, "Hq": hq,
+                        "kv_bytes": int(lens.astype(np.int64).sum()) * HKV * D * 4, "us": times,
+                        "dev_us": dev_times})
         best = min(times, key=times.get)
-        log(f"{fam:9s} B={B:3d} Nmax={n_max:6d}: best {best:15s} {times[best]:8.1f} us")
+        log(f"{fam:9s} Hq={hq:2d} B={B:3d} Nmax={n_max:6d}: best {best:15s} {times[best]:8.1f} us")
     return results
 
 
@@ -169,50 +212,76 @@ def regret(params, results):
     return float(np.mean(r)), float(np.max(r))
 
 
+def _pick(cands):
+    """The chosen candidate of a search: (score, device score, params) tuples;
+    the lowest calibration score wins, and candidates within TIE of it are
+    told apart by their device-time score (graph-replayed steps), where the
+    measurements have one.  Ties keep the search order."""
+    best = min(c[0] for c in cands)
+    near = [c for c in cands if c[0] <= best * TIE]
+    if all(c[1] is not None for c in near):
+        return min(near, key=lambda c: c[1])
+    return min(cands, key=lambda c: c[0])
+
+
+def _has_dev(results):
+    return all("dev_us" in r for r in results)
+
+
 def fit_wq_rule(results):
     """(c_min, c_max, target, long_splits) of the workqueue's split rule
     minimising the mean ratio of the rule's workqueue time to the best
     workqueue time, over the traces long enough for the workqueue to be a
-    candidate (N_max >= 1024)."""
+    candidate (N_max >= 1024); near-ties go to the better device time."""
     rows = [r for r in results if r["n_max"] >= 1024]
+    dev = _has_dev(rows)
     best_wq = [min(r["us"][f"workqueue:{c}"] for c in WORKQUEUE_C) for r in rows]
-    best_rule, best_score = None, math.inf
+    best_dev = [min(r["dev_us"][f"workqueue:{c}"] for c in WORKQUEUE_C) for r in rows] if dev else None
+    cands = []
     for c_min, c_max, target, ls in itertools.product(WORKQUEUE_C, WORKQUEUE_C, WQ_TARGETS,
                                                       WQ_LONG_SPLITS):
         if c_max < c_min or (target == 0 and (c_max != c_min or ls != 0)):
             continue
-        score = float(np.mean([
-            r["us"][f"workqueue:{wq_split(r['B'], r['n_max'], c_min, c_max, target, ls)}"] / b
-            for r, b in zip(rows, best_wq)]))
-        if score < best_score - 1e-12:
-            best_rule, best_score = (c_min, c_max, target, ls), score
-    return best_rule
+        keys = [f"workqueue:{wq_split(r['B'], r['n_max'], c_min, c_max, target, ls)}" for r in rows]
+        score = float(np.mean([r["us"][k] / b for r, k, b in zip(rows, keys, best_wq)]))
+        dscore = float(np.mean([r["dev_us"][k] / b for r, k, b in zip(rows, keys, best_dev)])) if dev else None
+        cands.append((score, dscore, (c_min, c_max, target, ls)))
+    return _pick(cands)[2]
 
 
 def fit(results):
     c_min, c_max, target, ls = fit_wq_rule(results)
     names = [f"{n}:{c}" for n, c in routes()]
+    dev = _has_dev(results)
     tmat = np.array([[res["us"][k] for k in names] for res in results])
+    dmat = np.array([[res["dev_us"][k] for k in names] for res in results]) if dev else None
     best = tmat.min(axis=1)
+    dbest = dmat.min(axis=1) if dev else None
     Bv = np.array([res["B"] for res in results])
     Nv = np.array([res["n_max"] for res in results])
     col = {k: i for i, k in enumerate(names)}
-    wq = np.array([res["us"][f"workqueue:{wq_split(res['B'], res['n_max'], c_min, c_max, target, ls)}"]
-                   for res in results])
-    single = tmat[:, col["single:0"]]
-    best_params, best_score = None, math.inf
+    wq_col = np.array([col[f"workqueue:{wq_split(res['B'], res['n_max'], c_min, c_max, target, ls)}"]
+                       for res in results])
+    rows = np.arange(len(results))
+    cands = []
     for bmin_tok, bmax_b, wmin_tok, wmin_b in itertools.product(TOKEN_CUTS, BATCH_CUTS_MAX,
                                                                 TOKEN_CUTS, BATCH_CUTS_MIN):
         is_b = (Bv >= 1) & (Bv <= bmax_b) & (Nv >= bmin_tok)
         is_w = ~is_b & (Bv >= wmin_b) & (Nv >= wmin_tok)
         for c_b in BUCKETED_C:
-            bk = tmat[:, col[f"bucketed:{c_b}"]]
-            chosen = np.where(is_b, bk, np.where(is_w, wq, single))
-            score = float(np.mean(chosen / best))
-            if score < best_score - 1e-12:
-                best_score = score
-                best_params = (bmin_tok, bmax_b, wmin_tok, wmin_b, c_min, c_b, c_max, target, ls)
-    return best_params, best_score
+            chosen_col = np.where(is_b, col[f"bucketed:{c_b}"], np.where(is_w, wq_col, col["single:0"]))
+            score = float(np.mean(tmat[rows, chosen_col] / best))
+            dscore = float(np.mean(dmat[rows, chosen_col] / dbest)) if dev else None
+            cands.append((score, dscore, (bmin_tok, bmax_b, wmin_tok, wmin_b, c_min, c_b, c_max, target, ls)))
+    score, _, params = _pick(cands)
+    return params, score
+
+
+def device_regret(params, results):
+    """Mean and worst device-time ratio of the chosen route to the best one."""
+    r = [res["dev_us"][choose(params, res["B"], res["n_max"])] / min(res["dev_us"].values())
+         for res in results]
+    return float(np.mean(r)), float(np.max(r))
 
 
 # ----------------------------------------------------------- learned model
@@ -234,6 +303,11 @@ def features(B: int, n_max: int, n_sum: int) -> np.ndarray:
 
 def trace_features(res) -> np.ndarray:
     return features(res["B"], res["n_max"], res["kv_bytes"] // (HKV * D * 4))
+
+
+def group4(results):
+    """The G=4 traces (the learned model's features do not include G)."""
+    return [r for r in results if r.get("Hq", HQ) == HQ]
 
 
 def fit_cost_model(results):
@@ -280,16 +354,21 @@ def render_markdown(out: dict) -> str:
              "    python -m paged_kv_gqa_09_gb300.calibrate --from-json policy_calibration.json "
              "--md policy_calibration.md", "",
              "Grid: families bucketed / bimodal / uniform / Zipf x B in {1,2,4,8,16,32,64} x N_max in",
-             "{256..65536}; Hq=32, Hkv=8, d=128, page_size 16. Routes: bucketed split C in {128..2048},",
+             "{256..65536}; Hq=32, Hkv=8, d=128, page_size 16; plus bimodal / uniform at G=8 (Hq=64) x B in",
+             "{8,16,32,64} x N_max in {4096..65536}. Routes: bucketed split C in {128..2048},",
              "workqueue C in {256..4096} (its plan built inside the decode), single pass. Time = median",
              "synchronized wall-clock per decode step through the C ABI (launches and host planning",
-             "included). Policy parameters searched to minimise",
-             "the mean chosen/best time ratio on the calibration seed 20260622, then checked on held-out seed",
-             "20260623.", "",
+             "included); each route's device time is also taken, from its step captured ten times in a",
+             "CUDA graph and replayed. Policy parameters searched to minimise the mean chosen/best",
+             "wall-clock ratio on the calibration seed 20260622 (sets within 0.25% of the best, closer",
+             "than two full runs agree, are told apart by the device-time ratio), then checked on",
+             "held-out seed 20260623.", "",
              f"Frozen in `pkv_policy_default`: {p}", "",
              f"- calibration seed mean regret: {out['calibration_mean_regret']:.3f}",
              "- held-out seed mean / max regret: "
-             f"{out['heldout_mean_max_regret'][0]:.3f} / {out['heldout_mean_max_regret'][1]:.2f}",
+             f"{out['heldout_mean_max_regret'][0]:.3f} / {out['heldout_mean_max_regret'][1]:.2f}"
+             + (f" (device time: {out['heldout_device_regret'][0]:.3f} / {out['heldout_device_regret'][1]:.2f})"
+                if out.get("heldout_device_regret") else ""),
              "- the pages' routing with its own cut-offs (B=1 -> bucketed, B>=8 -> workqueue, long = 4096,",
              "  C=1024), held-out mean / max regret: "
              f"{out['pages_structure_default_heldout_regret'][0]:.3f} / "
@@ -301,12 +380,29 @@ def render_markdown(out: dict) -> str:
         for B in BATCHES:
             cells = []
             for n in NMAX:
-                res = next(r for r in held if r["family"] == fam and r["B"] == B and r["n_max"] == n)
+                res = next(r for r in held if r["family"] == fam and r["B"] == B and r["n_max"] == n
+                           and r.get("Hq", HQ) == HQ)
                 best = min(res["us"], key=res["us"].get)
                 ratio = res["us"][choose(pv, B, n)] / res["us"][best]
                 name, c = best.split(":")
                 cells.append(f"{ratio:.2f} {short[name]}" + (f":{c}" if name != "single" else ""))
             lines.append(f"| {B} | " + " | ".join(cells) + " |")
+        lines.append("")
+    g8 = [r for r in held if r.get("Hq", HQ) == HQ_G8]
+    if g8:
+        lines += ["Held-out, G=8 (Hq=64) traces: chosen/best time ratio, best route, and the chosen workqueue C", "",
+                  "| family, B \\ N_max | " + " | ".join(str(n) for n in G8_NMAX) + " |",
+                  "|---|" + "---|" * len(G8_NMAX)]
+        for fam in G8_FAMILIES:
+            for B in G8_BATCHES:
+                cells = []
+                for n in G8_NMAX:
+                    res = next(r for r in g8 if r["family"] == fam and r["B"] == B and r["n_max"] == n)
+                    best = min(res["us"], key=res["us"].get)
+                    ch = choose(pv, B, n)
+                    name, c = best.split(":")
+                    cells.append(f"{res['us'][ch] / res['us'][best]:.2f} {short[name]}:{c} ({ch.split(':')[1]})")
+                lines.append(f"| {fam}, {B} | " + " | ".join(cells) + " |")
         lines.append("")
     worst = max(held, key=lambda r: r["us"][choose(pv, r["B"], r["n_max"])] / min(r["us"].values()))
     wr = worst["us"][choose(pv, worst["B"], worst["n_max"])] / min(worst["us"].values())
@@ -321,7 +417,9 @@ def render_markdown(out: dict) -> str:
               "Per route, log(step time) fitted by least squares on features of the batch the host knows:",
               "f = [1, lb, ln, ls, lb*ln, lb^2, ln^2, fill, fill*lb, ls^2] with lb = log2 B, ln = log2 N_max,",
               "ls = log2 sum N_i, fill = sum N_i / (B N_max); the route of smallest predicted time is chosen",
-              "(`pkv_policy_learned`; coefficients in `api.cu`, printed by the command above).", "",
+              "(`pkv_policy_learned`; coefficients in `api.cu`, printed by the command above). The features",
+              "do not include G, so the model is fitted and scored on the G=4 traces; the thresholds' row",
+              "covers the whole grid.", "",
               "| policy | calibration seed mean / max regret | held-out seed mean / max regret |",
               "|---|---|---|",
               f"| thresholds on (B, N_max) (`pkv_policy`) | {out['calibration_mean_regret']:.3f} / - | "
@@ -338,7 +436,7 @@ def render_markdown(out: dict) -> str:
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default="policy_calibration.json")
-    ap.add_argument("--reps", type=int, default=7)
+    ap.add_argument("--reps", type=int, default=25)
     ap.add_argument("--from-json", default=None,
                     help="refit from an earlier run's measurements instead of timing")
     ap.add_argument("--md", default=None, help="also write the markdown summary here")
@@ -350,7 +448,7 @@ def main(argv=None):
         cal = measure(T.CALIBRATION_SEED, a.reps)
         held = None
     params, score = fit(cal)
-    model = fit_cost_model(cal)
+    model = fit_cost_model(group4(cal))
     if held is None:
         held = measure(T.HELDOUT_SEED, a.reps)
     # the pages' routing with RTX 3060-era cut-offs, one fixed C per route
@@ -359,9 +457,10 @@ def main(argv=None):
         "params": dict(zip(PARAM_NAMES, params)),
         "calibration_mean_regret": score,
         "heldout_mean_max_regret": regret(params, held),
+        "heldout_device_regret": device_regret(params, held) if _has_dev(held) else None,
         "pages_structure_default_heldout_regret": regret(pages_default, held),
-        "learned_model_calibration_regret": model_regret(model, cal),
-        "learned_model_heldout_regret": model_regret(model, held),
+        "learned_model_calibration_regret": model_regret(model, group4(cal)),
+        "learned_model_heldout_regret": model_regret(model, group4(held)),
         "learned_model": {k: [float(x) for x in w] for k, w in model.items()},
         "calibration": cal, "heldout": held,
     }

@@ -895,15 +895,15 @@ void pkv_policy_default(pkv_policy_cfg_t *c)
 {
     if (!c)
         return;
-    c->bucketed_min_tokens = 16384;
-    c->bucketed_max_batch = 1;
-    c->workqueue_min_tokens = 1024;
+    c->bucketed_min_tokens = 1024;
+    c->bucketed_max_batch = 4;
+    c->workqueue_min_tokens = 2048;
     c->workqueue_min_batch = 1;
     c->split_tokens = 256;
-    c->bucketed_split_tokens = 1024;
-    c->workqueue_max_split_tokens = 4096;
+    c->bucketed_split_tokens = 512;
+    c->workqueue_max_split_tokens = 1024;
     c->workqueue_target_splits = 32;
-    c->workqueue_min_long_splits = 16;
+    c->workqueue_min_long_splits = 8;
 }
 
 int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t *out_path,
@@ -944,17 +944,17 @@ int pkv_policy(int32_t B, int32_t n_max, const pkv_policy_cfg_t *cfg, pkv_path_t
 // workqueue with its plan built inside the decode and its full splits claimed
 // kv heads side by side); held-out seed 20260623 mean regret 1.028 (worst 1.27x).
 static const pkv_cost_route_t kGb300Routes[] = {
-    {0, 128, {6.43522312f, 0.155240338f, 0.0571267949f, -0.826889369f, -9.77361572e-05f, 0.00964326087f, 0.00721835884f, 0.289587404f, -0.0323441347f, 0.0324759047f}},
-    {0, 256, {6.90634468f, 0.11561489f, 0.073463712f, -0.876175914f, 0.00222917506f, 0.00446850577f, 0.00291227527f, 0.228681386f, -0.0486112449f, 0.0362076469f}},
-    {0, 512, {6.97477146f, 0.0467281537f, 0.0915738729f, -0.871211625f, 0.00683948306f, 0.0035246084f, 0.000610483019f, 0.202537233f, -0.0440913988f, 0.036392998f}},
-    {0, 1024, {6.64072924f, -0.0816791098f, 0.118714733f, -0.800035849f, 0.0142438209f, 0.0063186658f, -0.00191515287f, 0.137929795f, -0.032207293f, 0.0340349367f}},
-    {0, 2048, {5.68597151f, -0.165830935f, 0.279803845f, -0.765341357f, 0.0179909369f, 0.0104575887f, -0.00777931812f, 0.0742148421f, -0.00307055634f, 0.031764219f}},
-    {1, 256, {7.44703206f, 0.0913338033f, -0.0127198193f, -0.85044607f, -0.00677249923f, 0.00184801015f, 0.00303694876f, -0.0062896096f, -0.00326680161f, 0.0389004989f}},
-    {1, 512, {7.34024419f, 0.0797576955f, 0.0538422433f, -0.869031817f, -0.00540252892f, -0.000320753882f, -0.00106146329f, -0.0132930549f, -0.0136234939f, 0.0399044083f}},
-    {1, 1024, {6.63672175f, 0.132269447f, 0.29915563f, -0.969923251f, -0.00846007637f, -0.000978926262f, -0.01053147f, 0.0130306204f, -0.0200417429f, 0.0427458306f}},
-    {1, 2048, {5.30163159f, 0.157605606f, 0.610701627f, -1.03036989f, -0.0108301085f, 0.000341900614f, -0.0219543845f, 0.0201782586f, -0.0148247786f, 0.043745093f}},
-    {1, 4096, {3.57397556f, 0.181893212f, 0.938083449f, -1.05388292f, -0.0154596275f, 0.00527058079f, -0.032130546f, -0.0361358704f, 0.0165122995f, 0.0426512845f}},
-    {2, 1024, {5.438266f, -0.164636353f, -0.215992675f, -0.377090117f, -0.00801042101f, 0.0382226743f, 0.0292699102f, -0.40541281f, 0.171905311f, 0.0130644566f}},
+    {0, 128, {6.32596585f, 0.161054287f, 0.0567319871f, -0.817394585f, -0.000291889516f, 0.00947691535f, 0.00720108639f, 0.278543951f, -0.0380039254f, 0.0323045397f}},
+    {0, 256, {6.76135326f, 0.123543866f, 0.0806977112f, -0.874130438f, 0.00196533382f, 0.00523261849f, 0.00287883712f, 0.237565484f, -0.0550019129f, 0.0360926702f}},
+    {0, 512, {6.92285841f, 0.0309477548f, 0.0682869668f, -0.84860889f, 0.00766998863f, 0.0044188007f, 0.00124586854f, 0.18332268f, -0.0487189545f, 0.0359124603f}},
+    {0, 1024, {6.54865388f, -0.10686691f, 0.105374087f, -0.776884156f, 0.0154875338f, 0.00774054743f, -0.00151910083f, 0.116170665f, -0.0313161385f, 0.0333337912f}},
+    {0, 2048, {5.55392319f, -0.180748252f, 0.278615937f, -0.747356823f, 0.0184875087f, 0.011382734f, -0.00797789108f, 0.054136097f, -0.00713310756f, 0.0314061685f}},
+    {1, 256, {7.80428606f, 0.100382416f, 0.00343302636f, -0.906483809f, -0.00775595531f, 0.00188807613f, 0.00241907309f, -0.0205244659f, -0.00163554316f, 0.0405911339f}},
+    {1, 512, {7.81364181f, 0.119356165f, 0.102866709f, -0.977378568f, -0.00810699919f, -0.000969304075f, -0.00273632032f, -0.00624230515f, -0.0159528335f, 0.0432357342f}},
+    {1, 1024, {7.10032599f, 0.144580042f, 0.320125701f, -1.04372929f, -0.00945893095f, -0.00183146496f, -0.0113625829f, 0.00372923372f, -0.0141489341f, 0.0448997306f}},
+    {1, 2048, {5.59301125f, 0.194205683f, 0.655522869f, -1.10398165f, -0.0133785116f, -0.000962689672f, -0.0234915754f, 0.0112598486f, -0.00844457495f, 0.0458395646f}},
+    {1, 4096, {3.79049579f, 0.210621293f, 0.959115882f, -1.09954352f, -0.017013829f, 0.00504941651f, -0.0323231097f, -0.0105836929f, 0.0205952306f, 0.0434405961f}},
+    {2, 1024, {5.19843729f, -0.169887795f, -0.194825525f, -0.369044046f, -0.00811396268f, 0.0392129519f, 0.0286692397f, -0.410672607f, 0.169898182f, 0.0128228085f}},
 };
 
 void pkv_cost_model_default(pkv_cost_model_t *m)

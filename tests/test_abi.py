@@ -197,7 +197,7 @@ def test_policy_routes_by_batch_and_length(L):
     assert api.pkv_policy(0, 10 ** 6, custom)[0] == P.PKV_PATH_SINGLE_PASS   # empty batch
     d = api.pkv_policy_default()
     assert d.split_tokens > 0 and d.bucketed_split_tokens > 0
-    path, C = api.pkv_policy(1, 32768)
+    path, C = api.pkv_policy(1, d.bucketed_min_tokens)
     assert path == P.PKV_PATH_BUCKETED_SPLIT and C == d.bucketed_split_tokens
     assert api.pkv_policy(64, 65536)[0] == P.PKV_PATH_WORKQUEUE
     with pytest.raises(_lib.PkvError):

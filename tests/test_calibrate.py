@@ -142,3 +142,14 @@ def test_workqueue_split_rule():
     assert calibrate.wq_split(8, 2903, 256, 4096, 32, 16) == 256
     assert calibrate.wq_split(8, 8192, 256, 4096, 32, 16) == 512    # 8192 / 1024 would leave 8
     assert calibrate.wq_split(64, 65536, 256, 4096, 32, 16) == 4096
+
+
+def test_near_ties_go_to_the_better_device_time():
+    """Parameter sets within the calibration's resolution (TIE) of the best
+    wall-clock regret are told apart by device-time regret; a set outside it
+    never wins on device time alone, and without device times the wall clock
+    decides."""
+    best, near, far = 1.040, 1.040 * calibrate.TIE * 0.9999, 1.040 * calibrate.TIE * 1.001
+    assert calibrate._pick([(best, 1.05, "a"), (near, 1.01, "b")])[2] == "b"
+    assert calibrate._pick([(best, 1.05, "a"), (far, 1.00, "c")])[2] == "a"
+    assert calibrate._pick([(near, None, "b"), (best, None, "a")])[2] == "a"
