@@ -516,6 +516,10 @@ int pkv_decode_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, 
 
 namespace {
 
+// (row, head) pairs from which the merge gives each pair one warp instead of
+// a four-warp CTA.
+constexpr int64_t kMergeRowCtaPairs = 2048;
+
 int run_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const int32_t *sl,
               const float *part, void *o, float *lse, void *stream, const int32_t *rows,
               int n_rows)
@@ -540,6 +544,8 @@ int run_merge(const pkv_shape_t *s, const pkv_plan_cfg_t *c, void *d_ws, const i
     p.mode = c->path == PKV_PATH_WORKQUEUE ? kModeQueue : kModeRect;
     p.len_cap = len_cap(s);
     p.state_rows_cap = slots / s->Hq;
+    // many (row, head) pairs: one warp each, all resident in one wave
+    p.row_cta = (int64_t)p.n_rows * s->Hq >= kMergeRowCtaPairs ? 1 : 0;
     cudaError_t e = launch_merge(s->d, p, static_cast<cudaStream_t>(stream), true);
     if (e != cudaSuccess)
         return cuda_fail(e, "merge launch");

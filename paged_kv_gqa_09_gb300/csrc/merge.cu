@@ -23,15 +23,23 @@ constexpr int kMergeWarps = 4;
 constexpr int kEarlyBaseRows = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+// kRowCta = false: one CTA per (row, head), its four warps folding states
+// j = w, w + 4, ... and meeting in shared memory (rows of many splits, few
+// (row, head) pairs).  kRowCta = true: one warp per (row, head), a CTA serving
+// four heads of one row, each warp folding all of its row's states (batches of
+// many (row, head) pairs with few splits each: a quarter of the CTAs, all
+// resident at once, and no exchange).
+template <int D, bool kRowCta>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergeParams p)
 {
     constexpr int VPL = D / 32;  // values per lane: 4 (d=128) or 2 (d=64)
     __shared__ float s_max[kMergeWarps];
     __shared__ float s_l[kMergeWarps];
-    __shared__ __align__(16) float s_acc[kMergeWarps][D];
+    __shared__ __align__(16) float s_acc[kRowCta ? 1 : kMergeWarps][D];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int lr = blockIdx.x / p.Hq, h = blockIdx.x - lr * p.Hq;
+    const int cpr = kRowCta ? (p.Hq + kMergeWarps - 1) / kMergeWarps : p.Hq;  // CTAs per row
+    const int lr = blockIdx.x / cpr;
+    const int h = kRowCta ? (blockIdx.x - lr * cpr) * kMergeWarps + warp : blockIdx.x - lr * cpr;
     // The merge reads the row list and the lengths while the decode it follows
     // is still running: both are inputs that no kernel writes between a step's
     // decode and its merge (an append that advances the lengths finished before
@@ -70,7 +78,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
     // global memory, so the next one may be scheduled as soon as this one runs
     pdl_wait();
     pdl_trigger();
-    if (lr >= p.n_rows)
+    if (lr >= p.n_rows || h >= p.Hq)
         return;
     if (!early) {
         i = p.rows ? p.rows[lr] : lr;  // row of the batch
@@ -92,7 +100,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
         n = min(n, p.S_b);
     }
     if (bad || n == 0) {
-        if (warp == 0) {
+        if (kRowCta || warp == 0) {
             __half *out = p.o + (size_t)wg * D + lane * VPL;
             const __half fill = bad ? __float2half(NAN) : __float2half(0.f);
 #pragma unroll
@@ -111,7 +119,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
     for (int v = 0; v < VPL; ++v)
         acc[v] = 0.f;
 #pragma unroll 8
-    for (int j = warp; j < n; j += kMergeWarps) {
+    for (int j = kRowCta ? 0 : warp; j < n; j += kRowCta ? 1 : kMergeWarps) {
         const int64_t slot = (base + j) * p.Hq + h;
         const float mj = p.part_m[slot];
         const float lj = p.part_l[slot];
@@ -135,6 +143,23 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
         for (int v = 0; v < VPL; ++v)
             acc[v] = acc[v] * so + x[v] * sj;
         Mw = mn;
+    }
+    __half *out = p.o + (size_t)wg * D + lane * VPL;
+    if constexpr (kRowCta) {
+        // the warp holds the whole (row, head): normalise and write
+        const float inv = 1.f / L;
+        float o[VPL];
+#pragma unroll
+        for (int v = 0; v < VPL; ++v)
+            o[v] = acc[v] * inv;
+        if constexpr (VPL == 4) {
+            *reinterpret_cast<uint2 *>(out) = make_uint2(pack_half2(o[0], o[1]), pack_half2(o[2], o[3]));
+        } else {
+            *reinterpret_cast<uint32_t *>(out) = pack_half2(o[0], o[1]);
+        }
+        if (p.lse && lane == 0)
+            p.lse[wg] = Mw + logf(L);
+        return;
     }
     if (lane == 0) {
         s_max[warp] = Mw;
@@ -166,7 +191,6 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
             t += s_acc[w2][lane * VPL + v] * sc[w2];
         o[v] = t * inv;
     }
-    __half *out = p.o + (size_t)wg * D + lane * VPL;
     if constexpr (VPL == 4) {
         *reinterpret_cast<uint2 *>(out) = make_uint2(pack_half2(o[0], o[1]), pack_half2(o[2], o[3]));
     } else {
@@ -347,12 +371,15 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAtt
 
 cudaError_t launch_merge(int d, const MergeParams &p, cudaStream_t s, bool pdl)
 {
-    const int blocks = p.n_rows * p.Hq > 0 ? p.n_rows * p.Hq : 1;
+    const int per_row = p.row_cta ? (p.Hq + kMergeWarps - 1) / kMergeWarps : p.Hq;
+    const int blocks = p.n_rows * per_row > 0 ? p.n_rows * per_row : 1;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = make_cfg(dim3(blocks), dim3(32 * kMergeWarps), s, attr, pdl);
-    if (d == 128)
-        return cudaLaunchKernelEx(&cfg, merge_kernel<128>, p);
-    return cudaLaunchKernelEx(&cfg, merge_kernel<64>, p);
+    if (p.row_cta)
+        return d == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<128, true>, p)
+                        : cudaLaunchKernelEx(&cfg, merge_kernel<64, true>, p);
+    return d == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<128, false>, p)
+                    : cudaLaunchKernelEx(&cfg, merge_kernel<64, false>, p);
 }
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s, bool pdl)

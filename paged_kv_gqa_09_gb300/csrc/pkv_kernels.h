@@ -93,6 +93,7 @@ struct MergeParams {
     int B, Hq, C, S_b, mode;
     int len_cap;
     int64_t state_rows_cap;  // partial-state rows the buffer holds
+    int row_cta;             // one warp per (row, head), four heads of a row per CTA
 };
 
 struct AppendParams {

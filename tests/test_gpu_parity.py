@@ -254,6 +254,27 @@ def test_group_sizes_and_head_dims(Hq, Hkv, dd, path):
     close_lse(lse, lref)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,dd", [(64, 32, 8, 128), (64, 32, 8, 64), (400, 6, 2, 128),
+                                        (600, 4, 2, 128)])
+@pytest.mark.parametrize("path", [BUCKETED, WORKQUEUE])
+def test_merge_with_a_warp_per_row_and_head(B, Hq, Hkv, dd, path):
+    """Batches of at least 2048 (row, head) pairs merge with one warp per pair
+    and four heads of a row per CTA (Hq = 6: the row's second CTA has two idle
+    warps; B = 600: the workqueue merge reads its offsets after the wait);
+    rows of 0 to 11 splits, empty rows included."""
+    rng = np.random.default_rng(B * 10 + Hq + dd)
+    lens = rng.integers(0, 700, size=B)
+    lens[::17] = 0
+    lens[5] = 704  # exactly 11 splits of C = 64
+    tr, q, k, v = case(lens.tolist(), Hq=Hq, Hkv=Hkv, d=dd, P=16, C=64, seed=B + Hq + dd)
+    d = upload(tr, q, k, v)
+    o, lse, ws, _ = run_path(tr, d, path)
+    check_error_free(ws)
+    oref, lref = oracle_out(tr, q, k, v)
+    close(o, oref)
+    close_lse(lse, lref)
+
+
 def test_wide_table_shared_pages_and_big_pool():
     tr, q, k, v = case([500, 300, 77, 0, 1], Hq=8, Hkv=2, P=16, C=128, extra_pages=40,
                        extra_cols=5, share_prefix_pages=10)
