@@ -4,13 +4,15 @@
 // Merge: "PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM
 // Serving on Commodity GPUs", technical summary, Methodology 1, "Sequence
 // splitting": a separate kernel combines the partial online-softmax states
-// exactly.  One 4-warp CTA per (row i, query head h) reads only the row's
+// exactly.  Each (row i, query head h) reads only the row's
 // n_i = ceil(N*_i / C) states (row-local bounds):
 //   M = max_j m_j; L = sum_j l_j e^{m_j - M}; o = sum_j acc_j e^{m_j - M} / L;
 //   lse = M + ln L; a row with N*_i = 0 gets o = 0, lse = -inf.
 // The states are few and were just written (L2-resident), so the kernel is
-// latency-bound: warp w takes states j = w, w+4, ... with all of its loads
-// in flight at once, and the four partial sums meet in shared memory.
+// latency-bound.  A 4-warp CTA per (row, head): warp w takes states
+// j = w, w+4, ... with all of its loads in flight at once, and the four
+// partial sums meet in shared memory; or, on batches of many (row, head)
+// pairs, one warp per pair and four heads of a row per CTA.
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
 
