@@ -32,6 +32,8 @@
 //               K rows of that stage; warp 0 merges the four states exactly,
 //               writes the task's partial state (m, l, acc) -- or, in single
 //               mode, o and lse -- and releases the stage for all four warps.
+//               While the producer waits for the previous kernel, warp 0
+//               prefetches the CTA's first tiles into L2.
 // Two CTAs per SM keep every task of a 256-task launch in flight at once, so
 // the DRAM bandwidth is shared per task rather than per wave of tasks.
 // Every barrier wait is bounded (1 s); a timeout records an error in the
