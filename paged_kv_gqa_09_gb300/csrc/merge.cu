@@ -120,31 +120,51 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergePara
 #pragma unroll
     for (int v = 0; v < VPL; ++v)
         acc[v] = 0.f;
-#pragma unroll 8
-    for (int j = kRowCta ? 0 : warp; j < n; j += kRowCta ? 1 : kMergeWarps) {
-        const int64_t slot = (base + j) * p.Hq + h;
-        const float mj = p.part_m[slot];
-        const float lj = p.part_l[slot];
-        const float *a = p.part_acc + slot * D + lane * VPL;
-        float x[VPL];
-        if constexpr (VPL == 4) {
-            const float4 t = *reinterpret_cast<const float4 *>(a);
-            x[0] = t.x;
-            x[1] = t.y;
-            x[2] = t.z;
-            x[3] = t.w;
-        } else {
-            const float2 t = *reinterpret_cast<const float2 *>(a);
-            x[0] = t.x;
-            x[1] = t.y;
-        }
-        const float mn = fmaxf(Mw, mj);
-        const float so = ex2((Mw - mn) * kLog2e), sj = ex2((mj - mn) * kLog2e);
-        L = L * so + lj * sj;
+    // states j = first, first + js, ... in batches of kBatch: a batch's loads
+    // are all issued before its first fold, so a warp waits one L2 round
+    // trip per batch rather than one per state
+    constexpr int kBatch = 8;
+    const int js = kRowCta ? 1 : kMergeWarps;
+    for (int j0 = kRowCta ? 0 : warp; j0 < n; j0 += kBatch * js) {
+        float mj[kBatch], lj[kBatch], x[kBatch][VPL];
 #pragma unroll
-        for (int v = 0; v < VPL; ++v)
-            acc[v] = acc[v] * so + x[v] * sj;
-        Mw = mn;
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * js;
+            mj[u] = -INFINITY;
+            lj[u] = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v)
+                x[u][v] = 0.f;
+            if (j < n) {
+                const int64_t slot = (base + j) * p.Hq + h;
+                mj[u] = p.part_m[slot];
+                lj[u] = p.part_l[slot];
+                const float *a = p.part_acc + slot * D + lane * VPL;
+                if constexpr (VPL == 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(a);
+                    x[u][0] = t.x;
+                    x[u][1] = t.y;
+                    x[u][2] = t.z;
+                    x[u][3] = t.w;
+                } else {
+                    const float2 t = *reinterpret_cast<const float2 *>(a);
+                    x[u][0] = t.x;
+                    x[u][1] = t.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (j0 + u * js >= n)
+                break;
+            const float mn = fmaxf(Mw, mj[u]);
+            const float so = ex2((Mw - mn) * kLog2e), sj = ex2((mj[u] - mn) * kLog2e);
+            L = L * so + lj[u] * sj;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v)
+                acc[v] = acc[v] * so + x[u][v] * sj;
+            Mw = mn;
+        }
     }
     __half *out = p.o + (size_t)wg * D + lane * VPL;
     if constexpr (kRowCta) {
