@@ -262,29 +262,49 @@ __device__ void grid_merge(const DecodeParams &p, uint8_t *basep, volatile int *
 #pragma unroll
             for (int v = 0; v < VPL; ++v)
                 acc[v] = 0.f;
-#pragma unroll 8
-            for (int j = warp; j < n; j += kCW) {
-                const int64_t slot = (int64_t)(base + j) * p.Hq + h;
-                const float mj = __ldcg(p.part_m + slot), lj = __ldcg(p.part_l + slot);
-                float x[VPL];
-                if constexpr (VPL == 4) {
-                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(p.part_acc + slot * D) + lane);
-                    x[0] = t.x;
-                    x[1] = t.y;
-                    x[2] = t.z;
-                    x[3] = t.w;
-                } else {
-                    const float2 t = __ldcg(reinterpret_cast<const float2 *>(p.part_acc + slot * D) + lane);
-                    x[0] = t.x;
-                    x[1] = t.y;
-                }
-                const float mn = fmaxf(Mw, mj);
-                const float so = ex2((Mw - mn) * kLog2e), sj = ex2((mj - mn) * kLog2e);
-                Lw = Lw * so + lj * sj;
+            // states j = warp, warp + kCW, ... in batches of kBatch, each
+            // batch's loads issued before its first fold (one L2 round trip
+            // per batch); read past L1, since this launch wrote them
+            constexpr int kBatch = 8;
+            for (int j0 = warp; j0 < n; j0 += kBatch * kCW) {
+                float mj[kBatch], lj[kBatch], x[kBatch][VPL];
 #pragma unroll
-                for (int v = 0; v < VPL; ++v)
-                    acc[v] = acc[v] * so + x[v] * sj;
-                Mw = mn;
+                for (int q = 0; q < kBatch; ++q) {
+                    const int j = j0 + q * kCW;
+                    mj[q] = -INFINITY;
+                    lj[q] = 0.f;
+#pragma unroll
+                    for (int v = 0; v < VPL; ++v)
+                        x[q][v] = 0.f;
+                    if (j < n) {
+                        const int64_t slot = (int64_t)(base + j) * p.Hq + h;
+                        mj[q] = __ldcg(p.part_m + slot);
+                        lj[q] = __ldcg(p.part_l + slot);
+                        if constexpr (VPL == 4) {
+                            const float4 t = __ldcg(reinterpret_cast<const float4 *>(p.part_acc + slot * D) + lane);
+                            x[q][0] = t.x;
+                            x[q][1] = t.y;
+                            x[q][2] = t.z;
+                            x[q][3] = t.w;
+                        } else {
+                            const float2 t = __ldcg(reinterpret_cast<const float2 *>(p.part_acc + slot * D) + lane);
+                            x[q][0] = t.x;
+                            x[q][1] = t.y;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < kBatch; ++q) {
+                    if (j0 + q * kCW >= n)
+                        break;
+                    const float mn = fmaxf(Mw, mj[q]);
+                    const float so = ex2((Mw - mn) * kLog2e), sj = ex2((mj[q] - mn) * kLog2e);
+                    Lw = Lw * so + lj[q] * sj;
+#pragma unroll
+                    for (int v = 0; v < VPL; ++v)
+                        acc[v] = acc[v] * so + x[q][v] * sj;
+                    Mw = mn;
+                }
             }
             if (lane == 0) {
                 s_m[warp] = Mw;
