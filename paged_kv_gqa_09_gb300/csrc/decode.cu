@@ -574,8 +574,24 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmK, const CUten
                         const int4 *qsrc = reinterpret_cast<const int4 *>(
                             p.q + ((size_t)cur.i * p.Hq + (size_t)cur.g * G) * D);
                         int4 *qdst = reinterpret_cast<int4 *>(basep + (kdst - sbase) + 2 * L::kTileBytes);
-                        for (int x = lane; x < G * D / 8; x += 32)
-                            qdst[x] = qsrc[x];
+                        if constexpr (MODE == kModeQueue) {
+                            for (int x = lane; x < G * D / 8; x += 32)
+                                qdst[x] = qsrc[x];
+                        } else {
+                            // all of a lane's loads first, then its stores: one round
+                            // trip (a step's first and only task per CTA on one-row
+                            // launches; the workqueue measured ~0.2% slower with it)
+                            constexpr int kQPerLane = kMaxG * D / 8 / 32;
+                            int4 qv[kQPerLane];
+#pragma unroll
+                            for (int u = 0; u < kQPerLane; ++u)
+                                if (lane + 32 * u < G * D / 8)
+                                    qv[u] = qsrc[lane + 32 * u];
+#pragma unroll
+                            for (int u = 0; u < kQPerLane; ++u)
+                                if (lane + 32 * u < G * D / 8)
+                                    qdst[lane + 32 * u] = qv[u];
+                        }
                         __syncwarp();
                         if (lane == 0)
                             mbar_arrive(full);
