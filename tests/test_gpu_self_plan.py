@@ -229,3 +229,35 @@ def test_host_loop_graph_and_paged_decoder():
         check_error_free(loop.ws)
         close(ho, oref)
         close_lse(hl, lref)
+
+
+def test_random_batches_match_oracle():
+    """Seeded random batches -- B up to 512, page sizes 8..64, C = 1..16 pages,
+    Hkv 1..8, G 1..8, d 64 or 128, lengths from 0 to 20 splits with empty rows
+    mixed in -- through both plan modes: the plan (header, offsets, canonical
+    and balance-ordered lists) bit-exact against the oracle and the definition
+    of the order, the outputs within tolerance."""
+    rng = np.random.default_rng(20261203)
+    for case in range(24):
+        B = int(rng.choice([1, 3, 8, 31, 33, 64, 200, 512]))
+        P = int(rng.choice([8, 16, 64]))
+        C = P * int(rng.choice([1, 2, 4, 16]))
+        Hkv, G, d = int(rng.choice([1, 2, 8])), int(rng.choice([1, 4, 8])), int(rng.choice([64, 128]))
+        maxlen = int(rng.choice([C, 4 * C, 20 * C])) if B < 200 else min(int(rng.choice([C, 4 * C])), 1024)
+        lens = rng.integers(0, min(maxlen, 16384) + 1, size=B)
+        lens[rng.random(B) < 0.1] = 0
+        tr = T.custom_trace(lens.tolist(), Hkv * G, Hkv, d, P, C, seed=case, extra_cols=1)
+        q = T.gen_q(tr)
+        k, v = T.gen_kv(tr, poison_unused=True)
+        d_in = upload(tr, q, k, v)
+        oref, lref = oracle_out(tr, q, k, v)
+        want, want_off = oracle.plan_compact(tr.seq_lens, tr.Hq, tr.Hkv, C)
+        for plan in (IN_DECODE, SEPARATE):
+            o, lse, ws, _ = run_path(tr, d_in, WORKQUEUE, plan=plan)
+            check_error_free(ws)
+            count, off, tasks, h, ordered = read_plan(ws, tr.B, with_order=True)
+            assert count == want.shape[0], (case, plan)
+            assert np.array_equal(off, want_off) and np.array_equal(tasks, want), (case, plan)
+            assert np.array_equal(ordered, expected_order(want, tr.seq_lens, C)), (case, plan)
+            close(o, oref, f"case {case}, plan mode {plan}")
+            close_lse(lse, lref)
