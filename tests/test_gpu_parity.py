@@ -275,6 +275,28 @@ def test_merge_with_a_warp_per_row_and_head(B, Hq, Hkv, dd, path):
     close_lse(lse, lref)
 
 
+def test_random_batches_on_every_path():
+    """Seeded random batches on the bucketed split, the workqueue (plan
+    kernel) and the single pass: B up to 64, page sizes 8..256, C = 1..8
+    pages, Hkv 1..8, G 1..8, d 64 or 128, rows of 0 to 40 pages."""
+    rng = np.random.default_rng(20261204)
+    for n in range(16):
+        B = int(rng.choice([1, 2, 5, 16, 64]))
+        P = int(rng.choice([8, 16, 32, 256]))
+        C = P * int(rng.choice([1, 2, 8]))
+        Hkv, G, dd = int(rng.choice([1, 2, 8])), int(rng.choice([1, 3, 8])), int(rng.choice([64, 128]))
+        lens = rng.integers(0, 40 * P + 1, size=B)
+        lens[rng.random(B) < 0.15] = 0
+        tr, q, k, v = case(lens.tolist(), Hq=Hkv * G, Hkv=Hkv, d=dd, P=P, C=C, seed=100 + n)
+        d = upload(tr, q, k, v)
+        oref, lref = oracle_out(tr, q, k, v)
+        for path in (BUCKETED, WORKQUEUE, SINGLE):
+            o, lse, ws, _ = run_path(tr, d, path)
+            check_error_free(ws)
+            close(o, oref, f"case {n}, path {path}")
+            close_lse(lse, lref)
+
+
 def test_wide_table_shared_pages_and_big_pool():
     tr, q, k, v = case([500, 300, 77, 0, 1], Hq=8, Hkv=2, P=16, C=128, extra_pages=40,
                        extra_cols=5, share_prefix_pages=10)
